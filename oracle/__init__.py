@@ -1,0 +1,150 @@
+"""CPU fp64 oracle for LazyAttention (test infrastructure only).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package. The product (``paged_kv_cache_57_gb300``) never
+imports it, and it imports nothing from the product.
+
+The arithmetic lives in ``lazy_oracle.c`` (plain C, fp64, OpenMP); this module
+compiles it with gcc and marshals arrays. Definitions and citations are in the
+C file's header. Parity status: the attention output is pinned only through the
+checks in ``tests/test_oracle_pins.py`` (brute force from raw keys, the
+relative-offset identity, textbook reductions and closed forms); the pages
+print no numeric worked example of LazyAttention itself.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lazy_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "liblazyoracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_i32p = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
+_f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liblazyoracle.so`` (gcc, -O2, OpenMP)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99", _SRC,
+                               "-o", tmp, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_SO)
+            L.lo_rope_rotate.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double, _f64p, _f64p]
+            L.lo_softmax_dot.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, _f64p, _f64p, _f64p]
+            L.lo_tiled_softmax_dot.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, _f64p, _f64p,
+                                               ctypes.c_int, _f64p]
+            L.lo_kv_cache_bytes.restype = ctypes.c_double
+            L.lo_kv_cache_bytes.argtypes = [ctypes.c_double] * 6
+            L.lo_num_threads.restype = ctypes.c_int
+            L.lo_set_num_threads.argtypes = [ctypes.c_int]
+            L.lo_attention.restype = ctypes.c_int
+            L.lo_attention.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                ctypes.c_int, ctypes.c_int, ctypes.c_void_p, _i32p, _i32p, ctypes.c_void_p,
+                ctypes.c_void_p, ctypes.c_int64, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p, _f64p]
+            _lib = L
+    return _lib
+
+
+def num_threads() -> int:
+    return int(lib().lo_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    lib().lo_set_num_threads(int(n))
+
+
+def rope_rotate(x: np.ndarray, n: float, theta: float) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(x)
+    lib().lo_rope_rotate(x.shape[-1], float(theta), float(n), x, y)
+    return y
+
+
+def softmax_dot(q, K, V) -> np.ndarray:
+    q, K, V = (np.ascontiguousarray(a, dtype=np.float64) for a in (q, K, V))
+    out = np.empty(V.shape[1], np.float64)
+    lib().lo_softmax_dot(K.shape[0], q.shape[0], q, K, V, out)
+    return out
+
+
+def tiled_softmax_dot(q, K, V, tile: int) -> np.ndarray:
+    q, K, V = (np.ascontiguousarray(a, dtype=np.float64) for a in (q, K, V))
+    out = np.empty(V.shape[1], np.float64)
+    lib().lo_tiled_softmax_dot(K.shape[0], q.shape[0], q, K, V, int(tile), out)
+    return out
+
+
+def kv_cache_bytes(layers, heads, head_dim, seq, batch, elt_bytes) -> float:
+    return float(lib().lo_kv_cache_bytes(layers, heads, head_dim, seq, batch, elt_bytes))
+
+
+def _bits(t) -> tuple:
+    """(numpy view of the stored bits, dtype code) of a CPU torch tensor."""
+    import torch
+    t = t.contiguous()
+    if t.dtype == torch.float32:
+        return t.numpy(), 0
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy(), 1
+    raise TypeError(f"oracle reads fp32 or bf16 stored tensors, not {t.dtype}")
+
+
+def query_rows(w):
+    """(q_seq, q_m) for every query row of a workload."""
+    if w.kind == "decode":
+        return np.arange(w.num_seqs, dtype=np.int32), np.asarray(w.q_pos, np.int32)
+    cu = np.asarray(w.cu_seqlens_q)
+    q_seq = np.repeat(np.arange(w.num_seqs, dtype=np.int32), np.diff(cu)).astype(np.int32)
+    q_m = np.concatenate([w.q_start[s] + np.arange(cu[s + 1] - cu[s]) for s in range(w.num_seqs)] or
+                         [np.zeros(0)]).astype(np.int32)
+    return q_seq, q_m
+
+
+def attention(w, rows: Optional[Sequence[int]] = None, sm_scale: float = 0.0,
+              k_pool=None, v_pool=None) -> np.ndarray:
+    """fp64 reference output of workload ``w`` for the query rows ``rows`` (all by
+    default): decode rows are sequences, prefill rows are chunk tokens.
+    Returns [len(rows), Hq, d]."""
+    q_seq, q_m = query_rows(w)
+    q = w.q
+    if rows is not None:
+        rows = np.asarray(rows, dtype=np.int64)
+        q_seq, q_m, q = q_seq[rows], q_m[rows], w.q[rows]
+    qb, dt = _bits(q)
+    kb, dk = _bits(w.k_pool if k_pool is None else k_pool)
+    vb, dv = _bits(w.v_pool if v_pool is None else v_pool)
+    assert dt == dk == dv
+    nq = qb.shape[0]
+    out = np.zeros((nq, w.num_q_heads, w.head_dim), np.float64)
+    rc = lib().lo_attention(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, float(w.rope_theta),
+                            float(sm_scale), dt, nq, qb.ctypes.data, np.ascontiguousarray(q_seq, np.int32),
+                            np.ascontiguousarray(q_m, np.int32), kb.ctypes.data, vb.ctypes.data,
+                            int(kb.shape[0]), np.ascontiguousarray(w.seg_indptr, np.int32),
+                            np.ascontiguousarray(w.seg_doc, np.int32), np.ascontiguousarray(w.seg_len, np.int32),
+                            np.ascontiguousarray(w.seq_pos0, np.int32),
+                            np.ascontiguousarray(w.doc_block_indptr, np.int32),
+                            np.ascontiguousarray(w.doc_blocks, np.int32), out)
+    if rc != 0:
+        raise ValueError("oracle: malformed layout")
+    return out
