@@ -1,0 +1,418 @@
+#!/usr/bin/env python3
+"""Benchmark of LazyAttention decode (and prefill) over a paged, position-agnostic KV cache.
+
+Default workload: Llama-3.1-8B-shaped decode, bf16, 32 q / 8 KV heads, d=128,
+batch 64, contexts of 8 Zipf(1.0)-drawn 512-token documents from a 256-document
+pool plus a 64-token private suffix (4160 tokens), RoPE theta 5e5. One step is
+one decode call (split kernel + combine) for the whole batch, one layer.
+
+Prints ONE JSON line (rank 0). ``value`` is logical KV GB/s: K+V bytes of every
+token of every context divided by the device time of the decode call, inputs
+resident in HBM, L2 flushed between steps. Extra keys carry the roofline against
+the unique-block HBM bound, the no-sharing control, the lazy-vs-pre-rotated
+overhead, prefill TFLOP/s, an end-to-end figure through host buffers, clocks and
+the CPU oracle baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LazyAttn decode KV GB/s (% HBM peak); prefill TFLOP/s; lazy-RoPE overhead %"
+WORKLOAD = "llama8b_decode"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), float(j.get("bf16_tflops_sustained", j["bf16_tflops"])), \
+            "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.samples, self.proc = index, [], None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 7:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[3 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def build_device(w, lazy=True, k_pool=None):
+    import torch
+    from paged_kv_cache_57_gb300 import lazy_attn as L
+    p = L.make_params(num_seqs=w.num_seqs, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                      head_dim=w.head_dim, num_pool_blocks=w.num_pool_blocks,
+                      max_blocks_per_seq=max(1, w.max_blocks_per_seq), dtype=w.dtype, rope_theta=w.rope_theta,
+                      lazy=lazy)
+    c = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    words, seq_lens = L.pack_block_words(p, len(w.doc_len), c(w.seg_indptr), c(w.seg_doc), c(w.seg_len),
+                                         c(w.seq_pos0), c(w.doc_block_indptr), c(w.doc_blocks))
+    d = dict(p=p, q=w.q.cuda(), k=(w.k_pool if k_pool is None else k_pool).cuda(), v=w.v_pool.cuda(), words=words,
+             seq_lens=seq_lens, rope=L.rope_table_init(p))
+    if w.kind == "decode":
+        d["q_pos"] = c(w.q_pos)
+        d["ws"] = torch.empty(max(1, L.decode_workspace_bytes(p)), dtype=torch.uint8, device="cuda")
+        d["out"] = torch.empty_like(d["q"])
+    else:
+        d["cu"] = c(w.cu_seqlens_q)
+        d["q_start"] = c(w.q_start)
+        d["max_q"] = int(np.diff(w.cu_seqlens_q).max())
+        d["out"] = torch.empty_like(d["q"])
+    return d
+
+
+def run_decode(d, lazy=None):
+    from paged_kv_cache_57_gb300 import lazy_attn as L
+    p = d["p"]
+    if lazy is not None:
+        p.lazy = int(lazy)
+    L.decode(p, d["q"], d["k"], d["v"], d["words"], d["seq_lens"], d["q_pos"], d["rope"], out=d["out"],
+             workspace=d["ws"])
+
+
+def run_prefill(d, lazy=None):
+    from paged_kv_cache_57_gb300 import lazy_attn as L
+    p = d["p"]
+    if lazy is not None:
+        p.lazy = int(lazy)
+    L.prefill(p, d["q"], d["cu"], d["q_start"], d["max_q"], d["k"], d["v"], d["words"], d["seq_lens"], d["rope"],
+              out=d["out"])
+
+
+def time_steps(fn, steps, warmup, flush):
+    """Per-step device time (s) with CUDA events on the launching stream, L2 flushed before each step."""
+    import torch
+    st = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.add_(1)
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        flush.add_(1)
+        a.record(st)
+        fn()
+        b.record(st)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e-3 for a, b in evs]
+
+
+def decode_bytes(w):
+    from paged_kv_cache_57_gb300 import workloads as W
+    elt = 2 if w.dtype == "bf16" else 4
+    io = 2 * w.q.numel() * elt + 4 * w.num_seqs * (max(1, w.max_blocks_per_seq) + 2)
+    return dict(logical=W.kv_bytes_logical(w) + io, unique=W.kv_bytes_unique(w) + io, blocks=W.kv_bytes_blocks(w) + io,
+                kv_logical=W.kv_bytes_logical(w))
+
+
+def prefill_flops(w):
+    """4 d Hq sum_s (C_s N_ctx,s + C_s (C_s + 1) / 2): exact causal count, no rotation."""
+    cu = np.asarray(w.cu_seqlens_q)
+    tot = 0
+    for s in range(w.num_seqs):
+        C = int(cu[s + 1] - cu[s])
+        nctx = int(w.tokens_per_seq()[s]) - C
+        tot += C * nctx + C * (C + 1) // 2
+    return 4 * w.head_dim * w.num_q_heads * tot
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+
+def oracle_sample_rate(w, budget_s=10.0, seqs_per_call=2):
+    """Runs the oracle over consecutive sequences of ``w`` until ``budget_s`` has elapsed;
+    returns (logical KV GB/s, seconds, sequences, threads)."""
+    import oracle
+    from paged_kv_cache_57_gb300 import workloads as W
+    oracle.build()
+    elt = 2 if w.dtype == "bf16" else 4
+    toks = w.tokens_per_seq()
+    t0 = time.perf_counter()
+    done, nbytes = 0, 0
+    while True:
+        rows = [(done + i) % w.num_seqs for i in range(seqs_per_call)]
+        oracle.attention(w, rows=rows)
+        nbytes += int(sum(toks[r] for r in rows)) * w.num_kv_heads * w.head_dim * 2 * elt
+        done += seqs_per_call
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return nbytes / el / 1e9, el, done, oracle.num_threads()
+
+
+def reference_arm(args):
+    """The oracle timed on the host cores, as the reference arm."""
+    import oracle
+    from paged_kv_cache_57_gb300 import workloads as W
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = W.FULL[WORKLOAD]()
+    oracle.build()
+    elt = 2
+    toks = w.tokens_per_seq()
+    per_step = 2  # sequences per step (all heads)
+    times, nbytes = [], 0
+    for i in range(args.warmup + args.steps):
+        rows = [(2 * i + j) % w.num_seqs for j in range(per_step)]
+        t0 = time.perf_counter()
+        oracle.attention(w, rows=rows)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            nbytes += int(sum(toks[r] for r in rows)) * w.num_kv_heads * w.head_dim * 2 * elt
+    total = sum(times)
+    value = nbytes / total / 1e9
+    cores = oracle.num_threads()
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": w.num_seqs, "context": int(toks[0]),
+                       "heads": [w.num_q_heads, w.num_kv_heads], "head_dim": w.head_dim,
+                       "step": f"{per_step} sequences x all heads (bounded sample)"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{per_step} sequences per step, {args.steps} steps"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="headline decode only (used for ncu launch lists)")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    import torch.distributed as dist
+    from paged_kv_cache_57_gb300 import build
+    from paged_kv_cache_57_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    if rank == 0:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    build.build()  # no-op once built
+    from paged_kv_cache_57_gb300 import lazy_attn as L
+
+    hbm, tf_burst, tf_sust, peak_src = _peaks()
+    # Weak scaling: each rank decodes its own batch (a different seed), no data exchange.
+    w = W.decode_zipf(WORKLOAD, batch=64, hq=32, hkv=8, docs_per_seq=8, doc_tokens=512, pool_docs=256,
+                      zipf_s=1.0, suffix_tokens=64, seed=20260002 + 1000 * rank)
+    d = build_device(w)
+    nbytes = decode_bytes(w)
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device="cuda")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    fn = lambda: run_decode(d, lazy=True)
+    for _ in range(args.warmup):
+        flush.add_(1)
+        fn()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = L.launch_count()
+    t_wall0 = time.perf_counter()
+    per_step = time_steps(fn, args.steps, 0, flush)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    launches = L.launch_count() - launches0
+    clk = clocks.stop()
+    t_dev = sum(per_step)
+    t_max = t_dev
+    if world > 1:
+        tt = torch.tensor([t_dev], device="cuda", dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    ms = 1e3 * t_max / args.steps
+    value = world * nbytes["kv_logical"] * args.steps / t_max / 1e9
+    avg = t_dev / args.steps
+    achieved = nbytes["unique"] / avg / 1e9
+
+    extras = {}
+    if not args.no_extras and rank == 0:
+        extras = measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust)
+    e2e = measure_e2e(args, d, w, nbytes) if rank == 0 else None
+
+    if world > 1:
+        dist.barrier()
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": w.num_seqs, "context": int(w.tokens_per_seq()[0]),
+                   "heads": [w.num_q_heads, w.num_kv_heads], "head_dim": w.head_dim, "rope_theta": w.rope_theta,
+                   "docs": "8 x 512 Zipf(1.0) of 256 + 64 private", "l2": "flushed before every step",
+                   "parallelism": f"weak x{world} (independent batches)"},
+        "decode": {"tokens_per_s": world * w.num_seqs / (t_max / args.steps),
+                   "kv_gbs_logical": value, "kv_gbs_unique": world * nbytes["unique"] * args.steps / t_max / 1e9,
+                   "bytes_logical": nbytes["logical"], "bytes_unique": nbytes["unique"],
+                   "hbm_frac_unique_of_measured": achieved / hbm, "hbm_frac_unique_of_8tbs": achieved / 8000.0,
+                   "ms_median": 1e3 * statistics.median(per_step)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": None, "peak_source": peak_src,
+                     "kernel": "decode call (split kernel + combine); bytes = unique K/V blocks + q + out + words"},
+        "gpu_launches": launches, "wall_s_timed": t_wall, "clocks": clk, "e2e": e2e,
+    }
+    line.update(extras)
+    if not args.no_cpu_baseline:
+        v, el, nseq, cores = oracle_sample_rate(w, budget_s=10.0)
+        line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{nseq} sequences of the same workload (all heads), {el:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_e2e(args, d, w, nbytes):
+    """Same decode through the public API with the step's inputs copied from pinned host
+    memory (q, block words, seq_lens, q_pos) and the output read back, per step. The KV
+    pool is the resident cache (it persists across steps), not a per-step input."""
+    import torch
+    from paged_kv_cache_57_gb300 import lazy_attn as L
+    steps = max(3, min(args.steps, 50))
+    hq = d["q"].cpu().pin_memory()
+    hw = d["words"].cpu().pin_memory()
+    hs = d["seq_lens"].cpu().pin_memory()
+    hp = d["q_pos"].cpu().pin_memory()
+    hout = torch.empty_like(d["out"], device="cpu").pin_memory()
+    q, words, sl, qp = (torch.empty_like(x, device="cuda") for x in (hq, hw, hs, hp))
+    st = torch.cuda.current_stream()
+    times = []
+    for i in range(steps + 3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        q.copy_(hq, non_blocking=True)
+        words.copy_(hw, non_blocking=True)
+        sl.copy_(hs, non_blocking=True)
+        qp.copy_(hp, non_blocking=True)
+        L.decode(d["p"], q, d["k"], d["v"], words, sl, qp, d["rope"], out=d["out"], workspace=d["ws"])
+        hout.copy_(d["out"], non_blocking=True)
+        b.record(st)
+        b.synchronize()
+        if i >= 3:
+            times.append(a.elapsed_time(b) * 1e-3)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hw, hs, hp))
+    d2h = hout.numel() * hout.element_size()
+    return {"value": nbytes["kv_logical"] / statistics.mean(times) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * statistics.mean(times)}
+
+
+def measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust):
+    import torch
+    from paged_kv_cache_57_gb300 import lazy_attn as L
+    from paged_kv_cache_57_gb300 import workloads as W
+    out = {}
+    n = max(20, min(args.steps, 200))
+    # Lazy overhead: same pool and block table, rotation compiled out (interleaved A/B).
+    t1, t0 = [], []
+    for _ in range(4):
+        t1 += time_steps(lambda: run_decode(d, lazy=True), n // 4, 2, flush)
+        t0 += time_steps(lambda: run_decode(d, lazy=False), n // 4, 2, flush)
+    d["p"].lazy = 1
+    dec_over = 100.0 * (statistics.median(t1) / statistics.median(t0) - 1.0)
+    out["lazy_overhead_pct"] = {"decode": dec_over, "decode_ms_lazy": 1e3 * statistics.median(t1),
+                                "decode_ms_prerotated": 1e3 * statistics.median(t0),
+                                "pages_h100_context": {"decode_latency": 0.13, "prefill_flops_m128": 0.59}}
+    # No-sharing control: logical bytes = unique bytes = DRAM bytes.
+    wc = W.FULL["llama8b_decode_noshare"]()
+    dc = build_device(wc)
+    tc = time_steps(lambda: run_decode(dc), n, 3, flush)
+    bc = decode_bytes(wc)
+    gbs = bc["unique"] / statistics.median(tc) / 1e9
+    out["noshare_control"] = {"workload": "llama8b_decode_noshare", "gbs": gbs, "frac_of_measured": gbs / hbm,
+                              "frac_of_8tbs": gbs / 8000.0, "ms_median": 1e3 * statistics.median(tc)}
+    del dc
+    # Prefill (Llama-3.1-8B-shaped, 8 x (6 x 1024 docs + 256-token chunk)).
+    try:
+        wp = W.FULL["llama8b_prefill"]()
+        dp = build_device(wp)
+        fl = prefill_flops(wp)
+        tp = time_steps(lambda: run_prefill(dp, lazy=True), n, 3, flush)
+        tp0 = time_steps(lambda: run_prefill(dp, lazy=False), n, 3, flush)
+        tfl = fl / statistics.median(tp) / 1e12
+        out["prefill"] = {"workload": "llama8b_prefill", "tflops": tfl, "frac_of_burst": tfl / tf_burst,
+                          "frac_of_sustained": tfl / tf_sust, "gflop_per_step": fl / 1e9,
+                          "ms_median": 1e3 * statistics.median(tp),
+                          "lazy_overhead_pct": 100.0 * (statistics.median(tp) / statistics.median(tp0) - 1.0)}
+    except L.LazyAttnError as e:
+        out["prefill"] = {"unavailable": str(e)}
+    return out
+
+
+if __name__ == "__main__":
+    sys.exit(main())

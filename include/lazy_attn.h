@@ -1,0 +1,216 @@
+/*
+ * lazy_attn.h -- C ABI of a LazyAttention library for one NVIDIA GB300 (sm_103a).
+ *
+ * LazyAttention (technical summary "Resumo Técnico: LazyAttention", gist.science,
+ * paper 2606.04302) keeps the KV cache position-agnostic: each cached document's
+ * K rows are stored once, rotated at the document's own local positions
+ * 0..len-1, V unrotated, in 16-token physical blocks ("KV Cache, Flash Attention
+ * & Otimização de Inferência", section "PagedAttention"). Position is applied on
+ * the fly inside the attention kernel ("Metodologia: Codificação Posicional
+ * Diferida"): RoPE scores depend only on the relative offset,
+ * <R_m q, R_p k> = <R_{m-p} q, k> ("Equivalência Matemática").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Memory: every tensor is allocated and owned by the caller. Pointers named
+ *    `*_host` are host memory; every other tensor pointer is device memory of
+ *    the current CUDA device. The library allocates no device memory. Its only
+ *    global state is one status word per device (see lazy_attn_device_status).
+ *  - Asynchrony: compute calls only enqueue kernels on `stream` and return; they
+ *    are re-entrant.
+ *  - Errors: argument and layout errors that can be seen on the host are
+ *    returned synchronously, and nothing is launched. A failed launch returns
+ *    LAZY_ERR_CUDA. Conditions that are only visible on the device (a block id
+ *    outside the pool, a position outside the rotation table, a pipeline wait
+ *    that timed out, a layout error found by the device packer) never trap:
+ *    the kernel skips the offending access, sets a bit in the device status
+ *    word and returns. Outputs are then unspecified.
+ *  - Numerics: dtype LAZY_F32 computes in fp32; LAZY_BF16 multiplies bf16
+ *    operands on the tensor cores with fp32 accumulation and fp32 softmax.
+ *
+ * Layout (one layer)
+ * ------------------
+ *  k_pool, v_pool  [num_pool_blocks][num_kv_heads][16][head_dim], dtype. One
+ *                  (block, head) is 16*head_dim contiguous elements.
+ *  block_words     [num_seqs][max_blocks_per_seq] uint32, one word per logical
+ *                  block b of a sequence ("Implementação Técnica", Decoding:
+ *                  block ID and offset packed in one register):
+ *                      word = ((uint32)off << id_bits) | phys_id
+ *                  phys_id = physical block index (low id_bits bits);
+ *                  off = 16*b - p as a signed (32-id_bits)-bit two's complement
+ *                  field, where p is the global start position of the document
+ *                  that block b belongs to. The kernel recovers p = 16*b - off.
+ *                  Storing the block-relative form keeps both fields in 32 bits
+ *                  for pools of up to 2^id_bits blocks and contexts of 2^17+
+ *                  tokens.
+ *  seq_lens        [num_seqs] int32. A sequence spans nb = ceil(seq_lens/16)
+ *                  logical blocks. Every document starts a fresh logical block,
+ *                  so a document whose length is not a multiple of 16 leaves
+ *                  unused slots at the end of its last block. Valid slots of
+ *                  block b: seq_lens - 16*(nb-1) if b == nb-1; else
+ *                  ((p_{b+1} - p_b - 1) & 15) + 1 if p_{b+1} != p_b; else 16.
+ *                  Documents of a sequence are contiguous in position
+ *                  (p_next = p + used length) and each is used from its first
+ *                  token (a prefix is allowed).
+ *  RoPE            rotate-half pairs (i, i + head_dim/2), frequencies
+ *                  w_i = rope_theta^(-2i/head_dim).
+ */
+#ifndef LAZY_ATTN_H_
+#define LAZY_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *lazy_stream_t; /* same type as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  LAZY_OK = 0,
+  LAZY_ERR_INVALID_ARG = 1, /* null pointer, bad size or head count */
+  LAZY_ERR_UNSUPPORTED = 2, /* a shape or dtype this build has no kernel for */
+  LAZY_ERR_WORKSPACE = 3,   /* workspace or table buffer too small */
+  LAZY_ERR_LAYOUT = 4,      /* documents/blocks do not form a valid block table */
+  LAZY_ERR_CUDA = 5,        /* a CUDA call or launch failed */
+  LAZY_ERR_DEVICE = 6       /* the device status word reported a fault */
+} lazy_status;
+
+typedef enum { LAZY_F32 = 0, LAZY_BF16 = 1 } lazy_dtype;
+
+/* Bits of the per-device status word. */
+#define LAZY_DEV_BAD_BLOCK_ID 0x1u /* a word's phys_id >= num_pool_blocks (block skipped) */
+#define LAZY_DEV_POS_RANGE 0x2u    /* |rotation offset| >= 2^20 (rotation clamped) */
+#define LAZY_DEV_TIMEOUT 0x4u      /* a pipeline wait gave up after its limit */
+#define LAZY_DEV_LAYOUT 0x8u       /* the device packer met an invalid layout */
+#define LAZY_DEV_BAD_LEN 0x10u     /* seq_lens < 0 or > 16*max_blocks_per_seq (clamped) */
+
+/* Largest |offset| the rotation table covers (positions and offsets). */
+#define LAZY_MAX_ROPE_OFFSET (1 << 20)
+
+typedef struct {
+  int32_t num_seqs;           /* B >= 0 */
+  int32_t num_q_heads;        /* Hq; Hq % Hkv == 0; q-head h reads KV head h / (Hq/Hkv) */
+  int32_t num_kv_heads;       /* Hkv >= 1 */
+  int32_t head_dim;           /* d: 64 or 128 */
+  int32_t block_size;         /* must be 16 */
+  int32_t num_pool_blocks;    /* rows of k_pool / v_pool, < 2^id_bits */
+  int32_t max_blocks_per_seq; /* row stride of block_words */
+  int32_t id_bits;            /* 8..24; 0 selects the default 18 */
+  int32_t dtype;              /* lazy_dtype of q, pools and out */
+  int32_t lazy;               /* 1: rotate on the fly (LazyAttention). 0: control -- the pool
+                                 already holds absolute-position K, no per-document rotation */
+  double rope_theta;          /* 1e4, 5e5, ... */
+  float sm_scale;             /* softmax scale; 0 selects 1/sqrt(head_dim) */
+  int32_t num_splits;         /* decode split-K factor; 0 = choose from the shapes and SM count */
+} lazy_attn_params;
+
+/* Human-readable name of a lazy_status value. Never NULL. */
+const char *lazy_attn_status_string(int status);
+
+/* ---------------------------------------------------------------- rotation table
+ * cos/sin of n*w_i for the offsets the kernels need, computed once per
+ * (head_dim, rope_theta) in fp64 on the device and stored as fp32 pairs:
+ * table[0][a][i] = (cos, sin)(a*w_i), table[1][b][i] = (cos, sin)(1024*b*w_i),
+ * a, b in [0, 1024). The kernels combine the two levels with the angle-sum
+ * identity, which keeps every angle up to 2^20 exact to a few fp32 ulps.
+ * Layout: float2 [2][1024][head_dim/2]. Caller-owned device memory of at least
+ * lazy_attn_rope_table_bytes(p) bytes; read-only to every other call. */
+size_t lazy_attn_rope_table_bytes(const lazy_attn_params *p);
+int lazy_attn_rope_table_init(const lazy_attn_params *p, void *table, size_t table_bytes,
+                              lazy_stream_t stream);
+
+/* ---------------------------------------------------------------- block-word packer
+ * Builds block_words and seq_lens from per-sequence document lists (CSR):
+ *   seg_indptr [B+1]; segment k of sequence s (seg_indptr[s] <= k < seg_indptr[s+1])
+ *   uses the first seg_len[k] >= 1 tokens of document seg_doc[k];
+ *   seq_pos0 [B] (may be NULL = all 0): global position of the sequence's first
+ *   token; segment k starts at p_k = seq_pos0[s] + sum of earlier seg_len;
+ *   doc_block_indptr [num_docs+1], doc_blocks: physical block ids of each
+ *   document in token order.
+ * Words past a sequence's last block are written as 0.
+ *
+ * Host form: every array is host memory; validates and packs on the host. Returns
+ * LAZY_ERR_LAYOUT on a segment longer than its document, a block id outside the
+ * pool or id field, an offset that does not fit, or more than max_blocks_per_seq
+ * blocks in a sequence. */
+int lazy_attn_pack_block_words_host(const lazy_attn_params *p, int32_t num_docs, const int32_t *seg_indptr_host,
+                                    const int32_t *seg_doc_host, const int32_t *seg_len_host,
+                                    const int32_t *seq_pos0_host, const int32_t *doc_block_indptr_host,
+                                    const int32_t *doc_blocks_host, uint32_t *block_words_host,
+                                    int32_t *seq_lens_host);
+
+/* Device form: every array is device memory (seq_pos0 may be NULL); one warp per
+ * sequence packs on the GPU. Layout errors set LAZY_DEV_LAYOUT in the status word
+ * and write seq_lens[s] = 0 for the offending sequence. Same output bits as the
+ * host form. */
+int lazy_attn_pack_block_words(const lazy_attn_params *p, int32_t num_docs, const int32_t *seg_indptr,
+                               const int32_t *seg_doc, const int32_t *seg_len, const int32_t *seq_pos0,
+                               const int32_t *doc_block_indptr, const int32_t *doc_blocks,
+                               uint32_t *block_words, int32_t *seq_lens, lazy_stream_t stream);
+
+/* ---------------------------------------------------------------- decode
+ * One query per sequence ("Implementação Técnica", item 2, Decoding: query tile
+ * M = 1; the query is re-rotated only when the relative offset changes, i.e. at
+ * a new document; memory traffic is K and V only).
+ *   q       [B][Hq][d] dtype, UNROTATED
+ *   q_pos   [B] int32 absolute position m of each query; every cached key must
+ *           sit at a position <= m (all keys in the table are attended to)
+ *   out     [B][Hq][d] dtype: softmax(<R_{m-p} q, K_stored> * sm_scale) V
+ *           (zero for a sequence with seq_lens == 0)
+ *   workspace: device scratch for split-K partials, at least
+ *           lazy_attn_decode_workspace_bytes(p) bytes (0 when one split suffices),
+ *           256-byte aligned; not read before it is written.
+ * lazy == 0 (control): q is rotated once by R_m and the pool is read as already
+ * holding absolute-position keys. */
+size_t lazy_attn_decode_workspace_bytes(const lazy_attn_params *p);
+int lazy_attn_decode(const lazy_attn_params *p, const void *q, const void *k_pool, const void *v_pool,
+                     const uint32_t *block_words, const int32_t *seq_lens, const int32_t *q_pos,
+                     const void *rope_table, void *out, void *workspace, size_t workspace_bytes,
+                     lazy_stream_t stream);
+
+/* ---------------------------------------------------------------- prefill
+ * Varlen query chunks ("Implementação Técnica", item 1, Prefilling): chunk s
+ * has C_s = cu_seqlens_q[s+1] - cu_seqlens_q[s] query rows at absolute
+ * positions q_start[s] + i. Its own K/V must already be in the pool as the
+ * LAST document of the sequence (C_s tokens, p = q_start[s]); query row i
+ * attends to every key of the earlier documents and to chunk keys j <= i.
+ * Q is rotated once by R_m per row; each 16-row K block is rotated once, by
+ * R_p of its document (one relative rotation per tile, no unrotate pass).
+ *   q            [total_q][Hq][d] bf16, UNROTATED
+ *   cu_seqlens_q [B+1] int32 device; q_start [B] int32 device
+ *   max_q_len    >= every C_s (sizes the grid); total_q = cu_seqlens_q[B]
+ *   out          [total_q][Hq][d] bf16
+ * Only LAZY_BF16 is supported. */
+size_t lazy_attn_prefill_workspace_bytes(const lazy_attn_params *p, int32_t total_q);
+int lazy_attn_prefill(const lazy_attn_params *p, const void *q, const int32_t *cu_seqlens_q,
+                      const int32_t *q_start, int32_t total_q, int32_t max_q_len, const void *k_pool,
+                      const void *v_pool, const uint32_t *block_words, const int32_t *seq_lens,
+                      const void *rope_table, void *out, void *workspace, size_t workspace_bytes,
+                      lazy_stream_t stream);
+
+/* ---------------------------------------------------------------- test support
+ * Copies every logical K/V slot of every sequence through the decode kernel's
+ * own load path (word decode, TMA block loads, hole rule) into dense buffers:
+ *   k_out, v_out [B][Hkv][16*max_blocks_per_seq][d] dtype; slot t of logical
+ *   block b lands at row 16*b + t; slots that are not valid (holes, past
+ *   seq_lens) are written as 0.
+ *   pos_out [B][16*max_blocks_per_seq] int32: the absolute position of each
+ *   valid slot's token, -1 for invalid slots (may be NULL). */
+int lazy_attn_debug_gather(const lazy_attn_params *p, const void *k_pool, const void *v_pool,
+                           const uint32_t *block_words, const int32_t *seq_lens, void *k_out, void *v_out,
+                           int32_t *pos_out, lazy_stream_t stream);
+
+/* Reads (and, if clear != 0, zeroes) the current device's status word. Waits for
+ * all work on the device first. Returns LAZY_OK, or LAZY_ERR_CUDA. */
+int lazy_attn_device_status(uint32_t *flags_out, int clear);
+
+/* Number of kernel launches the library has issued in this process (all devices);
+ * lets a caller count GPU work done inside a timed region. */
+uint64_t lazy_attn_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LAZY_ATTN_H_ */

@@ -1,0 +1,417 @@
+// api.cu -- the C ABI declared in include/lazy_attn.h: argument checks, host-side
+// block-word packing, tensor-map encoding, split planning and kernel launches.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+// The per-device status word (one copy per device the library is loaded on).
+__device__ unsigned int g_lazy_status = 0u;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kDefaultIdBits = 18;
+constexpr int kDefaultSmCount = 152;  // used only when no device is visible (size queries)
+
+std::atomic<uint64_t> g_launches{0};
+std::mutex g_mu;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+struct Checked {
+  int id_bits = kDefaultIdBits;
+  int G = 1;
+};
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+unsigned int* status_ptr() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_lazy_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+int sm_count() {
+  const int dev = current_device();
+  if (dev < 0) return kDefaultSmCount;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sm_count[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return kDefaultSmCount;
+    }
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+bool encoder_ready() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// 2-D bf16 view [rows][d] with 16-row x 64-column boxes, 128-byte swizzle.
+bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, int d, uint32_t box_rows) {
+  if (!encoder_ready()) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 view of q [total_q][Hq][d]: boxes of 64 columns x 1 head x box_rows rows.
+bool encode_q_map(CUtensorMap* m, const void* base, uint64_t total_q, int hq, int d, uint32_t box_rows) {
+  if (!encoder_ready()) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hq, (cuuint64_t)total_q};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)hq * d * 2};
+  cuuint32_t box[3] = {64, 1, box_rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int check_params(const lazy_attn_params* p, Checked* c) {
+  if (!p) return LAZY_ERR_INVALID_ARG;
+  if (p->num_seqs < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 || p->num_q_heads % p->num_kv_heads != 0)
+    return LAZY_ERR_INVALID_ARG;
+  if (p->num_pool_blocks < 0 || p->max_blocks_per_seq < 0 || p->max_blocks_per_seq > (1 << 26))
+    return LAZY_ERR_INVALID_ARG;
+  if (p->block_size != lazy::kBlock) return LAZY_ERR_UNSUPPORTED;
+  if (p->head_dim != 64 && p->head_dim != 128) return LAZY_ERR_UNSUPPORTED;
+  if (p->dtype != LAZY_F32 && p->dtype != LAZY_BF16) return LAZY_ERR_UNSUPPORTED;
+  if (p->lazy != 0 && p->lazy != 1) return LAZY_ERR_INVALID_ARG;
+  if (!(p->rope_theta > 0.0) || !std::isfinite(p->rope_theta)) return LAZY_ERR_INVALID_ARG;
+  if (!(p->sm_scale >= 0.f) || !std::isfinite(p->sm_scale)) return LAZY_ERR_INVALID_ARG;
+  if (p->num_splits < 0) return LAZY_ERR_INVALID_ARG;
+  c->id_bits = p->id_bits ? p->id_bits : kDefaultIdBits;
+  if (c->id_bits < 8 || c->id_bits > 24) return LAZY_ERR_INVALID_ARG;
+  if ((int64_t)p->num_pool_blocks > ((int64_t)1 << c->id_bits)) return LAZY_ERR_INVALID_ARG;
+  c->G = p->num_q_heads / p->num_kv_heads;
+  return LAZY_OK;
+}
+
+float scale_log2(const lazy_attn_params* p) {
+  const double s = p->sm_scale > 0.f ? (double)p->sm_scale : 1.0 / std::sqrt((double)p->head_dim);
+  return (float)(s * 1.4426950408889634);  // log2(e)
+}
+
+// Split-K plan: about four waves of two CTAs per SM, at least 16 blocks per split.
+void plan_splits(const lazy_attn_params* p, int* splits, int* bps) {
+  const int mb = p->max_blocks_per_seq > 0 ? p->max_blocks_per_seq : 1;
+  int s = p->num_splits;
+  if (s <= 0) {
+    const int64_t units = (int64_t)(p->num_seqs > 0 ? p->num_seqs : 1) * p->num_kv_heads;
+    const int64_t target = (int64_t)sm_count() * 2 * 4;
+    s = (int)((target + units - 1) / units);
+    const int max_s = mb / 16 > 1 ? mb / 16 : 1;
+    s = s < max_s ? s : max_s;
+  }
+  s = s < 1 ? 1 : (s > mb ? mb : s);
+  *bps = (mb + s - 1) / s;
+  *splits = (mb + *bps - 1) / *bps;
+}
+
+size_t decode_ws_bytes(const lazy_attn_params* p, int splits) {
+  if (splits <= 1) return 0;
+  const size_t parts = (size_t)p->num_seqs * p->num_q_heads * splits;
+  return parts * p->head_dim * sizeof(float) + parts * 2 * sizeof(float);
+}
+
+int launched(cudaError_t e) {
+  if (e != cudaSuccess) return LAZY_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return LAZY_OK;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* lazy_attn_status_string(int status) {
+  switch (status) {
+    case LAZY_OK: return "LAZY_OK";
+    case LAZY_ERR_INVALID_ARG: return "LAZY_ERR_INVALID_ARG: invalid argument";
+    case LAZY_ERR_UNSUPPORTED: return "LAZY_ERR_UNSUPPORTED: shape or dtype not supported";
+    case LAZY_ERR_WORKSPACE: return "LAZY_ERR_WORKSPACE: workspace or table too small or misaligned";
+    case LAZY_ERR_LAYOUT: return "LAZY_ERR_LAYOUT: documents and blocks do not form a valid block table";
+    case LAZY_ERR_CUDA: return "LAZY_ERR_CUDA: a CUDA call or launch failed";
+    case LAZY_ERR_DEVICE: return "LAZY_ERR_DEVICE: the device status word reported a fault";
+    default: return "unknown lazy_attn status";
+  }
+}
+
+uint64_t lazy_attn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t lazy_attn_rope_table_bytes(const lazy_attn_params* p) {
+  Checked c;
+  if (check_params(p, &c) != LAZY_OK) return 0;
+  return (size_t)2 * lazy::kTableEntries * (p->head_dim / 2) * sizeof(float2);
+}
+
+int lazy_attn_rope_table_init(const lazy_attn_params* p, void* table, size_t table_bytes, lazy_stream_t stream) {
+  Checked c;
+  int rc = check_params(p, &c);
+  if (rc != LAZY_OK) return rc;
+  if (!table) return LAZY_ERR_INVALID_ARG;
+  if (table_bytes < lazy_attn_rope_table_bytes(p) || !aligned16(table)) return LAZY_ERR_WORKSPACE;
+  return launched(lazy::launch_rope_table(static_cast<float2*>(table), p->head_dim, p->rope_theta,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int lazy_attn_pack_block_words_host(const lazy_attn_params* p, int32_t num_docs, const int32_t* seg_indptr,
+                                    const int32_t* seg_doc, const int32_t* seg_len, const int32_t* seq_pos0,
+                                    const int32_t* doc_block_indptr, const int32_t* doc_blocks,
+                                    uint32_t* block_words, int32_t* seq_lens) {
+  Checked c;
+  int rc = check_params(p, &c);
+  if (rc != LAZY_OK) return rc;
+  const int B = p->num_seqs, MB = p->max_blocks_per_seq;
+  if (num_docs < 0) return LAZY_ERR_INVALID_ARG;
+  if (B > 0 && (!seg_indptr || !block_words || !seq_lens)) return LAZY_ERR_INVALID_ARG;
+  if (B > 0 && seg_indptr[B] > seg_indptr[0] && (!seg_doc || !seg_len || !doc_block_indptr || !doc_blocks))
+    return LAZY_ERR_INVALID_ARG;
+  const uint32_t id_mask = (1u << c.id_bits) - 1u;
+  const int64_t off_lo = -((int64_t)1 << (31 - c.id_bits)), off_hi = ((int64_t)1 << (31 - c.id_bits)) - 1;
+  for (int s = 0; s < B; ++s) {
+    uint32_t* wrow = block_words + (size_t)s * MB;
+    const int k0 = seg_indptr[s], k1 = seg_indptr[s + 1];
+    if (k1 < k0) return LAZY_ERR_LAYOUT;
+    int64_t blk = 0, pos = seq_pos0 ? seq_pos0[s] : 0;
+    int last_len = 0;
+    for (int k = k0; k < k1; ++k) {
+      const int doc = seg_doc[k], len = seg_len[k];
+      if (doc < 0 || doc >= num_docs || len < 1) return LAZY_ERR_LAYOUT;
+      const int dblk = doc_block_indptr[doc + 1] - doc_block_indptr[doc];
+      if ((int64_t)len > (int64_t)lazy::kBlock * dblk) return LAZY_ERR_LAYOUT;
+      const int nbk = (len + lazy::kBlock - 1) / lazy::kBlock;
+      if (blk + nbk > MB) return LAZY_ERR_LAYOUT;
+      for (int q = 0; q < nbk; ++q) {
+        const int phys = doc_blocks[doc_block_indptr[doc] + q];
+        const int64_t off = (int64_t)lazy::kBlock * (blk + q) - pos;
+        if (phys < 0 || phys >= p->num_pool_blocks || (uint32_t)phys > id_mask || off < off_lo || off > off_hi)
+          return LAZY_ERR_LAYOUT;
+        wrow[blk + q] = ((uint32_t)(int32_t)off << c.id_bits) | ((uint32_t)phys & id_mask);
+      }
+      blk += nbk;
+      pos += len;
+      last_len = len;
+    }
+    for (int64_t b = blk; b < MB; ++b) wrow[b] = 0u;
+    const int last_blocks = (last_len + lazy::kBlock - 1) / lazy::kBlock;
+    seq_lens[s] = blk == 0 ? 0 : (int32_t)(lazy::kBlock * blk - (lazy::kBlock * last_blocks - last_len));
+  }
+  return LAZY_OK;
+}
+
+int lazy_attn_pack_block_words(const lazy_attn_params* p, int32_t num_docs, const int32_t* seg_indptr,
+                               const int32_t* seg_doc, const int32_t* seg_len, const int32_t* seq_pos0,
+                               const int32_t* doc_block_indptr, const int32_t* doc_blocks, uint32_t* block_words,
+                               int32_t* seq_lens, lazy_stream_t stream) {
+  Checked c;
+  int rc = check_params(p, &c);
+  if (rc != LAZY_OK) return rc;
+  if (num_docs < 0) return LAZY_ERR_INVALID_ARG;
+  if (p->num_seqs == 0) return LAZY_OK;
+  if (!seg_indptr || !seg_doc || !seg_len || !doc_block_indptr || !doc_blocks || !block_words || !seq_lens)
+    return LAZY_ERR_INVALID_ARG;
+  unsigned int* st = status_ptr();
+  if (!st) return LAZY_ERR_CUDA;
+  lazy::PackArgs a{seg_indptr, seg_doc, seg_len, seq_pos0, doc_block_indptr, doc_blocks, block_words, seq_lens, st,
+                   p->num_seqs, num_docs, p->max_blocks_per_seq, c.id_bits, p->num_pool_blocks};
+  return launched(lazy::launch_pack(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t lazy_attn_decode_workspace_bytes(const lazy_attn_params* p) {
+  Checked c;
+  if (check_params(p, &c) != LAZY_OK) return 0;
+  int splits, bps;
+  plan_splits(p, &splits, &bps);
+  return decode_ws_bytes(p, splits);
+}
+
+int lazy_attn_decode(const lazy_attn_params* p, const void* q, const void* k_pool, const void* v_pool,
+                     const uint32_t* block_words, const int32_t* seq_lens, const int32_t* q_pos,
+                     const void* rope_table, void* out, void* workspace, size_t workspace_bytes,
+                     lazy_stream_t stream) {
+  Checked c;
+  int rc = check_params(p, &c);
+  if (rc != LAZY_OK) return rc;
+  if (p->num_seqs == 0) return LAZY_OK;
+  if (!q || !k_pool || !v_pool || !block_words || !seq_lens || !q_pos || !rope_table || !out)
+    return LAZY_ERR_INVALID_ARG;
+  if (p->num_pool_blocks == 0 || p->max_blocks_per_seq == 0) return LAZY_ERR_INVALID_ARG;
+  if (p->dtype == LAZY_F32 && c.G > 32) return LAZY_ERR_UNSUPPORTED;
+  if (p->dtype == LAZY_BF16 && c.G > 64) return LAZY_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) || !aligned16(rope_table))
+    return LAZY_ERR_INVALID_ARG;
+  int splits, bps;
+  plan_splits(p, &splits, &bps);
+  const size_t need = decode_ws_bytes(p, splits);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return LAZY_ERR_WORKSPACE;
+  unsigned int* st = status_ptr();
+  if (!st) return LAZY_ERR_CUDA;
+  const size_t parts = (size_t)p->num_seqs * p->num_q_heads * splits;
+  lazy::DecodeArgs a{};
+  a.q = q;
+  a.words = block_words;
+  a.seq_lens = seq_lens;
+  a.q_pos = q_pos;
+  a.rope = static_cast<const float2*>(rope_table);
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.out = out;
+  a.ws_o = need ? static_cast<float*>(workspace) : nullptr;
+  a.ws_ml = need ? static_cast<float*>(workspace) + parts * p->head_dim : nullptr;
+  a.status = st;
+  a.B = p->num_seqs;
+  a.Hq = p->num_q_heads;
+  a.Hkv = p->num_kv_heads;
+  a.G = c.G;
+  a.D = p->head_dim;
+  a.max_blocks = p->max_blocks_per_seq;
+  a.id_bits = c.id_bits;
+  a.num_pool_blocks = p->num_pool_blocks;
+  a.splits = splits;
+  a.bps = bps;
+  a.scale_log2 = scale_log2(p);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (p->dtype == LAZY_F32) {
+    rc = launched(lazy::launch_decode_f32(a, p->lazy != 0, cs));
+  } else {
+    CUtensorMap kmap, vmap;
+    const uint64_t rows = (uint64_t)p->num_pool_blocks * p->num_kv_heads * lazy::kBlock;
+    if (!encode_rows_map(&kmap, k_pool, rows, p->head_dim, lazy::kBlock) ||
+        !encode_rows_map(&vmap, v_pool, rows, p->head_dim, lazy::kBlock))
+      return LAZY_ERR_CUDA;
+    rc = launched(lazy::launch_decode_bf16(a, p->lazy != 0, kmap, vmap, cs));
+  }
+  if (rc != LAZY_OK || splits == 1) return rc;
+  return launched(lazy::launch_combine(a, p->dtype == LAZY_BF16, cs));
+}
+
+size_t lazy_attn_prefill_workspace_bytes(const lazy_attn_params* p, int32_t total_q) {
+  (void)p;
+  (void)total_q;
+  return 0;
+}
+
+int lazy_attn_prefill(const lazy_attn_params* p, const void* q, const int32_t* cu_seqlens_q, const int32_t* q_start,
+                      int32_t total_q, int32_t max_q_len, const void* k_pool, const void* v_pool,
+                      const uint32_t* block_words, const int32_t* seq_lens, const void* rope_table, void* out,
+                      void* workspace, size_t workspace_bytes, lazy_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  Checked c;
+  int rc = check_params(p, &c);
+  if (rc != LAZY_OK) return rc;
+  if (p->dtype != LAZY_BF16 || p->head_dim != 128) return LAZY_ERR_UNSUPPORTED;
+  if (total_q < 0 || max_q_len < 0) return LAZY_ERR_INVALID_ARG;
+  if (p->num_seqs == 0 || total_q == 0 || max_q_len == 0) return LAZY_OK;
+  if (!q || !cu_seqlens_q || !q_start || !k_pool || !v_pool || !block_words || !seq_lens || !rope_table || !out)
+    return LAZY_ERR_INVALID_ARG;
+  if (p->num_pool_blocks == 0 || p->max_blocks_per_seq == 0) return LAZY_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) || !aligned16(rope_table))
+    return LAZY_ERR_INVALID_ARG;
+  unsigned int* st = status_ptr();
+  if (!st) return LAZY_ERR_CUDA;
+  CUtensorMap qmap, kmap, vmap;
+  const uint64_t rows = (uint64_t)p->num_pool_blocks * p->num_kv_heads * lazy::kBlock;
+  if (!encode_q_map(&qmap, q, (uint64_t)total_q, p->num_q_heads, p->head_dim, 128) ||
+      !encode_rows_map(&kmap, k_pool, rows, p->head_dim, lazy::kBlock) ||
+      !encode_rows_map(&vmap, v_pool, rows, p->head_dim, lazy::kBlock))
+    return LAZY_ERR_CUDA;
+  lazy::PrefillArgs a{};
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.q_start = q_start;
+  a.words = block_words;
+  a.seq_lens = seq_lens;
+  a.rope = static_cast<const float2*>(rope_table);
+  a.out = out;
+  a.status = st;
+  a.B = p->num_seqs;
+  a.Hq = p->num_q_heads;
+  a.Hkv = p->num_kv_heads;
+  a.G = c.G;
+  a.D = p->head_dim;
+  a.total_q = total_q;
+  a.max_q_len = max_q_len;
+  a.max_blocks = p->max_blocks_per_seq;
+  a.id_bits = c.id_bits;
+  a.num_pool_blocks = p->num_pool_blocks;
+  a.scale_log2 = scale_log2(p);
+  cudaError_t e = lazy::launch_prefill(a, p->lazy != 0, qmap, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return LAZY_ERR_UNSUPPORTED;
+  return launched(e);
+}
+
+int lazy_attn_debug_gather(const lazy_attn_params* p, const void* k_pool, const void* v_pool,
+                           const uint32_t* block_words, const int32_t* seq_lens, void* k_out, void* v_out,
+                           int32_t* pos_out, lazy_stream_t stream) {
+  Checked c;
+  int rc = check_params(p, &c);
+  if (rc != LAZY_OK) return rc;
+  if (p->num_seqs == 0) return LAZY_OK;
+  if (!k_pool || !v_pool || !block_words || !seq_lens || !k_out || !v_out) return LAZY_ERR_INVALID_ARG;
+  if (p->num_pool_blocks == 0 || p->max_blocks_per_seq == 0) return LAZY_ERR_INVALID_ARG;
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_out) || !aligned16(v_out)) return LAZY_ERR_INVALID_ARG;
+  unsigned int* st = status_ptr();
+  if (!st) return LAZY_ERR_CUDA;
+  lazy::GatherArgs a{block_words, seq_lens, k_pool, v_pool, k_out, v_out, pos_out, st,
+                     p->num_seqs, p->num_kv_heads, p->head_dim, p->max_blocks_per_seq, c.id_bits,
+                     p->num_pool_blocks};
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (p->dtype == LAZY_F32) return launched(lazy::launch_gather_f32(a, cs));
+  CUtensorMap kmap, vmap;
+  const uint64_t rows = (uint64_t)p->num_pool_blocks * p->num_kv_heads * lazy::kBlock;
+  if (!encode_rows_map(&kmap, k_pool, rows, p->head_dim, lazy::kBlock) ||
+      !encode_rows_map(&vmap, v_pool, rows, p->head_dim, lazy::kBlock))
+    return LAZY_ERR_CUDA;
+  return launched(lazy::launch_gather_bf16(a, kmap, vmap, cs));
+}
+
+int lazy_attn_device_status(uint32_t* flags_out, int clear) {
+  if (!flags_out) return LAZY_ERR_INVALID_ARG;
+  if (!status_ptr()) return LAZY_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return LAZY_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_lazy_status, sizeof v) != cudaSuccess) return LAZY_ERR_CUDA;
+  if (clear) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_lazy_status, &zero, sizeof zero) != cudaSuccess) return LAZY_ERR_CUDA;
+  }
+  *flags_out = v;
+  return LAZY_OK;
+}
+
+}  // extern "C"

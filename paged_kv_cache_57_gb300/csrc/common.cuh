@@ -1,0 +1,186 @@
+// common.cuh -- device helpers shared by the LazyAttention kernels (sm_103a).
+//
+// Everything here is plain inline PTX or CUDA intrinsics: mbarrier pipelines with
+// bounded waits, TMA tile loads, ldmatrix / mma.sync fragments, the packed block
+// word, and the rotation table lookup.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/lazy_attn.h"
+
+namespace lazy {
+
+constexpr int kBlock = 16;             // tokens per physical block
+constexpr int kTableEntries = 1024;    // entries per rotation-table level
+constexpr int kTableShift = 10;        // log2(kTableEntries)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: any pipeline wait longer than this is a fault
+
+// ------------------------------------------------------------------ status word
+
+__device__ __forceinline__ void raise_status(unsigned int* status, unsigned int bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// ------------------------------------------------------------------ addresses / timers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ------------------------------------------------------------------ mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async proxy (TMA / tensor core).
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete. Gives up after
+// kWaitLimitNs, sets LAZY_DEV_TIMEOUT and returns false: callers then skip the
+// rest of their work, so the kernel always terminates.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      raise_status(status, LAZY_DEV_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------ TMA
+
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 2-D tiled load of one box into shared memory; completion is signalled on `bar`
+// as transaction bytes. x is the innermost (contiguous) coordinate in elements.
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                            int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a box written by TMA
+// with CU_TENSOR_MAP_SWIZZLE_128B (rows of 128 bytes, box base 1024-byte aligned).
+__device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) { return (r << 7) | (((c ^ r) & 7u) << 4); }
+
+// ------------------------------------------------------------------ warp-level MMA
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ------------------------------------------------------------------ block words
+
+struct BlockInfo {
+  int phys;    // physical block id
+  int p;       // global start position of the block's document
+};
+
+__device__ __forceinline__ BlockInfo decode_word(uint32_t w, int b, int id_bits) {
+  BlockInfo bi;
+  bi.phys = static_cast<int>(w & ((1u << id_bits) - 1u));
+  const int off = static_cast<int>(w) >> id_bits;  // arithmetic shift: signed field
+  bi.p = kBlock * b - off;
+  return bi;
+}
+
+// Valid slots of logical block b (see the layout notes in lazy_attn.h).
+__device__ __forceinline__ int block_valid(int b, int nb, int seq_len, int p_b, int p_next) {
+  if (b == nb - 1) return seq_len - kBlock * (nb - 1);
+  if (p_next != p_b) return ((p_next - p_b - 1) & (kBlock - 1)) + 1;
+  return kBlock;
+}
+
+// ------------------------------------------------------------------ rotation table
+
+// (cos, sin)(delta * w_i) from the two-level table: delta = 1024*hi + lo, and
+// the angle-sum identity combines the two fp64-exact entries in fp32.
+__device__ __forceinline__ float2 rope_cs(const float2* __restrict__ table, int half, int delta, int i,
+                                          unsigned int* status) {
+  int ad = delta < 0 ? -delta : delta;
+  if (ad >= LAZY_MAX_ROPE_OFFSET) {
+    raise_status(status, LAZY_DEV_POS_RANGE);
+    ad = LAZY_MAX_ROPE_OFFSET - 1;
+  }
+  const float2 lo = __ldg(&table[(ad & (kTableEntries - 1)) * half + i]);
+  const float2 hi = __ldg(&table[(kTableEntries + (ad >> kTableShift)) * half + i]);
+  const float c = fmaf(lo.x, hi.x, -lo.y * hi.y);
+  const float s = fmaf(lo.y, hi.x, lo.x * hi.y);
+  return make_float2(c, delta < 0 ? -s : s);
+}
+
+}  // namespace lazy

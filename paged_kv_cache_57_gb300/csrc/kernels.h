@@ -1,0 +1,80 @@
+// kernels.h -- internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lazy {
+
+struct DecodeArgs {
+  const void* q;             // [B][Hq][D] unrotated
+  const uint32_t* words;     // [B][max_blocks]
+  const int32_t* seq_lens;   // [B]
+  const int32_t* q_pos;      // [B]
+  const float2* rope;        // rotation table
+  const void* k_pool;        // [NB][Hkv][16][D] (plain-load kernels)
+  const void* v_pool;
+  void* out;                 // [B][Hq][D]
+  float* ws_o;               // [B][Hq][splits][D]
+  float* ws_ml;              // [B][Hq][splits][2]  (running max in log2 units, denominator)
+  unsigned int* status;      // device status word
+  int B, Hq, Hkv, G, D, max_blocks, id_bits, num_pool_blocks;
+  int splits, bps;           // split-K factor and logical blocks per split
+  float scale_log2;          // softmax scale * log2(e)
+};
+
+struct GatherArgs {
+  const uint32_t* words;
+  const int32_t* seq_lens;
+  const void* k_pool;
+  const void* v_pool;
+  void* k_out;               // [B][Hkv][16*max_blocks][D]
+  void* v_out;
+  int32_t* pos_out;          // [B][16*max_blocks] or null
+  unsigned int* status;
+  int B, Hkv, D, max_blocks, id_bits, num_pool_blocks;
+};
+
+struct PackArgs {
+  const int32_t* seg_indptr;
+  const int32_t* seg_doc;
+  const int32_t* seg_len;
+  const int32_t* seq_pos0;   // may be null
+  const int32_t* doc_block_indptr;
+  const int32_t* doc_blocks;
+  uint32_t* words;
+  int32_t* seq_lens;
+  unsigned int* status;
+  int B, num_docs, max_blocks, id_bits, num_pool_blocks;
+};
+
+struct PrefillArgs {
+  const int32_t* cu_seqlens_q;
+  const int32_t* q_start;
+  const uint32_t* words;
+  const int32_t* seq_lens;
+  const float2* rope;
+  void* out;                 // [total_q][Hq][D] bf16
+  unsigned int* status;
+  int B, Hq, Hkv, G, D, total_q, max_q_len, max_blocks, id_bits, num_pool_blocks;
+  float scale_log2;
+};
+
+// Every launcher returns the cudaError_t of its launch.
+cudaError_t launch_rope_table(float2* table, int head_dim, double theta, cudaStream_t st);
+cudaError_t launch_pack(const PackArgs& a, cudaStream_t st);
+cudaError_t launch_decode_f32(const DecodeArgs& a, bool lazy, cudaStream_t st);
+cudaError_t launch_decode_bf16(const DecodeArgs& a, bool lazy, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                               cudaStream_t st);
+cudaError_t launch_combine(const DecodeArgs& a, bool out_bf16, cudaStream_t st);
+cudaError_t launch_gather_bf16(const GatherArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                               cudaStream_t st);
+cudaError_t launch_gather_f32(const GatherArgs& a, cudaStream_t st);
+cudaError_t launch_prefill(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap, cudaStream_t st);
+
+// Shared-memory bytes a bf16 decode CTA needs (for occupancy-based split planning).
+int decode_bf16_smem_bytes(int D, int G);
+
+}  // namespace lazy

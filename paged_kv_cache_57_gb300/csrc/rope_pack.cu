@@ -1,0 +1,117 @@
+// rope_pack.cu -- rotation table initialisation and the device block-word packer.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace lazy {
+
+// table[0][a][i] = (cos, sin)(a * w_i), table[1][b][i] = (cos, sin)(1024 * b * w_i),
+// w_i = theta^(-2i/d), angles and sin/cos in fp64, stored as fp32.
+__global__ void rope_table_kernel(float2* table, int half, int head_dim, double theta) {
+  const int total = 2 * kTableEntries * half;
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += gridDim.x * blockDim.x) {
+    const int i = idx % half;
+    const int e = (idx / half) % kTableEntries;
+    const int level = idx / (half * kTableEntries);
+    const double w = pow(theta, -2.0 * (double)i / (double)head_dim);
+    const double n = level == 0 ? (double)e : (double)e * (double)kTableEntries;
+    double sn, cs;
+    sincos(n * w, &sn, &cs);
+    table[idx] = make_float2((float)cs, (float)sn);
+  }
+}
+
+cudaError_t launch_rope_table(float2* table, int head_dim, double theta, cudaStream_t st) {
+  const int half = head_dim / 2;
+  const int total = 2 * kTableEntries * half;
+  rope_table_kernel<<<(total + 255) / 256, 256, 0, st>>>(table, half, head_dim, theta);
+  return cudaGetLastError();
+}
+
+// One warp per sequence. Segments are taken 32 at a time: each lane checks one
+// segment, an inclusive warp scan gives every segment its first logical block
+// and start position, then the warp writes the words of those segments.
+__global__ void pack_words_kernel(const PackArgs a) {
+  const int warps_per_cta = blockDim.x >> 5;
+  const int s = blockIdx.x * warps_per_cta + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (s >= a.B) return;
+  const int k0 = a.seg_indptr[s], k1 = a.seg_indptr[s + 1];
+  const uint32_t id_mask = (1u << a.id_bits) - 1u;
+  const int off_lo = -(1 << (31 - a.id_bits)), off_hi = (1 << (31 - a.id_bits)) - 1;
+  uint32_t* wrow = a.words + (size_t)s * a.max_blocks;
+  int blk = 0;                                 // first logical block of the next chunk
+  long long pos = a.seq_pos0 ? a.seq_pos0[s] : 0;  // start position of the next chunk
+  int last_len = 0;
+  bool bad = (k1 < k0);
+  for (int kb = k0; kb < k1 && !bad; kb += 32) {
+    const int k = kb + lane;
+    const bool live = k < k1;
+    int len = 0, nbk = 0, doc = 0;
+    bool err = false;
+    if (live) {
+      doc = a.seg_doc[k];
+      len = a.seg_len[k];
+      err = doc < 0 || doc >= a.num_docs || len < 1;
+      if (!err) {
+        const int dblk = a.doc_block_indptr[doc + 1] - a.doc_block_indptr[doc];
+        err = len > kBlock * dblk;
+        nbk = (len + kBlock - 1) / kBlock;
+      }
+    }
+    // inclusive scans of blocks and tokens
+    int sb = nbk;
+    long long sp = len;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int tb = __shfl_up_sync(0xffffffffu, sb, off);
+      const long long tp = __shfl_up_sync(0xffffffffu, sp, off);
+      if (lane >= off) sb += tb, sp += tp;
+    }
+    const int my_blk = blk + sb - nbk;
+    const long long my_pos = pos + sp - len;
+    bad = __any_sync(0xffffffffu, err) || (blk + __shfl_sync(0xffffffffu, sb, 31) > a.max_blocks);
+    if (bad) break;
+    // every segment of this chunk, lanes over its blocks
+    const int nlive = min(32, k1 - kb);
+    for (int j = 0; j < nlive; ++j) {
+      const int dj = __shfl_sync(0xffffffffu, doc, j);
+      const int bj = __shfl_sync(0xffffffffu, my_blk, j);
+      const long long pj = __shfl_sync(0xffffffffu, my_pos, j);
+      const int nj = __shfl_sync(0xffffffffu, nbk, j);
+      const int* ids = a.doc_blocks + a.doc_block_indptr[dj];
+      bool e2 = false;
+      for (int q = lane; q < nj; q += 32) {
+        const int phys = ids[q];
+        const long long off = (long long)kBlock * (bj + q) - pj;
+        e2 |= phys < 0 || phys >= a.num_pool_blocks || (uint32_t)phys > id_mask || off < off_lo || off > off_hi;
+        wrow[bj + q] = ((uint32_t)(int)off << a.id_bits) | ((uint32_t)phys & id_mask);
+      }
+      bad |= __any_sync(0xffffffffu, e2);
+    }
+    last_len = __shfl_sync(0xffffffffu, len, nlive - 1);
+    blk += __shfl_sync(0xffffffffu, sb, 31);
+    pos += __shfl_sync(0xffffffffu, sp, 31);
+  }
+  if (bad) {
+    if (lane == 0) {
+      raise_status(a.status, LAZY_DEV_LAYOUT);
+      a.seq_lens[s] = 0;
+    }
+    for (int b = lane; b < a.max_blocks; b += 32) wrow[b] = 0u;
+    return;
+  }
+  for (int b = blk + lane; b < a.max_blocks; b += 32) wrow[b] = 0u;
+  if (lane == 0) {
+    const int last_blocks = (last_len + kBlock - 1) / kBlock;
+    a.seq_lens[s] = blk == 0 ? 0 : kBlock * blk - (kBlock * last_blocks - last_len);
+  }
+}
+
+cudaError_t launch_pack(const PackArgs& a, cudaStream_t st) {
+  if (a.B == 0) return cudaSuccess;
+  const int warps = 4;
+  pack_words_kernel<<<(a.B + warps - 1) / warps, 32 * warps, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace lazy

@@ -1,0 +1,243 @@
+"""Python binding of the LazyAttention C ABI (``include/lazy_attn.h``).
+
+Argument marshalling only: every function here checks shapes and dtypes of
+torch tensors, then passes raw pointers, sizes and the current CUDA stream to
+``liblazyattn.so``. All computation happens in the library's CUDA kernels (or,
+for ``pack_block_words_host``, in its C++ host code). Importing this module
+raises if the library has not been built: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "liblazyattn.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m paged_kv_cache_57_gb300.build`")
+_lib = ctypes.CDLL(LIB_PATH)
+
+LAZY_OK, LAZY_ERR_INVALID_ARG, LAZY_ERR_UNSUPPORTED, LAZY_ERR_WORKSPACE, LAZY_ERR_LAYOUT, LAZY_ERR_CUDA, \
+    LAZY_ERR_DEVICE = range(7)
+LAZY_F32, LAZY_BF16 = 0, 1
+LAZY_DEV_BAD_BLOCK_ID, LAZY_DEV_POS_RANGE, LAZY_DEV_TIMEOUT, LAZY_DEV_LAYOUT, LAZY_DEV_BAD_LEN = 1, 2, 4, 8, 16
+BLOCK = 16
+
+EXPORTED = (
+    "lazy_attn_status_string", "lazy_attn_rope_table_bytes", "lazy_attn_rope_table_init",
+    "lazy_attn_pack_block_words_host", "lazy_attn_pack_block_words", "lazy_attn_decode_workspace_bytes",
+    "lazy_attn_decode", "lazy_attn_prefill_workspace_bytes", "lazy_attn_prefill", "lazy_attn_debug_gather",
+    "lazy_attn_device_status", "lazy_attn_launch_count",
+)
+
+
+class Params(ctypes.Structure):
+    """Mirror of ``lazy_attn_params``."""
+    _fields_ = [
+        ("num_seqs", ctypes.c_int32), ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32), ("num_pool_blocks", ctypes.c_int32),
+        ("max_blocks_per_seq", ctypes.c_int32), ("id_bits", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("lazy", ctypes.c_int32), ("rope_theta", ctypes.c_double), ("sm_scale", ctypes.c_float),
+        ("num_splits", ctypes.c_int32),
+    ]
+
+
+class LazyAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+_vp, _sz, _i32, _u64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_uint64
+_P = ctypes.POINTER(Params)
+_sig = {
+    "lazy_attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "lazy_attn_rope_table_bytes": (_sz, [_P]),
+    "lazy_attn_rope_table_init": (ctypes.c_int, [_P, _vp, _sz, _vp]),
+    "lazy_attn_pack_block_words_host": (ctypes.c_int, [_P, _i32] + [_vp] * 8),
+    "lazy_attn_pack_block_words": (ctypes.c_int, [_P, _i32] + [_vp] * 8 + [_vp]),
+    "lazy_attn_decode_workspace_bytes": (_sz, [_P]),
+    "lazy_attn_decode": (ctypes.c_int, [_P] + [_vp] * 9 + [_sz, _vp]),
+    "lazy_attn_prefill_workspace_bytes": (_sz, [_P, _i32]),
+    "lazy_attn_prefill": (ctypes.c_int, [_P, _vp, _vp, _vp, _i32, _i32] + [_vp] * 7 + [_sz, _vp]),
+    "lazy_attn_debug_gather": (ctypes.c_int, [_P] + [_vp] * 7 + [_vp]),
+    "lazy_attn_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
+    "lazy_attn_launch_count": (_u64, []),
+}
+for _name, (_res, _args) in _sig.items():
+    _f = getattr(_lib, _name)
+    _f.restype, _f.argtypes = _res, _args
+
+
+def status_string(status: int) -> str:
+    return _lib.lazy_attn_status_string(int(status)).decode()
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != LAZY_OK:
+        raise LazyAttnError(rc, where)
+
+
+def make_params(*, num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int, num_pool_blocks: int,
+                max_blocks_per_seq: int, dtype: str = "bf16", rope_theta: float = 5e5, lazy: bool = True,
+                sm_scale: float = 0.0, id_bits: int = 0, num_splits: int = 0) -> Params:
+    return Params(num_seqs, num_q_heads, num_kv_heads, head_dim, BLOCK, num_pool_blocks, max_blocks_per_seq,
+                  id_bits, LAZY_BF16 if dtype == "bf16" else LAZY_F32, int(bool(lazy)), float(rope_theta),
+                  float(sm_scale), num_splits)
+
+
+def _dptr(t: Optional[torch.Tensor], name: str, dtype=None, device_required=True):
+    if t is None:
+        return None
+    if device_required and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _tdt(p: Params):
+    return torch.bfloat16 if p.dtype == LAZY_BF16 else torch.float32
+
+
+# ---------------------------------------------------------------- rotation table
+
+def rope_table_bytes(p: Params) -> int:
+    return int(_lib.lazy_attn_rope_table_bytes(ctypes.byref(p)))
+
+
+def rope_table_init(p: Params, table: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    n = rope_table_bytes(p)
+    if n == 0:
+        raise LazyAttnError(LAZY_ERR_INVALID_ARG, "rope_table_bytes")
+    if table is None:
+        table = torch.empty(n, dtype=torch.uint8, device="cuda")
+    _check(_lib.lazy_attn_rope_table_init(ctypes.byref(p), _dptr(table, "table"), table.numel() * table.element_size(),
+                                          _stream(stream)), "rope_table_init")
+    return table
+
+
+# ---------------------------------------------------------------- packer
+
+def _i32_np(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a), dtype=np.int32)
+
+
+def pack_block_words_host(p: Params, num_docs: int, seg_indptr, seg_doc, seg_len, seq_pos0, doc_block_indptr,
+                          doc_blocks):
+    """Host packer; arrays are numpy-compatible. Returns (words [B, max_blocks] uint32, seq_lens [B] int32)."""
+    B, MB = p.num_seqs, p.max_blocks_per_seq
+    words = np.zeros((B, MB), dtype=np.uint32)
+    seq_lens = np.zeros(B, dtype=np.int32)
+    # None stays NULL; an empty array is passed as a valid (never read) one-element buffer.
+    arrs = [None if x is None else (_i32_np(x) if np.size(x) else np.zeros(1, np.int32))
+            for x in (seg_indptr, seg_doc, seg_len, seq_pos0, doc_block_indptr, doc_blocks)]
+    ptrs = [None if a is None else a.ctypes.data for a in arrs]
+    rc = _lib.lazy_attn_pack_block_words_host(ctypes.byref(p), int(num_docs), *ptrs, words.ctypes.data,
+                                              seq_lens.ctypes.data)
+    _check(rc, "pack_block_words_host")
+    return words, seq_lens
+
+
+def pack_block_words(p: Params, num_docs: int, seg_indptr: torch.Tensor, seg_doc: torch.Tensor,
+                     seg_len: torch.Tensor, seq_pos0: Optional[torch.Tensor], doc_block_indptr: torch.Tensor,
+                     doc_blocks: torch.Tensor, block_words: Optional[torch.Tensor] = None,
+                     seq_lens: Optional[torch.Tensor] = None, stream=None):
+    """Device packer; every tensor is int32 on the GPU. Returns (block_words, seq_lens)."""
+    if block_words is None:
+        block_words = torch.empty((p.num_seqs, p.max_blocks_per_seq), dtype=torch.int32, device="cuda")
+    if seq_lens is None:
+        seq_lens = torch.empty(p.num_seqs, dtype=torch.int32, device="cuda")
+    i32 = torch.int32
+    rc = _lib.lazy_attn_pack_block_words(
+        ctypes.byref(p), int(num_docs), _dptr(seg_indptr, "seg_indptr", i32), _dptr(seg_doc, "seg_doc", i32),
+        _dptr(seg_len, "seg_len", i32), _dptr(seq_pos0, "seq_pos0", i32),
+        _dptr(doc_block_indptr, "doc_block_indptr", i32), _dptr(doc_blocks, "doc_blocks", i32),
+        _dptr(block_words, "block_words"), _dptr(seq_lens, "seq_lens", i32), _stream(stream))
+    _check(rc, "pack_block_words")
+    return block_words, seq_lens
+
+
+# ---------------------------------------------------------------- decode / prefill
+
+def decode_workspace_bytes(p: Params) -> int:
+    return int(_lib.lazy_attn_decode_workspace_bytes(ctypes.byref(p)))
+
+
+def decode(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, block_words: torch.Tensor,
+           seq_lens: torch.Tensor, q_pos: torch.Tensor, rope_table: torch.Tensor, out: Optional[torch.Tensor] = None,
+           workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    dt = _tdt(p)
+    if out is None:
+        out = torch.empty_like(q)
+    nws = decode_workspace_bytes(p)
+    if workspace is None and nws:
+        workspace = torch.empty(nws, dtype=torch.uint8, device=q.device)
+    wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = _lib.lazy_attn_decode(ctypes.byref(p), _dptr(q, "q", dt), _dptr(k_pool, "k_pool", dt),
+                               _dptr(v_pool, "v_pool", dt), _dptr(block_words, "block_words"),
+                               _dptr(seq_lens, "seq_lens", torch.int32), _dptr(q_pos, "q_pos", torch.int32),
+                               _dptr(rope_table, "rope_table"), _dptr(out, "out", dt),
+                               _dptr(workspace, "workspace"), wsz, _stream(stream))
+    _check(rc, "decode")
+    return out
+
+
+def prefill_workspace_bytes(p: Params, total_q: int) -> int:
+    return int(_lib.lazy_attn_prefill_workspace_bytes(ctypes.byref(p), int(total_q)))
+
+
+def prefill(p: Params, q: torch.Tensor, cu_seqlens_q: torch.Tensor, q_start: torch.Tensor, max_q_len: int,
+            k_pool: torch.Tensor, v_pool: torch.Tensor, block_words: torch.Tensor, seq_lens: torch.Tensor,
+            rope_table: torch.Tensor, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+            stream=None) -> torch.Tensor:
+    dt = _tdt(p)
+    if out is None:
+        out = torch.empty_like(q)
+    wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = _lib.lazy_attn_prefill(ctypes.byref(p), _dptr(q, "q", dt), _dptr(cu_seqlens_q, "cu_seqlens_q", torch.int32),
+                                _dptr(q_start, "q_start", torch.int32), int(q.shape[0]), int(max_q_len),
+                                _dptr(k_pool, "k_pool", dt), _dptr(v_pool, "v_pool", dt),
+                                _dptr(block_words, "block_words"), _dptr(seq_lens, "seq_lens", torch.int32),
+                                _dptr(rope_table, "rope_table"), _dptr(out, "out", dt), _dptr(workspace, "workspace"),
+                                wsz, _stream(stream))
+    _check(rc, "prefill")
+    return out
+
+
+def debug_gather(p: Params, k_pool: torch.Tensor, v_pool: torch.Tensor, block_words: torch.Tensor,
+                 seq_lens: torch.Tensor, with_pos: bool = True, stream=None):
+    dt = _tdt(p)
+    rows = BLOCK * p.max_blocks_per_seq
+    k_out = torch.empty((p.num_seqs, p.num_kv_heads, rows, p.head_dim), dtype=dt, device=k_pool.device)
+    v_out = torch.empty_like(k_out)
+    pos = torch.empty((p.num_seqs, rows), dtype=torch.int32, device=k_pool.device) if with_pos else None
+    rc = _lib.lazy_attn_debug_gather(ctypes.byref(p), _dptr(k_pool, "k_pool", dt), _dptr(v_pool, "v_pool", dt),
+                                     _dptr(block_words, "block_words"), _dptr(seq_lens, "seq_lens", torch.int32),
+                                     _dptr(k_out, "k_out"), _dptr(v_out, "v_out"), _dptr(pos, "pos_out"),
+                                     _stream(stream))
+    _check(rc, "debug_gather")
+    return k_out, v_out, pos
+
+
+def device_status(clear: bool = True) -> int:
+    v = ctypes.c_uint32(0)
+    _check(_lib.lazy_attn_device_status(ctypes.byref(v), int(bool(clear))), "device_status")
+    return int(v.value)
+
+
+def launch_count() -> int:
+    return int(_lib.lazy_attn_launch_count())

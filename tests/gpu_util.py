@@ -1,0 +1,84 @@
+"""Helpers for the GPU tests: move a workload to the device and compare outputs."""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+import torch
+
+# bf16: elementwise |gpu - ref| <= 2e-3 + 2e-2 |ref|; fp32: |gpu - ref| <= 1e-5.
+TOL = {"bf16": (2e-3, 2e-2), "f32": (1e-5, 0.0)}
+
+
+def la():
+    from paged_kv_cache_57_gb300 import build
+    build.build()
+    from paged_kv_cache_57_gb300 import lazy_attn
+    return lazy_attn
+
+
+@dataclasses.dataclass
+class Dev:
+    w: object
+    p: object
+    q: torch.Tensor
+    k_pool: torch.Tensor
+    v_pool: torch.Tensor
+    words: torch.Tensor
+    seq_lens: torch.Tensor
+    rope: torch.Tensor
+    q_pos: Optional[torch.Tensor] = None
+    cu_seqlens_q: Optional[torch.Tensor] = None
+    q_start: Optional[torch.Tensor] = None
+    max_q_len: int = 0
+
+
+def to_device(w, lazy: bool = True, num_splits: int = 0, pack_on_device: bool = True, k_pool=None) -> Dev:
+    L = la()
+    p = L.make_params(num_seqs=w.num_seqs, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                      head_dim=w.head_dim, num_pool_blocks=w.num_pool_blocks,
+                      max_blocks_per_seq=max(1, w.max_blocks_per_seq), dtype=w.dtype, rope_theta=w.rope_theta,
+                      lazy=lazy, num_splits=num_splits)
+    cuda = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    if pack_on_device:
+        words, seq_lens = L.pack_block_words(p, len(w.doc_len), cuda(w.seg_indptr), cuda(w.seg_doc),
+                                             cuda(w.seg_len), cuda(w.seq_pos0), cuda(w.doc_block_indptr),
+                                             cuda(w.doc_blocks) if len(w.doc_blocks) else cuda(np.zeros(1)))
+    else:
+        wh, sh = L.pack_block_words_host(p, len(w.doc_len), w.seg_indptr, w.seg_doc, w.seg_len, w.seq_pos0,
+                                         w.doc_block_indptr, w.doc_blocks)
+        words, seq_lens = torch.from_numpy(wh.view(np.int32)).cuda(), torch.from_numpy(sh).cuda()
+    d = Dev(w=w, p=p, q=w.q.cuda(), k_pool=(w.k_pool if k_pool is None else k_pool).cuda(), v_pool=w.v_pool.cuda(),
+            words=words, seq_lens=seq_lens, rope=L.rope_table_init(p))
+    if w.kind == "decode":
+        d.q_pos = cuda(w.q_pos)
+    else:
+        d.cu_seqlens_q = cuda(w.cu_seqlens_q)
+        d.q_start = cuda(w.q_start)
+        d.max_q_len = int(np.diff(w.cu_seqlens_q).max()) if w.num_seqs else 0
+    return d
+
+
+def decode(d: Dev, out=None) -> torch.Tensor:
+    L = la()
+    return L.decode(d.p, d.q, d.k_pool, d.v_pool, d.words, d.seq_lens, d.q_pos, d.rope, out=out)
+
+
+def prefill(d: Dev) -> torch.Tensor:
+    L = la()
+    return L.prefill(d.p, d.q, d.cu_seqlens_q, d.q_start, d.max_q_len, d.k_pool, d.v_pool, d.words, d.seq_lens,
+                     d.rope)
+
+
+def assert_close(got: torch.Tensor, ref: np.ndarray, dtype: str, what: str = "") -> float:
+    g = got.detach().float().cpu().double().numpy()
+    atol, rtol = TOL[dtype]
+    err = np.abs(g - ref)
+    bad = err > atol + rtol * np.abs(ref)
+    assert np.isfinite(g).all(), f"{what}: non-finite output"
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - (atol + rtol * np.abs(ref))), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements outside tolerance; worst at {i}: "
+                             f"gpu={g[i]!r} ref={ref[i]!r}")
+    return float(err.max())

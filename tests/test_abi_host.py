@@ -1,0 +1,175 @@
+"""CPU tests of the C ABI: symbols, argument checks and the host packer.
+
+Nothing here launches a kernel; every call either returns before touching CUDA
+(argument and layout checks, size queries) or is pure host code (the packer).
+The expected words are rebuilt from the generator's document lists by plain
+Python, independently of the library.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+from paged_kv_cache_57_gb300 import build as B
+from paged_kv_cache_57_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def la():
+    B.build()
+    from paged_kv_cache_57_gb300 import lazy_attn
+    return lazy_attn
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "lazy_attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(lazy_attn_\w+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(la):
+    names = declared_symbols()
+    assert len(names) >= 12
+    lib = ctypes.CDLL(la.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(la.EXPORTED)
+    out = subprocess.run(["nm", "-D", "--defined-only", la.LIB_PATH], capture_output=True, text=True).stdout
+    for n in names:
+        assert re.search(rf"\bT {n}\b", out), n
+
+
+def test_status_strings(la):
+    for s in range(7):
+        assert la.status_string(s).startswith("LAZY_")
+    assert "unknown" in la.status_string(99)
+
+
+def _params(la, w, **kw):
+    return la.make_params(num_seqs=w.num_seqs, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                          head_dim=w.head_dim, num_pool_blocks=w.num_pool_blocks,
+                          max_blocks_per_seq=kw.pop("max_blocks", w.max_blocks_per_seq), dtype=w.dtype,
+                          rope_theta=w.rope_theta, **kw)
+
+
+def expected_blocks(w, s):
+    """(phys, p, valid) per logical block, from the document lists."""
+    out = []
+    p = int(w.seq_pos0[s])
+    for doc, L in w.seq_segments(s):
+        base = int(w.doc_block_indptr[doc])
+        for j in range((L + 15) // 16):
+            out.append((int(w.doc_blocks[base + j]), p, min(16, L - 16 * j)))
+        p += L
+    return out
+
+
+def unpack(word, b, id_bits):
+    phys = int(word) & ((1 << id_bits) - 1)
+    off = int(np.int32(np.uint32(word))) >> id_bits
+    return phys, 16 * b - off
+
+
+def valid_by_rule(ps, b, nb, seq_len):
+    if b == nb - 1:
+        return seq_len - 16 * (nb - 1)
+    if ps[b + 1] != ps[b]:
+        return ((ps[b + 1] - ps[b] - 1) & 15) + 1
+    return 16
+
+
+def _workloads():
+    yield W.tiny_fp32()
+    yield W.tiny_fp32(shift=3000)
+    yield W.decode_zipf("d", batch=5, hq=8, hkv=2, d=64, docs_per_seq=4, doc_tokens=48, pool_docs=7,
+                        zipf_s=1.0, suffix_tokens=9, seed=5)
+    yield W.prefill_zipf("p", batch=3, hq=4, hkv=2, d=64, docs_per_seq=2, doc_tokens=40, pool_docs=4,
+                         zipf_s=1.2, chunk_tokens=[1, 17, 130], seed=6)
+    d, p = W.mixed_mqa(n_decode=6, n_prefill=2, chunk=40, hq=4, hkv=1, d=64, pool_docs=30, ctx_lo=50,
+                       ctx_hi=3000, doc_lo=5, doc_hi=300, seed=7)
+    yield d
+    yield p
+
+
+@pytest.mark.parametrize("w", list(_workloads()), ids=lambda w: f"{w.name}-{w.num_seqs}")
+def test_host_packer_round_trip(la, w):
+    p = _params(la, w)
+    words, seq_lens = la.pack_block_words_host(p, len(w.doc_len), w.seg_indptr, w.seg_doc, w.seg_len, w.seq_pos0,
+                                               w.doc_block_indptr, w.doc_blocks)
+    id_bits = 18
+    for s in range(w.num_seqs):
+        exp = expected_blocks(w, s)
+        nb = len(exp)
+        assert seq_lens[s] == (16 * (nb - 1) + exp[-1][2] if nb else 0)
+        got = [unpack(words[s, b], b, id_bits) for b in range(nb)]
+        assert [g[0] for g in got] == [e[0] for e in exp]
+        assert [g[1] for g in got] == [e[1] for e in exp]
+        ps = [g[1] for g in got]
+        assert [valid_by_rule(ps, b, nb, int(seq_lens[s])) for b in range(nb)] == [e[2] for e in exp]
+        assert (words[s, nb:] == 0).all()
+
+
+def test_host_packer_rejects_bad_layouts(la):
+    w = W.decode_zipf("bad", batch=2, hq=4, hkv=2, d=64, docs_per_seq=2, doc_tokens=20, pool_docs=3, zipf_s=1.0,
+                      seed=8)
+    p = _params(la, w)
+    args = [w.seg_indptr, w.seg_doc, w.seg_len, w.seq_pos0, w.doc_block_indptr, w.doc_blocks]
+
+    def run(params=p, **repl):
+        a = dict(zip(["seg_indptr", "seg_doc", "seg_len", "seq_pos0", "doc_block_indptr", "doc_blocks"],
+                     [x.copy() for x in args]))
+        for k, fn in repl.items():
+            a[k] = fn(a[k])
+        with pytest.raises(la.LazyAttnError) as e:
+            la.pack_block_words_host(params, len(w.doc_len), *a.values())
+        return e.value.status
+
+    def set_at(i, v):
+        def f(x):
+            x[i] = v
+            return x
+        return f
+
+    assert run(seg_len=set_at(0, 33)) == la.LAZY_ERR_LAYOUT      # longer than its document
+    assert run(seg_len=set_at(0, 0)) == la.LAZY_ERR_LAYOUT       # empty segment
+    assert run(seg_doc=set_at(0, 99)) == la.LAZY_ERR_LAYOUT      # unknown document
+    assert run(doc_blocks=set_at(0, w.num_pool_blocks)) == la.LAZY_ERR_LAYOUT  # outside the pool
+    assert run(seq_pos0=set_at(0, 9000)) == la.LAZY_ERR_LAYOUT   # off = -9000 does not fit 14 bits
+    small = _params(la, w, max_blocks=1)
+    assert run(params=small) == la.LAZY_ERR_LAYOUT               # too many blocks for the table
+
+
+def test_argument_checks_return_before_cuda(la):
+    w = W.tiny_fp32()
+    bad = [dict(head_dim=96), dict(num_kv_heads=3), dict(id_bits=30), dict(num_splits=-1)]
+    for kw in bad:
+        p = _params(la, w)
+        for k, v in kw.items():
+            setattr(p, k, v)
+        st = la._lib.lazy_attn_decode(ctypes.byref(p), *([None] * 9), 0, None)
+        assert st in (la.LAZY_ERR_UNSUPPORTED, la.LAZY_ERR_INVALID_ARG), kw
+    p = _params(la, w)
+    p.block_size = 32
+    assert la._lib.lazy_attn_decode(ctypes.byref(p), *([None] * 9), 0, None) == la.LAZY_ERR_UNSUPPORTED
+    p = _params(la, w)
+    assert la._lib.lazy_attn_decode(ctypes.byref(p), *([None] * 9), 0, None) == la.LAZY_ERR_INVALID_ARG
+    p.dtype = la.LAZY_F32
+    assert la._lib.lazy_attn_prefill(ctypes.byref(p), None, None, None, 1, 1, *([None] * 7), 0, None) \
+        == la.LAZY_ERR_UNSUPPORTED
+
+
+def test_size_queries(la):
+    w = W.FULL["tiny_fp32"]()
+    p = _params(la, w)
+    assert la.rope_table_bytes(p) == 2 * 1024 * 32 * 8
+    p.head_dim = 128
+    assert la.rope_table_bytes(p) == 2 * 1024 * 64 * 8
+    p.num_splits = 1
+    assert la.decode_workspace_bytes(p) == 0
+    p.num_splits, p.max_blocks_per_seq = 4, 64
+    assert la.decode_workspace_bytes(p) == 1 * 4 * 4 * (128 + 2) * 4
