@@ -81,13 +81,13 @@ typedef enum { LAZY_F32 = 0, LAZY_BF16 = 1 } lazy_dtype;
 
 /* Bits of the per-device status word. */
 #define LAZY_DEV_BAD_BLOCK_ID 0x1u /* a word's phys_id >= num_pool_blocks (block skipped) */
-#define LAZY_DEV_POS_RANGE 0x2u    /* |rotation offset| >= 2^20 (rotation clamped) */
+#define LAZY_DEV_POS_RANGE 0x2u    /* |rotation offset| >= LAZY_MAX_ROPE_OFFSET (offset clamped) */
 #define LAZY_DEV_TIMEOUT 0x4u      /* a pipeline wait gave up after its limit */
 #define LAZY_DEV_LAYOUT 0x8u       /* the device packer met an invalid layout */
 #define LAZY_DEV_BAD_LEN 0x10u     /* seq_lens < 0 or > 16*max_blocks_per_seq (clamped) */
 
 /* Largest |offset| the rotation table covers (positions and offsets). */
-#define LAZY_MAX_ROPE_OFFSET (1 << 20)
+#define LAZY_MAX_ROPE_OFFSET (1 << 24)
 
 typedef struct {
   int32_t num_seqs;           /* B >= 0 */
@@ -110,13 +110,16 @@ typedef struct {
 const char *lazy_attn_status_string(int status);
 
 /* ---------------------------------------------------------------- rotation table
- * cos/sin of n*w_i for the offsets the kernels need, computed once per
- * (head_dim, rope_theta) in fp64 on the device and stored as fp32 pairs:
- * table[0][a][i] = (cos, sin)(a*w_i), table[1][b][i] = (cos, sin)(1024*b*w_i),
- * a, b in [0, 1024). The kernels combine the two levels with the angle-sum
- * identity, which keeps every angle up to 2^20 exact to a few fp32 ulps.
- * Layout: float2 [2][1024][head_dim/2]. Caller-owned device memory of at least
- * lazy_attn_rope_table_bytes(p) bytes; read-only to every other call. */
+ * Per-frequency rotation rates in turns, t_i = w_i / (2 pi), computed in fp64 on
+ * the device once per (head_dim, rope_theta) and stored as an unevaluated sum of
+ * two fp32 values (hi, lo). For an integer offset n the kernels form n*t_i with
+ * an error-free product, drop the whole turns exactly (n*t_i - rint(n*t_i) is
+ * exact in fp32), and evaluate cos/sin(2 pi * fraction) with sincospif. The
+ * angle error stays below about 5e-7 rad for every |n| < LAZY_MAX_ROPE_OFFSET,
+ * with no memory access per offset.
+ * Layout: float2 [head_dim/2] = (hi, lo). Caller-owned device memory of at least
+ * lazy_attn_rope_table_bytes(p) bytes, 16-byte aligned; read-only to every other
+ * call. */
 size_t lazy_attn_rope_table_bytes(const lazy_attn_params *p);
 int lazy_attn_rope_table_init(const lazy_attn_params *p, void *table, size_t table_bytes,
                               lazy_stream_t stream);
@@ -201,6 +204,12 @@ int lazy_attn_prefill(const lazy_attn_params *p, const void *q, const int32_t *c
 int lazy_attn_debug_gather(const lazy_attn_params *p, const void *k_pool, const void *v_pool,
                            const uint32_t *block_words, const int32_t *seq_lens, void *k_out, void *v_out,
                            int32_t *pos_out, lazy_stream_t stream);
+
+/* Evaluates the kernels' rotation for n offsets: cs_out[k][i] = (cos, sin) of
+ * deltas[k] * w_i, i < head_dim/2, with the device function the attention
+ * kernels use. deltas [n] int32 device; cs_out [n][head_dim/2] float2 device. */
+int lazy_attn_debug_rope(const lazy_attn_params *p, const void *rope_table, const int32_t *deltas, int32_t n,
+                         void *cs_out, lazy_stream_t stream);
 
 /* Reads (and, if clear != 0, zeroes) the current device's status word. Waits for
  * all work on the device first. Returns LAZY_OK, or LAZY_ERR_CUDA. */

@@ -176,7 +176,7 @@ uint64_t lazy_attn_launch_count(void) { return g_launches.load(std::memory_order
 size_t lazy_attn_rope_table_bytes(const lazy_attn_params* p) {
   Checked c;
   if (check_params(p, &c) != LAZY_OK) return 0;
-  return (size_t)2 * lazy::kTableEntries * (p->head_dim / 2) * sizeof(float2);
+  return (size_t)(p->head_dim / 2) * sizeof(float2);
 }
 
 int lazy_attn_rope_table_init(const lazy_attn_params* p, void* table, size_t table_bytes, lazy_stream_t stream) {
@@ -398,6 +398,20 @@ int lazy_attn_debug_gather(const lazy_attn_params* p, const void* k_pool, const 
       !encode_rows_map(&vmap, v_pool, rows, p->head_dim, lazy::kBlock))
     return LAZY_ERR_CUDA;
   return launched(lazy::launch_gather_bf16(a, kmap, vmap, cs));
+}
+
+int lazy_attn_debug_rope(const lazy_attn_params* p, const void* rope_table, const int32_t* deltas, int32_t n,
+                         void* cs_out, lazy_stream_t stream) {
+  Checked c;
+  int rc = check_params(p, &c);
+  if (rc != LAZY_OK) return rc;
+  if (n < 0) return LAZY_ERR_INVALID_ARG;
+  if (n == 0) return LAZY_OK;
+  if (!rope_table || !deltas || !cs_out || !aligned16(rope_table)) return LAZY_ERR_INVALID_ARG;
+  unsigned int* st = status_ptr();
+  if (!st) return LAZY_ERR_CUDA;
+  return launched(lazy::launch_debug_rope(static_cast<const float2*>(rope_table), deltas, n, p->head_dim,
+                                          static_cast<float2*>(cs_out), st, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int lazy_attn_device_status(uint32_t* flags_out, int clear) {

@@ -15,8 +15,6 @@
 namespace lazy {
 
 constexpr int kBlock = 16;             // tokens per physical block
-constexpr int kTableEntries = 1024;    // entries per rotation-table level
-constexpr int kTableShift = 10;        // log2(kTableEntries)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: any pipeline wait longer than this is a fault
 
 // ------------------------------------------------------------------ status word
@@ -165,22 +163,25 @@ __device__ __forceinline__ int block_valid(int b, int nb, int seq_len, int p_b, 
   return kBlock;
 }
 
-// ------------------------------------------------------------------ rotation table
+// ------------------------------------------------------------------ rotation
 
-// (cos, sin)(delta * w_i) from the two-level table: delta = 1024*hi + lo, and
-// the angle-sum identity combines the two fp64-exact entries in fp32.
-__device__ __forceinline__ float2 rope_cs(const float2* __restrict__ table, int half, int delta, int i,
-                                          unsigned int* status) {
-  int ad = delta < 0 ? -delta : delta;
-  if (ad >= LAZY_MAX_ROPE_OFFSET) {
+// (cos, sin)(delta * w) for a frequency given in turns, t = w / (2 pi), stored as
+// t.x + t.y. The product delta * t.x is split exactly into ph + pe (error-free
+// product with one FMA); ph - rint(ph) is exact in fp32, so the fraction of a
+// turn is formed with two small roundings and sincospif evaluates it without a
+// range reduction. |angle error| is below about 5e-7 rad for |delta| < 2^24.
+__device__ __forceinline__ float2 rope_cs(float2 t, int delta, unsigned int* status) {
+  if (delta >= LAZY_MAX_ROPE_OFFSET || delta <= -LAZY_MAX_ROPE_OFFSET) {
     raise_status(status, LAZY_DEV_POS_RANGE);
-    ad = LAZY_MAX_ROPE_OFFSET - 1;
+    delta = delta > 0 ? LAZY_MAX_ROPE_OFFSET - 1 : -(LAZY_MAX_ROPE_OFFSET - 1);
   }
-  const float2 lo = __ldg(&table[(ad & (kTableEntries - 1)) * half + i]);
-  const float2 hi = __ldg(&table[(kTableEntries + (ad >> kTableShift)) * half + i]);
-  const float c = fmaf(lo.x, hi.x, -lo.y * hi.y);
-  const float s = fmaf(lo.y, hi.x, lo.x * hi.y);
-  return make_float2(c, delta < 0 ? -s : s);
+  const float n = static_cast<float>(delta);  // exact: |delta| < 2^24
+  const float ph = n * t.x;
+  const float pe = fmaf(n, t.x, -ph);  // n * t.x == ph + pe exactly
+  const float f = (ph - rintf(ph)) + (pe + n * t.y);
+  float s, c;
+  sincospif(2.f * f, &s, &c);
+  return make_float2(c, s);
 }
 
 }  // namespace lazy

@@ -66,55 +66,102 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// One logical block, executed by a whole warp: decode the word, fill the stage's
-// metadata, then lane 0 arms the stage's full barrier and issues the TMA loads.
+// Warp-uniform bounded wait: every lane polls, and the warp gives up together.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* status) {
+  const bool ok = mbar_wait(bar, parity, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// The producer warp of a split: blocks b0 .. b0+n-1 of one sequence. Words are
+// fetched 32 at a time (one per lane) one chunk ahead, so no word load sits on
+// the issue path. Per block: wait for the stage to be free, write the stage's
+// metadata (document start p, valid slots, and cos/sin of (m - p) when the
+// document changes -- computed in registers, no memory access), then lane 0
+// arms the full barrier and issues the TMA loads of the block's K and V rows.
 // Invalid block ids are not loaded: the stage is marked empty (nvalid = 0).
-template <int D, bool WITH_CS>
-__device__ __forceinline__ void produce_block(int lane, int b, int nb, int seq_len, const uint32_t* __restrict__ wrow,
-                                              int id_bits, int num_pool_blocks, int hkv, int kvh,
-                                              StageMeta<D / 2>* meta, uint8_t* stage, uint64_t* full,
-                                              const CUtensorMap* kmap, const CUtensorMap* vmap, int m_pos,
-                                              const float2* __restrict__ rope, int& p_prev,
-                                              float2 (&cs)[(D / 2 + 31) / 32], unsigned int* status) {
-  constexpr int NBOX = D / 64;
-  constexpr int BOX_BYTES = kBlock * 128;
-  constexpr int HALF = D / 2;
-  const BlockInfo bi = decode_word(__ldg(&wrow[b]), b, id_bits);
-  int p_next = bi.p;
-  if (b + 1 < nb) p_next = decode_word(__ldg(&wrow[b + 1]), b + 1, id_bits).p;
-  int nvalid = block_valid(b, nb, seq_len, bi.p, p_next);
-  nvalid = nvalid < 0 ? 0 : (nvalid > kBlock ? kBlock : nvalid);
-  const bool ok = bi.phys < num_pool_blocks;
-  if (!ok) {
-    nvalid = 0;
-    if (lane == 0) raise_status(status, LAZY_DEV_BAD_BLOCK_ID);
-  }
+// Returns the number of blocks issued (all of them unless a wait timed out).
+template <int D, bool WITH_CS, int NS, int STAGE_BYTES>
+__device__ __forceinline__ int producer_loop(int lane, int b0, int n, int nb, int seq_len,
+                                             const uint32_t* __restrict__ wrow, int id_bits, int num_pool_blocks,
+                                             int hkv, int kvh, StageMeta<D / 2>* meta, uint8_t* stages,
+                                             uint64_t* full, uint64_t* empty, const CUtensorMap* kmap,
+                                             const CUtensorMap* vmap, int m_pos, const float2* __restrict__ turns,
+                                             unsigned int* status) {
+  constexpr int HALF = D / 2, CPL = HALF / 32, NBOX = D / 64, BOX_BYTES = kBlock * 128;
+  float2 tr[CPL], cs[CPL];
   if constexpr (WITH_CS) {
-    if (bi.p != p_prev) {
 #pragma unroll
-      for (int j = 0; j < HALF / 32; ++j) cs[j] = rope_cs(rope, HALF, m_pos - bi.p, lane + 32 * j, status);
-      p_prev = bi.p;
+    for (int j = 0; j < CPL; ++j) tr[j] = __ldg(&turns[lane + 32 * j]);
+  }
+  int p_cur = INT_MIN;
+  auto load_chunk = [&](int c0, uint32_t& w, uint32_t& wn) {
+    const int r = c0 + lane, b = b0 + r;
+    w = r < n ? __ldg(&wrow[b]) : 0u;
+    wn = (r < n && b + 1 < nb) ? __ldg(&wrow[b + 1]) : 0u;
+  };
+  uint32_t wa = 0, wna = 0, wb = 0, wnb = 0;
+  load_chunk(0, wa, wna);
+  int issued = 0;
+  for (int c0 = 0; c0 < n; c0 += 32) {
+    if (c0 + 32 < n) load_chunk(c0 + 32, wb, wnb);
+    const int r = c0 + lane, b = b0 + r;
+    const BlockInfo bi = decode_word(wa, b, id_bits);
+    const int pn = (b + 1 < nb) ? decode_word(wna, b + 1, id_bits).p : bi.p;
+    int nv = block_valid(b, nb, seq_len, bi.p, pn);
+    nv = nv < 0 ? 0 : (nv > kBlock ? kBlock : nv);
+    if (bi.phys >= num_pool_blocks) {
+      nv = 0;
+      if (r < n) raise_status(status, LAZY_DEV_BAD_BLOCK_ID);
     }
+    const int cnt = min(32, n - c0);
+    for (int j = 0; j < cnt; ++j) {
+      const int i = c0 + j, st = i % NS;
+      const int phys = __shfl_sync(0xffffffffu, bi.phys, j);
+      const int p = __shfl_sync(0xffffffffu, bi.p, j);
+      const int nvalid = __shfl_sync(0xffffffffu, nv, j);
+      if (i >= NS && !warp_wait(&empty[st], ((i / NS) & 1) ^ 1, status)) return issued;
+      StageMeta<HALF>* m = &meta[st];
+      if constexpr (WITH_CS) {
+        if (p != p_cur) {
 #pragma unroll
-    for (int j = 0; j < HALF / 32; ++j) meta->cs[lane + 32 * j] = cs[j];
-  }
-  if (lane == 0) {
-    meta->p = bi.p;
-    meta->nvalid = nvalid;
-  }
-  __syncwarp();
-  if (lane == 0) {
-    if (ok) {
-      mbar_arrive_expect_tx(full, 2 * NBOX * BOX_BYTES);
-      const int y = (bi.phys * hkv + kvh) * kBlock;
+          for (int jj = 0; jj < CPL; ++jj) cs[jj] = rope_cs(tr[jj], m_pos - p, status);
+          p_cur = p;
+        }
 #pragma unroll
-      for (int bx = 0; bx < NBOX; ++bx) tma_load_2d(stage + bx * BOX_BYTES, kmap, full, bx * 64, y);
+        for (int jj = 0; jj < CPL; ++jj) m->cs[lane + 32 * jj] = cs[jj];
+      }
+      if (lane == 0) {
+        m->p = p;
+        m->nvalid = nvalid;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        uint64_t* fb = &full[st];
+        uint8_t* stage = stages + st * STAGE_BYTES;
+        if (phys < num_pool_blocks) {
+          mbar_arrive_expect_tx(fb, 2 * NBOX * BOX_BYTES);
+          const int y = (phys * hkv + kvh) * kBlock;
 #pragma unroll
-      for (int bx = 0; bx < NBOX; ++bx) tma_load_2d(stage + (NBOX + bx) * BOX_BYTES, vmap, full, bx * 64, y);
-    } else {
-      mbar_arrive(full);
+          for (int bx = 0; bx < NBOX; ++bx) tma_load_2d(stage + bx * BOX_BYTES, kmap, fb, bx * 64, y);
+#pragma unroll
+          for (int bx = 0; bx < NBOX; ++bx) tma_load_2d(stage + (NBOX + bx) * BOX_BYTES, vmap, fb, bx * 64, y);
+        } else {
+          mbar_arrive(fb);
+        }
+      }
+      issued = i + 1;
     }
+    wa = wb;
+    wna = wnb;
   }
+  return issued;
+}
+
+// Bounded wait, by lane 0, for every copy this CTA still has in flight.
+template <int NS>
+__device__ __forceinline__ void drain_copies(int lane, int issued, uint64_t* full, unsigned int* status) {
+  if (lane == 0)
+    for (int i = max(0, issued - NS); i < issued; ++i) mbar_wait(&full[i % NS], (i / NS) & 1, status);
 }
 
 // A fragments of R_delta q for rows (mt*16 + g, mt*16 + g + 8), g = lane/4.
@@ -200,23 +247,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT>::NTHREADS)
       tma_prefetch_map(&kmap);
       tma_prefetch_map(&vmap);
     }
-    int p_prev = INT_MIN;
-    float2 cs[(C::HALF + 31) / 32];
-    int issued = 0;
-    for (int i = 0; i < n; ++i) {
-      const int st = i % C::NS;
-      if (i >= C::NS && !mbar_wait(&empty[st], ((i / C::NS) & 1) ^ 1, a.status)) {
-        abort_flag = 1;
-        break;
-      }
-      produce_block<D, LAZY>(lane, b0 + i, nb, seq_len, wrow, a.id_bits, a.num_pool_blocks, a.Hkv, kvh, &meta[st],
-                             stages + st * C::STAGE_BYTES, &full[st], &kmap, &vmap, m_pos, a.rope, p_prev, cs,
-                             a.status);
-      issued = i + 1;
-    }
-    // Every copy this CTA issued must land before the CTA exits (bounded).
-    if (lane == 0)
-      for (int i = max(0, issued - C::NS); i < issued; ++i) mbar_wait(&full[i % C::NS], (i / C::NS) & 1, a.status);
+    const int issued = producer_loop<D, LAZY, C::NS, C::STAGE_BYTES>(
+        lane, b0, n, nb, seq_len, wrow, a.id_bits, a.num_pool_blocks, a.Hkv, kvh, meta, stages, full, empty, &kmap,
+        &vmap, m_pos, a.rope, a.status);
+    if (issued < n) abort_flag = 1;
+    drain_copies<C::NS>(lane, issued, full, a.status);
   } else {
     // ------------------------------------------------------------ consumers
     const int team = warp / MT, mt = warp % MT;
@@ -229,12 +264,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT>::NTHREADS)
     int p_prev = INT_MIN;
     if constexpr (!LAZY) {
       // Control: the pool holds absolute-position keys; rotate q once by R_m.
-      build_q_frags<D>(qa, qs, mt, lane, [&](int i) { return rope_cs(a.rope, C::HALF, m_pos, i, a.status); });
+      build_q_frags<D>(qa, qs, mt, lane, [&](int i) { return rope_cs(__ldg(&a.rope[i]), m_pos, a.status); });
     }
     const float sl2 = a.scale_log2;
     for (int i = team; i < n; i += C::TEAMS) {
       const int st = i % C::NS;
-      if (!mbar_wait(&full[st], (i / C::NS) & 1, a.status)) {
+      if (!warp_wait(&full[st], (i / C::NS) & 1, a.status)) {
         abort_flag = 1;
         break;
       }
@@ -463,22 +498,14 @@ __global__ void __launch_bounds__(64) gather_bf16_kernel(const GatherArgs a, con
   __nv_bfloat16* kout = static_cast<__nv_bfloat16*>(a.k_out) + ((size_t)s * a.Hkv + kvh) * rows * D;
   __nv_bfloat16* vout = static_cast<__nv_bfloat16*>(a.v_out) + ((size_t)s * a.Hkv + kvh) * rows * D;
   if (warp == 0) {
-    int p_prev = INT_MIN;
-    float2 cs[(HALF + 31) / 32];
-    int issued = 0;
-    for (int i = 0; i < nb; ++i) {
-      const int st = i % NS;
-      if (i >= NS && !mbar_wait(&empty[st], ((i / NS) & 1) ^ 1, a.status)) break;
-      produce_block<D, false>(lane, i, nb, seq_len, wrow, a.id_bits, a.num_pool_blocks, a.Hkv, kvh, &meta[st],
-                              stages + st * 2 * KV_BYTES, &full[st], &kmap, &vmap, 0, nullptr, p_prev, cs, a.status);
-      issued = i + 1;
-    }
-    if (lane == 0)
-      for (int i = max(0, issued - NS); i < issued; ++i) mbar_wait(&full[i % NS], (i / NS) & 1, a.status);
+    const int issued = producer_loop<D, false, NS, 2 * KV_BYTES>(lane, 0, nb, nb, seq_len, wrow, a.id_bits,
+                                                                 a.num_pool_blocks, a.Hkv, kvh, meta, stages, full,
+                                                                 empty, &kmap, &vmap, 0, nullptr, a.status);
+    drain_copies<NS>(lane, issued, full, a.status);
   } else {
     for (int i = 0; i < nb; ++i) {
       const int st = i % NS;
-      if (!mbar_wait(&full[st], (i / NS) & 1, a.status)) break;
+      if (!warp_wait(&full[st], (i / NS) & 1, a.status)) break;
       const int p = meta[st].p, nvalid = meta[st].nvalid;
       const uint8_t* kb = stages + st * 2 * KV_BYTES;
       const uint8_t* vb = kb + KV_BYTES;

@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kF32Threads) decode_f32_kernel(const DecodeArg
   auto rotate = [&](int delta) {
     for (int h = warp; h < a.G; h += 4)
       for (int i = lane; i < HALF; i += 32) {
-        const float2 c = rope_cs(a.rope, HALF, delta, i, a.status);
+        const float2 c = rope_cs(__ldg(&a.rope[i]), delta, a.status);
         const float x = qraw[h * D + i], y = qraw[h * D + i + HALF];
         qrot[h * D + i] = fmaf(x, c.x, -y * c.y);
         qrot[h * D + i + HALF] = fmaf(y, c.x, x * c.y);

@@ -12,7 +12,7 @@ struct DecodeArgs {
   const uint32_t* words;     // [B][max_blocks]
   const int32_t* seq_lens;   // [B]
   const int32_t* q_pos;      // [B]
-  const float2* rope;        // rotation table
+  const float2* rope;        // rotation table: per-frequency turns (hi, lo)
   const void* k_pool;        // [NB][Hkv][16][D] (plain-load kernels)
   const void* v_pool;
   void* out;                 // [B][Hq][D]
@@ -63,6 +63,8 @@ struct PrefillArgs {
 
 // Every launcher returns the cudaError_t of its launch.
 cudaError_t launch_rope_table(float2* table, int head_dim, double theta, cudaStream_t st);
+cudaError_t launch_debug_rope(const float2* table, const int32_t* deltas, int n, int head_dim, float2* out,
+                              unsigned int* status, cudaStream_t st);
 cudaError_t launch_pack(const PackArgs& a, cudaStream_t st);
 cudaError_t launch_decode_f32(const DecodeArgs& a, bool lazy, cudaStream_t st);
 cudaError_t launch_decode_bf16(const DecodeArgs& a, bool lazy, const CUtensorMap& kmap, const CUtensorMap& vmap,

@@ -4,26 +4,34 @@
 
 namespace lazy {
 
-// table[0][a][i] = (cos, sin)(a * w_i), table[1][b][i] = (cos, sin)(1024 * b * w_i),
-// w_i = theta^(-2i/d), angles and sin/cos in fp64, stored as fp32.
+// t_i = w_i / (2 pi), w_i = theta^(-2i/d), in fp64, stored as fp32 (hi, lo).
 __global__ void rope_table_kernel(float2* table, int half, int head_dim, double theta) {
-  const int total = 2 * kTableEntries * half;
-  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += gridDim.x * blockDim.x) {
-    const int i = idx % half;
-    const int e = (idx / half) % kTableEntries;
-    const int level = idx / (half * kTableEntries);
-    const double w = pow(theta, -2.0 * (double)i / (double)head_dim);
-    const double n = level == 0 ? (double)e : (double)e * (double)kTableEntries;
-    double sn, cs;
-    sincos(n * w, &sn, &cs);
-    table[idx] = make_float2((float)cs, (float)sn);
-  }
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= half) return;
+  const double two_pi = 6.283185307179586476925286766559;
+  const double t = pow(theta, -2.0 * (double)i / (double)head_dim) / two_pi;
+  const float hi = (float)t;
+  table[i] = make_float2(hi, (float)(t - (double)hi));
 }
 
 cudaError_t launch_rope_table(float2* table, int head_dim, double theta, cudaStream_t st) {
   const int half = head_dim / 2;
-  const int total = 2 * kTableEntries * half;
-  rope_table_kernel<<<(total + 255) / 256, 256, 0, st>>>(table, half, head_dim, theta);
+  rope_table_kernel<<<1, 128, 0, st>>>(table, half, head_dim, theta);
+  return cudaGetLastError();
+}
+
+__global__ void debug_rope_kernel(const float2* __restrict__ table, const int32_t* __restrict__ deltas, int n, int half,
+                                  float2* out, unsigned int* status) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n * half) return;
+  out[idx] = rope_cs(table[idx % half], deltas[idx / half], status);
+}
+
+cudaError_t launch_debug_rope(const float2* table, const int32_t* deltas, int n, int head_dim, float2* out,
+                              unsigned int* status, cudaStream_t st) {
+  const int total = n * (head_dim / 2);
+  if (total == 0) return cudaSuccess;
+  debug_rope_kernel<<<(total + 255) / 256, 256, 0, st>>>(table, deltas, n, head_dim / 2, out, status);
   return cudaGetLastError();
 }
 

@@ -32,7 +32,7 @@ EXPORTED = (
     "lazy_attn_status_string", "lazy_attn_rope_table_bytes", "lazy_attn_rope_table_init",
     "lazy_attn_pack_block_words_host", "lazy_attn_pack_block_words", "lazy_attn_decode_workspace_bytes",
     "lazy_attn_decode", "lazy_attn_prefill_workspace_bytes", "lazy_attn_prefill", "lazy_attn_debug_gather",
-    "lazy_attn_device_status", "lazy_attn_launch_count",
+    "lazy_attn_device_status", "lazy_attn_launch_count", "lazy_attn_debug_rope",
 )
 
 
@@ -68,6 +68,7 @@ _sig = {
     "lazy_attn_debug_gather": (ctypes.c_int, [_P] + [_vp] * 7 + [_vp]),
     "lazy_attn_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "lazy_attn_launch_count": (_u64, []),
+    "lazy_attn_debug_rope": (ctypes.c_int, [_P, _vp, _vp, _i32, _vp, _vp]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -231,6 +232,16 @@ def debug_gather(p: Params, k_pool: torch.Tensor, v_pool: torch.Tensor, block_wo
                                      _stream(stream))
     _check(rc, "debug_gather")
     return k_out, v_out, pos
+
+
+def debug_rope(p: Params, rope_table: torch.Tensor, deltas: torch.Tensor, stream=None) -> torch.Tensor:
+    """(cos, sin) of deltas[k] * w_i as the kernels compute them: [n, head_dim/2, 2] fp32."""
+    n = int(deltas.numel())
+    out = torch.empty((n, p.head_dim // 2, 2), dtype=torch.float32, device=deltas.device)
+    _check(_lib.lazy_attn_debug_rope(ctypes.byref(p), _dptr(rope_table, "rope_table"),
+                                     _dptr(deltas, "deltas", torch.int32), n, _dptr(out, "cs_out"), _stream(stream)),
+           "debug_rope")
+    return out
 
 
 def device_status(clear: bool = True) -> int:

@@ -22,17 +22,22 @@ def _clean_status():
 # ---------------------------------------------------------------- rotation table
 
 @pytest.mark.parametrize("d,theta", [(64, 1e4), (128, 5e5)])
-def test_rope_table_entries(d, theta):
+def test_rotation_matches_fp64(d, theta):
+    # cos/sin of n * w_i as the kernels evaluate them, against numpy fp64.
     L = la()
     p = L.make_params(num_seqs=1, num_q_heads=1, num_kv_heads=1, head_dim=d, num_pool_blocks=1,
                       max_blocks_per_seq=1, rope_theta=theta)
-    t = L.rope_table_init(p).view(torch.float32).view(2, 1024, d // 2, 2).cpu().double().numpy()
+    table = L.rope_table_init(p)
+    t = table.view(torch.float32).view(d // 2, 2).cpu().double().numpy()
     w = theta ** (-2.0 * np.arange(d // 2) / d)
-    n = np.arange(1024)
-    for lvl, scale in ((0, 1.0), (1, 1024.0)):
-        ang = (n[:, None] * scale) * w[None, :]
-        assert np.abs(t[lvl, :, :, 0] - np.cos(ang)).max() < 1e-7
-        assert np.abs(t[lvl, :, :, 1] - np.sin(ang)).max() < 1e-7
+    assert np.abs((t[:, 0] + t[:, 1]) * 2 * np.pi / w - 1).max() < 1e-14
+    rng = np.random.default_rng(9)
+    deltas = np.concatenate([np.arange(-5, 300), rng.integers(-(1 << 24) + 1, 1 << 24, 3000),
+                             [131072, 131071, 4160, 16384, (1 << 24) - 1, -(1 << 24) + 1]]).astype(np.int32)
+    cs = L.debug_rope(p, table, torch.from_numpy(deltas).cuda()).cpu().double().numpy()
+    ang = deltas[:, None].astype(np.float64) * w[None, :]
+    err = max(np.abs(cs[..., 0] - np.cos(ang)).max(), np.abs(cs[..., 1] - np.sin(ang)).max())
+    assert err < 1e-6, err
 
 
 # ---------------------------------------------------------------- packer and gather
@@ -142,6 +147,13 @@ def test_bf16_decode_split_sweep(splits):
     w = W.decode_zipf("splits", batch=3, hq=32, hkv=8, d=128, docs_per_seq=8, doc_tokens=96, pool_docs=10,
                       zipf_s=1.0, suffix_tokens=16, seed=61)
     _check_decode(w, num_splits=splits)
+
+
+def test_fp32_decode_long_context():
+    # offsets up to ~100k exercise the rotation far from the document start (fp32: 1e-5)
+    w = W.decode_zipf("f32long", batch=1, hq=4, hkv=1, d=128, theta=5e5, docs_per_seq=24, doc_tokens=4096,
+                      pool_docs=24, zipf_s=0.0, dtype="f32", seed=68)
+    _check_decode(w)
 
 
 def test_fp32_decode_gqa():
