@@ -1,0 +1,100 @@
+"""GPU parity of the tcgen05 prefill kernel against the CPU oracle (through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from brute import rope
+from gpu_util import assert_close, la, prefill, to_device
+from paged_kv_cache_57_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clean_status():
+    la().device_status(clear=True)
+    yield
+    assert la().device_status(clear=True) == 0, "device status word set"
+
+
+def _check(w, rows=None, lazy=True, k_pool=None):
+    dv = to_device(w, lazy=lazy, k_pool=k_pool)
+    out = prefill(dv)
+    ref = oracle.attention(w, rows=rows)
+    got = out if rows is None else out[torch.as_tensor(rows, device=out.device)]
+    return assert_close(got, ref, w.dtype, w.name)
+
+
+def test_prefill_single_tile():
+    w = W.prefill_zipf("p1", batch=1, hq=4, hkv=2, docs_per_seq=2, doc_tokens=64, pool_docs=3, zipf_s=1.0,
+                       chunk_tokens=128, seed=71)
+    _check(w)
+
+
+@pytest.mark.parametrize("chunks", [[1], [17, 130], [128, 256], [255, 3, 64]])
+def test_prefill_varlen_chunks(chunks):
+    w = W.prefill_zipf("pv", batch=len(chunks), hq=8, hkv=2, docs_per_seq=3, doc_tokens=200, pool_docs=5,
+                       zipf_s=1.2, chunk_tokens=chunks, seed=72 + len(chunks))
+    _check(w)
+
+
+def test_prefill_chunk_only_is_causal():
+    w = W.prefill_zipf("pc", batch=2, hq=4, hkv=4, docs_per_seq=0, doc_tokens=16, pool_docs=1, zipf_s=1.0,
+                       chunk_tokens=[300, 45], seed=74)
+    _check(w)
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (32, 1), (8, 8)])
+def test_prefill_gqa(hq, hkv):
+    w = W.prefill_zipf("pg", batch=2, hq=hq, hkv=hkv, docs_per_seq=2, doc_tokens=300, pool_docs=4, zipf_s=1.2,
+                       chunk_tokens=[200, 129], seed=75 + hq + hkv)
+    _check(w)
+
+
+def test_prefill_holes_and_partial_blocks():
+    _, p = W.mixed_mqa(n_decode=1, n_prefill=3, chunk=150, hq=8, hkv=1, pool_docs=60, ctx_lo=100, ctx_hi=3000,
+                       doc_lo=5, doc_hi=300, seed=76)
+    _check(p)
+
+
+def test_prefill_shift_invariance():
+    kw = dict(batch=2, hq=8, hkv=2, docs_per_seq=2, doc_tokens=96, pool_docs=3, zipf_s=1.0, chunk_tokens=[100, 37],
+              seed=77)
+    a = prefill(to_device(W.prefill_zipf("s0", **kw))).float().cpu().numpy()
+    ref = oracle.attention(W.prefill_zipf("s0", **kw))
+    for c in (16, 5000, 100000):
+        b = prefill(to_device(W.prefill_zipf("sc", shift=c, **kw)))
+        assert_close(b, ref, "bf16", f"shift {c}")
+    assert np.isfinite(a).all()
+
+
+def test_prefill_lazy0_control_on_materialised_pool():
+    w = W.prefill_zipf("pctl", batch=2, hq=8, hkv=2, docs_per_seq=2, doc_tokens=80, pool_docs=500, zipf_s=0.0,
+                       chunk_tokens=[70, 33], seed=78)
+    # distinct documents per sequence so that each pool block has one absolute position
+    assert len(set(w.seg_doc.tolist())) == len(w.seg_doc)
+    kabs = w.k_pool.double().clone()
+    for s in range(w.num_seqs):
+        p = 0
+        for doc, Ln in w.seq_segments(s):
+            for phys in w.doc_blocks[w.doc_block_indptr[doc]:w.doc_block_indptr[doc + 1]]:
+                kabs[phys] = torch.from_numpy(rope(kabs[phys].numpy(), p, w.rope_theta))
+            p += Ln
+    _check(w, lazy=False, k_pool=kabs.to(torch.bfloat16))
+
+
+def test_llama8b_prefill_full_sampled():
+    w = W.FULL["llama8b_prefill"]()
+    rng = np.random.default_rng(3)
+    cu = w.cu_seqlens_q
+    rows = sorted(set(int(cu[s]) + int(x) for s in range(w.num_seqs)
+                      for x in rng.choice(int(cu[s + 1] - cu[s]), 16, replace=False)))
+    _check(w, rows=rows)
+
+
+def test_mixed_prefill_full_sampled():
+    _, p = W.mixed_mqa()
+    rng = np.random.default_rng(4)
+    rows = sorted(int(x) for x in rng.choice(p.q.shape[0], 24, replace=False))
+    _check(p, rows=rows)
