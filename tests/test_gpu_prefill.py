@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from brute import rope
-from gpu_util import assert_close, la, prefill, to_device
+from gpu_util import assert_close, few_key_slack, la, prefill, to_device
 from paged_kv_cache_57_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -23,7 +23,7 @@ def _check(w, rows=None, lazy=True, k_pool=None):
     out = prefill(dv)
     ref = oracle.attention(w, rows=rows)
     got = out if rows is None else out[torch.as_tensor(rows, device=out.device)]
-    return assert_close(got, ref, w.dtype, w.name)
+    return assert_close(got, ref, w.dtype, w.name, slack=few_key_slack(w, rows))
 
 
 def test_prefill_single_tile():
@@ -62,10 +62,12 @@ def test_prefill_shift_invariance():
     kw = dict(batch=2, hq=8, hkv=2, docs_per_seq=2, doc_tokens=96, pool_docs=3, zipf_s=1.0, chunk_tokens=[100, 37],
               seed=77)
     a = prefill(to_device(W.prefill_zipf("s0", **kw))).float().cpu().numpy()
-    ref = oracle.attention(W.prefill_zipf("s0", **kw))
+    w0 = W.prefill_zipf("s0", **kw)
+    ref = oracle.attention(w0)
     for c in (16, 5000, 100000):
-        b = prefill(to_device(W.prefill_zipf("sc", shift=c, **kw)))
-        assert_close(b, ref, "bf16", f"shift {c}")
+        # a shift of 100000 needs a wider offset field: 12 id bits leave 20 signed bits
+        b = prefill(to_device(W.prefill_zipf("sc", shift=c, **kw), id_bits=12 if c > 8000 else 0))
+        assert_close(b, ref, "bf16", f"shift {c}", slack=few_key_slack(w0))
     assert np.isfinite(a).all()
 
 
