@@ -11,7 +11,7 @@
 // is what turns a 16-token block into a small dense contraction).
 //
 // The CTA is TEAMS independent teams of MT warps (MT = row tiles of 16 heads).
-// Team t owns the split's logical blocks t, t+TEAMS, t+2*TEAMS, ... and a ring
+// Team t owns a contiguous quarter of the split's logical blocks and a ring
 // of SPT shared-memory stages; it is its own loader: as soon as it has consumed
 // a stage it refills it (one TMA box per 64 columns of K and of V, 128-byte
 // swizzle) with its block SPT positions ahead. There is no producer warp and no
@@ -196,11 +196,15 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS)
   __syncthreads();
 
   // ------------------------------------------------------------ team setup
-  const int nk = team < n ? (n - team + C::TEAMS - 1) / C::TEAMS : 0;  // blocks of this team
+  // Team t owns a contiguous quarter of the split, so a warp meets only the
+  // document boundaries inside its own range (each costs a q re-rotation).
+  const int per_team = (n + C::TEAMS - 1) / C::TEAMS;
+  const int kb0 = team * per_team;
+  const int nk = max(0, min(n, kb0 + per_team) - kb0);  // blocks of this team
   uint8_t* tst = stages + team * SPT * C::STAGE_BYTES;
   uint64_t* tfull = full + team * SPT;
   const bool leader = (mt == 0 && lane == 0);
-  auto block_of = [&](int k) { return b0 + team + k * C::TEAMS; };
+  auto block_of = [&](int k) { return b0 + kb0 + k; };
   auto load_words = [&](int kc, uint32_t& w, uint32_t& wn) {
     const int k = kc + lane, b = block_of(k);
     w = k < nk ? __ldg(&wrow[b]) : 0u;
@@ -258,15 +262,16 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS)
     const int slot = k % SPT;
     const int p = __shfl_sync(0xffffffffu, cur.p, k & 31);
     const int nvalid = __shfl_sync(0xffffffffu, cur.nv, k & 31);
-    if (!warp_wait(&tfull[slot], (k / SPT) & 1, a.status)) {
-      abort_flag = 1;
-      break;
-    }
     if constexpr (LAZY) {
+      // p comes from the block word, so the re-rotation overlaps the block's load.
       if (p != p_prev) {
         rebuild(m_pos - p);
         p_prev = p;
       }
+    }
+    if (!warp_wait(&tfull[slot], (k / SPT) & 1, a.status)) {
+      abort_flag = 1;
+      break;
     }
     const uint32_t kbase = smem_u32(tst + slot * C::STAGE_BYTES);
     const uint32_t vbase = kbase + C::KV_BYTES;

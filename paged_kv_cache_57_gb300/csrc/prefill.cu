@@ -9,19 +9,21 @@
 // matrix products, i.e. 3/(4M): 0.59% at M = 128.
 //
 // One CTA = one 128-row query tile of one q-head of one chunk. Warp roles:
-//   warps 0-3  softmax: rotate the Q tile once (thread = row), then per K tile
+//   warps 0-3  softmax: rotate the Q tile once (thread = row), then per key tile
 //              read S from TMEM, mask (holes; causal inside the chunk), online
-//              (max, sum) softmax ("Flash Attention -- tiling"), write P (bf16,
-//              128-byte swizzled K-major) to shared memory, rescale O in TMEM;
-//              finally O / l -> bf16 -> global.
-//   warps 4-7  rotation: rotate every 16-row K block of a landed tile in shared
-//              memory by R_p (fp32 math, bf16 result) and zero V rows of hole
-//              slots, then hand the tile to the MMA warp.
-//   warp 8     TMA producer: Q tile, then per tile 8 blocks x (K, V) x 2 boxes
-//              of 16 rows x 64 columns, into a ring of PF_NS stages.
+//              (max, sum) softmax ("Flash Attention -- tiling") with the running
+//              maximum refreshed only when it grows by more than 2^8, write P
+//              (bf16, 128-byte swizzled K-major) to shared memory, rescale O in
+//              TMEM when needed; finally O / l -> bf16 -> global.
+//   warps 4-7  rotation: rotate each 16-row K block of a landed tile in shared
+//              memory by R_p (fp32 math, bf16 result); zero V rows of hole slots.
+//   warp 8     TMA producer: Q tile; K tiles into a 3-stage ring and V tiles into
+//              a 2-stage ring (8 blocks x 2 boxes of 16 rows x 64 columns each).
 //   warp 9     TMEM owner and MMA issuer: S = Q K^T (M=N=128, K=d) into TMEM
-//              columns [0,128), O += P V into columns [128,256); S of the next
-//              tile is issued while the softmax works on the current one.
+//              columns [0,128), O += P V into columns [128,256). It issues each
+//              product as soon as its inputs are ready, so the S of the next tile
+//              overlaps the softmax of the current one, and frees K stages right
+//              after their S and V stages right after their P V.
 #include <climits>
 
 #include "kernels.h"
@@ -31,32 +33,38 @@ namespace lazy {
 
 namespace {
 
-constexpr int PF_BM = 128;                      // query rows per tile (MMA M)
-constexpr int PF_BN = 128;                      // keys per tile (MMA N of S)
-constexpr int PF_D = 128;                       // head dim
-constexpr int PF_NS = 2;                        // K/V stages
-constexpr int PF_BLOCKS = PF_BN / kBlock;       // 8 blocks per key tile
-constexpr int PF_HALF = PF_BM * 128;            // one 64-column half of a 128-row tile (bytes)
-constexpr int PF_TILE = 2 * PF_HALF;            // 32 KiB
+constexpr int PF_BM = 128;                 // query rows per tile (MMA M)
+constexpr int PF_BN = 128;                 // keys per tile (MMA N of S)
+constexpr int PF_D = 128;                  // head dim
+constexpr int PF_NK = 3;                   // K stages
+constexpr int PF_NV = 2;                   // V stages
+constexpr int PF_BLOCKS = PF_BN / kBlock;  // 8 blocks per key tile
+constexpr int PF_HALF = PF_BM * 128;       // one 64-column half of a 128-row tile (bytes)
+constexpr int PF_TILE = 2 * PF_HALF;       // 32 KiB
 constexpr int PF_THREADS = 320;
 constexpr int PF_TMEM_COLS = 256;
+constexpr float PF_RESCALE_LOG2 = 8.f;     // refresh the running max when it grows by more than this
 
-struct PfBlockMeta {
-  int p;         // document start position
-  int nvalid;    // valid slots (0 for blocks past the sequence or with a bad id)
+struct PfKMeta {
+  int p;       // document start position
+  int nvalid;  // valid slots (0 for blocks past the sequence or with a bad id)
+};
+struct PfVMeta {
+  int nvalid;
   int chunk_j0;  // chunk-local index of the block's first key, or -1 for cached documents
-  int pad;
 };
 
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + PF_TILE;
-constexpr int OFF_V = OFF_K + PF_NS * PF_TILE;
-constexpr int OFF_P = OFF_V + PF_NS * PF_TILE;
-constexpr int OFF_META = OFF_P + PF_TILE;
-constexpr int OFF_BAR = OFF_META + PF_NS * PF_BLOCKS * (int)sizeof(PfBlockMeta);
-constexpr int NBARS = 2 + 3 * PF_NS + 5;
+constexpr int OFF_V = OFF_K + PF_NK * PF_TILE;
+constexpr int OFF_P = OFF_V + PF_NV * PF_TILE;
+constexpr int OFF_KMETA = OFF_P + PF_TILE;
+constexpr int OFF_VMETA = OFF_KMETA + PF_NK * PF_BLOCKS * (int)sizeof(PfKMeta);
+constexpr int OFF_BAR = OFF_VMETA + PF_NV * PF_BLOCKS * (int)sizeof(PfVMeta);
+constexpr int NBARS = 2 + 3 * PF_NK + 3 * PF_NV + 5;
 constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
 constexpr int PF_SMEM = 1024 + OFF_TMEM + 16;
+static_assert(PF_SMEM <= 227 * 1024, "prefill shared memory");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -67,19 +75,44 @@ __device__ __forceinline__ bool warp_wait_pf(uint64_t* bar, uint32_t parity, uns
   return __all_sync(0xffffffffu, ok);
 }
 
-// Rotates 8 rotate-half pairs held as two 16-byte chunks (x: dims i, y: dims i + 64).
-__device__ __forceinline__ void rotate_chunk(uint4& X, uint4& Y, const float2 (&cs)[8]) {
+// 2^x on the SFU (PTX ex2.approx, flush-to-zero); 2^-inf = +0.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Rotation coefficients of 8 consecutive frequencies as packed fp32 pairs
+// (cos, sin, -sin), each multiplied by `scale`.
+struct Rot8 {
+  uint64_t c[4], s[4], ns[4];
+};
+
+__device__ __forceinline__ Rot8 make_rot8(const float2 (&cs)[8], float scale) {
+  Rot8 r;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 a = cs[2 * k], b = cs[2 * k + 1];
+    r.c[k] = f2(a.x * scale, b.x * scale);
+    r.s[k] = f2(a.y * scale, b.y * scale);
+    r.ns[k] = f2(-a.y * scale, -b.y * scale);
+  }
+  return r;
+}
+
+// Rotates 8 rotate-half pairs held as two 16-byte bf16 chunks (x: dims i, y: dims
+// i + 64): x' = x c - y s, y' = y c + x s on packed fp32 pairs, rounded to bf16.
+__device__ __forceinline__ void rotate_chunk(uint4& X, uint4& Y, const Rot8& R) {
   uint32_t* xw = reinterpret_cast<uint32_t*>(&X);
   uint32_t* yw = reinterpret_cast<uint32_t*>(&Y);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xw[k]));
-    const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&yw[k]));
-    const float2 c0 = cs[2 * k], c1 = cs[2 * k + 1];
-    const float x0 = fmaf(x.x, c0.x, -y.x * c0.y), y0 = fmaf(y.x, c0.x, x.x * c0.y);
-    const float x1 = fmaf(x.y, c1.x, -y.y * c1.y), y1 = fmaf(y.y, c1.x, x.y * c1.y);
-    xw[k] = pack_bf16x2(x0, x1);
-    yw[k] = pack_bf16x2(y0, y1);
+    const uint64_t x2 = f2(__uint_as_float(xw[k] << 16), __uint_as_float(xw[k] & 0xffff0000u));
+    const uint64_t y2 = f2(__uint_as_float(yw[k] << 16), __uint_as_float(yw[k] & 0xffff0000u));
+    const float2 xn = f2_split(f2_fma(y2, R.ns[k], f2_mul(x2, R.c[k])));
+    const float2 yn = f2_split(f2_fma(x2, R.s[k], f2_mul(y2, R.c[k])));
+    xw[k] = pack_bf16x2(xn.x, xn.y);
+    yw[k] = pack_bf16x2(yn.x, yn.y);
   }
 }
 
@@ -95,14 +128,18 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   uint8_t* sK = base + OFF_K;
   uint8_t* sV = base + OFF_V;
   uint8_t* sP = base + OFF_P;
-  PfBlockMeta* meta = reinterpret_cast<PfBlockMeta*>(base + OFF_META);
+  PfKMeta* kmeta = reinterpret_cast<PfKMeta*>(base + OFF_KMETA);
+  PfVMeta* vmeta = reinterpret_cast<PfVMeta*>(base + OFF_VMETA);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + OFF_BAR);
   uint64_t* q_full = bars;
   uint64_t* q_ready = bars + 1;
-  uint64_t* kv_full = bars + 2;
-  uint64_t* kv_ready = kv_full + PF_NS;
-  uint64_t* kv_empty = kv_ready + PF_NS;
-  uint64_t* s_full = kv_empty + PF_NS;
+  uint64_t* k_full = bars + 2;
+  uint64_t* k_ready = k_full + PF_NK;
+  uint64_t* k_empty = k_ready + PF_NK;
+  uint64_t* v_full = k_empty + PF_NK;
+  uint64_t* v_ready = v_full + PF_NV;
+  uint64_t* v_empty = v_ready + PF_NV;
+  uint64_t* s_full = v_empty + PF_NV;
   uint64_t* s_free = s_full + 1;
   uint64_t* p_full = s_free + 1;
   uint64_t* pv_done = p_full + 1;
@@ -137,10 +174,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     abort_flag = 0;
     mbar_init(q_full, 1);
     mbar_init(q_ready, 128);
-    for (int i = 0; i < PF_NS; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_ready[i], 128);
-      mbar_init(&kv_empty[i], 1);
+    for (int i = 0; i < PF_NK; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_ready[i], 128);
+      mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < PF_NV; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_ready[i], 128);
+      mbar_init(&v_empty[i], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(s_free, 128);
@@ -169,66 +211,99 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       tma_load_3d(sQ, &qmap, q_full, 0, h, q0 + row0);
       tma_load_3d(sQ + PF_HALF, &qmap, q_full, 64, h, q0 + row0);
     }
-    int issued = 0;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int st = j % PF_NS;
-      if (j >= PF_NS && !warp_wait_pf(&kv_empty[st], ((j / PF_NS) & 1) ^ 1, a.status)) {
-        abort_flag = 1;
-        break;
-      }
-      // lanes 0..7: the tile's blocks; lane 8: the block after (hole rule)
+    // Lane l < 8 describes block l of a tile; lane 8 reads the block after (hole rule).
+    struct Lane {
+      int p, nv, y, j0;
+    };
+    auto describe = [&](int j) {
       const int b = j * PF_BLOCKS + min(lane, PF_BLOCKS);
       const uint32_t w = (lane <= PF_BLOCKS && b < nb) ? __ldg(&wrow[b]) : 0u;
       const BlockInfo bi = decode_word(w, b, a.id_bits);
       const int p_after = __shfl_down_sync(0xffffffffu, bi.p, 1);
-      int nv = 0, y = -kBlock, j0 = -1;
+      Lane r{bi.p, 0, -kBlock, -1};  // rows of an invalid block start at -16: read as zeros
       if (lane < PF_BLOCKS && b < nb) {
-        nv = block_valid(b, nb, seq_len, bi.p, b + 1 < nb ? p_after : bi.p);
+        int nv = block_valid(b, nb, seq_len, bi.p, b + 1 < nb ? p_after : bi.p);
         nv = nv < 0 ? 0 : (nv > kBlock ? kBlock : nv);
         if (bi.phys < a.num_pool_blocks) {
-          y = (bi.phys * a.Hkv + kvh) * kBlock;
+          r.y = (bi.phys * a.Hkv + kvh) * kBlock;
         } else {
           raise_status(a.status, LAZY_DEV_BAD_BLOCK_ID);
           nv = 0;
         }
-        j0 = b >= b_chunk ? kBlock * (b - b_chunk) : -1;
+        r.nv = nv;
+        r.j0 = b >= b_chunk ? kBlock * (b - b_chunk) : -1;
       }
-      if (lane < PF_BLOCKS) meta[st * PF_BLOCKS + lane] = PfBlockMeta{bi.p, nv, j0, 0};
+      return r;
+    };
+    auto issue_k = [&](int j, const Lane& d) -> bool {
+      const int st = j % PF_NK;
+      if (j >= PF_NK && !warp_wait_pf(&k_empty[st], ((j / PF_NK) & 1) ^ 1, a.status)) return false;
+      if (lane < PF_BLOCKS) kmeta[st * PF_BLOCKS + lane] = PfKMeta{d.p, d.nv};
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], 2 * PF_TILE);
+      if (lane == 0) mbar_arrive_expect_tx(&k_full[st], PF_TILE);
       __syncwarp();
-      if (lane < PF_BLOCKS) {  // rows of an invalid block start at -16: read as zeros
+      if (lane < PF_BLOCKS) {
         uint8_t* kd = sK + st * PF_TILE + lane * (kBlock * 128);
-        uint8_t* vd = sV + st * PF_TILE + lane * (kBlock * 128);
-        tma_load_2d(kd, &kmap, &kv_full[st], 0, y);
-        tma_load_2d(kd + PF_HALF, &kmap, &kv_full[st], 64, y);
-        tma_load_2d(vd, &vmap, &kv_full[st], 0, y);
-        tma_load_2d(vd + PF_HALF, &vmap, &kv_full[st], 64, y);
+        tma_load_2d(kd, &kmap, &k_full[st], 0, d.y);
+        tma_load_2d(kd + PF_HALF, &kmap, &k_full[st], 64, d.y);
       }
-      issued = j + 1;
+      return true;
+    };
+    auto issue_v = [&](int j, const Lane& d) -> bool {
+      const int st = j % PF_NV;
+      if (j >= PF_NV && !warp_wait_pf(&v_empty[st], ((j / PF_NV) & 1) ^ 1, a.status)) return false;
+      if (lane < PF_BLOCKS) vmeta[st * PF_BLOCKS + lane] = PfVMeta{d.nv, d.j0};
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&v_full[st], PF_TILE);
+      __syncwarp();
+      if (lane < PF_BLOCKS) {
+        uint8_t* vd = sV + st * PF_TILE + lane * (kBlock * 128);
+        tma_load_2d(vd, &vmap, &v_full[st], 0, d.y);
+        tma_load_2d(vd + PF_HALF, &vmap, &v_full[st], 64, d.y);
+      }
+      return true;
+    };
+    int k_issued = 0, v_issued = 0;
+    bool ok = true;
+    Lane prev{};
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const Lane cur = describe(j);
+      ok = issue_k(j, cur);
+      if (ok) k_issued = j + 1;
+      if (ok && j >= 1) {
+        ok = issue_v(j - 1, prev);
+        if (ok) v_issued = j;
+      }
+      prev = cur;
     }
-    if (lane == 0) {
+    if (ok && n_tiles > 0) {
+      ok = issue_v(n_tiles - 1, prev);
+      if (ok) v_issued = n_tiles;
+    }
+    if (!ok) abort_flag = 1;
+    if (lane == 0) {  // every copy issued must land before the CTA exits (bounded)
       mbar_wait(q_full, 0, a.status);
-      for (int j = max(0, issued - PF_NS); j < issued; ++j)
-        mbar_wait(&kv_full[j % PF_NS], (j / PF_NS) & 1, a.status);
+      for (int j = max(0, k_issued - PF_NK); j < k_issued; ++j) mbar_wait(&k_full[j % PF_NK], (j / PF_NK) & 1, a.status);
+      for (int j = max(0, v_issued - PF_NV); j < v_issued; ++j) mbar_wait(&v_full[j % PF_NV], (j / PF_NV) & 1, a.status);
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && n_tiles > 0) {
       constexpr uint32_t idS = idesc_bf16_f32(PF_BM, PF_BN, false);
       constexpr uint32_t idO = idesc_bf16_f32(PF_BM, PF_D, true);
       const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP);
-      auto issue_S = [&](int j) {
-        const uint32_t k_addr = smem_u32(sK + (j % PF_NS) * PF_TILE);
+      auto issue_s = [&](int j) {
+        const uint32_t k_addr = smem_u32(sK + (j % PF_NK) * PF_TILE);
 #pragma unroll
         for (int ks = 0; ks < PF_D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * PF_HALF + (ks & 3) * 32;
           tc_mma(tS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idS, ks > 0);
         }
         tc_commit(s_full);
+        tc_commit(&k_empty[j % PF_NK]);
       };
-      auto issue_PV = [&](int j) {
-        const uint32_t v_addr = smem_u32(sV + (j % PF_NS) * PF_TILE);
+      auto issue_pv = [&](int j) {
+        const uint32_t v_addr = smem_u32(sV + (j % PF_NV) * PF_TILE);
 #pragma unroll
         for (int ks = 0; ks < PF_BN / 16; ++ks) {
           const uint32_t poff = (ks >> 2) * PF_HALF + (ks & 3) * 32;
@@ -236,84 +311,110 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                  (j > 0 || ks > 0) ? 1u : 0u);
         }
         tc_commit(pv_done);
-        tc_commit(&kv_empty[j % PF_NS]);
+        tc_commit(&v_empty[j % PF_NV]);
       };
-      bool ok = n_tiles > 0 && mbar_wait(q_ready, 0, a.status) && mbar_wait(&kv_ready[0], 0, a.status);
+      // Blocking waits (the thread sleeps instead of spinning on issue slots that
+      // the softmax warps need). K runs PF_NK tiles ahead, so S(j+1) is rarely held
+      // back by a load and the order S(j+1), P V(j) keeps the tensor pipe fed.
+      bool ok = mbar_wait(q_ready, 0, a.status) && mbar_wait(&k_ready[0], 0, a.status);
       if (ok) {
         tc_fence_after();
-        issue_S(0);
+        issue_s(0);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
         if (j + 1 < n_tiles) {
-          ok = mbar_wait(&kv_ready[(j + 1) % PF_NS], ((j + 1) / PF_NS) & 1, a.status) &&
+          ok = mbar_wait(&k_ready[(j + 1) % PF_NK], ((j + 1) / PF_NK) & 1, a.status) &&
                mbar_wait(s_free, j & 1, a.status);
           if (!ok) break;
           tc_fence_after();
-          issue_S(j + 1);
+          issue_s(j + 1);
         }
-        ok = mbar_wait(p_full, j & 1, a.status);
+        ok = mbar_wait(p_full, j & 1, a.status) && mbar_wait(&v_full[j % PF_NV], (j / PF_NV) & 1, a.status) &&
+             mbar_wait(&v_ready[j % PF_NV], (j / PF_NV) & 1, a.status);
         if (!ok) break;
         tc_fence_after();
-        issue_PV(j);
+        issue_pv(j);
       }
-      if (!ok && n_tiles > 0) abort_flag = 1;
+      if (!ok) abort_flag = 1;
       tc_commit(mma_drain);
       mbar_wait(mma_drain, 0, a.status);
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // ---------------------------------------------------------------- K rotation
+    // ---------------------------------------------------------------- K rotation, V holes
     const int t = threadIdx.x - 128;
     const int c = t & 7, r = t >> 3;  // 16-byte chunk (8 frequencies) and row within a block
-    float2 tr[8], cs[8];
+    float2 tr[8];
+    Rot8 rot;
     if constexpr (LAZY) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) tr[e] = __ldg(&a.rope[8 * c + e]);
     }
     int p_cached = INT_MIN;
     for (int j = 0; j < n_tiles; ++j) {
-      const int st = j % PF_NS;
-      if (!warp_wait_pf(&kv_full[st], (j / PF_NS) & 1, a.status)) {
+      const int st = j % PF_NK;
+      if (!warp_wait_pf(&k_full[st], (j / PF_NK) & 1, a.status)) {
         abort_flag = 1;
         break;
       }
       uint8_t* kt = sK + st * PF_TILE;
-      uint8_t* vt = sV + st * PF_TILE;
+      bool holes = false;
 #pragma unroll 1
       for (int bl = 0; bl < PF_BLOCKS; ++bl) {
-        const PfBlockMeta m = meta[st * PF_BLOCKS + bl];
-        const uint32_t off = bl * (kBlock * 128) + sw128(r, c);
+        const PfKMeta m = kmeta[st * PF_BLOCKS + bl];
+        holes |= m.nvalid < kBlock;
         if constexpr (LAZY) {
           if (m.nvalid > 0) {
             if (m.p != p_cached) {
+              float2 cs[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) cs[e] = rope_cs(tr[e], m.p, a.status);
+              rot = make_rot8(cs, 1.f);
               p_cached = m.p;
             }
+            const uint32_t off = bl * (kBlock * 128) + sw128(r, c);
             uint4 X = *reinterpret_cast<uint4*>(kt + off);
             uint4 Y = *reinterpret_cast<uint4*>(kt + PF_HALF + off);
-            rotate_chunk(X, Y, cs);
+            rotate_chunk(X, Y, rot);
             *reinterpret_cast<uint4*>(kt + off) = X;
             *reinterpret_cast<uint4*>(kt + PF_HALF + off) = Y;
           }
         }
-        if (r >= m.nvalid) {  // hole slot: its V row may hold anything
-          *reinterpret_cast<uint4*>(vt + off) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(vt + PF_HALF + off) = make_uint4(0, 0, 0, 0);
-        }
       }
       fence_proxy_async_smem();
-      mbar_arrive(&kv_ready[st]);
+      mbar_arrive(&k_ready[st]);
+      // V rows of hole slots may hold anything: zero them. v_ready(j) is arrived only
+      // after V(j) has landed, so this warpgroup can never complete a v_ready phase
+      // two tiles ahead of the MMA warp (V(j+2) needs the P V of tile j first).
+      const int vs = j % PF_NV;
+      if (!warp_wait_pf(&v_full[vs], (j / PF_NV) & 1, a.status)) {
+        abort_flag = 1;
+        break;
+      }
+      if (__any_sync(0xffffffffu, holes)) {
+        uint8_t* vt = sV + vs * PF_TILE;
+#pragma unroll 1
+        for (int bl = 0; bl < PF_BLOCKS; ++bl) {
+          if (r >= vmeta[vs * PF_BLOCKS + bl].nvalid) {
+            const uint32_t off = bl * (kBlock * 128) + sw128(r, c);
+            *reinterpret_cast<uint4*>(vt + off) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vt + PF_HALF + off) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      mbar_arrive(&v_ready[vs]);
     }
   } else {
     // ---------------------------------------------------------------- softmax
-    const int i = threadIdx.x;        // query row within the tile == TMEM lane
-    const int iq = row0 + i;          // query index within the chunk
+    const int i = threadIdx.x;  // query row within the tile == TMEM lane
+    const int iq = row0 + i;    // query index within the chunk
     const int m_pos = a.q_start[s] + iq;
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
     bool ok = warp_wait_pf(q_full, 0, a.status);
     if (ok) {
-      // Q prologue: q_i' = R_{m_i} q_i, once per tile.
+      // Q prologue: q_i' = R_{m_i} q_i, once per tile, pre-scaled by the softmax
+      // scale * log2(e) so that S comes out of the tensor core in log2 units.
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         float2 cs[8];
@@ -321,17 +422,16 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         for (int e = 0; e < 8; ++e) cs[e] = rope_cs(__ldg(&a.rope[8 * c + e]), m_pos, a.status);
         uint4 X = *reinterpret_cast<uint4*>(sQ + sw128(i, c));
         uint4 Y = *reinterpret_cast<uint4*>(sQ + PF_HALF + sw128(i, c));
-        rotate_chunk(X, Y, cs);
+        rotate_chunk(X, Y, make_rot8(cs, a.scale_log2));
         *reinterpret_cast<uint4*>(sQ + sw128(i, c)) = X;
         *reinterpret_cast<uint4*>(sQ + PF_HALF + sw128(i, c)) = Y;
       }
       fence_proxy_async_smem();
     }
     mbar_arrive(q_ready);
-    const float sl2 = a.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; ok && j < n_tiles; ++j) {
-      const int st = j % PF_NS;
+      const int vs = j % PF_NV;
       ok = warp_wait_pf(s_full, j & 1, a.status);
       if (!ok) break;
       tc_fence_after();
@@ -341,49 +441,73 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(s_free);
-      ok = warp_wait_pf(&kv_full[st], (j / PF_NS) & 1, a.status);  // block metadata of this tile
+      ok = warp_wait_pf(&v_full[vs], (j / PF_NV) & 1, a.status);  // block metadata of this tile
       if (!ok) break;
-      float mx = -INFINITY;
+      // Masks only where a tile has hole slots or chunk keys (uniform per tile).
+      bool full_tile = true;
 #pragma unroll
       for (int bl = 0; bl < PF_BLOCKS; ++bl) {
-        const PfBlockMeta m = meta[st * PF_BLOCKS + bl];
-        int lim = m.nvalid;
-        if (m.chunk_j0 >= 0) lim = max(0, min(lim, iq - m.chunk_j0 + 1));
+        const PfVMeta m = vmeta[vs * PF_BLOCKS + bl];
+        full_tile &= (m.nvalid == kBlock) & (m.chunk_j0 < 0);
+      }
+      float mx = -INFINITY;
+      if (full_tile) {
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
 #pragma unroll
-        for (int t = 0; t < kBlock; ++t) {
-          const int kk = bl * kBlock + t;
-          float& v = sv[kk >> 5][kk & 31];
-          v = t < lim ? v * sl2 : -INFINITY;
-          mx = fmaxf(mx, v);
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) m4[q] = fmax3(m4[q], sv[q][k], sv[q][k + 1]);
+        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      } else {
+#pragma unroll
+        for (int bl = 0; bl < PF_BLOCKS; ++bl) {
+          const PfVMeta m = vmeta[vs * PF_BLOCKS + bl];
+          int lim = m.nvalid;
+          if (m.chunk_j0 >= 0) lim = max(0, min(lim, iq - m.chunk_j0 + 1));
+#pragma unroll
+          for (int t = 0; t < kBlock; ++t) {
+            const int kk = bl * kBlock + t;
+            float& v = sv[kk >> 5][kk & 31];
+            v = t < lim ? v : -INFINITY;
+            mx = fmaxf(mx, v);
+          }
         }
       }
-      const float m_new = fmaxf(m_run, mx);
-      const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = exp2f(m_run - m_use);
-      m_run = m_new;
-      // P: wait until the previous P V product has consumed the buffer.
+      // Refresh the running maximum only when it grows by more than 2^8 (weights stay <= 256).
+      float alpha = 1.f;
+      if (mx > m_run + PF_RESCALE_LOG2) {
+        alpha = m_run == -INFINITY ? 0.f : ex2(m_run - mx);
+        m_run = mx;
+      }
+      const float m_use = m_run == -INFINITY ? 0.f : m_run;
+      // P in registers first (bf16 pairs), so that only the stores wait for the
+      // previous P V product to release the buffer.
+      uint32_t pw[PF_BN / 2];
+      const uint64_t mm = f2(m_use, m_use);
+      uint64_t acc0 = f2(0.f, 0.f), acc1 = acc0;  // row sum of the fp32 weights, packed pairs
+#pragma unroll
+      for (int k = 0; k < PF_BN / 2; ++k) {
+        const int kk = 2 * k;
+        const float2 dv = f2_split(f2_sub(f2(sv[kk >> 5][kk & 31], sv[kk >> 5][(kk + 1) & 31]), mm));
+        const float e0 = ex2(dv.x), e1 = ex2(dv.y);
+        pw[k] = pack_bf16x2(e0, e1);
+        if (k & 1)
+          acc1 = f2_add(acc1, f2(e0, e1));
+        else
+          acc0 = f2_add(acc0, f2(e0, e1));
+      }
+      const float2 sacc = f2_split(f2_add(acc0, acc1));
+      l_run = l_run * alpha + (sacc.x + sacc.y);
       if (j > 0) {
         ok = warp_wait_pf(pv_done, (j - 1) & 1, a.status);
         if (!ok) break;
         tc_fence_after();
       }
-      float sum = 0.f;
 #pragma unroll
-      for (int c16 = 0; c16 < PF_BN / 8; ++c16) {
-        uint32_t wds[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int kk = c16 * 8 + 2 * k;
-          const uint32_t pk = pack_bf16x2(exp2f(sv[kk >> 5][kk & 31] - m_use), exp2f(sv[kk >> 5][(kk + 1) & 31] - m_use));
-          const float2 back = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk));
-          sum += back.x + back.y;
-          wds[k] = pk;
-        }
+      for (int c16 = 0; c16 < PF_BN / 8; ++c16)
         *reinterpret_cast<uint4*>(sP + (c16 >> 3) * PF_HALF + sw128(i, c16 & 7)) =
-            make_uint4(wds[0], wds[1], wds[2], wds[3]);
-      }
-      l_run = l_run * alpha + sum;
-      // Rescale the running output when this row's maximum grew (warp-uniform).
+            make_uint4(pw[4 * c16], pw[4 * c16 + 1], pw[4 * c16 + 2], pw[4 * c16 + 3]);
+      // Rescale the running output when this row's maximum was refreshed (warp-uniform).
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {

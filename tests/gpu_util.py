@@ -85,31 +85,29 @@ def visible_keys(w, rows=None) -> np.ndarray:
     return n if rows is None else n[np.asarray(rows)]
 
 
-FEW_KEYS = 128  # one key tile
-
-
-def few_key_slack(w, rows=None) -> np.ndarray:
-    """Extra allowance for rows that see fewer than FEW_KEYS keys. The bf16 tensor-core
-    path rounds the softmax weights P and the rotated query to bf16 (relative 2^-9
-    each); a weight perturbation of relative e moves the output by at most 2e * max|v|,
-    so each rounded operand contributes <= 2^-8 max|v|: 2^-7 max|v| for the two. With
-    many keys these errors average out and the stated tolerance holds; on short
-    contexts an output element near zero (values that cancel) can exceed it -- a plain
-    emulation of those two roundings shows the same excursions."""
-    n = visible_keys(w, rows)
-    vmax = float(np.nanmax(np.abs(w.v_pool.float().numpy())))
-    return np.where(n < FEW_KEYS, 2.0 ** -7 * vmax, 0.0)
-
-
-def assert_close(got: torch.Tensor, ref: np.ndarray, dtype: str, what: str = "", slack=None) -> float:
+def assert_close(got: torch.Tensor, ref: np.ndarray, dtype: str, what: str = "", emulate=None) -> float:
+    """Elementwise |gpu - ref| <= atol + rtol |ref| against the fp64 oracle. For bf16,
+    an element outside that bound passes only if it is within the same bound of the
+    bf16-operand emulation (tests/bf16_model.py) for its row: the deviation is then
+    the rounding of the tensor-core operands, not a wrong key, mask or rotation.
+    ``emulate(local_rows)`` returns the emulation for those rows of ``ref``."""
     g = got.detach().float().cpu().double().numpy()
     atol, rtol = TOL[dtype]
     err = np.abs(g - ref)
-    extra = 0.0 if slack is None else np.asarray(slack).reshape((-1,) + (1,) * (ref.ndim - 1))
-    bad = err > atol + rtol * np.abs(ref) + extra
+    bad = err > atol + rtol * np.abs(ref)
     assert np.isfinite(g).all(), f"{what}: non-finite output"
+    if bad.any() and emulate is not None:
+        rows = np.unique(np.nonzero(bad)[0])
+        emu = emulate(rows)
+        still = bad[rows] & (np.abs(g[rows] - emu) > atol + rtol * np.abs(emu))
+        if not still.any():
+            print(f"{what}: {int(bad.sum())} element(s) outside the oracle tolerance, all within it of the "
+                  f"bf16-operand emulation")
+            return float(err.max())
+        bad = np.zeros_like(bad)
+        bad[rows] = still
     if bad.any():
-        i = np.unravel_index(np.argmax(err - (atol + rtol * np.abs(ref) + extra)), err.shape)
+        i = np.unravel_index(np.argmax(np.where(bad, err, -1.0)), err.shape)
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements outside tolerance; worst at {i}: "
                              f"gpu={g[i]!r} ref={ref[i]!r}")
     return float(err.max())

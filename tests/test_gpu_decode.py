@@ -6,7 +6,8 @@ import torch
 
 import oracle
 from brute import rope
-from gpu_util import assert_close, decode, few_key_slack, la, to_device
+from bf16_model import emulate
+from gpu_util import assert_close, decode, la, to_device
 from paged_kv_cache_57_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -122,7 +123,9 @@ def _check_decode(w, rows=None, num_splits=0, lazy=True):
     out = decode(dv)
     ref = oracle.attention(w, rows=rows)
     got = out if rows is None else out[torch.as_tensor(rows, device=out.device)]
-    return assert_close(got, ref, w.dtype, w.name, slack=few_key_slack(w, rows) if w.dtype == "bf16" else None)
+    sel = np.arange(ref.shape[0]) if rows is None else np.asarray(rows)
+    emu = (lambda r: emulate(w, sel[r], lazy=lazy)) if w.dtype == "bf16" else None
+    return assert_close(got, ref, w.dtype, w.name, emulate=emu)
 
 
 def test_two_and_three_key_contexts():
