@@ -173,6 +173,29 @@ int lazy_attn_decode(const lazy_attn_params *p, const void *q, const void *k_poo
                      const void *rope_table, void *out, void *workspace, size_t workspace_bytes,
                      lazy_stream_t stream);
 
+/* ---------------------------------------------------------------- decode without allocation
+ * The pages have no counterpart for this entry point; it exists for callers that
+ * cannot allocate device memory for a workspace: an engine that has reserved nearly
+ * all of HBM for its KV-cache pool, a plugin limited to its host framework's
+ * buffers, or a latency-critical step that must not call cudaMalloc (which can
+ * synchronise the device).
+ * Same inputs, outputs and results as lazy_attn_decode, with no workspace
+ * argument: the split-K partials live in a file-scope static device array of
+ * LAZY_NOALLOC_SCRATCH_BYTES, which every GPU that loads the library holds until
+ * the process exits. The call allocates and frees nothing.
+ *  - Returns LAZY_ERR_WORKSPACE, launching nothing, when the split plan of `p`
+ *    needs more than LAZY_NOALLOC_SCRATCH_BYTES (lazy_attn_decode_workspace_bytes
+ *    tells the need; setting p->num_splits lower reduces it, and 1 needs none).
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture.
+ *  - Every call shares the one array: calls that overlap on the GPU (other
+ *    streams, other threads) race on it and must be serialised by the caller. */
+#define LAZY_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB */
+int lazy_attn_decode_noalloc(const lazy_attn_params *p, const void *q, const void *k_pool, const void *v_pool,
+                             const uint32_t *block_words, const int32_t *seq_lens, const int32_t *q_pos,
+                             const void *rope_table, void *out, lazy_stream_t stream);
+
 /* ---------------------------------------------------------------- prefill
  * Varlen query chunks ("Implementação Técnica", item 1, Prefilling): chunk s
  * has C_s = cu_seqlens_q[s+1] - cu_seqlens_q[s] query rows at absolute

@@ -32,8 +32,9 @@ EXPORTED = (
     "lazy_attn_status_string", "lazy_attn_rope_table_bytes", "lazy_attn_rope_table_init",
     "lazy_attn_pack_block_words_host", "lazy_attn_pack_block_words", "lazy_attn_decode_workspace_bytes",
     "lazy_attn_decode", "lazy_attn_prefill_workspace_bytes", "lazy_attn_prefill", "lazy_attn_debug_gather",
-    "lazy_attn_device_status", "lazy_attn_launch_count", "lazy_attn_debug_rope",
+    "lazy_attn_device_status", "lazy_attn_launch_count", "lazy_attn_debug_rope", "lazy_attn_decode_noalloc",
 )
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class Params(ctypes.Structure):
@@ -69,6 +70,7 @@ _sig = {
     "lazy_attn_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "lazy_attn_launch_count": (_u64, []),
     "lazy_attn_debug_rope": (ctypes.c_int, [_P, _vp, _vp, _i32, _vp, _vp]),
+    "lazy_attn_decode_noalloc": (ctypes.c_int, [_P] + [_vp] * 8 + [_vp]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -194,6 +196,21 @@ def decode(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tenso
                                _dptr(rope_table, "rope_table"), _dptr(out, "out", dt),
                                _dptr(workspace, "workspace"), wsz, _stream(stream))
     _check(rc, "decode")
+    return out
+
+
+def decode_noalloc(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                   block_words: torch.Tensor, seq_lens: torch.Tensor, q_pos: torch.Tensor, rope_table: torch.Tensor,
+                   out: torch.Tensor, stream=None) -> torch.Tensor:
+    """Decode whose split-K scratch is the library's static device array (for callers
+    that cannot allocate a workspace). ``out`` is required: the call allocates nothing.
+    Calls that overlap on the GPU share that array and must not run concurrently."""
+    dt = _tdt(p)
+    rc = _lib.lazy_attn_decode_noalloc(ctypes.byref(p), _dptr(q, "q", dt), _dptr(k_pool, "k_pool", dt),
+                                       _dptr(v_pool, "v_pool", dt), _dptr(block_words, "block_words"),
+                                       _dptr(seq_lens, "seq_lens", torch.int32), _dptr(q_pos, "q_pos", torch.int32),
+                                       _dptr(rope_table, "rope_table"), _dptr(out, "out", dt), _stream(stream))
+    _check(rc, "decode_noalloc")
     return out
 
 
