@@ -87,6 +87,28 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.samples)}
 
 
+# ------------------------------------------------------------------ multi-rank helpers
+
+def rank_seed(rank: int, base: int = 20260002) -> int:
+    """Weak scaling: every rank decodes its own batch, drawn with its own seed."""
+    return base + 1000 * rank
+
+
+def max_over_ranks(t: float, dist=None, device="cpu") -> float:
+    """The slowest rank's time (the whole job's time); identity on one rank."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return t
+    import torch
+    tt = torch.tensor([t], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_rate(bytes_per_rank_step: float, world: int, steps: int, t_max: float) -> float:
+    """Aggregate GB/s over all ranks: every rank processes the same volume per step."""
+    return world * bytes_per_rank_step * steps / t_max / 1e9
+
+
 # ------------------------------------------------------------------ helpers
 
 def build_device(w, lazy=True, k_pool=None):
@@ -263,7 +285,7 @@ def main():
     hbm, tf_burst, tf_sust, peak_src = _peaks()
     # Weak scaling: each rank decodes its own batch (a different seed), no data exchange.
     w = W.decode_zipf(WORKLOAD, batch=64, hq=32, hkv=8, docs_per_seq=8, doc_tokens=512, pool_docs=256,
-                      zipf_s=1.0, suffix_tokens=64, seed=20260002 + 1000 * rank)
+                      zipf_s=1.0, suffix_tokens=64, seed=rank_seed(rank))
     d = build_device(w)
     nbytes = decode_bytes(w)
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
@@ -289,13 +311,9 @@ def main():
     launches = L.launch_count() - launches0
     clk = clocks.stop()
     t_dev = sum(per_step)
-    t_max = t_dev
-    if world > 1:
-        tt = torch.tensor([t_dev], device="cuda", dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
+    t_max = max_over_ranks(t_dev, dist if world > 1 else None, device="cuda")
     ms = 1e3 * t_max / args.steps
-    value = world * nbytes["kv_logical"] * args.steps / t_max / 1e9
+    value = whole_job_rate(nbytes["kv_logical"], world, args.steps, t_max)
     avg = t_dev / args.steps
     achieved = nbytes["unique"] / avg / 1e9
 
