@@ -32,7 +32,7 @@
 #include "kernels.h"
 
 #ifndef LAZY_DECODE_SPT
-#define LAZY_DECODE_SPT 3  // stages per team
+#define LAZY_DECODE_SPT 2  // stages per team (2 lets three 4-warp CTAs share an SM)
 #endif
 
 namespace lazy {
@@ -156,7 +156,7 @@ __device__ __forceinline__ void build_q_frags(uint32_t (&qa)[D / 16][4], const f
 }
 
 template <int D, int MT, int SPT, bool LAZY>
-__global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS)
+__global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS, MT == 1 ? 3 : 1)
     decode_bf16_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap) {
   using C = DecodeCfg<D, MT, SPT>;
@@ -249,28 +249,35 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS)
 #pragma unroll
   for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
-  int p_prev = INT_MIN;
   const float sl2 = a.scale_log2;
-  int k = 0;
+  int k = 0, cbase = 0;  // next block of the team; first block of the current word chunk
+  int p_seg = nk > 0 ? __shfl_sync(0xffffffffu, cur.p, 0) : 0;
+  bool aborted = false;
+  // Outer loop: one pass per document run of the team's range (lazy only; the
+  // control runs it once). The q re-rotation sits here, outside the per-block
+  // loop, and overlaps the loads already in flight for the run's first block.
+  while (k < nk && !aborted) {
+    if constexpr (LAZY) rebuild(m_pos - p_seg);
   for (; k < nk; ++k) {
-    if (k > 0 && (k & 31) == 0) {  // advance the word chunk
+    if (k - cbase >= 32) {  // advance the word chunk
       if (!nxt_ready) nxt = describe(k, w_nxt, wn_nxt);
       cur = nxt;
       nxt_ready = false;
+      cbase += 32;
       if (k + 32 < nk) load_words(k + 32, w_nxt, wn_nxt);
     }
     const int slot = k % SPT;
-    const int p = __shfl_sync(0xffffffffu, cur.p, k & 31);
     const int nvalid = __shfl_sync(0xffffffffu, cur.nv, k & 31);
     if constexpr (LAZY) {
-      // p comes from the block word, so the re-rotation overlaps the block's load.
-      if (p != p_prev) {
-        rebuild(m_pos - p);
-        p_prev = p;
+      const int p = __shfl_sync(0xffffffffu, cur.p, k & 31);
+      if (p != p_seg) {  // next document: leave to re-rotate q, then resume at block k
+        p_seg = p;
+        break;
       }
     }
     if (!warp_wait(&tfull[slot], (k / SPT) & 1, a.status)) {
       abort_flag = 1;
+      aborted = true;
       break;
     }
     const uint32_t kbase = smem_u32(tst + slot * C::STAGE_BYTES);
@@ -364,6 +371,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS)
                                 &vmap);
       issued = kn + 1;
     }
+  }
   }
   // Copies still in flight (only after a timeout) must land before exit (bounded).
   if (leader)
