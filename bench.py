@@ -34,6 +34,24 @@ sys.path.insert(0, ROOT)
 METRIC = "LazyAttn decode KV GB/s (% HBM peak); prefill TFLOP/s; lazy-RoPE overhead %"
 WORKLOAD = "llama8b_decode"
 
+# DRAM bytes (read + write) per launch of the decode split kernel on this workload, from
+# the ncu capture summarised in profiles/decode_bf16_llama8b.md; valid only while the
+# kernel's sources hash to the value recorded with it.
+NCU_TRAFFIC = {"sources": ["paged_kv_cache_57_gb300/csrc/decode_bf16.cu", "paged_kv_cache_57_gb300/csrc/common.cuh"],
+               "sha16": "a626c8cea98bf1cd", "bytes_per_launch": 502075648 + 7224320}
+
+
+def _traffic_if_current():
+    import hashlib
+    h = hashlib.sha256()
+    try:
+        for f in NCU_TRAFFIC["sources"]:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+    except OSError:
+        return None
+    return NCU_TRAFFIC["bytes_per_launch"] if h.hexdigest()[:16] == NCU_TRAFFIC["sha16"] else None
+
 
 def _peaks():
     try:
@@ -341,7 +359,7 @@ def main():
                    "hbm_frac_unique_of_measured": achieved / hbm, "hbm_frac_unique_of_8tbs": achieved / 8000.0,
                    "ms_median": 1e3 * statistics.median(per_step)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": None, "peak_source": peak_src,
+                     "traffic": _traffic_if_current(), "peak_source": peak_src,
                      "kernel": "decode call (split kernel + combine); bytes = unique K/V blocks + q + out + words"},
         "gpu_launches": launches, "wall_s_timed": t_wall, "clocks": clk, "e2e": e2e,
     }
@@ -429,6 +447,40 @@ def measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust):
                           "lazy_overhead_pct": 100.0 * (statistics.median(tp) / statistics.median(tp0) - 1.0)}
     except L.LazyAttnError as e:
         out["prefill"] = {"unavailable": str(e)}
+    del dp
+    # Llama-3.1-70B-shaped decode: 32 x 16 x 1024 Zipf(1.0) of 512, pool capped at 1 GiB.
+    w4 = W.FULL["llama70b_decode"]()
+    d4 = build_device(w4)
+    t4 = time_steps(lambda: run_decode(d4, lazy=True), n, 3, flush)
+    t40 = time_steps(lambda: run_decode(d4, lazy=False), n, 3, flush)
+    b4 = decode_bytes(w4)
+    out["llama70b_decode"] = {"kv_gbs_logical": b4["kv_logical"] / statistics.median(t4) / 1e9,
+                              "kv_gbs_unique": b4["unique"] / statistics.median(t4) / 1e9,
+                              "tokens_per_s": w4.num_seqs / statistics.median(t4),
+                              "ms_median": 1e3 * statistics.median(t4),
+                              "lazy_overhead_pct": 100.0 * (statistics.median(t4) / statistics.median(t40) - 1.0)}
+    del d4
+    # Mixed continuous batch, MQA 32/1: 48 decode sequences + 4 prefill chunks of 512, one
+    # shared pool, both calls on one stream and timed as one step.
+    wd, wp = W.mixed_mqa()
+    dd = build_device(wd)
+    dp5 = build_device(wp, k_pool=None)
+    dp5["k"], dp5["v"] = dd["k"], dd["v"]  # the two halves index the same physical pool
+
+    def mixed_step():
+        run_decode(dd, lazy=True)
+        run_prefill(dp5, lazy=True)
+    t5 = time_steps(mixed_step, max(10, n // 2), 3, flush)
+    td = time_steps(lambda: run_decode(dd, lazy=True), max(10, n // 2), 3, flush)
+    tp = time_steps(lambda: run_prefill(dp5, lazy=True), max(10, n // 2), 3, flush)
+    b5 = decode_bytes(wd)
+    f5 = prefill_flops(wp)
+    out["mixed_mqa"] = {"step_ms": 1e3 * statistics.median(t5),
+                        "decode_ms": 1e3 * statistics.median(td), "prefill_ms": 1e3 * statistics.median(tp),
+                        "decode_kv_gbs_logical": b5["kv_logical"] / statistics.median(td) / 1e9,
+                        "decode_kv_gbs_unique": b5["unique"] / statistics.median(td) / 1e9,
+                        "prefill_tflops": f5 / statistics.median(tp) / 1e12,
+                        "decode_tokens": int(wd.tokens_per_seq().sum()), "prefill_gflop": f5 / 1e9}
     return out
 
 
