@@ -75,6 +75,9 @@ cudaError_t launch_gather_bf16(const GatherArgs& a, const CUtensorMap& kmap, con
 cudaError_t launch_gather_f32(const GatherArgs& a, cudaStream_t st);
 cudaError_t launch_prefill(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, cudaStream_t st);
+// Two query tiles (q-heads h, h+1 of one KV head) per CTA; needs an even GQA ratio.
+cudaError_t launch_prefill_pair(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                                const CUtensorMap& vmap, cudaStream_t st);
 
 // Shared-memory bytes a bf16 decode CTA needs (for occupancy-based split planning).
 int decode_bf16_smem_bytes(int D, int G);

@@ -564,6 +564,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, bool lazy, const CUtensorMap& q
                            const CUtensorMap& vmap, cudaStream_t st) {
   if (a.D != PF_D) return cudaErrorNotSupported;
   if (a.B == 0 || a.max_q_len == 0) return cudaSuccess;
+#ifndef LAZY_PREFILL_SINGLE_TILE
+  if (a.G % 2 == 0) return launch_prefill_pair(a, lazy, qmap, kmap, vmap, st);
+#endif
   dim3 grid((a.max_q_len + PF_BM - 1) / PF_BM, a.Hq, a.B);
   auto kern = lazy ? prefill_kernel<true> : prefill_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM);
