@@ -10,16 +10,17 @@
 //
 //   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B (thread = query row =
 //               TMEM lane). S is read from TMEM in 32-column chunks, twice: once
-//               for the row maximum, once for the weights, which go to the shared
-//               P buffer as bf16 (128-byte swizzled, K-major).
+//               for the row maximum, once for the weights, which are written back
+//               as bf16 pairs over the first 64 columns of the tile's own S (P
+//               stays in TMEM and is the A operand of P V).
 //   warps 8-11  K rotation (R_p per 16-row block, in shared memory) and V holes.
 //   warp 12     TMA producer: Q_A, Q_B; K ring x2, V ring x2.
-//   warp 13     TMEM owner (512 columns: S_A, S_B, O_A, O_B) and MMA issuer, in the
-//               order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1).
-//   warps 14-15 idle.
-// The single P buffer alternates: softmax A(j) writes it once PV_B(j-1) is done,
-// softmax B(j) once PV_A(j) is done; the same waits guarantee that the tile's own
-// previous P V has completed before it rescales O.
+//   warp 13     TMEM owner (512 columns: S_A/P_A, S_B/P_B, O_A, O_B) and MMA issuer,
+//               in the order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1).
+// Each tile has its own S/P columns, so the two tiles never wait for each other.
+// S_t(j+1) overwrites the P_t(j) that PV_t(j) reads, so the MMA warp issues it only
+// after PV_t(j) has completed; the softmax of tile t(j+1) therefore always finds
+// PV_t(j) done and may rescale O_t without a further wait.
 #include <climits>
 
 #include "prefill_common.cuh"
@@ -31,15 +32,14 @@ namespace {
 using namespace pf;
 
 constexpr int NK = 2, NV = 2;
-constexpr int THREADS = 512;
+constexpr int THREADS = 448;
 constexpr int TMEM_COLS = 512;
 
 constexpr int OFF_QA = 0;
 constexpr int OFF_QB = OFF_QA + TILE;
 constexpr int OFF_K = OFF_QB + TILE;
 constexpr int OFF_V = OFF_K + NK * TILE;
-constexpr int OFF_P = OFF_V + NV * TILE;
-constexpr int OFF_KMETA = OFF_P + TILE;
+constexpr int OFF_KMETA = OFF_V + NV * TILE;
 constexpr int OFF_VMETA = OFF_KMETA + NK * BLOCKS * (int)sizeof(KMeta);
 constexpr int OFF_BAR = OFF_VMETA + NV * BLOCKS * (int)sizeof(VMeta);
 constexpr int NBARS = 2 + 3 * NK + 3 * NV + 7;
@@ -58,7 +58,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sQ[2] = {base + OFF_QA, base + OFF_QB};
   uint8_t* sK = base + OFF_K;
   uint8_t* sV = base + OFF_V;
-  uint8_t* sP = base + OFF_P;
   KMeta* kmeta = reinterpret_cast<KMeta*>(base + OFF_KMETA);
   VMeta* vmeta = reinterpret_cast<VMeta*>(base + OFF_VMETA);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + OFF_BAR);
@@ -218,26 +217,26 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0 && n_tiles > 0) {
       constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);
       constexpr uint32_t idO = idesc_bf16_f32(BM, D, true);
-      const uint32_t p_addr = smem_u32(sP);
+      // Descriptors are built once; a byte offset moves the 14-bit start-address
+      // field by offset >> 4 (shared addresses stay below 2^18, so it never carries).
+      const uint64_t dQ[2] = {sdesc_sw128(smem_u32(sQ[0]), 16, 1024), sdesc_sw128(smem_u32(sQ[1]), 16, 1024)};
+      const uint64_t dK = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dV = sdesc_sw128(smem_u32(sV), HALF, 1024);
       auto issue_s = [&](int j, int t) {
-        const uint32_t q_addr = smem_u32(sQ[t]);
-        const uint32_t k_addr = smem_u32(sK + (j % NK) * TILE);
+        const uint64_t k0 = dK + (uint64_t)(((j % NK) * TILE) >> 4);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * HALF + (ks & 3) * 32;
-          tc_mma(tmem + 128 * t, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idS,
-                 ks > 0);
+          const uint32_t off = ((ks >> 2) * HALF + (ks & 3) * 32) >> 4;
+          tc_mma(tmem + 128 * t, dQ[t] + off, k0 + off, idS, ks > 0);
         }
         tc_commit(&s_full[t]);
       };
       auto issue_pv = [&](int j, int t) {
-        const uint32_t v_addr = smem_u32(sV + (j % NV) * TILE);
+        const uint64_t v0 = dV + (uint64_t)(((j % NV) * TILE) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint32_t poff = (ks >> 2) * HALF + (ks & 3) * 32;
-          tc_mma(tmem + 256 + 128 * t, sdesc_sw128(p_addr + poff, 16, 1024),
-                 sdesc_sw128(v_addr + ks * 2048, HALF, 1024), idO, (j > 0 || ks > 0) ? 1u : 0u);
-        }
+        for (int ks = 0; ks < BN / 16; ++ks)  // P_t: 8 TMEM columns (16 keys) per k-step
+          tc_mma_ta(tmem + 256 + 128 * t, tmem + 128 * t + 8 * ks, v0 + (uint32_t)(ks * 2048 >> 4), idO,
+                    (j > 0 || ks > 0) ? 1u : 0u);
         tc_commit(&pv_done[t]);
       };
       bool ok = mbar_wait(q_ready, 0, a.status) && mbar_wait(&k_ready[0], 0, a.status);
@@ -248,13 +247,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_commit(&k_empty[0]);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
+        const bool more = j + 1 < n_tiles;
         ok = mbar_wait(&p_full[0], j & 1, a.status) && mbar_wait(&v_full[j % NV], (j / NV) & 1, a.status) &&
              mbar_wait(&v_ready[j % NV], (j / NV) & 1, a.status);
         if (!ok) break;
         tc_fence_after();
         issue_pv(j, 0);
-        if (j + 1 < n_tiles) {
-          ok = mbar_wait(&k_ready[(j + 1) % NK], ((j + 1) / NK) & 1, a.status);
+        if (more) {  // S_A(j+1) overwrites P_A(j): wait for PV_A(j)
+          ok = mbar_wait(&k_ready[(j + 1) % NK], ((j + 1) / NK) & 1, a.status) && mbar_wait(&pv_done[0], j & 1, a.status);
           if (!ok) break;
           tc_fence_after();
           issue_s(j + 1, 0);
@@ -264,7 +264,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         issue_pv(j, 1);
         tc_commit(&v_empty[j % NV]);
-        if (j + 1 < n_tiles) {
+        if (more) {
+          ok = mbar_wait(&pv_done[1], j & 1, a.status);
+          if (!ok) break;
+          tc_fence_after();
           issue_s(j + 1, 1);
           tc_commit(&k_empty[(j + 1) % NK]);
         }
@@ -345,7 +348,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int iq = row0 + i;          // query index within the chunk
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t tS = tmem + 128 * t, tO = tmem + 256 + 128 * t;
-    uint64_t* other_pv = &pv_done[t ^ 1];
     bool ok = warp_wait(q_full, 0, a.status);
     if (ok) {
       // Q prologue: q_i' = R_{m_i} q_i, pre-scaled by sm_scale * log2(e).
@@ -396,15 +398,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         m_run = mx;
       }
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
-      // The shared P buffer is free, and this tile's previous P V is done, once the
-      // other tile's latest P V has completed.
-      const int other_phase = t == 0 ? j - 1 : j;
-      if (other_phase >= 0) {
-        ok = warp_wait(other_pv, other_phase & 1, a.status);
-        if (!ok) break;
-        tc_fence_after();
-      }
-      // Pass 2: weights -> bf16 P (shared memory), row sum in fp32.
+      // Pass 2: weights -> bf16 P over S's first 64 columns (chunk q's 16 words land on
+      // columns already read), row sum in fp32.
       const uint64_t mm = f2(m_use, m_use);
       uint64_t acc = f2(0.f, 0.f);
 #pragma unroll 1
@@ -425,16 +420,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           pw[k] = pack_bf16x2(e0, e1);
           acc = f2_add(acc, f2(e0, e1));
         }
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const int c16 = 4 * q + c4;  // 16-byte chunk of the row: keys 8 c16 .. 8 c16 + 7
-          *reinterpret_cast<uint4*>(sP + (c16 >> 3) * HALF + sw128(i, c16 & 7)) =
-              make_uint4(pw[4 * c4], pw[4 * c4 + 1], pw[4 * c4 + 2], pw[4 * c4 + 3]);
-        }
+        tmem_st16(tS + lane_base + 16 * q, pw);
       }
       const float2 sa = f2_split(acc);
       l_run = l_run * alpha + (sa.x + sa.y);
-      // Rescale the running output when this row's maximum was refreshed (warp-uniform).
+      // Rescale the running output when this row's maximum was refreshed (warp-uniform);
+      // PV_t(j-1) has completed, since S_t(j) was issued after it.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
@@ -445,9 +436,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int k = 0; k < 32; ++k) o[k] *= alpha;
           tmem_st32(tO + lane_base + 32 * q, o);
         }
-        tmem_st_wait();
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full[t]);
     }
