@@ -79,6 +79,10 @@ cudaError_t launch_prefill(const PrefillArgs& a, bool lazy, const CUtensorMap& q
 cudaError_t launch_prefill_pair(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, cudaStream_t st);
 
+// One query tile per CTA with the rotated Q tile in tensor memory; any GQA ratio.
+cudaError_t launch_prefill_tq(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                              const CUtensorMap& vmap, cudaStream_t st);
+
 // Shared-memory bytes a bf16 decode CTA needs (for occupancy-based split planning).
 int decode_bf16_smem_bytes(int D, int G);
 

@@ -1,6 +1,6 @@
 // prefill_pair.cu -- LazyAttention prefill with two query tiles per CTA (sm_103a).
 //
-// Same computation as prefill.cu ("Resumo Técnico: LazyAttention", "Implementação
+// The method of prefill.cu ("Resumo Técnico: LazyAttention", "Implementação
 // Técnica", item 1: one relative rotation R_p per K block, Q rotated once by R_m),
 // organised so that every loaded and rotated K/V tile serves 2 x 128 query rows:
 // tile A and tile B are q-heads h and h+1 of the same KV head, the same 128 chunk
@@ -14,7 +14,9 @@
 //               as bf16 pairs over the first 64 columns of the tile's own S (P
 //               stays in TMEM and is the A operand of P V).
 //   warps 8-11  K rotation (R_p per 16-row block, in shared memory) and V holes.
-//   warp 12     TMA producer: Q_A, Q_B; K ring x2, V ring x2.
+//   warp 12     TMA producer of Q_A, Q_B and the K ring (x2); warp 14 of the V ring
+//               (x2). A tile is 16 boxes of 16 rows x 64 columns, issued by 16 lanes
+//               at once: small TMA boxes only stream fast when many are in flight.
 //   warp 13     TMEM owner (512 columns: S_A/P_A, S_B/P_B, O_A, O_B) and MMA issuer,
 //               in the order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1).
 // Each tile has its own S/P columns, so the two tiles never wait for each other.
@@ -32,7 +34,7 @@ namespace {
 using namespace pf;
 
 constexpr int NK = 2, NV = 2;
-constexpr int THREADS = 448;
+constexpr int THREADS = 480;  // 15 warps
 constexpr int TMEM_COLS = 512;
 
 constexpr int OFF_QA = 0;
@@ -131,86 +133,81 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == 12) {
-    // ---------------------------------------------------------------- TMA producer
-    if (lane == 0) {
+  if (warp == 12 || warp == 14) {
+    // ---------------------------------------------------------------- TMA producers
+    const bool is_v = warp == 14;
+    if (!is_v && lane == 0) {
       tma_prefetch_map(&qmap);
       tma_prefetch_map(&kmap);
-      tma_prefetch_map(&vmap);
       mbar_arrive_expect_tx(q_full, 2 * TILE);
       for (int t = 0; t < 2; ++t) {
         tma_load_3d(sQ[t], &qmap, q_full, 0, h_of[t], q0 + row0);
         tma_load_3d(sQ[t] + HALF, &qmap, q_full, 64, h_of[t], q0 + row0);
       }
     }
-    struct Lane {
-      int p, nv, y, j0;
-    };
-    auto describe = [&](int j) {
+    if (is_v && lane == 0) tma_prefetch_map(&vmap);
+    // Block words are read 32 at a time, one chunk ahead: lane l holds the word of
+    // block cbase + l (wcur) and of block cbase + 32 + l (wnext).
+    int cbase = 0;
+    uint32_t wcur = lane < nb ? __ldg(&wrow[lane]) : 0u;
+    uint32_t wnext = 32 + lane < nb ? __ldg(&wrow[32 + lane]) : 0u;
+    const int ns = is_v ? NV : NK;
+    uint64_t* ful_ring = is_v ? v_full : k_full;
+    uint64_t* emp_ring = is_v ? v_empty : k_empty;
+    uint8_t* ring = is_v ? sV : sK;
+    const CUtensorMap* map = is_v ? &vmap : &kmap;
+    int issued = 0;
+    bool ok = true;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      if (j * BLOCKS >= cbase + 32) {  // warp-uniform: the tile starts in the next chunk
+        cbase += 32;
+        wcur = wnext;
+        wnext = cbase + 32 + lane < nb ? __ldg(&wrow[cbase + 32 + lane]) : 0u;
+      }
+      // Lanes 0..BLOCKS-1 describe the tile's blocks; lane BLOCKS takes the next
+      // block's word so that the tile's last block knows where the following one starts.
       const int b = j * BLOCKS + min(lane, BLOCKS);
-      const uint32_t w = (lane <= BLOCKS && b < nb) ? __ldg(&wrow[b]) : 0u;
+      const int rel = b - cbase;  // 0 .. 40
+      const uint32_t w0 = __shfl_sync(0xffffffffu, wcur, rel & 31);
+      const uint32_t w1 = __shfl_sync(0xffffffffu, wnext, rel & 31);
+      const uint32_t w = (lane <= BLOCKS && b < nb) ? (rel < 32 ? w0 : w1) : 0u;
       const BlockInfo bi = decode_word(w, b, a.id_bits);
       const int p_after = __shfl_down_sync(0xffffffffu, bi.p, 1);
-      Lane r{bi.p, 0, -kBlock, -1};  // rows of an invalid block start at -16: read as zeros
+      int y = -kBlock, nv = 0;  // rows of an invalid block start at -16: read as zeros
       if (lane < BLOCKS && b < nb) {
-        int nv = block_valid(b, nb, seq_len, bi.p, b + 1 < nb ? p_after : bi.p);
+        nv = block_valid(b, nb, seq_len, bi.p, b + 1 < nb ? p_after : bi.p);
         nv = nv < 0 ? 0 : (nv > kBlock ? kBlock : nv);
         if (bi.phys < a.num_pool_blocks) {
-          r.y = (bi.phys * a.Hkv + kvh) * kBlock;
+          y = (bi.phys * a.Hkv + kvh) * kBlock;
         } else {
-          raise_status(a.status, LAZY_DEV_BAD_BLOCK_ID);
+          if (!is_v) raise_status(a.status, LAZY_DEV_BAD_BLOCK_ID);
           nv = 0;
         }
-        r.nv = nv;
-        r.j0 = b >= b_chunk ? kBlock * (b - b_chunk) : -1;
       }
-      return r;
-    };
-    auto issue = [&](int j, const Lane& d, bool is_v) -> bool {
-      const int ns = is_v ? NV : NK;
+      const int ybox = __shfl_sync(0xffffffffu, y, (lane >> 1) & 7);  // lane l loads half l & 1 of block l >> 1
       const int st = j % ns;
-      uint64_t* emp = is_v ? &v_empty[st] : &k_empty[st];
-      uint64_t* ful = is_v ? &v_full[st] : &k_full[st];
-      if (j >= ns && !warp_wait(emp, ((j / ns) & 1) ^ 1, a.status)) return false;
+      if (j >= ns && !warp_wait(&emp_ring[st], ((j / ns) & 1) ^ 1, a.status)) {
+        ok = false;
+        break;
+      }
       if (lane < BLOCKS) {
         if (is_v)
-          vmeta[st * BLOCKS + lane] = VMeta{d.nv, d.j0};
+          vmeta[st * BLOCKS + lane] = VMeta{nv, b >= b_chunk ? kBlock * (b - b_chunk) : -1};
         else
-          kmeta[st * BLOCKS + lane] = KMeta{d.p, d.nv};
+          kmeta[st * BLOCKS + lane] = KMeta{bi.p, nv};
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(ful, TILE);
+      if (lane == 0) mbar_arrive_expect_tx(&ful_ring[st], TILE);
       __syncwarp();
-      if (lane < BLOCKS) {
-        uint8_t* dst = (is_v ? sV : sK) + st * TILE + lane * (kBlock * 128);
-        const CUtensorMap* map = is_v ? &vmap : &kmap;
-        tma_load_2d(dst, map, ful, 0, d.y);
-        tma_load_2d(dst + HALF, map, ful, 64, d.y);
-      }
-      return true;
-    };
-    int k_issued = 0, v_issued = 0;
-    bool ok = true;
-    Lane prev{};
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      const Lane cur = describe(j);
-      ok = issue(j, cur, false);
-      if (ok) k_issued = j + 1;
-      if (ok && j >= 1) {
-        ok = issue(j - 1, prev, true);
-        if (ok) v_issued = j;
-      }
-      prev = cur;
-    }
-    if (ok && n_tiles > 0) {
-      ok = issue(n_tiles - 1, prev, true);
-      if (ok) v_issued = n_tiles;
+      if (lane < 2 * BLOCKS)
+        tma_load_2d(ring + st * TILE + (lane & 1) * HALF + (lane >> 1) * (kBlock * 128), map, &ful_ring[st],
+                    (lane & 1) * 64, ybox);
+      issued = j + 1;
     }
     if (!ok) abort_flag = 1;
     if (lane == 0) {  // every copy issued must land before the CTA exits (bounded)
-      mbar_wait(q_full, 0, a.status);
-      for (int j = max(0, k_issued - NK); j < k_issued; ++j) mbar_wait(&k_full[j % NK], (j / NK) & 1, a.status);
-      for (int j = max(0, v_issued - NV); j < v_issued; ++j) mbar_wait(&v_full[j % NV], (j / NV) & 1, a.status);
+      if (!is_v) mbar_wait(q_full, 0, a.status);
+      for (int j = max(0, issued - ns); j < issued; ++j) mbar_wait(&ful_ring[j % ns], (j / ns) & 1, a.status);
     }
   } else if (warp == 13) {
     // ---------------------------------------------------------------- MMA issuer
@@ -376,7 +373,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int q = 0; q < 4; ++q) {
         float sv[32];
         tmem_ld32(tS + lane_base + 32 * q, sv);
-        tmem_ld_wait();
+        tmem_ld_wait(sv);
         if (full_tile) {
           float m2[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -406,7 +403,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int q = 0; q < 4; ++q) {
         float sv[32];
         tmem_ld32(tS + lane_base + 32 * q, sv);
-        tmem_ld_wait();
+        tmem_ld_wait(sv);
         if (!full_tile) {
 #pragma unroll
           for (int k = 0; k < 32; ++k)
@@ -431,7 +428,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int q = 0; q < 4; ++q) {
           float o[32];
           tmem_ld32(tO + lane_base + 32 * q, o);
-          tmem_ld_wait();
+          tmem_ld_wait(o);
 #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] *= alpha;
           tmem_st32(tO + lane_base + 32 * q, o);
@@ -453,7 +450,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         float o[32];
         if (n_tiles > 0) {
           tmem_ld32(tO + lane_base + 32 * q, o);
-          tmem_ld_wait();
+          tmem_ld_wait(o);
         } else {
 #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] = 0.f;
