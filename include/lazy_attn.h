@@ -117,9 +117,14 @@ const char *lazy_attn_status_string(int status);
  * exact in fp32), and evaluate cos/sin(2 pi * fraction) with sincospif. The
  * angle error stays below about 5e-7 rad for every |n| < LAZY_MAX_ROPE_OFFSET,
  * with no memory access per offset.
- * Layout: float2 [head_dim/2] = (hi, lo). Caller-owned device memory of at least
- * lazy_attn_rope_table_bytes(p) bytes, 16-byte aligned; read-only to every other
- * call. */
+ * A second part holds (cos, sin)(i * w_f) for the row offsets i = 0 .. LAZY_ROPE_ROWS-1
+ * of a prefill query tile, also computed in fp64 and rounded to fp32: a tile whose
+ * rows sit at base + i gets its angles by angle addition from the tile's base angles
+ * (sincospif once per frequency per tile instead of once per row).
+ * Layout: float2 [head_dim/2] = (hi, lo), then float2 [LAZY_ROPE_ROWS][head_dim/2] =
+ * (cos, sin). Caller-owned device memory of at least lazy_attn_rope_table_bytes(p)
+ * bytes, 16-byte aligned; read-only to every other call. */
+#define LAZY_ROPE_ROWS 128
 size_t lazy_attn_rope_table_bytes(const lazy_attn_params *p);
 int lazy_attn_rope_table_init(const lazy_attn_params *p, void *table, size_t table_bytes,
                               lazy_stream_t stream);

@@ -176,7 +176,7 @@ uint64_t lazy_attn_launch_count(void) { return g_launches.load(std::memory_order
 size_t lazy_attn_rope_table_bytes(const lazy_attn_params* p) {
   Checked c;
   if (check_params(p, &c) != LAZY_OK) return 0;
-  return (size_t)(p->head_dim / 2) * sizeof(float2);
+  return (size_t)(p->head_dim / 2) * (1 + LAZY_ROPE_ROWS) * sizeof(float2);
 }
 
 int lazy_attn_rope_table_init(const lazy_attn_params* p, void* table, size_t table_bytes, lazy_stream_t stream) {

@@ -35,6 +35,20 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsign
   return __all_sync(0xffffffffu, ok);
 }
 
+// Named barrier `id` (1..15; 0 is __syncthreads) over n threads (a multiple of 32).
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+// The same barrier with an AND reduction of v over the participating threads.
+__device__ __forceinline__ bool named_and(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
 // 2^x on the SFU (PTX ex2.approx, flush-to-zero); 2^-inf = +0.
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -76,18 +90,51 @@ __device__ __forceinline__ void rotate_chunk(uint4& X, uint4& Y, const Rot8& R) 
   }
 }
 
-// Rotates row `i` of a 128-row Q tile in place (both 64-column halves, 128-byte
-// swizzled) by R_m, pre-scaled by `scale`.
-__device__ __forceinline__ void rotate_q_row(uint8_t* sQ, int i, int m, float scale, const float2* __restrict__ rope,
-                                             unsigned int* status) {
-#pragma unroll 1
-  for (int c = 0; c < 8; ++c) {
-    float2 cs[8];
+// Query rows of a tile sit at positions base + i, i = 16 k + r < 128. The tile's
+// base angles (cos, sin)(base w_f) take one sincospif per frequency per CTA; the
+// table rows i = 16 k (k < 8) and i = r (r < 16), 24 rows, are copied to shared
+// memory once per CTA; row i's angles then follow by two angle additions (a few
+// fp32 operations, about 3 ulp), with no global-memory latency per row.
+constexpr int kAngleRows = 24;
+
+__device__ __forceinline__ float2 add_angles(float2 a, float2 b) {
+  return make_float2(fmaf(a.x, b.x, -a.y * b.y), fmaf(a.y, b.x, a.x * b.y));
+}
+
+// Copies table rows 0, 16, ..., 112 then 0 .. 15 (D/2 entries each) to sm_rows,
+// thread tid of n.
+__device__ __forceinline__ void load_angle_rows(float2* sm_rows, const float2* __restrict__ rope, int tid, int n) {
+  const float4* src = reinterpret_cast<const float4*>(rope + D / 2);  // row part of the table
+  float4* dst = reinterpret_cast<float4*>(sm_rows);
+  for (int idx = tid; idx < kAngleRows * (D / 4); idx += n) {
+    const int row = idx / (D / 4), col = idx % (D / 4);
+    const int src_row = row < 8 ? 16 * row : row - 8;
+    dst[idx] = __ldg(&src[src_row * (D / 4) + col]);
+  }
+}
+
+// Rotation coefficients of the 8 frequencies of chunk c for row offset i.
+__device__ __forceinline__ Rot8 row_rot8(const float2* base_cs, const float2* sm_rows, int i, int c, float scale) {
+  const float2* a16 = sm_rows + (i >> 4) * (D / 2);
+  const float2* a1 = sm_rows + (8 + (i & 15)) * (D / 2);
+  float2 cs[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) cs[e] = rope_cs(__ldg(&rope[8 * c + e]), m, status);
+  for (int e = 0; e < 8; ++e) {
+    const int f = 8 * c + e;
+    cs[e] = add_angles(add_angles(base_cs[f], a16[f]), a1[f]);
+  }
+  return make_rot8(cs, scale);
+}
+
+// Rotates chunks [c0, c1) of row i of a 128-row Q tile in place (both 64-column
+// halves, 128-byte swizzled) by R_{base+i}, pre-scaled by `scale`.
+__device__ __forceinline__ void rotate_q_row(uint8_t* sQ, int i, int c0, int c1, const float2* base_cs,
+                                             const float2* sm_rows, float scale) {
+#pragma unroll 1
+  for (int c = c0; c < c1; ++c) {
     uint4 X = *reinterpret_cast<uint4*>(sQ + sw128(i, c));
     uint4 Y = *reinterpret_cast<uint4*>(sQ + HALF + sw128(i, c));
-    rotate_chunk(X, Y, make_rot8(cs, scale));
+    rotate_chunk(X, Y, row_rot8(base_cs, sm_rows, i, c, scale));
     *reinterpret_cast<uint4*>(sQ + sw128(i, c)) = X;
     *reinterpret_cast<uint4*>(sQ + HALF + sw128(i, c)) = Y;
   }

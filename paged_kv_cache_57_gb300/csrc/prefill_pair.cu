@@ -45,8 +45,11 @@ constexpr int OFF_KMETA = OFF_V + NV * TILE;
 constexpr int OFF_VMETA = OFF_KMETA + NK * BLOCKS * (int)sizeof(KMeta);
 constexpr int OFF_BAR = OFF_VMETA + NV * BLOCKS * (int)sizeof(VMeta);
 constexpr int NBARS = 2 + 3 * NK + 3 * NV + 7;
-constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
+constexpr int OFF_QCS = (OFF_BAR + NBARS * 8 + 15) & ~15;  // float2 [64]: the tiles' base angles
+constexpr int OFF_ROWS = OFF_QCS + (D / 2) * 8;  // float2 [24][64]: angles of row offsets 16 k and r
+constexpr int OFF_TMEM = OFF_ROWS + kAngleRows * (D / 2) * 8;
 constexpr int SMEM = 1024 + OFF_TMEM + 16;
+static_assert(OFF_QCS % 16 == 0 && OFF_ROWS % 16 == 0, "angle rows are written as 16-byte vectors");
 static_assert(SMEM <= 227 * 1024, "prefill (pair) shared memory");
 
 }  // namespace
@@ -75,6 +78,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* p_full = s_full + 2;     // [2]
   uint64_t* pv_done = p_full + 2;    // [2]
   uint64_t* mma_drain = pv_done + 2;
+  float2* base_cs = reinterpret_cast<float2*>(base + OFF_QCS);
+  float2* angle_rows = reinterpret_cast<float2*>(base + OFF_ROWS);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base + OFF_TMEM);
   __shared__ int abort_flag;
 
@@ -345,10 +350,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int iq = row0 + i;          // query index within the chunk
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t tS = tmem + 128 * t, tO = tmem + 256 + 128 * t;
+    // Q prologue: q_i' = R_{m_i} q_i, pre-scaled by sm_scale * log2(e); both tiles
+    // hold rows at m_i = q_start + row0 + i.
+    if (threadIdx.x < D / 2) base_cs[threadIdx.x] = rope_cs(__ldg(&a.rope[threadIdx.x]), a.q_start[s] + row0, a.status);
+    load_angle_rows(angle_rows, a.rope, threadIdx.x, 256);
+    named_sync(1, 256);
     bool ok = warp_wait(q_full, 0, a.status);
     if (ok) {
-      // Q prologue: q_i' = R_{m_i} q_i, pre-scaled by sm_scale * log2(e).
-      rotate_q_row(sQ[t], i, a.q_start[s] + iq, a.scale_log2, a.rope, a.status);
+      rotate_q_row(sQ[t], i, 0, 8, base_cs, angle_rows, a.scale_log2);
       fence_proxy_async_smem();
     }
     mbar_arrive(q_ready);

@@ -16,7 +16,7 @@
 //               a 64-thread named barrier); each keeps its own partial row sum.
 //   warps 8-11  K rotation (R_p per 16-row block, in shared memory) and V holes.
 //   warp 12     TMA producer of Q and the K ring (x3, 32 KiB stages); warp 14 of the
-//               V ring (x3). A tile is 16 boxes of 16 rows x 64 columns, issued by 16
+//               V ring (x2). A tile is 16 boxes of 16 rows x 64 columns, issued by 16
 //               lanes at once: small TMA boxes only stream fast when many are in flight.
 //   warp 13     TMEM owner and MMA issuer.
 // TMEM columns: [0,128) S buffer 0, [128,256) S buffer 1, [256,384) O, [384,448) Q',
@@ -36,7 +36,7 @@ namespace {
 
 using namespace pf;
 
-constexpr int NK = 3, NV = 3;
+constexpr int NK = 3, NV = 2;
 constexpr int THREADS = 480;  // 15 warps
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t COL_O = 256, COL_Q = 384, COL_P = 448;
@@ -48,41 +48,28 @@ constexpr int OFF_KMETA = OFF_V + NV * TILE;
 constexpr int OFF_VMETA = OFF_KMETA + NK * BLOCKS * (int)sizeof(KMeta);
 constexpr int OFF_BAR = OFF_VMETA + NV * BLOCKS * (int)sizeof(VMeta);
 constexpr int NBARS = 2 + 3 * NK + 3 * NV + 2 + 1 + 1 + 1 + 1;
-constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
+constexpr int OFF_QCS = (OFF_BAR + NBARS * 8 + 15) & ~15;  // float2 [64]: the tile's base angles
+constexpr int OFF_ROWS = OFF_QCS + (D / 2) * 8;  // float2 [24][64]: angles of row offsets 16 k and r
+constexpr int OFF_TMEM = OFF_ROWS + kAngleRows * (D / 2) * 8;
 constexpr int SMEM = 1024 + OFF_TMEM + 16;
+static_assert(OFF_QCS % 16 == 0 && OFF_ROWS % 16 == 0, "angle rows are written as 16-byte vectors");
 static_assert(SMEM <= 227 * 1024, "prefill (TMEM Q) shared memory");
 
 // Named barriers (0 is __syncthreads): 1 = the 256 softmax threads, 2 + quadrant =
 // the 64 threads that share one quadrant of rows.
 constexpr int BAR_SOFTMAX = 1, BAR_PAIR0 = 2;
 
-__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
-
-// Barrier with an AND reduction over the participating threads.
-__device__ __forceinline__ bool named_and(int id, int n, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
-
-// Chunks c0 .. c0+3 of row i of the staged Q tile rotated by R_m and pre-scaled,
-// stored as packed bf16 pairs to TMEM lane (lane_base + thread) from column tq:
-// dims 0..63 in columns [tq, tq + 32), dims 64..127 in [tq + 32, tq + 64)
+// Chunks c0 .. c0+3 of row i of the staged Q tile rotated by R_{base+i} and
+// pre-scaled, stored as packed bf16 pairs to TMEM lane (lane_base + thread) from
+// column tq: dims 0..63 in columns [tq, tq + 32), dims 64..127 in [tq + 32, tq + 64)
 // (column w = dims 2w, 2w + 1 of its half).
-__device__ __forceinline__ void store_rotated_q(const uint8_t* sQ, int i, int c0, int m, float scale,
-                                                const float2* __restrict__ rope, unsigned int* status, uint32_t tq) {
+__device__ __forceinline__ void store_rotated_q(const uint8_t* sQ, int i, int c0, const float2* base_cs,
+                                                const float2* sm_rows, float scale, uint32_t tq) {
 #pragma unroll 1
   for (int c = c0; c < c0 + 4; ++c) {
-    float2 cs[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) cs[e] = rope_cs(__ldg(&rope[8 * c + e]), m, status);
     uint4 X = *reinterpret_cast<const uint4*>(sQ + sw128(i, c));
     uint4 Y = *reinterpret_cast<const uint4*>(sQ + HALF + sw128(i, c));
-    rotate_chunk(X, Y, make_rot8(cs, scale));
+    rotate_chunk(X, Y, row_rot8(base_cs, sm_rows, i, c, scale));
     tmem_st4(tq + 4 * c, X);
     tmem_st4(tq + 32 + 4 * c, Y);
   }
@@ -115,6 +102,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* pv_done = p_full + 1;
   uint64_t* o_done = pv_done + 1;   // the last P V has completed (one phase)
   uint64_t* mma_drain = o_done + 1;
+  float2* base_cs = reinterpret_cast<float2*>(base + OFF_QCS);
+  float2* angle_rows = reinterpret_cast<float2*>(base + OFF_ROWS);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base + OFF_TMEM);
   __shared__ int abort_flag;
 
@@ -400,11 +389,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
     const uint32_t tO = tmem + COL_O + lane_base + 64 * hc;  // this thread's 64 columns of O
     const uint32_t tP = tmem + COL_P + lane_base + 32 * hc;  // and its 32 columns of P
+    // Q prologue: q_i' = R_{m_i} q_i, pre-scaled by sm_scale * log2(e), to TMEM
+    // (this thread: dims 32 hc .. 32 hc + 31 of each half); m_i = q_start + row0 + i.
+    if (threadIdx.x < D / 2) base_cs[threadIdx.x] = rope_cs(__ldg(&a.rope[threadIdx.x]), a.q_start[s] + row0, a.status);
+    load_angle_rows(angle_rows, a.rope, threadIdx.x, 256);
+    named_sync(BAR_SOFTMAX, 256);
     bool ok = warp_wait(q_full, 0, a.status);
     if (ok) {
-      // Q prologue: q_i' = R_{m_i} q_i, pre-scaled by sm_scale * log2(e), to TMEM
-      // (this thread: dims 32 hc .. 32 hc + 31 of each half).
-      store_rotated_q(sQ, i, 4 * hc, a.q_start[s] + iq, a.scale_log2, a.rope, a.status,
+      store_rotated_q(sQ, i, 4 * hc, base_cs, angle_rows, a.scale_log2,
                       tmem + COL_Q + lane_base);
       tmem_st_wait();
       tc_fence_before();

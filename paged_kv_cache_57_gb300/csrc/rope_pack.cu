@@ -5,18 +5,29 @@
 namespace lazy {
 
 // t_i = w_i / (2 pi), w_i = theta^(-2i/d), in fp64, stored as fp32 (hi, lo).
+// Entries [0, half): the turns (hi, lo). Entries half + i * half + f: (cos, sin)(i w_f)
+// for the prefill row offsets i < LAZY_ROPE_ROWS. Everything in fp64, rounded once.
 __global__ void rope_table_kernel(float2* table, int half, int head_dim, double theta) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= half) return;
-  const double two_pi = 6.283185307179586476925286766559;
-  const double t = pow(theta, -2.0 * (double)i / (double)head_dim) / two_pi;
-  const float hi = (float)t;
-  table[i] = make_float2(hi, (float)(t - (double)hi));
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= half * (1 + LAZY_ROPE_ROWS)) return;
+  const int f = idx % half, row = idx / half - 1;
+  const double w = pow(theta, -2.0 * (double)f / (double)head_dim);
+  if (row < 0) {
+    const double two_pi = 6.283185307179586476925286766559;
+    const double t = w / two_pi;
+    const float hi = (float)t;
+    table[idx] = make_float2(hi, (float)(t - (double)hi));
+  } else {
+    double sn, cs;
+    sincos((double)row * w, &sn, &cs);
+    table[idx] = make_float2((float)cs, (float)sn);
+  }
 }
 
 cudaError_t launch_rope_table(float2* table, int head_dim, double theta, cudaStream_t st) {
   const int half = head_dim / 2;
-  rope_table_kernel<<<1, 128, 0, st>>>(table, half, head_dim, theta);
+  const int total = half * (1 + LAZY_ROPE_ROWS);
+  rope_table_kernel<<<(total + 255) / 256, 256, 0, st>>>(table, half, head_dim, theta);
   return cudaGetLastError();
 }
 

@@ -166,9 +166,9 @@ def test_argument_checks_return_before_cuda(la):
 def test_size_queries(la):
     w = W.FULL["tiny_fp32"]()
     p = _params(la, w)
-    assert la.rope_table_bytes(p) == 32 * 8
+    assert la.rope_table_bytes(p) == 32 * 8 * 129
     p.head_dim = 128
-    assert la.rope_table_bytes(p) == 64 * 8
+    assert la.rope_table_bytes(p) == 64 * 8 * 129
     p.num_splits = 1
     assert la.decode_workspace_bytes(p) == 0
     p.num_splits, p.max_blocks_per_seq = 4, 64

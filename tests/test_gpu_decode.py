@@ -29,9 +29,15 @@ def test_rotation_matches_fp64(d, theta):
     p = L.make_params(num_seqs=1, num_q_heads=1, num_kv_heads=1, head_dim=d, num_pool_blocks=1,
                       max_blocks_per_seq=1, rope_theta=theta)
     table = L.rope_table_init(p)
-    t = table.view(torch.float32).view(d // 2, 2).cpu().double().numpy()
+    full = table.view(torch.float32).view(-1, 2).cpu().double().numpy()
+    t = full[: d // 2]
     w = theta ** (-2.0 * np.arange(d // 2) / d)
     assert np.abs((t[:, 0] + t[:, 1]) * 2 * np.pi / w - 1).max() < 1e-14
+    # Row part: (cos, sin)(i * w_f) for the prefill row offsets i < LAZY_ROPE_ROWS, rounded once.
+    rows = full[d // 2:].reshape(128, d // 2, 2)
+    ang_r = np.arange(128)[:, None] * w[None, :]
+    assert np.abs(rows[..., 0] - np.cos(ang_r)).max() < 6e-8
+    assert np.abs(rows[..., 1] - np.sin(ang_r)).max() < 6e-8
     rng = np.random.default_rng(9)
     deltas = np.concatenate([np.arange(-5, 300), rng.integers(-(1 << 24) + 1, 1 << 24, 3000),
                              [131072, 131071, 4160, 16384, (1 << 24) - 1, -(1 << 24) + 1]]).astype(np.int32)
