@@ -4,7 +4,9 @@
 Default workload: Llama-3.1-8B-shaped decode, bf16, 32 q / 8 KV heads, d=128,
 batch 64, contexts of 8 Zipf(1.0)-drawn 512-token documents from a 256-document
 pool plus a 64-token private suffix (4160 tokens), RoPE theta 5e5. One step is
-one decode call (split kernel + combine) for the whole batch, one layer.
+one shared-run decode call (lazy_attn_decode_shared: work-item kernel + combine)
+for the whole batch, one layer; the per-sequence entry point (lazy_attn_decode) is
+timed beside it.
 
 Prints ONE JSON line (rank 0). ``value`` is logical KV GB/s: K+V bytes of every
 token of every context divided by the device time of the decode call, inputs
@@ -34,11 +36,13 @@ sys.path.insert(0, ROOT)
 METRIC = "LazyAttn decode KV GB/s (% HBM peak); prefill TFLOP/s; lazy-RoPE overhead %"
 WORKLOAD = "llama8b_decode"
 
-# DRAM bytes (read + write) per launch of the decode split kernel on this workload, from
-# the ncu capture summarised in profiles/decode_bf16_llama8b.md; valid only while the
-# kernel's sources hash to the value recorded with it.
-NCU_TRAFFIC = {"sources": ["paged_kv_cache_57_gb300/csrc/decode_bf16.cu", "paged_kv_cache_57_gb300/csrc/common.cuh"],
-               "sha16": "a626c8cea98bf1cd", "bytes_per_launch": 502075648 + 7224320}
+# DRAM bytes (read + write) per launch of the shared-run decode kernel on this workload,
+# from the ncu capture summarised in profiles/; valid only while the kernel's sources
+# hash to the value recorded with it (otherwise the bench reports traffic as null).
+NCU_TRAFFIC = {"sources": ["paged_kv_cache_57_gb300/csrc/decode_shared.cu",
+                           "paged_kv_cache_57_gb300/csrc/decode_block.cuh",
+                           "paged_kv_cache_57_gb300/csrc/common.cuh"],
+               "sha16": "", "bytes_per_launch": 0}
 
 
 def _traffic_if_current():
@@ -145,6 +149,12 @@ def build_device(w, lazy=True, k_pool=None):
         d["q_pos"] = c(w.q_pos)
         d["ws"] = torch.empty(max(1, L.decode_workspace_bytes(p)), dtype=torch.uint8, device="cuda")
         d["out"] = torch.empty_like(d["q"])
+        if w.dtype == "bf16":  # shared-run plan (host planner, copied to the device)
+            items, slot_indptr = L.plan_shared_host(p, len(w.doc_len), w.seg_indptr, w.seg_doc, w.seg_len,
+                                                    w.doc_block_indptr, w.doc_blocks)
+            d["plan"] = L.SharedPlan(items, slot_indptr)
+            d["ws_sh"] = torch.empty(max(1, L.decode_shared_workspace_bytes(p, d["plan"].num_slots)),
+                                     dtype=torch.uint8, device="cuda")
     else:
         d["cu"] = c(w.cu_seqlens_q)
         d["q_start"] = c(w.q_start)
@@ -153,13 +163,19 @@ def build_device(w, lazy=True, k_pool=None):
     return d
 
 
-def run_decode(d, lazy=None):
+def run_decode(d, lazy=None, path="shared"):
+    """One decode call: ``shared`` = lazy_attn_decode_shared (each cited document chunk read
+    once per KV head for the whole batch), ``seq`` = lazy_attn_decode (per sequence)."""
     from paged_kv_cache_57_gb300 import lazy_attn as L
     p = d["p"]
     if lazy is not None:
         p.lazy = int(lazy)
-    L.decode(p, d["q"], d["k"], d["v"], d["words"], d["seq_lens"], d["q_pos"], d["rope"], out=d["out"],
-             workspace=d["ws"])
+    if path == "shared":
+        L.decode_shared(p, d["q"], d["k"], d["v"], d["words"], d["q_pos"], d["rope"], d["plan"], out=d["out"],
+                        workspace=d["ws_sh"])
+    else:
+        L.decode(p, d["q"], d["k"], d["v"], d["words"], d["seq_lens"], d["q_pos"], d["rope"], out=d["out"],
+                 workspace=d["ws"])
 
 
 def run_prefill(d, lazy=None):
@@ -277,10 +293,18 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="headline decode only (used for ncu launch lists)")
+    ap.add_argument("--decode-path", default="shared", choices=["shared", "seq"],
+                    help="decode entry point timed by --workload (shared-run or per-sequence)")
+    ap.add_argument("--workload", default=None, choices=sorted(["llama8b_decode", "llama8b_decode_noshare",
+                                                                "llama8b_prefill", "llama70b_decode",
+                                                                "llama70b_decode_noshare"]),
+                    help="time one workload alone and print its own line (used for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         return reference_arm(args)
+    if args.workload:
+        return single_workload(args)
 
     import torch
     import torch.distributed as dist
@@ -352,6 +376,7 @@ def main():
         "config": {"workload": WORKLOAD, "batch": w.num_seqs, "context": int(w.tokens_per_seq()[0]),
                    "heads": [w.num_q_heads, w.num_kv_heads], "head_dim": w.head_dim, "rope_theta": w.rope_theta,
                    "docs": "8 x 512 Zipf(1.0) of 256 + 64 private", "l2": "flushed before every step",
+                   "decode_path": "shared-run (lazy_attn_decode_shared)",
                    "parallelism": f"weak x{world} (independent batches)"},
         "decode": {"tokens_per_s": world * w.num_seqs / (t_max / args.steps),
                    "kv_gbs_logical": value, "kv_gbs_unique": world * nbytes["unique"] * args.steps / t_max / 1e9,
@@ -360,7 +385,8 @@ def main():
                    "ms_median": 1e3 * statistics.median(per_step)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": _traffic_if_current(), "peak_source": peak_src,
-                     "kernel": "decode call (split kernel + combine); bytes = unique K/V blocks + q + out + words"},
+                     "kernel": "shared-run decode call (decode_shared_kernel + combine); bytes = unique K/V "
+                               "blocks + q + out + words"},
         "gpu_launches": launches, "wall_s_timed": t_wall, "clocks": clk, "e2e": e2e,
     }
     line.update(extras)
@@ -374,35 +400,58 @@ def main():
     return 0
 
 
+def single_workload(args):
+    """One workload on one GPU, timed alone: the command the ncu captures run."""
+    import torch
+    from paged_kv_cache_57_gb300 import build
+    from paged_kv_cache_57_gb300 import workloads as W
+    torch.cuda.set_device(0)
+    build.build()
+    w = W.FULL[args.workload]()
+    d = build_device(w)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device="cuda")
+    if w.kind == "decode":
+        t = time_steps(lambda: run_decode(d, lazy=True, path=args.decode_path), args.steps, args.warmup, flush)
+        v, unit = decode_bytes(w)["kv_logical"] / statistics.median(t) / 1e9, "GB/s"
+    else:
+        t = time_steps(lambda: run_prefill(d, lazy=True), args.steps, args.warmup, flush)
+        v, unit = prefill_flops(w) / statistics.median(t) / 1e12, "TFLOP/s"
+    print(json.dumps({"workload": args.workload, "value": v, "unit": unit, "steps": args.steps,
+                      "warmup": args.warmup, "ms_median": 1e3 * statistics.median(t)}), flush=True)
+    return 0
+
+
 def measure_e2e(args, d, w, nbytes):
-    """Same decode through the public API with the step's inputs copied from pinned host
-    memory (q, block words, seq_lens, q_pos) and the output read back, per step. The KV
-    pool is the resident cache (it persists across steps), not a per-step input."""
+    """Same decode through the public API (shared-run path) with the step's inputs copied
+    from pinned host memory (q, block words, q positions, the plan's items and slot
+    offsets) and the output read back, per step. The KV pool is the resident cache (it
+    persists across steps), not a per-step input."""
     import torch
     from paged_kv_cache_57_gb300 import lazy_attn as L
     steps = max(3, min(args.steps, 50))
-    hq = d["q"].cpu().pin_memory()
-    hw = d["words"].cpu().pin_memory()
-    hs = d["seq_lens"].cpu().pin_memory()
-    hp = d["q_pos"].cpu().pin_memory()
+    plan = d["plan"]
+    host = [x.cpu().pin_memory() for x in (d["q"], d["words"], d["q_pos"], plan.items, plan.slot_indptr)]
+    dev = [torch.empty_like(x, device="cuda") for x in host]
+    q, words, qp, items, slot_indptr = dev
+    dplan = L.SharedPlan.__new__(L.SharedPlan)
+    dplan.__dict__.update(plan.__dict__)
+    dplan.items, dplan.slot_indptr = items, slot_indptr
     hout = torch.empty_like(d["out"], device="cpu").pin_memory()
-    q, words, sl, qp = (torch.empty_like(x, device="cuda") for x in (hq, hw, hs, hp))
     st = torch.cuda.current_stream()
     times = []
     for i in range(steps + 3):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(st)
-        q.copy_(hq, non_blocking=True)
-        words.copy_(hw, non_blocking=True)
-        sl.copy_(hs, non_blocking=True)
-        qp.copy_(hp, non_blocking=True)
-        L.decode(d["p"], q, d["k"], d["v"], words, sl, qp, d["rope"], out=d["out"], workspace=d["ws"])
+        for h, g in zip(host, dev):
+            g.copy_(h, non_blocking=True)
+        L.decode_shared(d["p"], q, d["k"], d["v"], words, qp, d["rope"], dplan, out=d["out"], workspace=d["ws_sh"])
         hout.copy_(d["out"], non_blocking=True)
         b.record(st)
         b.synchronize()
         if i >= 3:
             times.append(a.elapsed_time(b) * 1e-3)
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hw, hs, hp))
+    h2d = sum(x.numel() * x.element_size() for x in host)
     d2h = hout.numel() * hout.element_size()
     return {"value": nbytes["kv_logical"] / statistics.mean(times) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * statistics.mean(times)}
@@ -414,24 +463,40 @@ def measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust):
     from paged_kv_cache_57_gb300 import workloads as W
     out = {}
     n = max(20, min(args.steps, 200))
-    # Lazy overhead: same pool and block table, rotation compiled out (interleaved A/B).
-    t1, t0 = [], []
-    for _ in range(4):
-        t1 += time_steps(lambda: run_decode(d, lazy=True), n // 4, 2, flush)
-        t0 += time_steps(lambda: run_decode(d, lazy=False), n // 4, 2, flush)
-    d["p"].lazy = 1
-    dec_over = 100.0 * (statistics.median(t1) / statistics.median(t0) - 1.0)
-    out["lazy_overhead_pct"] = {"decode": dec_over, "decode_ms_lazy": 1e3 * statistics.median(t1),
-                                "decode_ms_prerotated": 1e3 * statistics.median(t0),
+    nb8 = decode_bytes(w)
+
+    def ab(dd, path):
+        """Interleaved A/B: lazy rotation vs the same kernel with rotation compiled out
+        (same pool and block table). Returns (median lazy s, median control s)."""
+        t1, t0 = [], []
+        for _ in range(4):
+            t1 += time_steps(lambda: run_decode(dd, lazy=True, path=path), n // 4, 2, flush)
+            t0 += time_steps(lambda: run_decode(dd, lazy=False, path=path), n // 4, 2, flush)
+        dd["p"].lazy = 1
+        return statistics.median(t1), statistics.median(t0)
+
+    sh1, sh0 = ab(d, "shared")
+    sq1, sq0 = ab(d, "seq")
+    out["lazy_overhead_pct"] = {"decode": 100.0 * (sh1 / sh0 - 1.0), "decode_ms_lazy": 1e3 * sh1,
+                                "decode_ms_prerotated": 1e3 * sh0,
+                                "decode_per_sequence_path": 100.0 * (sq1 / sq0 - 1.0),
                                 "pages_h100_context": {"decode_latency": 0.13, "prefill_flops_m128": 0.59}}
+    # The per-sequence path (lazy_attn_decode) on the same workload, for comparison.
+    out["decode_per_sequence_path"] = {"ms_median": 1e3 * sq1, "kv_gbs_logical": nb8["kv_logical"] / sq1 / 1e9,
+                                       "kv_gbs_unique": nb8["unique"] / sq1 / 1e9,
+                                       "hbm_frac_unique_of_measured": nb8["unique"] / sq1 / 1e9 / hbm}
     # No-sharing control: logical bytes = unique bytes = DRAM bytes.
     wc = W.FULL["llama8b_decode_noshare"]()
     dc = build_device(wc)
-    tc = time_steps(lambda: run_decode(dc), n, 3, flush)
     bc = decode_bytes(wc)
-    gbs = bc["unique"] / statistics.median(tc) / 1e9
-    out["noshare_control"] = {"workload": "llama8b_decode_noshare", "gbs": gbs, "frac_of_measured": gbs / hbm,
-                              "frac_of_8tbs": gbs / 8000.0, "ms_median": 1e3 * statistics.median(tc)}
+    ctl = {"workload": "llama8b_decode_noshare"}
+    for path in ("shared", "seq"):
+        tc = statistics.median(time_steps(lambda: run_decode(dc, path=path), n, 3, flush))
+        gbs = bc["unique"] / tc / 1e9
+        key = "" if path == "shared" else "per_sequence_"
+        ctl.update({key + "gbs": gbs, key + "frac_of_measured": gbs / hbm, key + "frac_of_8tbs": gbs / 8000.0,
+                    key + "ms_median": 1e3 * tc})
+    out["noshare_control"] = ctl
     del dc
     # Prefill (Llama-3.1-8B-shaped, 8 x (6 x 1024 docs + 256-token chunk)).
     try:
@@ -451,14 +516,15 @@ def measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust):
     # Llama-3.1-70B-shaped decode: 32 x 16 x 1024 Zipf(1.0) of 512, pool capped at 1 GiB.
     w4 = W.FULL["llama70b_decode"]()
     d4 = build_device(w4)
-    t4 = time_steps(lambda: run_decode(d4, lazy=True), n, 3, flush)
-    t40 = time_steps(lambda: run_decode(d4, lazy=False), n, 3, flush)
     b4 = decode_bytes(w4)
-    out["llama70b_decode"] = {"kv_gbs_logical": b4["kv_logical"] / statistics.median(t4) / 1e9,
-                              "kv_gbs_unique": b4["unique"] / statistics.median(t4) / 1e9,
-                              "tokens_per_s": w4.num_seqs / statistics.median(t4),
-                              "ms_median": 1e3 * statistics.median(t4),
-                              "lazy_overhead_pct": 100.0 * (statistics.median(t4) / statistics.median(t40) - 1.0)}
+    s41, s40 = ab(d4, "shared")
+    q41, _ = ab(d4, "seq")
+    out["llama70b_decode"] = {"kv_gbs_logical": b4["kv_logical"] / s41 / 1e9,
+                              "kv_gbs_unique": b4["unique"] / s41 / 1e9,
+                              "hbm_frac_unique_of_measured": b4["unique"] / s41 / 1e9 / hbm,
+                              "tokens_per_s": w4.num_seqs / s41, "ms_median": 1e3 * s41,
+                              "lazy_overhead_pct": 100.0 * (s41 / s40 - 1.0),
+                              "per_sequence_path_ms": 1e3 * q41}
     del d4
     # Mixed continuous batch, MQA 32/1: 48 decode sequences + 4 prefill chunks of 512, one
     # shared pool, both calls on one stream and timed as one step.

@@ -178,6 +178,56 @@ int lazy_attn_decode(const lazy_attn_params *p, const void *q, const void *k_poo
                      const void *rope_table, void *out, void *workspace, size_t workspace_bytes,
                      lazy_stream_t stream);
 
+/* ---------------------------------------------------------------- shared-run decode
+ * The same decode result as lazy_attn_decode, for batches whose sequences cite
+ * the same cached documents. Because stored keys carry no global position
+ * ("Metodologia: Codificação Posicional Diferida"), one physical block serves
+ * every sequence that cites it, at whatever offset each places it; this entry
+ * point reads each such block once per KV head for the whole batch instead of
+ * once per sequence, and applies each sequence's own relative rotation R_{m-p}
+ * to its query ("Implementação Técnica", item 2: one rotation per document run).
+ *
+ * Plan (host): lazy_attn_plan_shared_host takes the document lists of the
+ * block-word packer (same arguments, host memory). Occurrences of one document
+ * with the same used length read the same physical blocks; they are grouped,
+ * split into sets of at most LAZY_PLAN_MAX_MEMBERS members and 64 query rows
+ * (members x query heads per KV head), and each set's blocks are cut into chunks
+ * of chunk_blocks / RT logical blocks, RT = 1, 2 or 4 tiles of 16 rows (0 selects
+ * chunk_blocks = 32 for up to 8 query heads per KV head, 64 up to 16, else 128).
+ * It writes
+ *   items_host [num_items][LAZY_PLAN_ITEM_INTS] int32, one work item each:
+ *     [0] src_seq, [1] b0, [2] nblk, [3] last_valid, [4] nmem, [5..7] 0: nblk
+ *         logical blocks of sequence src_seq from block b0, all full but the
+ *         last (last_valid slots), computed for nmem members;
+ *     [8 + 4j ..] member j < nmem: {seq, b0, slot, 0}: sequence seq holds the
+ *         same physical blocks at its logical blocks b0 .. b0+nblk-1 and its
+ *         partial result goes to `slot`; unused member entries are 0;
+ *   slot_indptr_host [B+1]: the slots of sequence s are slot_indptr[s] ..
+ *     slot_indptr[s+1]-1;
+ *   counts_host [2] = {num_items, num_slots}.
+ * Items are ordered heaviest first. `capacity` bounds the item count (the number
+ * of logical blocks in the batch always suffices). Returns LAZY_ERR_LAYOUT on the
+ * packer's layout errors, and LAZY_ERR_WORKSPACE if capacity is too small.
+ *
+ * Decode: items and slot_indptr copied to device memory unchanged (items 16-byte
+ * aligned), block_words packed from the same document lists. workspace: at least
+ * lazy_attn_decode_shared_workspace_bytes(p, num_slots) bytes, 16-byte aligned.
+ * bf16 only; at most 64 query heads per KV head. A member whose first block does
+ * not hold the item's physical block, or an item outside the table, sets
+ * LAZY_DEV_LAYOUT and is skipped. */
+#define LAZY_PLAN_MAX_MEMBERS 16
+#define LAZY_PLAN_ITEM_INTS (8 + 4 * LAZY_PLAN_MAX_MEMBERS)
+int lazy_attn_plan_shared_host(const lazy_attn_params *p, int32_t num_docs, const int32_t *seg_indptr_host,
+                               const int32_t *seg_doc_host, const int32_t *seg_len_host,
+                               const int32_t *doc_block_indptr_host, const int32_t *doc_blocks_host,
+                               int32_t chunk_blocks, int32_t capacity, int32_t *items_host,
+                               int32_t *slot_indptr_host, int32_t *counts_host);
+size_t lazy_attn_decode_shared_workspace_bytes(const lazy_attn_params *p, int32_t num_slots);
+int lazy_attn_decode_shared(const lazy_attn_params *p, const void *q, const void *k_pool, const void *v_pool,
+                            const uint32_t *block_words, const int32_t *q_pos, const void *rope_table,
+                            int32_t num_items, const int32_t *items, int32_t num_slots, const int32_t *slot_indptr,
+                            void *out, void *workspace, size_t workspace_bytes, lazy_stream_t stream);
+
 /* ---------------------------------------------------------------- decode without allocation
  * The pages have no counterpart for this entry point; it exists for callers that
  * cannot allocate device memory for a workspace: an engine that has reserved nearly

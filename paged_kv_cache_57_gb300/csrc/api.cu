@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -318,6 +319,93 @@ int lazy_attn_decode(const lazy_attn_params* p, const void* q, const void* k_poo
   }
   if (rc != LAZY_OK || splits == 1) return rc;
   return launched(lazy::launch_combine(a, p->dtype == LAZY_BF16, cs));
+}
+
+int lazy_attn_plan_shared_host(const lazy_attn_params* p, int32_t num_docs, const int32_t* seg_indptr,
+                               const int32_t* seg_doc, const int32_t* seg_len, const int32_t* doc_block_indptr,
+                               const int32_t* doc_blocks, int32_t chunk_blocks, int32_t capacity, int32_t* items,
+                               int32_t* slot_indptr, int32_t* counts) {
+  Checked c;
+  int rc = check_params(p, &c);
+  if (rc != LAZY_OK) return rc;
+  if (num_docs < 0 || capacity < 0 || chunk_blocks < 0 || !slot_indptr || !counts) return LAZY_ERR_INVALID_ARG;
+  if (p->num_seqs > 0 && !seg_indptr) return LAZY_ERR_INVALID_ARG;
+  if (p->num_seqs > 0 && seg_indptr[p->num_seqs] > seg_indptr[0] &&
+      (!seg_doc || !seg_len || !doc_block_indptr || !doc_blocks || !items))
+    return LAZY_ERR_INVALID_ARG;
+  if (c.G > 64) return LAZY_ERR_UNSUPPORTED;
+  const int cb = chunk_blocks > 0 ? chunk_blocks : (c.G <= 8 ? 32 : (c.G <= 16 ? 64 : 128));
+  return lazy::plan_shared_host(p->num_seqs, c.G, p->max_blocks_per_seq, p->num_pool_blocks, num_docs, seg_indptr,
+                                seg_doc, seg_len, doc_block_indptr, doc_blocks, cb, capacity, items, slot_indptr,
+                                counts);
+}
+
+size_t lazy_attn_decode_shared_workspace_bytes(const lazy_attn_params* p, int32_t num_slots) {
+  Checked c;
+  if (check_params(p, &c) != LAZY_OK || num_slots < 0) return 0;
+  size_t bytes = (size_t)num_slots * p->num_q_heads * (p->head_dim + 2) * sizeof(float);
+#ifdef LAZY_DECODE_TRACE
+  bytes += (size_t)64 << 20;  // phase timestamps, 64 bytes per CTA
+#endif
+  return bytes;
+}
+
+int lazy_attn_decode_shared(const lazy_attn_params* p, const void* q, const void* k_pool, const void* v_pool,
+                            const uint32_t* block_words, const int32_t* q_pos, const void* rope_table,
+                            int32_t num_items, const int32_t* items, int32_t num_slots, const int32_t* slot_indptr,
+                            void* out, void* workspace, size_t workspace_bytes, lazy_stream_t stream) {
+  Checked c;
+  int rc = check_params(p, &c);
+  if (rc != LAZY_OK) return rc;
+  if (p->dtype != LAZY_BF16) return LAZY_ERR_UNSUPPORTED;
+  if (c.G > 64) return LAZY_ERR_UNSUPPORTED;
+  if (num_items < 0 || num_slots < 0) return LAZY_ERR_INVALID_ARG;
+  if (p->num_seqs == 0) return LAZY_OK;
+  if (!q || !k_pool || !v_pool || !block_words || !q_pos || !rope_table || !slot_indptr || !out)
+    return LAZY_ERR_INVALID_ARG;
+  if (num_items > 0 && (!items || num_slots == 0)) return LAZY_ERR_INVALID_ARG;
+  if ((int64_t)num_items * p->num_kv_heads > INT32_MAX) return LAZY_ERR_UNSUPPORTED;
+  if (p->num_pool_blocks == 0 || p->max_blocks_per_seq == 0) return LAZY_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) || !aligned16(rope_table) ||
+      (items && !aligned16(items)))
+    return LAZY_ERR_INVALID_ARG;
+  const size_t need = lazy_attn_decode_shared_workspace_bytes(p, num_slots);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return LAZY_ERR_WORKSPACE;
+  unsigned int* st = status_ptr();
+  if (!st) return LAZY_ERR_CUDA;
+  lazy::SharedDecodeArgs a{};
+  a.q = q;
+  a.words = block_words;
+  a.q_pos = q_pos;
+  a.rope = static_cast<const float2*>(rope_table);
+  a.items = items;
+  a.slot_indptr = slot_indptr;
+  a.out = out;
+  a.ws_o = static_cast<float*>(workspace);
+  a.ws_ml = need ? static_cast<float*>(workspace) + (size_t)num_slots * p->num_q_heads * p->head_dim : nullptr;
+  a.status = st;
+  a.B = p->num_seqs;
+  a.Hq = p->num_q_heads;
+  a.Hkv = p->num_kv_heads;
+  a.G = c.G;
+  a.D = p->head_dim;
+  a.max_blocks = p->max_blocks_per_seq;
+  a.id_bits = c.id_bits;
+  a.num_pool_blocks = p->num_pool_blocks;
+  a.num_items = num_items;
+  a.num_slots = num_slots;
+  a.scale_log2 = scale_log2(p);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (num_items > 0) {
+    CUtensorMap kmap, vmap;
+    const uint64_t rows = (uint64_t)p->num_pool_blocks * p->num_kv_heads * lazy::kBlock;
+    if (!encode_rows_map(&kmap, k_pool, rows, p->head_dim, lazy::kBlock) ||
+        !encode_rows_map(&vmap, v_pool, rows, p->head_dim, lazy::kBlock))
+      return LAZY_ERR_CUDA;
+    rc = launched(lazy::launch_decode_shared(a, p->lazy != 0, kmap, vmap, cs));
+    if (rc != LAZY_OK) return rc;
+  }
+  return launched(lazy::launch_shared_combine(a, cs));
 }
 
 size_t lazy_attn_prefill_workspace_bytes(const lazy_attn_params* p, int32_t total_q) {

@@ -28,7 +28,7 @@
 #include <cfloat>
 #include <climits>
 
-#include "common.cuh"
+#include "decode_block.cuh"
 #include "kernels.h"
 
 #ifndef LAZY_DECODE_SPT
@@ -58,41 +58,6 @@ struct DecodeCfg {
   static constexpr int SMEM = 1024 + STAGES_BYTES + QS_BYTES + BAR_BYTES;
 };
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
-// Warp-uniform bounded wait: every lane polls, and the warp gives up together.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* status) {
-  const bool ok = mbar_wait(bar, parity, status);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// Issues the TMA loads of one block's K and V rows (kv head kvh) into `stage`,
-// completing on `bar`; an invalid id is not loaded (the barrier is just arrived).
-template <int D>
-__device__ __forceinline__ void load_block(uint8_t* stage, uint64_t* bar, int phys, int num_pool_blocks, int hkv,
-                                           int kvh, const CUtensorMap* kmap, const CUtensorMap* vmap) {
-  constexpr int NBOX = D / 64, BOX_BYTES = kBlock * 128;
-  if (phys < num_pool_blocks) {
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, 2 * NBOX * BOX_BYTES);
-    const int y = (phys * hkv + kvh) * kBlock;
-#pragma unroll
-    for (int bx = 0; bx < NBOX; ++bx) tma_load_2d(stage + bx * BOX_BYTES, kmap, bar, bx * 64, y);
-#pragma unroll
-    for (int bx = 0; bx < NBOX; ++bx) tma_load_2d(stage + (NBOX + bx) * BOX_BYTES, vmap, bar, bx * 64, y);
-  } else {
-    mbar_arrive(bar);
-  }
-}
-
-// Per-lane description of one logical block: physical id, document start and
-// valid slots (0 and an out-of-pool id for a block that must not be loaded).
-struct LaneBlock {
-  int phys, p, nv;
-};
-
 __device__ __forceinline__ LaneBlock describe_block(bool live, int b, int nb, int seq_len, uint32_t w, uint32_t wn,
                                                     int id_bits, int num_pool_blocks, unsigned int* status) {
   LaneBlock r{num_pool_blocks, 0, 0};
@@ -111,14 +76,14 @@ __device__ __forceinline__ LaneBlock describe_block(bool live, int b, int nb, in
   return r;
 }
 
-// A fragments of R_delta q for rows (mt*16 + g, mt*16 + g + 8), g = lane/4.
+// A fragments of scale * R_delta q for rows (mt*16 + g, mt*16 + g + 8), g = lane/4.
 // The thread owns columns 16ks + 2t + {0,1,8,9}; ks and ks + D/32 hold the two
 // halves of the same rotate-half pairs, so each pair is rotated by one thread.
 // cs_of(ks, i) returns (cos, sin) for frequency i and is called by all lanes
 // with the same ks sequence (it may shuffle).
 template <int D, int QS_STRIDE, typename CsFn>
 __device__ __forceinline__ void build_q_frags(uint32_t (&qa)[D / 16][4], const float* __restrict__ qs, int mt,
-                                              int lane, CsFn cs_of) {
+                                              int lane, float scale, CsFn cs_of) {
   constexpr int HALF = D / 2;
   const int g = lane >> 2, t = lane & 3;
   const float* r0 = qs + (mt * 16 + g) * QS_STRIDE;
@@ -129,8 +94,9 @@ __device__ __forceinline__ void build_q_frags(uint32_t (&qa)[D / 16][4], const f
 #pragma unroll
     for (int e2 = 0; e2 < 2; ++e2) {
       const int i = 16 * ks + 2 * t + 8 * e2;  // columns i, i+1
-      const float2 c0 = cs_of(ks, i);
-      const float2 c1 = cs_of(ks, i + 1);
+      float2 c0 = cs_of(ks, i);
+      float2 c1 = cs_of(ks, i + 1);
+      c0.x *= scale, c0.y *= scale, c1.x *= scale, c1.y *= scale;
       const float2 x0 = *reinterpret_cast<const float2*>(r0 + i);
       const float2 y0 = *reinterpret_cast<const float2*>(r0 + i + HALF);
       const float2 x1 = *reinterpret_cast<const float2*>(r1 + i);
@@ -238,7 +204,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS, MT == 1 ? 3 :
   auto rebuild = [&](int delta) {
 #pragma unroll
     for (int j = 0; j < CPL; ++j) cs[j] = rope_cs(tr[j], delta, a.status);
-    build_q_frags<D, C::QS_STRIDE>(qa, qs, mt, lane, [&](int ks, int i) {
+    build_q_frags<D, C::QS_STRIDE>(qa, qs, mt, lane, a.scale_log2, [&](int ks, int i) {
       const float2 v = cs[(16 * ks) >> 5];
       return make_float2(__shfl_sync(0xffffffffu, v.x, i & 31), __shfl_sync(0xffffffffu, v.y, i & 31));
     });
@@ -249,7 +215,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS, MT == 1 ? 3 :
 #pragma unroll
   for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
-  const float sl2 = a.scale_log2;
+  const LdsmLane ln = ldsm_lane(lane);
   int k = 0, cbase = 0;  // next block of the team; first block of the current word chunk
   int p_seg = nk > 0 ? __shfl_sync(0xffffffffu, cur.p, 0) : 0;
   bool aborted = false;
@@ -275,88 +241,19 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS, MT == 1 ? 3 :
         break;
       }
     }
-    if (!warp_wait(&tfull[slot], (k / SPT) & 1, a.status)) {
+    bool ok = warp_wait(&tfull[slot], (k / SPT) & 1, a.status);
+    if (ok) attend_block<D>(smem_u32(tst + slot * C::STAGE_BYTES), ln, qa, nvalid, o, m_r, l_r, lane);
+    // The team's warps are all done with this stage (and agree to go on) before it is refilled.
+    if constexpr (MT > 1) ok = team_and(team, 32 * MT, ok);
+    if (!ok) {
       abort_flag = 1;
       aborted = true;
       break;
     }
-    const uint32_t kbase = smem_u32(tst + slot * C::STAGE_BYTES);
-    const uint32_t vbase = kbase + C::KV_BYTES;
-
-    // S = q' K^T for the 16 keys: two n-tiles of 8 keys.
-    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    {
-      const int mat = lane >> 3;
-      const int key = (mat >> 1) * 8 + (lane & 7);
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const int chunk = 2 * ks + (mat & 1);
-        uint32_t r[4];
-        ldsm_x4(r, kbase + (chunk >> 3) * C::BOX_BYTES + sw128(key, chunk & 7));
-        mma_16816(sacc[0], qa[ks], r[0], r[1]);
-        mma_16816(sacc[1], qa[ks], r[2], r[3]);
-      }
-    }
-    // Online softmax over this block (rows g and g+8 of the tile).
-    uint32_t pa[4];
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      float sv[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = (e >> 1) * 8 + 2 * t + (e & 1);
-        const float v = sacc[e >> 1][2 * rr + (e & 1)] * sl2;
-        sv[e] = key < nvalid ? v : -INFINITY;
-      }
-      float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m_r[rr], mx);
-      const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = exp2f(m_r[rr] - m_use);
-      m_r[rr] = m_new;
-      const uint32_t lo = pack_bf16x2(exp2f(sv[0] - m_use), exp2f(sv[1] - m_use));
-      const uint32_t hi = pack_bf16x2(exp2f(sv[2] - m_use), exp2f(sv[3] - m_use));
-      pa[rr] = lo;      // keys 2t, 2t+1     (a0 / a1)
-      pa[2 + rr] = hi;  // keys 8+2t, 8+2t+1 (a2 / a3)
-      const __nv_bfloat162 lb = *reinterpret_cast<const __nv_bfloat162*>(&lo);
-      const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162*>(&hi);
-      l_r[rr] = l_r[rr] * alpha + (__low2float(lb) + __high2float(lb)) + (__low2float(hb) + __high2float(hb));
-      if (alpha != 1.f) {
-#pragma unroll
-        for (int j = 0; j < D / 8; ++j) {
-          o[j][2 * rr] *= alpha;
-          o[j][2 * rr + 1] *= alpha;
-        }
-      }
-    }
-    // O += P V: V^T fragments via ldmatrix.trans, two d-tiles per load.
-    {
-      const int mat = lane >> 3;
-      const int key = (mat & 1) * 8 + (lane & 7);
-      uint32_t m0 = 0xffffffffu, m1 = 0xffffffffu;
-      if (nvalid < kBlock) {  // hole slots may hold anything: zero their V
-        const int k0 = 2 * t;
-        m0 = (k0 < nvalid ? 0x0000ffffu : 0u) | (k0 + 1 < nvalid ? 0xffff0000u : 0u);
-        m1 = (k0 + 8 < nvalid ? 0x0000ffffu : 0u) | (k0 + 9 < nvalid ? 0xffff0000u : 0u);
-      }
-#pragma unroll
-      for (int c = 0; c < D / 16; ++c) {
-        const int chunk = 2 * c + (mat >> 1);
-        uint32_t r[4];
-        ldsm_x4_trans(r, vbase + (chunk >> 3) * C::BOX_BYTES + sw128(key, chunk & 7));
-        mma_16816(o[2 * c], pa, r[0] & m0, r[1] & m1);
-        mma_16816(o[2 * c + 1], pa, r[2] & m0, r[3] & m1);
-      }
-    }
+    __syncwarp();
     // Refill this stage with the team's block SPT positions ahead.
     const int kn = k + SPT;
     if (kn < nk) {
-      if constexpr (MT > 1) {
-        asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(32 * MT) : "memory");
-      } else {
-        __syncwarp();
-      }
       int phys;
       if ((kn >> 5) == (k >> 5)) {
         phys = __shfl_sync(0xffffffffu, cur.phys, kn & 31);

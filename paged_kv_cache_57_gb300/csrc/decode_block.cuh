@@ -1,0 +1,196 @@
+// decode_block.cuh -- the per-block step shared by the bf16 decode kernels: one
+// 16-token K/V block (TMA-written, 128-byte swizzled boxes of 64 columns) against
+// one 16-row tile of rotated queries held as mma.sync A fragments.
+//
+// S = q' K^T with mma.sync m16n8k16 (bf16 in, fp32 accumulate), then the online
+// (max, sum) softmax of "KV Cache, Flash Attention & Otimização de Inferência",
+// "Flash Attention -- tiling" (running maximum in log2 units, rescale of the
+// running output when it grows), then O += P V with P rounded to bf16.
+#pragma once
+
+#include "common.cuh"
+
+namespace lazy {
+
+template <int D>
+struct BlockGeom {
+  static constexpr int NBOX = D / 64;             // 64-column (128-byte) TMA boxes per row
+  static constexpr int BOX_BYTES = kBlock * 128;  // one box: 16 rows x 128 bytes
+  static constexpr int KV_BYTES = NBOX * BOX_BYTES;
+  static constexpr int STAGE_BYTES = 2 * KV_BYTES;  // K then V
+};
+
+// Issues the TMA loads of one block's K and V rows (kv head kvh) into `stage`,
+// completing on `bar`; an id outside the pool is not loaded (the barrier is just
+// arrived, and the caller treats the block as empty).
+template <int D>
+__device__ __forceinline__ void load_block(uint8_t* stage, uint64_t* bar, int phys, int num_pool_blocks, int hkv,
+                                           int kvh, const CUtensorMap* kmap, const CUtensorMap* vmap) {
+  using G = BlockGeom<D>;
+  if (phys < num_pool_blocks) {
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, G::STAGE_BYTES);
+    const int y = (phys * hkv + kvh) * kBlock;
+#pragma unroll
+    for (int bx = 0; bx < G::NBOX; ++bx) tma_load_2d(stage + bx * G::BOX_BYTES, kmap, bar, bx * 64, y);
+#pragma unroll
+    for (int bx = 0; bx < G::NBOX; ++bx) tma_load_2d(stage + (G::NBOX + bx) * G::BOX_BYTES, vmap, bar, bx * 64, y);
+  } else {
+    mbar_arrive(bar);
+  }
+}
+
+// Per-lane ldmatrix offsets inside a stage, computed once per kernel. In a box
+// written with the 128-byte swizzle, 16-byte chunk c of row r sits at
+// (r << 7) | ((c ^ r) & 7) << 4. A lane's chunk for k-step ks is 2 ks plus a
+// lane bit, so its offset is the lane constant below XOR ((2 ks) & 7) << 4
+// (bits 4-6 only), plus 2048 bytes per 64-column box.
+struct LdsmLane {
+  uint32_t k;  // K tile (B operand of S = q' K^T), keys (mat >> 1) * 8 + lane % 8
+  uint32_t v;  // V tile (transposed B operand of O += P V), keys (mat & 1) * 8 + lane % 8
+};
+
+__device__ __forceinline__ LdsmLane ldsm_lane(int lane) {
+  const uint32_t mat = (uint32_t)lane >> 3;
+  const uint32_t kk = (mat >> 1) * 8 + (lane & 7);
+  const uint32_t vk = (mat & 1) * 8 + (lane & 7);
+  LdsmLane r;
+  r.k = (kk << 7) + ((((mat & 1) ^ kk) & 7) << 4);
+  r.v = (vk << 7) + ((((mat >> 1) ^ vk) & 7) << 4);
+  return r;
+}
+
+// The running maximum is refreshed only when a block's maximum exceeds it by
+// more than this (log2 units): weights then stay below 2^8, and the output and
+// sum are rescaled rarely.
+constexpr float kDecodeRescaleLog2 = 8.f;
+
+// One block for the warp's 16-row tile: rows g = lane/4 and g + 8 hold the
+// running state (reference maximum m_r and sum l_r per row, o in accumulator
+// layout). The query fragments carry the softmax scale and log2(e), so scores
+// come out in log2 units. Only the first `nvalid` slots of the block are keys;
+// the others (holes, an unloaded block) get weight 0 and their V rows are masked
+// out of the product.
+template <int D>
+__device__ __forceinline__ void attend_block(uint32_t kbase, LdsmLane ln, const uint32_t (&qa)[D / 16][4], int nvalid,
+                                             float (&o)[D / 8][4], float (&m_r)[2], float (&l_r)[2], int lane) {
+  using G = BlockGeom<D>;
+  const int t = lane & 3;
+  const uint32_t ka = kbase + ln.k;
+  const uint32_t va = kbase + G::KV_BYTES + ln.v;
+  // S = q' K^T for the 16 keys: two n-tiles of 8 keys, each summed in two
+  // independent chains (even and odd k-steps) to halve the dependent MMA latency.
+  float sc[2][2][4];
+#pragma unroll
+  for (int n = 0; n < 2; ++n)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) sc[n][c][0] = sc[n][c][1] = sc[n][c][2] = sc[n][c][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    uint32_t r[4];
+    ldsm_x4(r, (ka ^ (uint32_t)(((2 * ks) & 7) << 4)) + (ks >> 2) * G::BOX_BYTES);
+    mma_16816(sc[0][ks & 1], qa[ks], r[0], r[1]);
+    mma_16816(sc[1][ks & 1], qa[ks], r[2], r[3]);
+  }
+  // sv[rr][e]: row g + 8 rr, key (e >> 1) * 8 + 2t + (e & 1).
+  float sv[2][4];
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sv[rr][e] = sc[e >> 1][0][2 * rr + (e & 1)] + sc[e >> 1][1][2 * rr + (e & 1)];
+  const bool partial = nvalid < kBlock;  // warp-uniform
+  if (partial) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int key = (e >> 1) * 8 + 2 * t + (e & 1);
+      if (key >= nvalid) sv[0][e] = sv[1][e] = -INFINITY;
+    }
+  }
+  uint32_t pa[4];
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    float mx = fmaxf(fmaxf(sv[rr][0], sv[rr][1]), fmaxf(sv[rr][2], sv[rr][3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    if (mx > m_r[rr] + kDecodeRescaleLog2) {  // first valid key, or a much larger score
+      const float alpha = fast_ex2(m_r[rr] - mx);  // 0 while the row had no key
+      m_r[rr] = mx;
+      l_r[rr] *= alpha;
+#pragma unroll
+      for (int j = 0; j < D / 8; ++j) {
+        o[j][2 * rr] *= alpha;
+        o[j][2 * rr + 1] *= alpha;
+      }
+    }
+    const float mu = m_r[rr] == -INFINITY ? 0.f : m_r[rr];
+    const uint32_t lo = pack_bf16x2(fast_ex2(sv[rr][0] - mu), fast_ex2(sv[rr][1] - mu));
+    const uint32_t hi = pack_bf16x2(fast_ex2(sv[rr][2] - mu), fast_ex2(sv[rr][3] - mu));
+    pa[rr] = lo;      // keys 2t, 2t+1     (a0 / a1)
+    pa[2 + rr] = hi;  // keys 8+2t, 8+2t+1 (a2 / a3)
+    // The row sum uses the same bf16-rounded weights as the product.
+    l_r[rr] += (__uint_as_float(lo << 16) + __uint_as_float(lo & 0xffff0000u)) +
+               (__uint_as_float(hi << 16) + __uint_as_float(hi & 0xffff0000u));
+  }
+  // O += P V: V^T fragments via ldmatrix.trans, two d-tiles per load.
+  if (!partial) {
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+      uint32_t r[4];
+      ldsm_x4_trans(r, (va ^ (uint32_t)(((2 * c) & 7) << 4)) + (c >> 2) * G::BOX_BYTES);
+      mma_16816(o[2 * c], pa, r[0], r[1]);
+      mma_16816(o[2 * c + 1], pa, r[2], r[3]);
+    }
+  } else {  // hole slots may hold anything (even NaN): zero their V
+    const int k0 = 2 * t;
+    const uint32_t m0 = (k0 < nvalid ? 0x0000ffffu : 0u) | (k0 + 1 < nvalid ? 0xffff0000u : 0u);
+    const uint32_t m1 = (k0 + 8 < nvalid ? 0x0000ffffu : 0u) | (k0 + 9 < nvalid ? 0xffff0000u : 0u);
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+      uint32_t r[4];
+      ldsm_x4_trans(r, (va ^ (uint32_t)(((2 * c) & 7) << 4)) + (c >> 2) * G::BOX_BYTES);
+      mma_16816(o[2 * c], pa, r[0] & m0, r[1] & m1);
+      mma_16816(o[2 * c + 1], pa, r[2] & m0, r[3] & m1);
+    }
+  }
+}
+
+// Per-lane description of one logical block: physical id (num_pool_blocks for a
+// block that must not be loaded), document start and valid slots.
+struct LaneBlock {
+  int phys, p, nv;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Warp-uniform bounded wait: every lane polls, and the warp gives up together.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* status) {
+  const bool ok = mbar_wait(bar, parity, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Named barrier of team t (ids 1..4; 0 is __syncthreads) over the team's n threads,
+// with an AND of `ok` over them: a warp whose wait gave up makes the whole team
+// leave together, so no teammate is left at a barrier the others never reach.
+// Literal ids let the compiler see which barriers a kernel uses.
+__device__ __forceinline__ bool team_and(int t, int n, bool ok) {
+  uint32_t r;
+  const uint32_t v = ok ? 1u : 0u;
+#define LAZY_TEAM_AND(ID)                                                                                      \
+  asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, " #ID                 \
+               ", %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"                                                       \
+               : "=r"(r)                                                                                       \
+               : "r"(v), "r"(n)                                                                                \
+               : "memory")
+  switch (t) {
+    case 0: LAZY_TEAM_AND(1); break;
+    case 1: LAZY_TEAM_AND(2); break;
+    case 2: LAZY_TEAM_AND(3); break;
+    default: LAZY_TEAM_AND(4); break;
+  }
+#undef LAZY_TEAM_AND
+  return r != 0;
+}
+
+}  // namespace lazy

@@ -1,0 +1,481 @@
+// decode_shared.cu -- LazyAttention decode over shared document runs (sm_103a).
+//
+// The position-agnostic cache ("Resumo Técnico: LazyAttention", "Metodologia:
+// Codificação Posicional Diferida") stores each document's K and V once, so a
+// batch in which many sequences cite the same documents holds each of those
+// blocks once in HBM, at whatever offset each sequence places it. This kernel
+// reads each such block once per KV head for the whole batch: a work item is one
+// chunk of one document occurrence shared by up to 16 sequences ("members"),
+// possibly at 16 different offsets p. Every member gets its own query rotation
+// R_{m-p} q ("Implementação Técnica", item 2: the query is rotated by the
+// relative offset, only once per document run), and all members' rotated query
+// heads become the rows of the mma.sync tiles that consume the block.
+//
+// CTA: 4 warps. An item has rows = members x g (g = Hq/Hkv query heads per KV
+// head), at most 64, i.e. RT = 1, 2 or 4 row tiles of 16. The warps form
+// TEAMS = 4/RT teams of RT warps; team t owns a contiguous part of the item's
+// blocks and a ring of 8/TEAMS TMA stages (the per-block step, loads and waits
+// are those of decode_bf16.cu). Teams merge in shared memory, and every
+// (member, query head) writes one fp32 partial (m, l, o) to its slot; the
+// combine kernel merges a sequence's slots with the online-softmax rescale.
+#include <cfloat>
+
+#include "decode_block.cuh"
+#include "kernels.h"
+
+namespace lazy {
+
+namespace {
+
+constexpr int kShWarps = 4;
+constexpr int kShThreads = 32 * kShWarps;
+constexpr int kShRows = 64;    // rows per item at most (4 row tiles)
+constexpr int kShStages = 8;   // TMA stages shared out among the teams
+constexpr int kShMembers = LAZY_PLAN_MAX_MEMBERS;
+constexpr int kItemInts = LAZY_PLAN_ITEM_INTS;  // 8 header ints + 4 per member
+static_assert(kItemInts == 8 + 4 * kShMembers && kItemInts % 4 == 0, "item record layout");
+
+template <int D>
+struct SharedCfg {
+  using G = BlockGeom<D>;
+  static constexpr int RED_STRIDE = D + 4;  // merge rows: o[D], m, l, padding to 16 bytes
+  static constexpr int RING_BYTES = kShStages * G::STAGE_BYTES;
+  static constexpr int MERGE_BYTES = kShRows * RED_STRIDE * 4;
+  static constexpr int BUF_BYTES = ((RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES) + 1023) / 1024 * 1024;
+  static constexpr int CS_BYTES = kShMembers * (D / 2) * 8;  // (cos, sin) per member and frequency
+  static constexpr int BAR_BYTES = kShStages * 8;
+  static constexpr int REC_BYTES = kItemInts * 4;
+  static constexpr int META_BYTES = 2 * kShMembers * 4;
+  static constexpr int SMEM = 1024 + BUF_BYTES + CS_BYTES + BAR_BYTES + REC_BYTES + META_BYTES;
+};
+
+}  // namespace
+
+// Optional per-CTA phase timestamps (build with -DLAZY_DECODE_TRACE): 8 x u64 per
+// CTA after the partials in the workspace: start, first loads issued, query
+// fragments ready, main loop done, end, (sm id, item), (row tiles, blocks).
+#ifdef LAZY_DECODE_TRACE
+#define LAZY_TRACE(i, v)                                                                                        \
+  do {                                                                                                          \
+    if (threadIdx.x == 0)                                                                                       \
+      reinterpret_cast<uint64_t*>(a.ws_ml + 2 * (size_t)a.num_slots * a.Hq)[8 * (size_t)blockIdx.x + (i)] = (v); \
+  } while (0)
+#else
+#define LAZY_TRACE(i, v) \
+  do {                   \
+  } while (0)
+#endif
+
+template <int D, bool LAZY>
+__global__ void __launch_bounds__(kShThreads, 3)
+    decode_shared_kernel(const SharedDecodeArgs a, const __grid_constant__ CUtensorMap kmap,
+                         const __grid_constant__ CUtensorMap vmap) {
+  using C = SharedCfg<D>;
+  using G = BlockGeom<D>;
+  constexpr int HALF = D / 2;
+  constexpr int NQ = D / 32;  // k-step pairs of a fragment row
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = align1024(smem_raw);
+  float2* cs_tab = reinterpret_cast<float2*>(ring + C::BUF_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + C::BUF_BYTES + C::CS_BYTES);
+  int* rec = reinterpret_cast<int*>(full + kShStages);  // the item record
+  int* m_delta = rec + kItemInts;                        // rotation offset of each member
+  int* m_ok = m_delta + kShMembers;                      // member passed its checks
+  __shared__ int abort_flag;
+
+  LAZY_TRACE(0, global_timer_ns());
+  const int kvh = blockIdx.x % a.Hkv;
+  const int item = blockIdx.x / a.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // ------------------------------------------------------------ item record (one round trip)
+  if (threadIdx.x < kItemInts / 4)
+    reinterpret_cast<int4*>(rec)[threadIdx.x] =
+        __ldg(reinterpret_cast<const int4*>(a.items) + (size_t)item * (kItemInts / 4) + threadIdx.x);
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < kShStages; ++i) mbar_init(&full[i], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int src = rec[0], b0 = rec[1], nblk = rec[2], last_nv = rec[3], nmem = rec[4];
+  const bool item_ok = src >= 0 && src < a.B && b0 >= 0 && nblk >= 1 && nblk <= a.max_blocks - b0 &&
+                       last_nv >= 1 && last_nv <= kBlock && nmem >= 1 && nmem <= kShMembers &&
+                       nmem * a.G <= kShRows;
+  if (!item_ok) {  // uniform over the CTA: nothing is loaded or written
+    if (threadIdx.x == 0) raise_status(a.status, LAZY_DEV_LAYOUT);
+    return;
+  }
+  auto mem_seq = [&](int m) { return rec[8 + 4 * m]; };
+  auto mem_b0 = [&](int m) { return rec[8 + 4 * m + 1]; };
+  auto mem_slot = [&](int m) { return rec[8 + 4 * m + 2]; };
+  auto seq_in_range = [&](int m) { return mem_seq(m) >= 0 && mem_seq(m) < a.B; };
+
+  // ------------------------------------------------------------ loads that depend only on the record
+  // Issued together, before any is used: the members' first-block words and query
+  // positions, the queries, and (below) the team's block words.
+  // A member's offset p comes from its own word for the run's first block, whose
+  // physical id must be the one the item loads (the source's).
+  uint32_t w_mem = 0u, w_src = 0u;
+  int qp_mem = 0;
+  const float2 t_freq = __ldg(&a.rope[threadIdx.x % HALF]);  // the only frequency this thread evaluates
+  bool mem_good = false;
+  if (threadIdx.x < nmem) {
+    const int m = threadIdx.x, seq = mem_seq(m), bm = mem_b0(m), slot = mem_slot(m);
+    mem_good = seq_in_range(m) && bm >= 0 && bm <= a.max_blocks - nblk && slot >= 0 && slot < a.num_slots;
+    if (mem_good) {
+      w_mem = __ldg(&a.words[(size_t)seq * a.max_blocks + bm]);
+      w_src = __ldg(&a.words[(size_t)src * a.max_blocks + b0]);
+      qp_mem = __ldg(&a.q_pos[seq]);
+    }
+  }
+  // Each lane's query elements: rows rt*16 + g and + 8, columns 16 ks + 2t + {0, 1, 8, 9}
+  // and their rotate-half partners + D/2 (bf16 pairs).
+  const int rows = nmem * a.G;
+  const int RT = rows <= 16 ? 1 : (rows <= 32 ? 2 : 4);
+  const int rt = warp % RT;
+  const int g = lane >> 2, t = lane & 3;
+  uint32_t qx[2][NQ][2], qy[2][NQ][2];
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const int r = rt * 16 + g + 8 * rr;
+    const int m = r / a.G, h = r - m * a.G;
+    const bool live = r < rows && seq_in_range(m);
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.q) +
+                                                             ((size_t)(live ? mem_seq(m) : 0) * a.Hq +
+                                                              (size_t)kvh * a.G + (live ? h : 0)) * D);
+#pragma unroll
+    for (int ks = 0; ks < NQ; ++ks)
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int i = 16 * ks + 2 * t + 8 * e2;
+        qx[rr][ks][e2] = live ? __ldg(qrow + i / 2) : 0u;
+        qy[rr][ks][e2] = live ? __ldg(qrow + (i + HALF) / 2) : 0u;
+      }
+  }
+
+  // ------------------------------------------------------------ teams and first loads
+  const int TEAMS = kShWarps / RT;
+  const int NS = kShStages / TEAMS;  // ring stages of each team: 2, 4 or 8
+  const int team = warp / RT;
+  const int per_team = (nblk + TEAMS - 1) / TEAMS;
+  const int kb0 = team * per_team;
+  const int nk = max(0, min(nblk, kb0 + per_team) - kb0);  // blocks of this team
+  uint8_t* tst = ring + team * NS * G::STAGE_BYTES;
+  uint64_t* tfull = full + team * NS;
+  const bool leader = (rt == 0 && lane == 0);
+  const uint32_t* wrow = a.words + (size_t)src * a.max_blocks + b0 + kb0;  // the team's block words
+  const uint32_t id_mask = (1u << a.id_bits) - 1u;
+  // Lane l describes team block kc + l: physical id (num_pool_blocks = do not load) and valid slots.
+  auto describe = [&](int kc, int& phys, int& nv) {
+    const int k = kc + lane;
+    phys = a.num_pool_blocks;
+    nv = 0;
+    if (k < nk) {
+      const int ph = (int)(__ldg(&wrow[k]) & id_mask);
+      if (ph < a.num_pool_blocks) {
+        phys = ph;
+        nv = (kb0 + k == nblk - 1) ? last_nv : kBlock;
+      } else {
+        raise_status(a.status, LAZY_DEV_BAD_BLOCK_ID);
+      }
+    }
+  };
+  int cur_phys, cur_nv, nxt_phys = a.num_pool_blocks, nxt_nv = 0;
+  describe(0, cur_phys, cur_nv);
+  if (nk > 32) describe(32, nxt_phys, nxt_nv);
+  int issued = 0;
+  {
+    const int pro = min(NS, nk);
+    for (int k = 0; k < pro; ++k) {
+      const int phys = __shfl_sync(0xffffffffu, cur_phys, k);
+      if (leader) load_block<D>(tst + k * G::STAGE_BYTES, &tfull[k], phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
+    }
+    issued = pro;
+  }
+  LAZY_TRACE(1, global_timer_ns());
+
+  if (threadIdx.x < nmem) {
+    const int m = threadIdx.x;
+    bool good = mem_good;
+    int delta = 0;
+    if (good) {
+      const BlockInfo mi = decode_word(w_mem, mem_b0(m), a.id_bits);
+      good = mi.phys == decode_word(w_src, b0, a.id_bits).phys;
+      delta = LAZY ? qp_mem - mi.p : qp_mem;
+    }
+    if (!good) raise_status(a.status, LAZY_DEV_LAYOUT);
+    m_ok[m] = good;
+    m_delta[m] = delta;
+  }
+  __syncthreads();  // m_delta, m_ok
+
+  // ------------------------------------------------------------ rotated query fragments
+  // (cos, sin)(delta_m w_f) for every member m and frequency f; each pair is rotated
+  // by the lane that holds both halves, scaled by sm_scale * log2(e), rounded to bf16.
+  static_assert(kShThreads % HALF == 0, "each thread evaluates one frequency");
+  for (int idx = threadIdx.x; idx < nmem * HALF; idx += kShThreads)
+    cs_tab[idx] = rope_cs(t_freq, m_delta[idx / HALF], a.status);
+  __syncthreads();
+  uint32_t qa[D / 16][4];
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const int r = rt * 16 + g + 8 * rr;
+    const int m = r / a.G;
+    const float2* cs = cs_tab + (r < rows ? m : 0) * HALF;
+    const float sc = (r < rows && m_ok[r < rows ? m : 0]) ? a.scale_log2 : 0.f;  // a failed member's rows are 0
+#pragma unroll
+    for (int ks = 0; ks < NQ; ++ks)
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int i = 16 * ks + 2 * t + 8 * e2;
+        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qx[rr][ks][e2]));
+        const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qy[rr][ks][e2]));
+        float2 c0 = cs[i], c1 = cs[i + 1];
+        c0.x *= sc, c0.y *= sc, c1.x *= sc, c1.y *= sc;
+        qa[ks][rr + 2 * e2] = pack_bf16x2(fmaf(x.x, c0.x, -y.x * c0.y), fmaf(x.y, c1.x, -y.y * c1.y));
+        qa[ks + NQ][rr + 2 * e2] = pack_bf16x2(fmaf(y.x, c0.x, x.x * c0.y), fmaf(y.y, c1.x, x.y * c1.y));
+      }
+  }
+  LAZY_TRACE(2, global_timer_ns());
+
+  // ------------------------------------------------------------ main loop
+  float o[D / 8][4];
+#pragma unroll
+  for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
+  const LdsmLane ln = ldsm_lane(lane);
+  bool nxt_ready = true;  // nxt holds chunk 32 (or nothing)
+  int k = 0;
+  for (; k < nk; ++k) {
+    if (k > 0 && (k & 31) == 0) {  // advance the word chunk
+      cur_phys = nxt_phys;
+      cur_nv = nxt_nv;
+      nxt_ready = false;
+    }
+    const int slot = k % NS;
+    const int nvalid = __shfl_sync(0xffffffffu, cur_nv, k & 31);
+    bool ok = warp_wait(&tfull[slot], (k / NS) & 1, a.status);
+    if (ok) attend_block<D>(smem_u32(tst + slot * G::STAGE_BYTES), ln, qa, nvalid, o, m_r, l_r, lane);
+    // The team's warps are all done with this stage (and agree to go on) before it is refilled.
+    if (RT > 1) ok = team_and(team, 32 * RT, ok);
+    if (!ok) {
+      abort_flag = 1;
+      break;
+    }
+    __syncwarp();
+    // Refill this stage with the team's block NS positions ahead.
+    const int kn = k + NS;
+    if (kn < nk) {
+      int phys;
+      if ((kn >> 5) == (k >> 5)) {
+        phys = __shfl_sync(0xffffffffu, cur_phys, kn & 31);
+      } else {
+        if (!nxt_ready) {
+          describe(kn & ~31, nxt_phys, nxt_nv);
+          nxt_ready = true;
+        }
+        phys = __shfl_sync(0xffffffffu, nxt_phys, kn & 31);
+      }
+      if (leader)
+        load_block<D>(tst + slot * G::STAGE_BYTES, &tfull[slot], phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
+      issued = kn + 1;
+    }
+  }
+  // Copies still in flight (only after a timeout) must land before exit (bounded).
+  if (leader)
+    for (int kk = k; kk < issued; ++kk) mbar_wait(&tfull[kk % NS], (kk / NS) & 1, a.status);
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    l_r[rr] += __shfl_xor_sync(0xffffffffu, l_r[rr], 1);
+    l_r[rr] += __shfl_xor_sync(0xffffffffu, l_r[rr], 2);
+  }
+
+  // ------------------------------------------------------------ partials
+  // One fp32 partial (m, l, o) per (member, query head) in the member's slot. A
+  // member that failed its checks leaves an empty partial (weight 0 in the combine).
+  __syncthreads();  // every team is done with its ring (the merge reuses it)
+  LAZY_TRACE(3, global_timer_ns());
+  if (abort_flag) return;
+  if (TEAMS == 1) {  // one team: write straight from the accumulators
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int r = rt * 16 + g + 8 * rr;
+      if (r >= rows) continue;
+      const int m = r / a.G, h = r - m * a.G;
+      if (mem_slot(m) < 0 || mem_slot(m) >= a.num_slots) continue;
+      const bool good = m_ok[m];
+      const size_t pidx = (size_t)mem_slot(m) * a.Hq + (size_t)kvh * a.G + h;
+      float* dst = a.ws_o + pidx * D + 2 * t;
+#pragma unroll
+      for (int j = 0; j < D / 8; ++j)
+        *reinterpret_cast<float2*>(dst + 8 * j) =
+            good ? make_float2(o[j][2 * rr], o[j][2 * rr + 1]) : make_float2(0.f, 0.f);
+      if (t == 0) *reinterpret_cast<float2*>(a.ws_ml + 2 * pidx) = good ? make_float2(m_r[rr], l_r[rr])
+                                                                         : make_float2(-INFINITY, 0.f);
+    }
+  } else {  // teams merge through shared memory, one warp per row, D/32 columns per lane
+    float* red = reinterpret_cast<float*>(ring);  // [TEAMS][RT*16][RED_STRIDE]
+    const int trows = RT * 16;
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int row = rt * 16 + g + 8 * rr;
+      if (row < rows) {
+        float* dst = red + ((size_t)team * trows + row) * C::RED_STRIDE;
+#pragma unroll
+        for (int j = 0; j < D / 8; ++j)
+          *reinterpret_cast<float2*>(dst + 8 * j + 2 * t) = make_float2(o[j][2 * rr], o[j][2 * rr + 1]);
+        if (t == 0) *reinterpret_cast<float2*>(dst + D) = make_float2(m_r[rr], l_r[rr]);
+      }
+    }
+    __syncthreads();
+    constexpr int PER = D / 32;
+    for (int r = warp; r < rows; r += kShWarps) {
+      const int m = r / a.G, h = r - m * a.G;
+      if (mem_slot(m) < 0 || mem_slot(m) >= a.num_slots) continue;
+      const bool good = m_ok[m];
+      float M = -INFINITY;
+      if (good)
+        for (int tm = 0; tm < TEAMS; ++tm) M = fmaxf(M, red[((size_t)tm * trows + r) * C::RED_STRIDE + D]);
+      float acc[PER], L = 0.f;
+#pragma unroll
+      for (int c = 0; c < PER; ++c) acc[c] = 0.f;
+      if (M != -INFINITY) {
+        for (int tm = 0; tm < TEAMS; ++tm) {
+          const float* srow = red + ((size_t)tm * trows + r) * C::RED_STRIDE;
+          const float w = fast_ex2(srow[D] - M);
+          L += w * srow[D + 1];
+#pragma unroll
+          for (int c = 0; c < PER; ++c) acc[c] += w * srow[PER * lane + c];
+        }
+      }
+      const size_t pidx = (size_t)mem_slot(m) * a.Hq + (size_t)kvh * a.G + h;
+      float* dst = a.ws_o + pidx * D + PER * lane;
+      if constexpr (PER == 4)
+        *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      else
+        *reinterpret_cast<float2*>(dst) = make_float2(acc[0], acc[1]);
+      if (lane == 0) *reinterpret_cast<float2*>(a.ws_ml + 2 * pidx) = make_float2(M, L);
+    }
+  }
+#ifdef LAZY_DECODE_TRACE
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    LAZY_TRACE(4, global_timer_ns());
+    LAZY_TRACE(5, ((uint64_t)item << 16) | smid);
+    LAZY_TRACE(6, ((uint64_t)nblk << 16) | (uint64_t)RT);
+  }
+#endif
+}
+
+// ------------------------------------------------------------------ combine
+// out[s][h] = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k over the sequence's
+// slots k in [slot_indptr[s], slot_indptr[s+1]); a sequence without slots gets 0.
+// One warp per (sequence, query head). Lanes first read 32 slots' (m, l) at a
+// time; the weights are then broadcast by shuffle while each lane accumulates its
+// D/32 output columns, eight slots' rows in flight at once.
+template <int D>
+__global__ void shared_combine_kernel(const SharedDecodeArgs a) {
+  const int wg = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wg >= a.B * a.Hq) return;
+  const int s = wg / a.Hq, h = wg - s * a.Hq;
+  int k0 = a.slot_indptr[s], k1 = a.slot_indptr[s + 1];
+  if (k0 < 0 || k1 < k0 || k1 > a.num_slots) {
+    if (lane == 0) raise_status(a.status, LAZY_DEV_LAYOUT);
+    k0 = k1 = 0;
+  }
+  const float2* ml = reinterpret_cast<const float2*>(a.ws_ml);
+  float M = -INFINITY;
+  for (int k = k0 + lane; k < k1; k += 32) M = fmaxf(M, ml[(size_t)k * a.Hq + h].x);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  constexpr int PER = D / 32;
+  float acc[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) acc[j] = 0.f;
+  float L = 0.f;
+  if (M != -INFINITY) {
+    for (int kc = k0; kc < k1; kc += 32) {
+      const int n = min(32, k1 - kc);
+      float w = 0.f;
+      if (lane < n) {
+        const float2 v = ml[(size_t)(kc + lane) * a.Hq + h];
+        w = fast_ex2(v.x - M);  // an empty slot (m = -inf) weighs 0
+        L += w * v.y;
+      }
+      int j = 0;
+      for (; j + 8 <= n; j += 8) {
+        float wj[8];
+        float vj[8][PER];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          wj[u] = __shfl_sync(0xffffffffu, w, j + u);
+          const float* src = a.ws_o + ((size_t)(kc + j + u) * a.Hq + h) * D + lane * PER;
+          if constexpr (PER == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(src);
+            vj[u][0] = v.x, vj[u][1] = v.y, vj[u][2] = v.z, vj[u][3] = v.w;
+          } else {
+            const float2 v = *reinterpret_cast<const float2*>(src);
+            vj[u][0] = v.x, vj[u][1] = v.y;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+          for (int c = 0; c < PER; ++c) acc[c] = fmaf(wj[u], vj[u][c], acc[c]);
+      }
+      for (; j < n; ++j) {
+        const float wk = __shfl_sync(0xffffffffu, w, j);
+        const float* src = a.ws_o + ((size_t)(kc + j) * a.Hq + h) * D + lane * PER;
+#pragma unroll
+        for (int c = 0; c < PER; ++c) acc[c] = fmaf(wk, src[c], acc[c]);
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + (size_t)wg * D + lane * PER;
+  if constexpr (PER == 4) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                                pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+
+template <int D, bool LAZY>
+static cudaError_t launch_shared_t(const SharedDecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                   cudaStream_t st) {
+  using C = SharedCfg<D>;
+  auto kern = decode_shared_kernel<D, LAZY>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const long long blocks = (long long)a.num_items * a.Hkv;
+  kern<<<(unsigned)blocks, kShThreads, C::SMEM, st>>>(a, kmap, vmap);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_shared(const SharedDecodeArgs& a, bool lazy, const CUtensorMap& kmap,
+                                 const CUtensorMap& vmap, cudaStream_t st) {
+  if (a.num_items == 0) return cudaSuccess;
+  if (a.D == 128) return lazy ? launch_shared_t<128, true>(a, kmap, vmap, st) : launch_shared_t<128, false>(a, kmap, vmap, st);
+  return lazy ? launch_shared_t<64, true>(a, kmap, vmap, st) : launch_shared_t<64, false>(a, kmap, vmap, st);
+}
+
+cudaError_t launch_shared_combine(const SharedDecodeArgs& a, cudaStream_t st) {
+  const int warps = a.B * a.Hq;
+  if (warps == 0) return cudaSuccess;
+  const int threads = 256, blocks = (warps + 7) / 8;
+  if (a.D == 128)
+    shared_combine_kernel<128><<<blocks, threads, 0, st>>>(a);
+  else
+    shared_combine_kernel<64><<<blocks, threads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace lazy

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/lazy_attn.h"
+
 namespace lazy {
 
 struct DecodeArgs {
@@ -61,6 +63,29 @@ struct PrefillArgs {
   float scale_log2;
 };
 
+// Shared-run decode (decode_shared.cu): one CTA per (work item, KV head).
+struct SharedDecodeArgs {
+  const void* q;             // [B][Hq][D] unrotated
+  const uint32_t* words;     // [B][max_blocks]
+  const int32_t* q_pos;      // [B]
+  const float2* rope;        // rotation table
+  const int32_t* items;      // [num_items][LAZY_PLAN_ITEM_INTS]: header, then members {seq, first block, slot}
+  const int32_t* slot_indptr;  // [B+1]
+  void* out;                 // [B][Hq][D] bf16
+  float* ws_o;               // [num_slots][Hq][D]
+  float* ws_ml;              // [num_slots][Hq][2]
+  unsigned int* status;
+  int B, Hq, Hkv, G, D, max_blocks, id_bits, num_pool_blocks;
+  int num_items, num_slots;
+  float scale_log2;
+};
+
+// Host planner of the shared-run decode (shared_plan.cu). counts = {items, slots}.
+int plan_shared_host(int B, int G, int max_blocks, int num_pool_blocks, int num_docs, const int32_t* seg_indptr,
+                     const int32_t* seg_doc, const int32_t* seg_len, const int32_t* doc_block_indptr,
+                     const int32_t* doc_blocks, int chunk_blocks, int capacity, int32_t* items, int32_t* slot_indptr,
+                     int32_t* counts);
+
 // Every launcher returns the cudaError_t of its launch.
 cudaError_t launch_rope_table(float2* table, int head_dim, double theta, cudaStream_t st);
 cudaError_t launch_debug_rope(const float2* table, const int32_t* deltas, int n, int head_dim, float2* out,
@@ -82,6 +107,10 @@ cudaError_t launch_prefill_pair(const PrefillArgs& a, bool lazy, const CUtensorM
 // One query tile per CTA with the rotated Q tile in tensor memory; any GQA ratio.
 cudaError_t launch_prefill_tq(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
                               const CUtensorMap& vmap, cudaStream_t st);
+
+cudaError_t launch_decode_shared(const SharedDecodeArgs& a, bool lazy, const CUtensorMap& kmap,
+                                 const CUtensorMap& vmap, cudaStream_t st);
+cudaError_t launch_shared_combine(const SharedDecodeArgs& a, cudaStream_t st);
 
 // Shared-memory bytes a bf16 decode CTA needs (for occupancy-based split planning).
 int decode_bf16_smem_bytes(int D, int G);

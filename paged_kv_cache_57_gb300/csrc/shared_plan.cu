@@ -1,0 +1,130 @@
+// shared_plan.cu -- host planner of the shared-run decode (decode_shared.cu).
+//
+// Input: the per-sequence document lists the block-word packer takes. Two
+// occurrences (segments) of the same document with the same used length read
+// identical physical blocks, whatever their offsets ("Metodologia: Codificação
+// Posicional Diferida": the stored keys carry no global position, which is what
+// makes them shareable), so they form one group. A group is split into sets of
+// at most LAZY_PLAN_MAX_MEMBERS members and at most 64 query rows (members x
+// query heads per KV head), i.e. RT = 1, 2 or 4 tiles of 16 rows. A set's blocks
+// are cut into chunks of chunk_blocks / RT logical blocks, so that every work
+// item costs about the same (blocks x row tiles); each (set, chunk) is one item,
+// and every member of the set owns one partial-result slot per chunk. The slots
+// of sequence s are slot_indptr[s] .. slot_indptr[s+1]-1.
+//
+// Items are ordered by decreasing cost (blocks x row tiles), and the items of one
+// set stay adjacent, so the CTAs that read the same blocks run at about the same
+// time.
+#include <algorithm>
+#include <map>
+#include <utility>
+#include <vector>
+
+#include "kernels.h"
+
+namespace lazy {
+
+int plan_shared_host(int B, int G, int max_blocks, int num_pool_blocks, int num_docs, const int32_t* seg_indptr,
+                     const int32_t* seg_doc, const int32_t* seg_len, const int32_t* doc_block_indptr,
+                     const int32_t* doc_blocks, int chunk_blocks, int capacity, int32_t* items, int32_t* slot_indptr,
+                     int32_t* counts) {
+  struct Occ {
+    int seq, b0;
+  };
+  const int kBlk = 16;
+  // ---- group the occurrences by (document, used length)
+  std::map<std::pair<int, int>, int> group_of;
+  std::vector<std::pair<int, int>> keys;  // (doc, len)
+  std::vector<std::vector<Occ>> groups;
+  for (int s = 0; s < B; ++s) {
+    const int k0 = seg_indptr[s], k1 = seg_indptr[s + 1];
+    if (k1 < k0) return LAZY_ERR_LAYOUT;
+    int64_t blk = 0;
+    for (int k = k0; k < k1; ++k) {
+      const int doc = seg_doc[k], len = seg_len[k];
+      if (doc < 0 || doc >= num_docs || len < 1) return LAZY_ERR_LAYOUT;
+      const int dblk = doc_block_indptr[doc + 1] - doc_block_indptr[doc];
+      if ((int64_t)len > (int64_t)kBlk * dblk) return LAZY_ERR_LAYOUT;
+      const int nbk = (len + kBlk - 1) / kBlk;
+      if (blk + nbk > max_blocks) return LAZY_ERR_LAYOUT;
+      for (int q = 0; q < nbk; ++q) {
+        const int phys = doc_blocks[doc_block_indptr[doc] + q];
+        if (phys < 0 || phys >= num_pool_blocks) return LAZY_ERR_LAYOUT;
+      }
+      const std::pair<int, int> key{doc, len};
+      auto f = group_of.find(key);
+      int gi;
+      if (f == group_of.end()) {
+        gi = (int)groups.size();
+        group_of.emplace(key, gi);
+        keys.push_back(key);
+        groups.emplace_back();
+      } else {
+        gi = f->second;
+      }
+      groups[gi].push_back(Occ{s, (int)blk});
+      blk += nbk;
+    }
+  }
+  // ---- member sets, their chunk length, and the slots each member needs
+  const int per_set = std::max(1, std::min(LAZY_PLAN_MAX_MEMBERS, 64 / G));
+  struct Set {
+    int group, first, n, rt, cb;
+  };
+  std::vector<Set> sets;
+  std::vector<int> nslots(B, 0);
+  for (int gi = 0; gi < (int)groups.size(); ++gi) {
+    const int nbk = (keys[gi].second + kBlk - 1) / kBlk;
+    for (int j0 = 0; j0 < (int)groups[gi].size(); j0 += per_set) {
+      const int n = std::min(per_set, (int)groups[gi].size() - j0);
+      const int rows = n * G;
+      const int rt = rows <= 16 ? 1 : (rows <= 32 ? 2 : 4);
+      const int cb = std::max(1, chunk_blocks / rt);
+      sets.push_back(Set{gi, j0, n, rt, cb});
+      for (int j = 0; j < n; ++j) nslots[groups[gi][j0 + j].seq] += (nbk + cb - 1) / cb;
+    }
+  }
+  slot_indptr[0] = 0;
+  for (int s = 0; s < B; ++s) slot_indptr[s + 1] = slot_indptr[s] + nslots[s];
+  // ---- items, one per (set, chunk)
+  struct Item {
+    int set, c0, nb, last, cost;
+  };
+  std::vector<Item> its;
+  for (int si = 0; si < (int)sets.size(); ++si) {
+    const Set& st = sets[si];
+    const int len = keys[st.group].second;
+    const int nbk = (len + kBlk - 1) / kBlk;
+    for (int c0 = 0; c0 < nbk; c0 += st.cb) {
+      const int nb = std::min(st.cb, nbk - c0);
+      const int last = (c0 + nb == nbk) ? ((len - 1) & (kBlk - 1)) + 1 : kBlk;
+      its.push_back(Item{si, c0, nb, last, nb * st.rt});
+    }
+  }
+  if ((int64_t)its.size() > capacity) return LAZY_ERR_WORKSPACE;
+  std::stable_sort(its.begin(), its.end(), [](const Item& x, const Item& y) { return x.cost > y.cost; });
+  std::vector<int> next(slot_indptr, slot_indptr + B);
+  for (size_t i = 0; i < its.size(); ++i) {
+    const Set& st = sets[its[i].set];
+    const std::vector<Occ>& occ = groups[st.group];
+    int32_t* d = items + (size_t)LAZY_PLAN_ITEM_INTS * i;
+    std::fill(d, d + LAZY_PLAN_ITEM_INTS, 0);
+    d[0] = occ[st.first].seq;
+    d[1] = occ[st.first].b0 + its[i].c0;
+    d[2] = its[i].nb;
+    d[3] = its[i].last;
+    d[4] = st.n;
+    for (int j = 0; j < st.n; ++j) {
+      const Occ& o = occ[st.first + j];
+      int32_t* m = d + 8 + 4 * j;
+      m[0] = o.seq;
+      m[1] = o.b0 + its[i].c0;
+      m[2] = next[o.seq]++;
+    }
+  }
+  counts[0] = (int32_t)its.size();
+  counts[1] = slot_indptr[B];
+  return LAZY_OK;
+}
+
+}  // namespace lazy

@@ -33,7 +33,10 @@ EXPORTED = (
     "lazy_attn_pack_block_words_host", "lazy_attn_pack_block_words", "lazy_attn_decode_workspace_bytes",
     "lazy_attn_decode", "lazy_attn_prefill_workspace_bytes", "lazy_attn_prefill", "lazy_attn_debug_gather",
     "lazy_attn_device_status", "lazy_attn_launch_count", "lazy_attn_debug_rope", "lazy_attn_decode_noalloc",
+    "lazy_attn_plan_shared_host", "lazy_attn_decode_shared_workspace_bytes", "lazy_attn_decode_shared",
 )
+PLAN_MAX_MEMBERS = 16
+PLAN_ITEM_INTS = 8 + 4 * PLAN_MAX_MEMBERS
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -71,6 +74,9 @@ _sig = {
     "lazy_attn_launch_count": (_u64, []),
     "lazy_attn_debug_rope": (ctypes.c_int, [_P, _vp, _vp, _i32, _vp, _vp]),
     "lazy_attn_decode_noalloc": (ctypes.c_int, [_P] + [_vp] * 8 + [_vp]),
+    "lazy_attn_plan_shared_host": (ctypes.c_int, [_P, _i32] + [_vp] * 5 + [_i32, _i32] + [_vp] * 3),
+    "lazy_attn_decode_shared_workspace_bytes": (_sz, [_P, _i32]),
+    "lazy_attn_decode_shared": (ctypes.c_int, [_P] + [_vp] * 6 + [_i32, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -211,6 +217,67 @@ def decode_noalloc(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: tor
                                        _dptr(seq_lens, "seq_lens", torch.int32), _dptr(q_pos, "q_pos", torch.int32),
                                        _dptr(rope_table, "rope_table"), _dptr(out, "out", dt), _stream(stream))
     _check(rc, "decode_noalloc")
+    return out
+
+
+class SharedPlan:
+    """Work list of the shared-run decode: the planner's host arrays and their device copies.
+
+    ``items_host`` is [num_items, PLAN_ITEM_INTS] int32 (header, then members
+    {seq, first block, slot, 0}); ``slot_indptr_host`` is [B+1]."""
+
+    def __init__(self, items: np.ndarray, slot_indptr: np.ndarray, device="cuda"):
+        self.items_host, self.slot_indptr_host = items, slot_indptr
+        self.num_items = int(items.shape[0])
+        self.num_slots = int(slot_indptr[-1]) if len(slot_indptr) else 0
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32).reshape(-1) if a.size else
+                                       np.zeros(PLAN_ITEM_INTS, np.int32)).to(device)
+        self.items, self.slot_indptr = t(items), t(slot_indptr)
+
+    def members(self, i: int) -> np.ndarray:
+        """[nmem, 4] member records of item i (host)."""
+        n = int(self.items_host[i, 4])
+        return self.items_host[i, 8: 8 + 4 * n].reshape(n, 4)
+
+
+def plan_shared_host(p: Params, num_docs: int, seg_indptr, seg_doc, seg_len, doc_block_indptr, doc_blocks,
+                     chunk_blocks: int = 0):
+    """Host planner of the shared-run decode. Returns (items [n, PLAN_ITEM_INTS], slot_indptr [B+1]), int32."""
+    arrs = [_i32_np(x) if np.size(x) else np.zeros(1, np.int32)
+            for x in (seg_indptr, seg_doc, seg_len, doc_block_indptr, doc_blocks)]
+    cap = int(np.sum((np.asarray(seg_len, dtype=np.int64) + BLOCK - 1) // BLOCK)) + 1
+    items = np.zeros((cap, PLAN_ITEM_INTS), np.int32)
+    slot_indptr = np.zeros(p.num_seqs + 1, np.int32)
+    counts = np.zeros(2, np.int32)
+    rc = _lib.lazy_attn_plan_shared_host(ctypes.byref(p), int(num_docs), *[a.ctypes.data for a in arrs],
+                                         int(chunk_blocks), cap, items.ctypes.data, slot_indptr.ctypes.data,
+                                         counts.ctypes.data)
+    _check(rc, "plan_shared_host")
+    return items[: counts[0]].copy(), slot_indptr
+
+
+def decode_shared_workspace_bytes(p: Params, num_slots: int) -> int:
+    return int(_lib.lazy_attn_decode_shared_workspace_bytes(ctypes.byref(p), int(num_slots)))
+
+
+def decode_shared(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, block_words: torch.Tensor,
+                  q_pos: torch.Tensor, rope_table: torch.Tensor, plan: SharedPlan, out: Optional[torch.Tensor] = None,
+                  workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    dt = _tdt(p)
+    if out is None:
+        out = torch.empty_like(q)
+    nws = decode_shared_workspace_bytes(p, plan.num_slots)
+    if workspace is None and nws:
+        workspace = torch.empty(nws, dtype=torch.uint8, device=q.device)
+    wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    i32 = torch.int32
+    rc = _lib.lazy_attn_decode_shared(ctypes.byref(p), _dptr(q, "q", dt), _dptr(k_pool, "k_pool", dt),
+                                      _dptr(v_pool, "v_pool", dt), _dptr(block_words, "block_words"),
+                                      _dptr(q_pos, "q_pos", i32), _dptr(rope_table, "rope_table"), plan.num_items,
+                                      _dptr(plan.items, "items", i32), plan.num_slots,
+                                      _dptr(plan.slot_indptr, "slot_indptr", i32), _dptr(out, "out", dt),
+                                      _dptr(workspace, "workspace"), wsz, _stream(stream))
+    _check(rc, "decode_shared")
     return out
 
 

@@ -1,8 +1,9 @@
 """Emulation of the bf16 tensor-core path's operand roundings (numpy fp64).
 
 The CUDA kernels multiply bf16 operands on the tensor cores: the rotated query
-q' (and, in prefill, the rotated key block R_p K) and the softmax weights P are
-rounded to bf16 before their products; everything else is fp32 or exact. On a
+q' (scaled by sm_scale * log2(e)), in prefill the rotated key block R_p K, and
+the softmax weights P are rounded to bf16 before their products; everything
+else is fp32 or exact. On a
 row whose output element is near zero (values that cancel), those two or three
 roundings alone can move the result by more than 2e-3 + 2e-2 |ref|.
 
@@ -63,15 +64,13 @@ def emulate(w, rows, lazy: bool = True, k_pool=None) -> np.ndarray:
             K = _bf16(rope(K.transpose(1, 0, 2), P, theta).transpose(1, 0, 2))  # one rotation by R_p, bf16
         for h in range(w.num_q_heads):
             kh = K[:, h // g]
+            # every kernel folds scale * log2(e) into q' before the bf16 rounding
             if w.kind == "decode" and lazy:
-                # q re-rotated by R_{m-p} per document, bf16
-                qd = {pp: _bf16(rope(q[r, h], m - pp, theta)) for pp in np.unique(P)}
-                sc = np.array([qd[P[j]] @ kh[j] for j in range(len(P))]) * scale
-            elif w.kind == "prefill":
-                # prefill folds scale * log2(e) into q' before the bf16 rounding
-                sc = kh @ _bf16(rope(q[r, h], m, theta) * scale)
+                # q re-rotated by R_{m-p} per document
+                qd = {pp: _bf16(rope(q[r, h], m - pp, theta) * scale) for pp in np.unique(P)}
+                sc = np.array([qd[P[j]] @ kh[j] for j in range(len(P))])
             else:
-                sc = (kh @ _bf16(rope(q[r, h], m, theta))) * scale
+                sc = kh @ _bf16(rope(q[r, h], m, theta) * scale)
             e = _bf16(np.exp2(sc - sc.max()))
             out[oi, h] = (e[:, None] * V[:, h // g]).sum(0) / e.sum()
     return _bf16(out)

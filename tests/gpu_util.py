@@ -111,3 +111,17 @@ def assert_close(got: torch.Tensor, ref: np.ndarray, dtype: str, what: str = "",
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements outside tolerance; worst at {i}: "
                              f"gpu={g[i]!r} ref={ref[i]!r}")
     return float(err.max())
+
+
+def shared_plan(d: Dev, chunk_blocks: int = 0):
+    """Host plan of the shared-run decode for the workload behind ``d``, copied to the device."""
+    L = la()
+    w = d.w
+    items, slot_indptr = L.plan_shared_host(d.p, len(w.doc_len), w.seg_indptr, w.seg_doc, w.seg_len,
+                                            w.doc_block_indptr, w.doc_blocks, chunk_blocks=chunk_blocks)
+    return L.SharedPlan(items, slot_indptr)
+
+
+def decode_shared(d: Dev, plan, out=None) -> torch.Tensor:
+    L = la()
+    return L.decode_shared(d.p, d.q, d.k_pool, d.v_pool, d.words, d.q_pos, d.rope, plan, out=out)

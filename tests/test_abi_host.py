@@ -173,3 +173,94 @@ def test_size_queries(la):
     assert la.decode_workspace_bytes(p) == 0
     p.num_splits, p.max_blocks_per_seq = 4, 64
     assert la.decode_workspace_bytes(p) == 1 * 4 * 4 * (128 + 2) * 4
+
+
+# ---------------------------------------------------------------- shared-run planner
+
+def _shared_workloads():
+    yield W.decode_zipf("sd", batch=9, hq=8, hkv=2, d=64, docs_per_seq=5, doc_tokens=600, pool_docs=4,
+                        zipf_s=1.0, suffix_tokens=9, seed=15)
+    yield W.decode_zipf("sd1", batch=40, hq=4, hkv=4, d=128, docs_per_seq=3, doc_tokens=40, pool_docs=2,
+                        zipf_s=1.0, seed=16)  # G = 1: items of up to 16 members, 16 rows
+    d, _ = W.mixed_mqa(n_decode=6, n_prefill=1, chunk=40, hq=8, hkv=1, d=64, pool_docs=30, ctx_lo=50,
+                       ctx_hi=3000, doc_lo=5, doc_hi=300, seed=17)
+    yield d
+
+
+@pytest.mark.parametrize("chunk", [0, 1, 3, 32])
+@pytest.mark.parametrize("w", list(_shared_workloads()), ids=lambda w: w.name)
+def test_shared_plan_covers_every_block_once(la, w, chunk):
+    """Every logical block of every sequence is computed exactly once, in a slot of
+    its own sequence, by an item whose source blocks are the same physical blocks."""
+    p = _params(la, w)
+    items, slot_indptr = la.plan_shared_host(p, len(w.doc_len), w.seg_indptr, w.seg_doc, w.seg_len,
+                                             w.doc_block_indptr, w.doc_blocks, chunk_blocks=chunk)
+    G = w.num_q_heads // w.num_kv_heads
+    exp = {s: expected_blocks(w, s) for s in range(w.num_seqs)}
+    cover = {s: np.zeros(len(exp[s]), np.int64) for s in range(w.num_seqs)}
+    slots_seen = set()
+    cost = []
+    for it in items:
+        src, b0, nb, last, nm = (int(x) for x in it[:5])
+        assert (it[5:8] == 0).all() and (it[8 + 4 * nm:] == 0).all()
+        assert 1 <= nm <= la.PLAN_MAX_MEMBERS and nm * G <= 64
+        rt = 1 if nm * G <= 16 else (2 if nm * G <= 32 else 4)
+        cost.append(nb * rt)
+        if chunk:
+            assert nb <= max(1, chunk // rt)
+        src_phys = [exp[src][b][0] for b in range(b0, b0 + nb)]
+        assert [exp[src][b][2] for b in range(b0, b0 + nb)] == [16] * (nb - 1) + [last]
+        for seq, bm, slot, zero in it[8: 8 + 4 * nm].reshape(nm, 4):
+            assert zero == 0
+            assert [exp[seq][b][0] for b in range(bm, bm + nb)] == src_phys
+            assert [exp[seq][b][2] for b in range(bm, bm + nb)] == [16] * (nb - 1) + [last]
+            assert len({exp[seq][b][1] for b in range(bm, bm + nb)}) == 1  # one document run
+            assert slot_indptr[seq] <= slot < slot_indptr[seq + 1]
+            assert slot not in slots_seen
+            slots_seen.add(slot)
+            cover[seq][bm:bm + nb] += 1
+    assert (np.diff(cost) <= 0).all()  # heaviest items first
+    assert len(slots_seen) == slot_indptr[-1]
+    for s in range(w.num_seqs):
+        assert (cover[s] == 1).all(), s
+    # Loads are shared: no more source blocks than logical ones.
+    assert items[:, 2].sum() <= sum(len(e) for e in exp.values())
+
+
+def test_shared_plan_rejects_bad_layouts(la):
+    w = W.decode_zipf("sbad", batch=2, hq=4, hkv=2, d=64, docs_per_seq=2, doc_tokens=20, pool_docs=3,
+                      zipf_s=1.0, seed=18)
+    p = _params(la, w)
+
+    def run(params=p, **repl):
+        a = dict(seg_indptr=w.seg_indptr.copy(), seg_doc=w.seg_doc.copy(), seg_len=w.seg_len.copy(),
+                 doc_block_indptr=w.doc_block_indptr.copy(), doc_blocks=w.doc_blocks.copy())
+        a.update(repl)
+        with pytest.raises(la.LazyAttnError) as e:
+            la.plan_shared_host(params, len(w.doc_len), *a.values())
+        return e.value.status
+
+    sl = w.seg_len.copy()
+    sl[0] = 33
+    assert run(seg_len=sl) == la.LAZY_ERR_LAYOUT
+    db = w.doc_blocks.copy()
+    db[0] = w.num_pool_blocks
+    assert run(doc_blocks=db) == la.LAZY_ERR_LAYOUT
+    assert run(params=_params(la, w, max_blocks=1)) == la.LAZY_ERR_LAYOUT
+    big = _params(la, w)
+    big.num_q_heads = 4 * 65
+    big.num_kv_heads = 4
+    assert run(params=big) == la.LAZY_ERR_UNSUPPORTED
+
+
+def test_shared_decode_argument_checks(la):
+    w = W.tiny_fp32()
+    p = _params(la, w)
+    null = [None] * 6
+    # fp32 has no shared-run kernel; bf16 with null pointers is an invalid argument; no CUDA call either way
+    assert la._lib.lazy_attn_decode_shared(ctypes.byref(p), *null, 1, None, 1, None, None, None, 0,
+                                           None) == la.LAZY_ERR_UNSUPPORTED
+    p.dtype = la.LAZY_BF16
+    assert la._lib.lazy_attn_decode_shared(ctypes.byref(p), *null, 1, None, 1, None, None, None, 0,
+                                           None) == la.LAZY_ERR_INVALID_ARG
+    assert la.decode_shared_workspace_bytes(p, 10) == 10 * 4 * (64 + 2) * 4
