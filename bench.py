@@ -42,7 +42,7 @@ WORKLOAD = "llama8b_decode"
 NCU_TRAFFIC = {"sources": ["paged_kv_cache_57_gb300/csrc/decode_shared.cu",
                            "paged_kv_cache_57_gb300/csrc/decode_block.cuh",
                            "paged_kv_cache_57_gb300/csrc/common.cuh"],
-               "sha16": "", "bytes_per_launch": 0}
+               "sha16": "ef7f182ca364252e", "bytes_per_launch": 301444864 + 25410560}
 
 
 def _traffic_if_current():
