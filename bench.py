@@ -160,6 +160,8 @@ def build_device(w, lazy=True, k_pool=None):
         d["q_start"] = c(w.q_start)
         d["max_q"] = int(np.diff(w.cu_seqlens_q).max())
         d["out"] = torch.empty_like(d["q"])
+        d["ws_pf"] = torch.empty(max(1, L.prefill_workspace_bytes(p, int(d["q"].shape[0]))), dtype=torch.uint8,
+                                 device="cuda")
     return d
 
 
@@ -184,7 +186,7 @@ def run_prefill(d, lazy=None):
     if lazy is not None:
         p.lazy = int(lazy)
     L.prefill(p, d["q"], d["cu"], d["q_start"], d["max_q"], d["k"], d["v"], d["words"], d["seq_lens"], d["rope"],
-              out=d["out"])
+              out=d["out"], workspace=d["ws_pf"])
 
 
 def time_steps(fn, steps, warmup, flush):

@@ -408,18 +408,24 @@ int lazy_attn_decode_shared(const lazy_attn_params* p, const void* q, const void
   return launched(lazy::launch_shared_combine(a, cs));
 }
 
+// The two-tile prefill (even GQA ratio) runs one persistent CTA per SM and needs a
+// workspace for the pieces of units that cross CTA ranges; the one-tile kernel none.
+static bool prefill_uses_stream(const lazy_attn_params* p, const Checked& c) {
+  return p->dtype == LAZY_BF16 && p->head_dim == 128 && c.G % 2 == 0;
+}
+
 size_t lazy_attn_prefill_workspace_bytes(const lazy_attn_params* p, int32_t total_q) {
-  (void)p;
   (void)total_q;
-  return 0;
+  Checked c;
+  if (check_params(p, &c) != LAZY_OK) return 0;
+  if (!prefill_uses_stream(p, c)) return 0;
+  return lazy::prefill_stream_workspace_bytes(current_device() >= 0 ? lazy::prefill_stream_grid() : kDefaultSmCount);
 }
 
 int lazy_attn_prefill(const lazy_attn_params* p, const void* q, const int32_t* cu_seqlens_q, const int32_t* q_start,
                       int32_t total_q, int32_t max_q_len, const void* k_pool, const void* v_pool,
                       const uint32_t* block_words, const int32_t* seq_lens, const void* rope_table, void* out,
                       void* workspace, size_t workspace_bytes, lazy_stream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   Checked c;
   int rc = check_params(p, &c);
   if (rc != LAZY_OK) return rc;
@@ -458,7 +464,17 @@ int lazy_attn_prefill(const lazy_attn_params* p, const void* q, const int32_t* c
   a.id_bits = c.id_bits;
   a.num_pool_blocks = p->num_pool_blocks;
   a.scale_log2 = scale_log2(p);
-  cudaError_t e = lazy::launch_prefill(a, p->lazy != 0, qmap, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
+  a.T = (max_q_len + lazy::pf_tile_rows - 1) / lazy::pf_tile_rows;
+  int grid = 0;
+  if (prefill_uses_stream(p, c)) {
+    grid = lazy::prefill_stream_grid();
+    const size_t need = lazy::prefill_stream_workspace_bytes(grid);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return LAZY_ERR_WORKSPACE;
+    a.counters = static_cast<int*>(workspace);
+    a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + lazy::prefill_stream_counter_bytes(grid));
+  }
+  cudaError_t e =
+      lazy::launch_prefill(a, p->lazy != 0, qmap, kmap, vmap, grid, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return LAZY_ERR_UNSUPPORTED;
   return launched(e);
 }

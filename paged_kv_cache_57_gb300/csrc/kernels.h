@@ -60,8 +60,15 @@ struct PrefillArgs {
   void* out;                 // [total_q][Hq][D] bf16
   unsigned int* status;
   int B, Hq, Hkv, G, D, total_q, max_q_len, max_blocks, id_bits, num_pool_blocks;
+  int T;                     // query tiles per sequence: ceil(max_q_len / 128)
   float scale_log2;
+  // Persistent (stream-K) kernel only: per-row arrival counters of split units,
+  // [grid + 1][2][128], zeroed before each launch; fp32 partials [2 * grid][2][128][132].
+  int* counters;
+  float* partials;
 };
+constexpr int PREFILL_PARTIAL_ROW_FLOATS = 128 + 4;
+constexpr int pf_tile_rows = 128;  // query rows per prefill tile
 
 // Shared-run decode (decode_shared.cu): one CTA per (work item, KV head).
 struct SharedDecodeArgs {
@@ -98,11 +105,17 @@ cudaError_t launch_combine(const DecodeArgs& a, bool out_bf16, cudaStream_t st);
 cudaError_t launch_gather_bf16(const GatherArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                cudaStream_t st);
 cudaError_t launch_gather_f32(const GatherArgs& a, cudaStream_t st);
+// Chooses the prefill kernel: the stream-K two-tile kernel for even GQA ratios (it
+// needs a.counters / a.partials and `grid` = prefill_stream_grid()), else the
+// TMEM-Q one-tile kernel.
 cudaError_t launch_prefill(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, cudaStream_t st);
-// Two query tiles (q-heads h, h+1 of one KV head) per CTA; needs an even GQA ratio.
-cudaError_t launch_prefill_pair(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                                const CUtensorMap& vmap, cudaStream_t st);
+                           const CUtensorMap& vmap, int grid, cudaStream_t st);
+// Two query tiles per CTA, one CTA per SM, stream-K over (unit, K tile); even GQA ratio.
+cudaError_t launch_prefill_stream(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                                  const CUtensorMap& vmap, int grid, cudaStream_t st);
+size_t prefill_stream_workspace_bytes(int grid);  // counters, then partials
+size_t prefill_stream_counter_bytes(int grid);
+int prefill_stream_grid();
 
 // One query tile per CTA with the rotated Q tile in tensor memory; any GQA ratio.
 cudaError_t launch_prefill_tq(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,

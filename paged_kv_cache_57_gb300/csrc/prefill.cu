@@ -10,20 +10,21 @@
 // products, i.e. 3/(4M): 0.59% at M = 128 rows per rotated key tile.
 //
 // Two kernels compute it:
-//   prefill_pair.cu  two query tiles per CTA (q-heads h, h+1 of one KV head), so
-//                    each loaded and rotated K/V tile serves 256 query rows; needs
-//                    an even GQA ratio.
-//   prefill_tq.cu    one query tile per CTA with Q' held in tensor memory; any
-//                    GQA ratio.
+//   prefill_stream.cu  two query tiles per CTA (q-heads h, h+1 of one KV head), so
+//                      each loaded and rotated K/V tile serves 256 query rows; one
+//                      persistent CTA per SM over a stream-K split of the work;
+//                      needs an even GQA ratio.
+//   prefill_tq.cu      one query tile per CTA with Q' held in tensor memory; any
+//                      GQA ratio.
 #include "kernels.h"
 
 namespace lazy {
 
 cudaError_t launch_prefill(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, cudaStream_t st) {
+                           const CUtensorMap& vmap, int grid, cudaStream_t st) {
   if (a.D != 128) return cudaErrorNotSupported;
   if (a.B == 0 || a.max_q_len == 0) return cudaSuccess;
-  if (a.G % 2 == 0) return launch_prefill_pair(a, lazy, qmap, kmap, vmap, st);
+  if (a.G % 2 == 0) return launch_prefill_stream(a, lazy, qmap, kmap, vmap, grid, st);
   return launch_prefill_tq(a, lazy, qmap, kmap, vmap, st);
 }
 

@@ -101,27 +101,28 @@ __device__ __forceinline__ float2 add_angles(float2 a, float2 b) {
   return make_float2(fmaf(a.x, b.x, -a.y * b.y), fmaf(a.y, b.x, a.x * b.y));
 }
 
-// Copies table rows 0, 16, ..., 112 then 0 .. 15 (D/2 entries each) to sm_rows,
-// thread tid of n.
+// Copies the table's rows for offsets 0, 16, ..., 112 (slots 0..7) and 0 .. 15
+// (slots 8..23) to sm_rows, frequency-major: entry (f, slot) at f * 24 + slot, so
+// that 32 threads rotating 32 consecutive rows read 16 consecutive entries (no bank
+// conflict) for the row offset and one broadcast entry for the multiple of 16.
+// Thread tid of n.
 __device__ __forceinline__ void load_angle_rows(float2* sm_rows, const float2* __restrict__ rope, int tid, int n) {
-  const float4* src = reinterpret_cast<const float4*>(rope + D / 2);  // row part of the table
-  float4* dst = reinterpret_cast<float4*>(sm_rows);
-  for (int idx = tid; idx < kAngleRows * (D / 4); idx += n) {
-    const int row = idx / (D / 4), col = idx % (D / 4);
-    const int src_row = row < 8 ? 16 * row : row - 8;
-    dst[idx] = __ldg(&src[src_row * (D / 4) + col]);
+  const float2* src = rope + D / 2;  // row part of the table: [row][D/2]
+  for (int idx = tid; idx < kAngleRows * (D / 2); idx += n) {
+    const int f = idx / kAngleRows, slot = idx % kAngleRows;
+    const int src_row = slot < 8 ? 16 * slot : slot - 8;
+    sm_rows[idx] = __ldg(&src[src_row * (D / 2) + f]);
   }
 }
 
 // Rotation coefficients of the 8 frequencies of chunk c for row offset i.
 __device__ __forceinline__ Rot8 row_rot8(const float2* base_cs, const float2* sm_rows, int i, int c, float scale) {
-  const float2* a16 = sm_rows + (i >> 4) * (D / 2);
-  const float2* a1 = sm_rows + (8 + (i & 15)) * (D / 2);
+  const int s16 = i >> 4, s1 = 8 + (i & 15);
   float2 cs[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const int f = 8 * c + e;
-    cs[e] = add_angles(add_angles(base_cs[f], a16[f]), a1[f]);
+    cs[e] = add_angles(add_angles(base_cs[f], sm_rows[f * kAngleRows + s16]), sm_rows[f * kAngleRows + s1]);
   }
   return make_rot8(cs, scale);
 }

@@ -292,6 +292,9 @@ def prefill(p: Params, q: torch.Tensor, cu_seqlens_q: torch.Tensor, q_start: tor
     dt = _tdt(p)
     if out is None:
         out = torch.empty_like(q)
+    nws = prefill_workspace_bytes(p, int(q.shape[0]))
+    if workspace is None and nws:
+        workspace = torch.empty(nws, dtype=torch.uint8, device=q.device)
     wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = _lib.lazy_attn_prefill(ctypes.byref(p), _dptr(q, "q", dt), _dptr(cu_seqlens_q, "cu_seqlens_q", torch.int32),
                                 _dptr(q_start, "q_start", torch.int32), int(q.shape[0]), int(max_q_len),

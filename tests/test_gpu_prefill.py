@@ -103,3 +103,59 @@ def test_mixed_prefill_full_sampled():
     rng = np.random.default_rng(4)
     rows = sorted(int(x) for x in rng.choice(p.q.shape[0], 24, replace=False))
     _check(p, rows=rows)
+
+
+# ---------------------------------------------------------------- stream-K splits
+
+def _split_units(w, sms):
+    """Host replica of the two-tile kernel's schedule: when all (sequence, tile, head pair)
+    units are about equally long, the first floor(units / sms) * sms run whole, one per
+    CTA; the rest are laid end to end by K tiles and cut into sms ranges of W tiles. Returns the units cut by a range
+    boundary, as (s, tile, hp, n, U0), and W."""
+    P = w.num_q_heads // 2
+    cu = np.asarray(w.cu_seqlens_q)
+    C = np.diff(cu)
+    T = int((C.max() + 127) // 128)
+    nb = w.blocks_per_seq()
+    units = []
+    for s in range(w.num_seqs):
+        for tile in range(T):
+            row0 = 128 * tile
+            if row0 >= C[s]:
+                continue
+            b_chunk = max(0, int(nb[s]) - (int(C[s]) + 15) // 16)
+            last_block = min(int(nb[s]) - 1, b_chunk + (min(int(C[s]), row0 + 128) - 1) // 16)
+            n = last_block // 8 + 1 if last_block >= 0 else 0
+            if n:
+                units += [(s, tile, hp, n) for hp in range(P)]
+    ns = [u[3] for u in units]
+    uniform = bool(units) and max(ns) * 4 <= min(ns) * 5
+    D = len(units) // sms * sms if uniform else 0
+    tot, out = 0, []
+    for s, tile, hp, n in units[D:]:
+        out.append((s, tile, hp, n, tot))
+        tot += n
+    W = -(-tot // sms) if tot else 0
+    return [u for u in out if u[4] // W != (u[4] + u[3] - 1) // W], W
+
+
+def test_prefill_one_unit_across_many_ctas():
+    # one sequence, one 128-row tile, one head pair: ~50 K tiles cut into ~50 one-tile pieces
+    w = W.prefill_zipf("psplit", batch=1, hq=2, hkv=1, docs_per_seq=6, doc_tokens=1000, pool_docs=6, zipf_s=0.0,
+                       chunk_tokens=[128], seed=79)
+    split, Wr = _split_units(w, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert split and Wr <= 2
+    _check(w)
+
+
+def test_llama8b_prefill_split_units_sampled():
+    w = W.FULL["llama8b_prefill"]()
+    split, _ = _split_units(w, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert len(split) > 50
+    cu = np.asarray(w.cu_seqlens_q)
+    rng = np.random.default_rng(6)
+    rows = set()
+    for s, tile, hp, n, U0 in split[:: max(1, len(split) // 12)]:
+        lo, hi = int(cu[s]) + 128 * tile, min(int(cu[s + 1]), int(cu[s]) + 128 * tile + 128)
+        rows.update(int(x) for x in rng.choice(np.arange(lo, hi), 4, replace=False))
+    _check(w, rows=sorted(rows))
