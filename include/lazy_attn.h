@@ -261,9 +261,18 @@ int lazy_attn_decode_noalloc(const lazy_attn_params *p, const void *q, const voi
  * R_p of its document (one relative rotation per tile, no unrotate pass).
  *   q            [total_q][Hq][d] bf16, UNROTATED
  *   cu_seqlens_q [B+1] int32 device; q_start [B] int32 device
- *   max_q_len    >= every C_s (sizes the grid); total_q = cu_seqlens_q[B]
+ *   max_q_len    >= every C_s (sizes the work list); total_q = cu_seqlens_q[B]
  *   out          [total_q][Hq][d] bf16
- * Only LAZY_BF16 is supported. */
+ *   workspace    at least lazy_attn_prefill_workspace_bytes(p, total_q) bytes,
+ *                16-byte aligned (LAZY_ERR_WORKSPACE otherwise). With an even GQA
+ *                ratio the kernel runs one persistent CTA per SM, each on an equal
+ *                share of the (query tile, head pair, K tile) iterations; a query tile
+ *                whose K tiles are shared out among several CTAs is merged through the
+ *                workspace (per-row arrival counters, which the call zeroes with one
+ *                cudaMemsetAsync on `stream`, and fp32 partial results). Its size
+ *                depends only on the SM count. Odd GQA ratios need none (0 bytes).
+ *                Calls that overlap on the GPU must not share a workspace.
+ * Only LAZY_BF16 with head_dim 128 is supported. */
 size_t lazy_attn_prefill_workspace_bytes(const lazy_attn_params *p, int32_t total_q);
 int lazy_attn_prefill(const lazy_attn_params *p, const void *q, const int32_t *cu_seqlens_q,
                       const int32_t *q_start, int32_t total_q, int32_t max_q_len, const void *k_pool,
