@@ -487,6 +487,27 @@ def measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust):
     out["decode_per_sequence_path"] = {"ms_median": 1e3 * sq1, "kv_gbs_logical": nb8["kv_logical"] / sq1 / 1e9,
                                        "kv_gbs_unique": nb8["unique"] / sq1 / 1e9,
                                        "hbm_frac_unique_of_measured": nb8["unique"] / sq1 / 1e9 / hbm}
+    # Eager-materialised baseline: per-sequence copies with K at absolute positions
+    # (lazy_attn_materialize), then the decode kernel's control path on the copies.
+    try:
+        k_e, v_e, w_e = L.materialize(d["p"], d["k"], d["v"], d["words"], d["seq_lens"], d["rope"])
+        tm = statistics.median(time_steps(lambda: L.materialize(d["p"], d["k"], d["v"], d["words"], d["seq_lens"],
+                                                                d["rope"]), max(10, n // 4), 3, flush))
+        de = dict(d, k=k_e, v=v_e, words=w_e)
+        de["p"] = L.make_params(num_seqs=w.num_seqs, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                                head_dim=w.head_dim, num_pool_blocks=int(k_e.shape[0]),
+                                max_blocks_per_seq=d["p"].max_blocks_per_seq, dtype=w.dtype, rope_theta=w.rope_theta,
+                                lazy=False)
+        te = statistics.median(time_steps(lambda: run_decode(de, path="seq"), n, 3, flush))
+        copies = 2 * k_e.numel() * k_e.element_size()
+        out["eager_materialised"] = {
+            "materialise_ms": 1e3 * tm, "decode_ms_on_copies": 1e3 * te, "lazy_decode_ms": 1e3 * sh1,
+            "copies_gb": copies / 1e9, "lazy_unique_kv_gb": W.kv_bytes_unique(w) / 1e9,
+            "lazy_decode_speedup_vs_eager": te / sh1,
+            "lazy_vs_eager_decode_overhead_pct": 100.0 * (sh1 / te - 1.0)}
+        del k_e, v_e, w_e, de
+    except L.LazyAttnError as e:
+        out["eager_materialised"] = {"unavailable": str(e)}
     # No-sharing control: logical bytes = unique bytes = DRAM bytes.
     wc = W.FULL["llama8b_decode_noshare"]()
     dc = build_device(wc)

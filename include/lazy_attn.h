@@ -280,6 +280,23 @@ int lazy_attn_prefill(const lazy_attn_params *p, const void *q, const int32_t *c
                       const void *rope_table, void *out, void *workspace, size_t workspace_bytes,
                       lazy_stream_t stream);
 
+/* ---------------------------------------------------------------- eager materialisation (baseline)
+ * The alternative the lazy method avoids ("Declaração do Problema"): a reused
+ * document's keys re-rotated to their absolute positions and copied per sequence.
+ * For every sequence s and logical block b < ceil(seq_lens[s]/16), writes block
+ * s*max_blocks_per_seq + b of k_out / v_out with K rotated by R_p (p of block b's
+ * document: R_p R_j k = R_{p+j} k) and V copied, and block_words_out[s][b] with that
+ * id and the same offset field (0 for b past the sequence). lazy_attn_decode with
+ * lazy = 0 on (k_out, v_out, block_words_out, seq_lens) then computes the same
+ * attention without per-document rotation and without any block shared.
+ *   k_out, v_out   [num_seqs * max_blocks_per_seq][Hkv][16][d] bf16
+ *   block_words_out [num_seqs][max_blocks_per_seq]
+ * Needs num_seqs * max_blocks_per_seq <= 2^id_bits (LAZY_ERR_LAYOUT otherwise).
+ * bf16 only. */
+int lazy_attn_materialize(const lazy_attn_params *p, const void *k_pool, const void *v_pool,
+                          const uint32_t *block_words, const int32_t *seq_lens, const void *rope_table, void *k_out,
+                          void *v_out, uint32_t *block_words_out, lazy_stream_t stream);
+
 /* ---------------------------------------------------------------- test support
  * Copies every logical K/V slot of every sequence through the decode kernel's
  * own load path (word decode, TMA block loads, hole rule) into dense buffers:

@@ -479,6 +479,28 @@ int lazy_attn_prefill(const lazy_attn_params* p, const void* q, const int32_t* c
   return launched(e);
 }
 
+int lazy_attn_materialize(const lazy_attn_params* p, const void* k_pool, const void* v_pool,
+                          const uint32_t* block_words, const int32_t* seq_lens, const void* rope_table, void* k_out,
+                          void* v_out, uint32_t* block_words_out, lazy_stream_t stream) {
+  Checked c;
+  int rc = check_params(p, &c);
+  if (rc != LAZY_OK) return rc;
+  if (p->dtype != LAZY_BF16) return LAZY_ERR_UNSUPPORTED;
+  if (p->num_seqs == 0) return LAZY_OK;
+  if (!k_pool || !v_pool || !block_words || !seq_lens || !rope_table || !k_out || !v_out || !block_words_out)
+    return LAZY_ERR_INVALID_ARG;
+  if (p->num_pool_blocks == 0 || p->max_blocks_per_seq == 0) return LAZY_ERR_INVALID_ARG;
+  if ((int64_t)p->num_seqs * p->max_blocks_per_seq > ((int64_t)1 << c.id_bits)) return LAZY_ERR_LAYOUT;
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_out) || !aligned16(v_out) || !aligned16(rope_table))
+    return LAZY_ERR_INVALID_ARG;
+  unsigned int* st = status_ptr();
+  if (!st) return LAZY_ERR_CUDA;
+  lazy::MaterializeArgs a{k_pool, v_pool, block_words, seq_lens, static_cast<const float2*>(rope_table), k_out, v_out,
+                          block_words_out, st, p->num_seqs, p->num_kv_heads, p->head_dim, p->max_blocks_per_seq,
+                          c.id_bits, p->num_pool_blocks};
+  return launched(lazy::launch_materialize(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int lazy_attn_debug_gather(const lazy_attn_params* p, const void* k_pool, const void* v_pool,
                            const uint32_t* block_words, const int32_t* seq_lens, void* k_out, void* v_out,
                            int32_t* pos_out, lazy_stream_t stream) {

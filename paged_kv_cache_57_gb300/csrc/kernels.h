@@ -87,6 +87,21 @@ struct SharedDecodeArgs {
   float scale_log2;
 };
 
+// Eager materialisation (materialize.cu): per-sequence copies with K at absolute positions.
+struct MaterializeArgs {
+  const void* k_pool;        // [NB][Hkv][16][D]
+  const void* v_pool;
+  const uint32_t* words;     // [B][max_blocks]
+  const int32_t* seq_lens;   // [B]
+  const float2* rope;        // rotation table
+  void* k_out;               // [B * max_blocks][Hkv][16][D]
+  void* v_out;
+  uint32_t* words_out;       // [B][max_blocks]
+  unsigned int* status;
+  int B, Hkv, D, max_blocks, id_bits, num_pool_blocks;
+};
+cudaError_t launch_materialize(const MaterializeArgs& a, cudaStream_t st);
+
 // Host planner of the shared-run decode (shared_plan.cu). counts = {items, slots}.
 int plan_shared_host(int B, int G, int max_blocks, int num_pool_blocks, int num_docs, const int32_t* seg_indptr,
                      const int32_t* seg_doc, const int32_t* seg_len, const int32_t* doc_block_indptr,

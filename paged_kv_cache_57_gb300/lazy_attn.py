@@ -34,6 +34,7 @@ EXPORTED = (
     "lazy_attn_decode", "lazy_attn_prefill_workspace_bytes", "lazy_attn_prefill", "lazy_attn_debug_gather",
     "lazy_attn_device_status", "lazy_attn_launch_count", "lazy_attn_debug_rope", "lazy_attn_decode_noalloc",
     "lazy_attn_plan_shared_host", "lazy_attn_decode_shared_workspace_bytes", "lazy_attn_decode_shared",
+    "lazy_attn_materialize",
 )
 PLAN_MAX_MEMBERS = 16
 PLAN_ITEM_INTS = 8 + 4 * PLAN_MAX_MEMBERS
@@ -76,6 +77,7 @@ _sig = {
     "lazy_attn_decode_noalloc": (ctypes.c_int, [_P] + [_vp] * 8 + [_vp]),
     "lazy_attn_plan_shared_host": (ctypes.c_int, [_P, _i32] + [_vp] * 5 + [_i32, _i32] + [_vp] * 3),
     "lazy_attn_decode_shared_workspace_bytes": (_sz, [_P, _i32]),
+    "lazy_attn_materialize": (ctypes.c_int, [_P] + [_vp] * 8 + [_vp]),
     "lazy_attn_decode_shared": (ctypes.c_int, [_P] + [_vp] * 6 + [_i32, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
 }
 for _name, (_res, _args) in _sig.items():
@@ -279,6 +281,23 @@ def decode_shared(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torc
                                       _dptr(workspace, "workspace"), wsz, _stream(stream))
     _check(rc, "decode_shared")
     return out
+
+
+def materialize(p: Params, k_pool: torch.Tensor, v_pool: torch.Tensor, block_words: torch.Tensor,
+                seq_lens: torch.Tensor, rope_table: torch.Tensor, stream=None):
+    """Eager baseline: per-sequence copies with K at absolute positions. Returns
+    (k_out, v_out, block_words_out) for lazy_attn_decode with lazy = 0."""
+    dt = _tdt(p)
+    nb = p.num_seqs * p.max_blocks_per_seq
+    k_out = torch.empty((nb,) + tuple(k_pool.shape[1:]), dtype=dt, device=k_pool.device)
+    v_out = torch.empty_like(k_out)
+    words_out = torch.empty((p.num_seqs, p.max_blocks_per_seq), dtype=torch.int32, device=k_pool.device)
+    rc = _lib.lazy_attn_materialize(ctypes.byref(p), _dptr(k_pool, "k_pool", dt), _dptr(v_pool, "v_pool", dt),
+                                    _dptr(block_words, "block_words"), _dptr(seq_lens, "seq_lens", torch.int32),
+                                    _dptr(rope_table, "rope_table"), _dptr(k_out, "k_out"), _dptr(v_out, "v_out"),
+                                    _dptr(words_out, "block_words_out"), _stream(stream))
+    _check(rc, "materialize")
+    return k_out, v_out, words_out
 
 
 def prefill_workspace_bytes(p: Params, total_q: int) -> int:
