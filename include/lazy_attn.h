@@ -192,9 +192,7 @@ int lazy_attn_decode(const lazy_attn_params *p, const void *q, const void *k_poo
  * with the same used length read the same physical blocks; they are grouped,
  * split into sets of at most LAZY_PLAN_MAX_MEMBERS members and 64 query rows
  * (members x query heads per KV head), and each set's blocks are cut into chunks
- * of chunk_blocks / RT logical blocks, RT = 1, 2 or 4 tiles of 16 rows (0 selects
- * chunk_blocks = 32 for up to 8 query heads per KV head, 64 up to 16, else 128).
- * It writes
+ * of chunk_blocks logical blocks (0 selects 32). It writes
  *   items_host [num_items][LAZY_PLAN_ITEM_INTS] int32, one work item each:
  *     [0] src_seq, [1] b0, [2] nblk, [3] last_valid, [4] nmem, [5..7] 0: nblk
  *         logical blocks of sequence src_seq from block b0, all full but the
@@ -205,7 +203,9 @@ int lazy_attn_decode(const lazy_attn_params *p, const void *q, const void *k_poo
  *   slot_indptr_host [B+1]: the slots of sequence s are slot_indptr[s] ..
  *     slot_indptr[s+1]-1;
  *   counts_host [2] = {num_items, num_slots}.
- * Items are ordered heaviest first. `capacity` bounds the item count (the number
+ * Items are ordered heaviest first (blocks x max(3, RT), RT = 1, 2 or 4 tiles of
+ * 16 query rows: loads, not the tensor cores, bound the light items).
+ * `capacity` bounds the item count (the number
  * of logical blocks in the batch always suffices). Returns LAZY_ERR_LAYOUT on the
  * packer's layout errors, and LAZY_ERR_WORKSPACE if capacity is too small.
  *

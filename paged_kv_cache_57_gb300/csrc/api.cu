@@ -88,6 +88,20 @@ bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, int d, uin
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 view of the same [rows][d] pool as (column in a 64-column half, row, half):
+// one box of 64 columns x box_rows rows x d/64 halves lands as the d/64 swizzled
+// 64-column boxes of encode_rows_map placed one after the other, in one copy.
+bool encode_block_map(CUtensorMap* m, const void* base, uint64_t rows, int d, uint32_t box_rows) {
+  if (!encoder_ready()) return false;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(d / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, (cuuint32_t)(d / 64)};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D bf16 view of q [total_q][Hq][d]: boxes of 64 columns x 1 head x box_rows rows.
 bool encode_q_map(CUtensorMap* m, const void* base, uint64_t total_q, int hq, int d, uint32_t box_rows) {
   if (!encoder_ready()) return false;
@@ -334,7 +348,7 @@ int lazy_attn_plan_shared_host(const lazy_attn_params* p, int32_t num_docs, cons
       (!seg_doc || !seg_len || !doc_block_indptr || !doc_blocks || !items))
     return LAZY_ERR_INVALID_ARG;
   if (c.G > 64) return LAZY_ERR_UNSUPPORTED;
-  const int cb = chunk_blocks > 0 ? chunk_blocks : (c.G <= 8 ? 32 : (c.G <= 16 ? 64 : 128));
+  const int cb = chunk_blocks > 0 ? chunk_blocks : 32;
   return lazy::plan_shared_host(p->num_seqs, c.G, p->max_blocks_per_seq, p->num_pool_blocks, num_docs, seg_indptr,
                                 seg_doc, seg_len, doc_block_indptr, doc_blocks, cb, capacity, items, slot_indptr,
                                 counts);
@@ -345,7 +359,7 @@ size_t lazy_attn_decode_shared_workspace_bytes(const lazy_attn_params* p, int32_
   if (check_params(p, &c) != LAZY_OK || num_slots < 0) return 0;
   size_t bytes = (size_t)num_slots * p->num_q_heads * (p->head_dim + 2) * sizeof(float);
 #ifdef LAZY_DECODE_TRACE
-  bytes += (size_t)64 << 20;  // phase timestamps, 64 bytes per CTA
+  bytes += (size_t)64 << 20;  // per-CTA trace counters
 #endif
   return bytes;
 }
@@ -399,8 +413,8 @@ int lazy_attn_decode_shared(const lazy_attn_params* p, const void* q, const void
   if (num_items > 0) {
     CUtensorMap kmap, vmap;
     const uint64_t rows = (uint64_t)p->num_pool_blocks * p->num_kv_heads * lazy::kBlock;
-    if (!encode_rows_map(&kmap, k_pool, rows, p->head_dim, lazy::kBlock) ||
-        !encode_rows_map(&vmap, v_pool, rows, p->head_dim, lazy::kBlock))
+    if (!encode_block_map(&kmap, k_pool, rows, p->head_dim, lazy::kBlock) ||
+        !encode_block_map(&vmap, v_pool, rows, p->head_dim, lazy::kBlock))
       return LAZY_ERR_CUDA;
     rc = launched(lazy::launch_decode_shared(a, p->lazy != 0, kmap, vmap, cs));
     if (rc != LAZY_OK) return rc;

@@ -51,6 +51,27 @@ struct SharedCfg {
 
 }  // namespace
 
+// One block's K and V rows of KV head kvh into `stage` (K then V, each as the D/64
+// swizzled 64-column boxes attend_block reads), with one 3-D copy each (the map
+// views a pool as (column in a 64-column half, row, half)); an id outside the
+// pool is not loaded (the barrier is just arrived). No proxy fence is needed
+// before the copies: the team's reads of the stage's previous contents have
+// returned (their values fed the MMAs) before the team barrier that precedes the
+// refill.
+template <int D>
+__device__ __forceinline__ void load_block_3d(uint8_t* stage, uint64_t* bar, int phys, int num_pool_blocks, int hkv,
+                                              int kvh, const CUtensorMap* kmap, const CUtensorMap* vmap) {
+  using G = BlockGeom<D>;
+  if (phys < num_pool_blocks) {
+    mbar_arrive_expect_tx(bar, G::STAGE_BYTES);
+    const int y = (phys * hkv + kvh) * kBlock;
+    tma_load_3d(stage, kmap, bar, 0, y, 0);
+    tma_load_3d(stage + G::KV_BYTES, vmap, bar, 0, y, 0);
+  } else {
+    mbar_arrive(bar);
+  }
+}
+
 // Optional per-CTA phase timestamps (build with -DLAZY_DECODE_TRACE): 8 x u64 per
 // CTA after the partials in the workspace: start, first loads issued, query
 // fragments ready, main loop done, end, (sm id, item), (row tiles, blocks).
@@ -188,7 +209,7 @@ __global__ void __launch_bounds__(kShThreads, 3)
     const int pro = min(NS, nk);
     for (int k = 0; k < pro; ++k) {
       const int phys = __shfl_sync(0xffffffffu, cur_phys, k);
-      if (leader) load_block<D>(tst + k * G::STAGE_BYTES, &tfull[k], phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
+      if (leader) load_block_3d<D>(tst + k * G::STAGE_BYTES, &tfull[k], phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
     }
     issued = pro;
   }
@@ -277,7 +298,7 @@ __global__ void __launch_bounds__(kShThreads, 3)
         phys = __shfl_sync(0xffffffffu, nxt_phys, kn & 31);
       }
       if (leader)
-        load_block<D>(tst + slot * G::STAGE_BYTES, &tfull[slot], phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
+        load_block_3d<D>(tst + slot * G::STAGE_BYTES, &tfull[slot], phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
       issued = kn + 1;
     }
   }

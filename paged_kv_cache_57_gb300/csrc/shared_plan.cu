@@ -7,12 +7,12 @@
 // makes them shareable), so they form one group. A group is split into sets of
 // at most LAZY_PLAN_MAX_MEMBERS members and at most 64 query rows (members x
 // query heads per KV head), i.e. RT = 1, 2 or 4 tiles of 16 rows. A set's blocks
-// are cut into chunks of chunk_blocks / RT logical blocks, so that every work
-// item costs about the same (blocks x row tiles); each (set, chunk) is one item,
-// and every member of the set owns one partial-result slot per chunk. The slots
-// of sequence s are slot_indptr[s] .. slot_indptr[s+1]-1.
+// are cut into chunks of chunk_blocks logical blocks; each (set, chunk) is one
+// item, and every member of the set owns one partial-result slot per chunk. The
+// slots of sequence s are slot_indptr[s] .. slot_indptr[s+1]-1.
 //
-// Items are ordered by decreasing cost (blocks x row tiles), and the items of one
+// Items are ordered by decreasing cost, blocks x max(3, RT): a block costs its
+// load until four warps' row tiles of tensor work outgrow it. The items of one
 // set stay adjacent, so the CTAs that read the same blocks run at about the same
 // time.
 #include <algorithm>
@@ -79,7 +79,7 @@ int plan_shared_host(int B, int G, int max_blocks, int num_pool_blocks, int num_
       const int n = std::min(per_set, (int)groups[gi].size() - j0);
       const int rows = n * G;
       const int rt = rows <= 16 ? 1 : (rows <= 32 ? 2 : 4);
-      const int cb = std::max(1, chunk_blocks / rt);
+      const int cb = std::max(1, chunk_blocks);
       sets.push_back(Set{gi, j0, n, rt, cb});
       for (int j = 0; j < n; ++j) nslots[groups[gi][j0 + j].seq] += (nbk + cb - 1) / cb;
     }
@@ -98,7 +98,7 @@ int plan_shared_host(int B, int G, int max_blocks, int num_pool_blocks, int num_
     for (int c0 = 0; c0 < nbk; c0 += st.cb) {
       const int nb = std::min(st.cb, nbk - c0);
       const int last = (c0 + nb == nbk) ? ((len - 1) & (kBlk - 1)) + 1 : kBlk;
-      its.push_back(Item{si, c0, nb, last, nb * st.rt});
+      its.push_back(Item{si, c0, nb, last, nb * std::max(3, st.rt)});
     }
   }
   if ((int64_t)its.size() > capacity) return LAZY_ERR_WORKSPACE;

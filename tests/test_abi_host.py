@@ -205,9 +205,8 @@ def test_shared_plan_covers_every_block_once(la, w, chunk):
         assert (it[5:8] == 0).all() and (it[8 + 4 * nm:] == 0).all()
         assert 1 <= nm <= la.PLAN_MAX_MEMBERS and nm * G <= 64
         rt = 1 if nm * G <= 16 else (2 if nm * G <= 32 else 4)
-        cost.append(nb * rt)
-        if chunk:
-            assert nb <= max(1, chunk // rt)
+        cost.append(nb * max(3, rt))
+        assert nb <= (chunk or 32)
         src_phys = [exp[src][b][0] for b in range(b0, b0 + nb)]
         assert [exp[src][b][2] for b in range(b0, b0 + nb)] == [16] * (nb - 1) + [last]
         for seq, bm, slot, zero in it[8: 8 + 4 * nm].reshape(nm, 4):
