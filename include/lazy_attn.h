@@ -203,8 +203,8 @@ int lazy_attn_decode(const lazy_attn_params *p, const void *q, const void *k_poo
  *   slot_indptr_host [B+1]: the slots of sequence s are slot_indptr[s] ..
  *     slot_indptr[s+1]-1;
  *   counts_host [2] = {num_items, num_slots}.
- * Items are ordered heaviest first (blocks x max(3, RT), RT = 1, 2 or 4 tiles of
- * 16 query rows: loads, not the tensor cores, bound the light items).
+ * Items are ordered by decreasing block count (ties in the order of first
+ * appearance of their document).
  * `capacity` bounds the item count (the number
  * of logical blocks in the batch always suffices). Returns LAZY_ERR_LAYOUT on the
  * packer's layout errors, and LAZY_ERR_WORKSPACE if capacity is too small.

@@ -11,10 +11,11 @@
 // item, and every member of the set owns one partial-result slot per chunk. The
 // slots of sequence s are slot_indptr[s] .. slot_indptr[s+1]-1.
 //
-// Items are ordered by decreasing cost, blocks x max(3, RT): a block costs its
-// load until four warps' row tiles of tensor work outgrow it. The items of one
-// set stay adjacent, so the CTAs that read the same blocks run at about the same
-// time.
+// Items are ordered by decreasing block count, and otherwise keep the order of
+// the groups, so items of 1, 2 and 4 row tiles stay mixed through the launch (an
+// SM then runs load-bound and tensor-bound items side by side). The items of one
+// group stay adjacent, so the CTAs that read the same blocks run at about the
+// same time.
 #include <algorithm>
 #include <map>
 #include <utility>
@@ -98,7 +99,7 @@ int plan_shared_host(int B, int G, int max_blocks, int num_pool_blocks, int num_
     for (int c0 = 0; c0 < nbk; c0 += st.cb) {
       const int nb = std::min(st.cb, nbk - c0);
       const int last = (c0 + nb == nbk) ? ((len - 1) & (kBlk - 1)) + 1 : kBlk;
-      its.push_back(Item{si, c0, nb, last, nb * std::max(3, st.rt)});
+      its.push_back(Item{si, c0, nb, last, nb});
     }
   }
   if ((int64_t)its.size() > capacity) return LAZY_ERR_WORKSPACE;

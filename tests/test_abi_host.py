@@ -204,8 +204,7 @@ def test_shared_plan_covers_every_block_once(la, w, chunk):
         src, b0, nb, last, nm = (int(x) for x in it[:5])
         assert (it[5:8] == 0).all() and (it[8 + 4 * nm:] == 0).all()
         assert 1 <= nm <= la.PLAN_MAX_MEMBERS and nm * G <= 64
-        rt = 1 if nm * G <= 16 else (2 if nm * G <= 32 else 4)
-        cost.append(nb * max(3, rt))
+        cost.append(nb)
         assert nb <= (chunk or 32)
         src_phys = [exp[src][b][0] for b in range(b0, b0 + nb)]
         assert [exp[src][b][2] for b in range(b0, b0 + nb)] == [16] * (nb - 1) + [last]
@@ -218,7 +217,7 @@ def test_shared_plan_covers_every_block_once(la, w, chunk):
             assert slot not in slots_seen
             slots_seen.add(slot)
             cover[seq][bm:bm + nb] += 1
-    assert (np.diff(cost) <= 0).all()  # heaviest items first
+    assert (np.diff(cost) <= 0).all()  # longest items first
     assert len(slots_seen) == slot_indptr[-1]
     for s in range(w.num_seqs):
         assert (cover[s] == 1).all(), s
