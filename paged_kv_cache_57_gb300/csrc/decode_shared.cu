@@ -105,6 +105,9 @@ __global__ void __launch_bounds__(kShThreads, 3)
   __shared__ int abort_flag;
 
   LAZY_TRACE(0, global_timer_ns());
+  // The combine kernel may be scheduled once every CTA of this grid has started;
+  // it waits for this grid's completion before it reads the partials.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int kvh = blockIdx.x % a.Hkv;
   const int item = blockIdx.x / a.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -393,11 +396,15 @@ __global__ void __launch_bounds__(kShThreads, 3)
 // ------------------------------------------------------------------ combine
 // out[s][h] = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k over the sequence's
 // slots k in [slot_indptr[s], slot_indptr[s+1]); a sequence without slots gets 0.
-// One warp per (sequence, query head). Lanes first read 32 slots' (m, l) at a
-// time; the weights are then broadcast by shuffle while each lane accumulates its
-// D/32 output columns, eight slots' rows in flight at once.
+// One warp per (sequence, query head), D/32 output columns per lane. Slots are
+// taken eight at a time with all their loads issued together (one memory round
+// trip per eight slots), folded in with the online rescale of the running
+// maximum. Launched as a programmatic dependent of the decode kernel: its CTAs
+// may become resident while the decode kernel's last CTAs run, and wait for the
+// decode grid's completion (and its partials) before reading anything.
 template <int D>
 __global__ void shared_combine_kernel(const SharedDecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int wg = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (wg >= a.B * a.Hq) return;
@@ -407,56 +414,52 @@ __global__ void shared_combine_kernel(const SharedDecodeArgs a) {
     if (lane == 0) raise_status(a.status, LAZY_DEV_LAYOUT);
     k0 = k1 = 0;
   }
-  const float2* ml = reinterpret_cast<const float2*>(a.ws_ml);
-  float M = -INFINITY;
-  for (int k = k0 + lane; k < k1; k += 32) M = fmaxf(M, ml[(size_t)k * a.Hq + h].x);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   constexpr int PER = D / 32;
+  constexpr int BATCH = 8;
+  const float2* ml = reinterpret_cast<const float2*>(a.ws_ml);
+  float M = -INFINITY, L = 0.f;
   float acc[PER];
 #pragma unroll
-  for (int j = 0; j < PER; ++j) acc[j] = 0.f;
-  float L = 0.f;
-  if (M != -INFINITY) {
-    for (int kc = k0; kc < k1; kc += 32) {
-      const int n = min(32, k1 - kc);
-      float w = 0.f;
-      if (lane < n) {
-        const float2 v = ml[(size_t)(kc + lane) * a.Hq + h];
-        w = fast_ex2(v.x - M);  // an empty slot (m = -inf) weighs 0
-        L += w * v.y;
-      }
-      int j = 0;
-      for (; j + 8 <= n; j += 8) {
-        float wj[8];
-        float vj[8][PER];
+  for (int c = 0; c < PER; ++c) acc[c] = 0.f;
+  for (int kc = k0; kc < k1; kc += BATCH) {
+    const int n = min(BATCH, k1 - kc);
+    float2 mlj[BATCH];
+    float vj[BATCH][PER];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          wj[u] = __shfl_sync(0xffffffffu, w, j + u);
-          const float* src = a.ws_o + ((size_t)(kc + j + u) * a.Hq + h) * D + lane * PER;
-          if constexpr (PER == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(src);
-            vj[u][0] = v.x, vj[u][1] = v.y, vj[u][2] = v.z, vj[u][3] = v.w;
-          } else {
-            const float2 v = *reinterpret_cast<const float2*>(src);
-            vj[u][0] = v.x, vj[u][1] = v.y;
-          }
+    for (int u = 0; u < BATCH; ++u) {
+      mlj[u] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+      for (int c = 0; c < PER; ++c) vj[u][c] = 0.f;
+      if (u < n) {
+        const size_t pidx = (size_t)(kc + u) * a.Hq + h;
+        mlj[u] = ml[pidx];
+        const float* src = a.ws_o + pidx * D + lane * PER;
+        if constexpr (PER == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          vj[u][0] = v.x, vj[u][1] = v.y, vj[u][2] = v.z, vj[u][3] = v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          vj[u][0] = v.x, vj[u][1] = v.y;
         }
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-#pragma unroll
-          for (int c = 0; c < PER; ++c) acc[c] = fmaf(wj[u], vj[u][c], acc[c]);
-      }
-      for (; j < n; ++j) {
-        const float wk = __shfl_sync(0xffffffffu, w, j);
-        const float* src = a.ws_o + ((size_t)(kc + j) * a.Hq + h) * D + lane * PER;
-#pragma unroll
-        for (int c = 0; c < PER; ++c) acc[c] = fmaf(wk, src[c], acc[c]);
       }
     }
-  }
+    float Mn = M;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    for (int u = 0; u < BATCH; ++u) Mn = fmaxf(Mn, mlj[u].x);
+    if (Mn == -INFINITY) continue;  // only empty slots so far
+    const float r = fast_ex2(M - Mn);  // 0 while nothing was folded in
+    L *= r;
+#pragma unroll
+    for (int c = 0; c < PER; ++c) acc[c] *= r;
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const float w = fast_ex2(mlj[u].x - Mn);  // an empty slot (m = -inf) weighs 0
+      L = fmaf(w, mlj[u].y, L);
+#pragma unroll
+      for (int c = 0; c < PER; ++c) acc[c] = fmaf(w, vj[u][c], acc[c]);
+    }
+    M = Mn;
+  }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + (size_t)wg * D + lane * PER;
   if constexpr (PER == 4) {
@@ -491,12 +494,18 @@ cudaError_t launch_decode_shared(const SharedDecodeArgs& a, bool lazy, const CUt
 cudaError_t launch_shared_combine(const SharedDecodeArgs& a, cudaStream_t st) {
   const int warps = a.B * a.Hq;
   if (warps == 0) return cudaSuccess;
-  const int threads = 256, blocks = (warps + 7) / 8;
-  if (a.D == 128)
-    shared_combine_kernel<128><<<blocks, threads, 0, st>>>(a);
-  else
-    shared_combine_kernel<64><<<blocks, threads, 0, st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((warps + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (a.D == 128) return cudaLaunchKernelEx(&cfg, shared_combine_kernel<128>, a);
+  return cudaLaunchKernelEx(&cfg, shared_combine_kernel<64>, a);
 }
 
 }  // namespace lazy
