@@ -10,7 +10,7 @@ timed beside it.
 
 Prints ONE JSON line (rank 0). ``value`` is logical KV GB/s: K+V bytes of every
 token of every context divided by the device time of the decode call, inputs
-resident in HBM, L2 flushed between steps. Extra keys carry the roofline against
+resident in HBM, L2 flushed between steps (written, then read, so no dirty lines remain). Extra keys carry the roofline against
 the unique-block HBM bound, the no-sharing control, the lazy-vs-pre-rotated
 overhead, prefill TFLOP/s, an end-to-end figure through host buffers, clocks and
 the CPU oracle baseline.
@@ -189,17 +189,41 @@ def run_prefill(d, lazy=None):
               out=d["out"], workspace=d["ws_pf"])
 
 
+class L2Flush:
+    """Evicts L2 before a timed step: writes a buffer of twice the L2 size (256 MB at
+    least), then reads a second one of the same size. The step then starts with a
+    cold L2 that holds no dirty lines: the written buffer's write-back to HBM
+    happens during the read pass, outside the timed region, instead of competing
+    with the step's own reads."""
+
+    def __init__(self, device):
+        import torch
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        n = max(2 * l2, 256 << 20) // 4
+        self.w = torch.empty(n, dtype=torch.float32, device="cuda")
+        self.r = torch.zeros(n, dtype=torch.float32, device="cuda")
+        self.acc = torch.zeros((), dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        import torch
+        self.w.add_(1)
+        torch.sum(self.r, dim=0, out=self.acc)
+
+
+L2_NOTE = "flushed before every step: 2x L2 written, then 2x L2 read (cold L2, no dirty lines)"
+
+
 def time_steps(fn, steps, warmup, flush):
     """Per-step device time (s) with CUDA events on the launching stream, L2 flushed before each step."""
     import torch
     st = torch.cuda.current_stream()
     for _ in range(warmup):
-        flush.add_(1)
+        flush()
         fn()
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for a, b in evs:
-        flush.add_(1)
+        flush()
         a.record(st)
         fn()
         b.record(st)
@@ -332,14 +356,13 @@ def main():
                       zipf_s=1.0, suffix_tokens=64, seed=rank_seed(rank))
     d = build_device(w)
     nbytes = decode_bytes(w)
-    l2 = torch.cuda.get_device_properties(local).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device="cuda")
+    flush = L2Flush(local)
 
     clocks = ClockSampler(local)
     clocks.start()
     fn = lambda: run_decode(d, lazy=True)
     for _ in range(args.warmup):
-        flush.add_(1)
+        flush()
         fn()
     torch.cuda.synchronize()
     if world > 1:
@@ -377,7 +400,7 @@ def main():
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": w.num_seqs, "context": int(w.tokens_per_seq()[0]),
                    "heads": [w.num_q_heads, w.num_kv_heads], "head_dim": w.head_dim, "rope_theta": w.rope_theta,
-                   "docs": "8 x 512 Zipf(1.0) of 256 + 64 private", "l2": "flushed before every step",
+                   "docs": "8 x 512 Zipf(1.0) of 256 + 64 private", "l2": L2_NOTE,
                    "decode_path": "shared-run (lazy_attn_decode_shared)",
                    "parallelism": f"weak x{world} (independent batches)"},
         "decode": {"tokens_per_s": world * w.num_seqs / (t_max / args.steps),
@@ -411,8 +434,7 @@ def single_workload(args):
     build.build()
     w = W.FULL[args.workload]()
     d = build_device(w)
-    l2 = torch.cuda.get_device_properties(0).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device="cuda")
+    flush = L2Flush(0)
     if w.kind == "decode":
         t = time_steps(lambda: run_decode(d, lazy=True, path=args.decode_path), args.steps, args.warmup, flush)
         v, unit = decode_bytes(w)["kv_logical"] / statistics.median(t) / 1e9, "GB/s"
