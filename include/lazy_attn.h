@@ -200,6 +200,10 @@ int lazy_attn_decode(const lazy_attn_params *p, const void *q, const void *k_poo
  *     [8 + 4j ..] member j < nmem: {seq, b0, slot, 0}: sequence seq holds the
  *         same physical blocks at its logical blocks b0 .. b0+nblk-1 and its
  *         partial result goes to `slot`; unused member entries are 0;
+ *     [72 + k] k < min(nblk, LAZY_PLAN_ITEM_BLOCK_IDS): physical id of the
+ *         item's block k (what src_seq's block word b0 + k names), 0 beyond: the
+ *         kernel starts the loads from these ids and checks them against the
+ *         block words (a mismatch sets LAZY_DEV_LAYOUT);
  *   slot_indptr_host [B+1]: the slots of sequence s are slot_indptr[s] ..
  *     slot_indptr[s+1]-1;
  *   counts_host [2] = {num_items, num_slots}.
@@ -216,7 +220,8 @@ int lazy_attn_decode(const lazy_attn_params *p, const void *q, const void *k_poo
  * not hold the item's physical block, or an item outside the table, sets
  * LAZY_DEV_LAYOUT and is skipped. */
 #define LAZY_PLAN_MAX_MEMBERS 16
-#define LAZY_PLAN_ITEM_INTS (8 + 4 * LAZY_PLAN_MAX_MEMBERS)
+#define LAZY_PLAN_ITEM_BLOCK_IDS 32
+#define LAZY_PLAN_ITEM_INTS (8 + 4 * LAZY_PLAN_MAX_MEMBERS + LAZY_PLAN_ITEM_BLOCK_IDS)
 int lazy_attn_plan_shared_host(const lazy_attn_params *p, int32_t num_docs, const int32_t *seg_indptr_host,
                                const int32_t *seg_doc_host, const int32_t *seg_len_host,
                                const int32_t *doc_block_indptr_host, const int32_t *doc_blocks_host,

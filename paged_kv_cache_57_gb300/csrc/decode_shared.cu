@@ -32,8 +32,11 @@ constexpr int kShThreads = 32 * kShWarps;
 constexpr int kShRows = 64;    // rows per item at most (4 row tiles)
 constexpr int kShStages = 8;   // TMA stages shared out among the teams
 constexpr int kShMembers = LAZY_PLAN_MAX_MEMBERS;
-constexpr int kItemInts = LAZY_PLAN_ITEM_INTS;  // 8 header ints + 4 per member
-static_assert(kItemInts == 8 + 4 * kShMembers && kItemInts % 4 == 0, "item record layout");
+constexpr int kItemInts = LAZY_PLAN_ITEM_INTS;  // 8 header ints, 4 per member, then block ids
+constexpr int kRecIds = 8 + 4 * kShMembers;      // offset of the block ids in the record
+constexpr int kRecBlocks = LAZY_PLAN_ITEM_BLOCK_IDS;
+static_assert(kItemInts == kRecIds + kRecBlocks && kItemInts % 4 == 0 && kItemInts / 4 <= kShThreads,
+              "item record layout");
 
 template <int D>
 struct SharedCfg {
@@ -189,14 +192,21 @@ __global__ void __launch_bounds__(kShThreads, 3)
   const bool leader = (rt == 0 && lane == 0);
   const uint32_t* wrow = a.words + (size_t)src * a.max_blocks + b0 + kb0;  // the team's block words
   const uint32_t id_mask = (1u << a.id_bits) - 1u;
-  // Lane l describes team block kc + l: physical id (num_pool_blocks = do not load) and valid slots.
+  // Physical id the record gives for item block kb < kRecBlocks.
+  auto rec_id = [&](int kb) { return rec[kRecIds + kb]; };
+  // Lane l describes team block kc + l: physical id (num_pool_blocks = do not load)
+  // and valid slots. The block word decides; where the record also names the block,
+  // the two must agree, else the block is skipped (its first load may have used the
+  // record's id) and the layout error is raised.
   auto describe = [&](int kc, int& phys, int& nv) {
     const int k = kc + lane;
     phys = a.num_pool_blocks;
     nv = 0;
     if (k < nk) {
       const int ph = (int)(__ldg(&wrow[k]) & id_mask);
-      if (ph < a.num_pool_blocks) {
+      if (kb0 + k < kRecBlocks && rec_id(kb0 + k) != ph) {
+        raise_status(a.status, LAZY_DEV_LAYOUT);
+      } else if (ph < a.num_pool_blocks) {
         phys = ph;
         nv = (kb0 + k == nblk - 1) ? last_nv : kBlock;
       } else {
@@ -204,18 +214,25 @@ __global__ void __launch_bounds__(kShThreads, 3)
       }
     }
   };
+  // First loads straight from the record's ids when it names all of them: they need
+  // not wait for the block words (which check them below).
+  const int pro = min(NS, nk);
+  const bool rec_first = kb0 + pro <= kRecBlocks;  // uniform over the team
+  if (rec_first && leader)
+    for (int k = 0; k < pro; ++k) {
+      const int rid = rec_id(kb0 + k);
+      const int phys = (rid >= 0 && rid < a.num_pool_blocks) ? rid : a.num_pool_blocks;
+      load_block_3d<D>(tst + k * G::STAGE_BYTES, &tfull[k], phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
+    }
   int cur_phys, cur_nv, nxt_phys = a.num_pool_blocks, nxt_nv = 0;
   describe(0, cur_phys, cur_nv);
   if (nk > 32) describe(32, nxt_phys, nxt_nv);
-  int issued = 0;
-  {
-    const int pro = min(NS, nk);
+  if (!rec_first)
     for (int k = 0; k < pro; ++k) {
       const int phys = __shfl_sync(0xffffffffu, cur_phys, k);
       if (leader) load_block_3d<D>(tst + k * G::STAGE_BYTES, &tfull[k], phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
     }
-    issued = pro;
-  }
+  int issued = pro;
   LAZY_TRACE(1, global_timer_ns());
 
   if (threadIdx.x < nmem) {

@@ -9,7 +9,9 @@
 // query heads per KV head), i.e. RT = 1, 2 or 4 tiles of 16 rows. A set's blocks
 // are cut into chunks of chunk_blocks logical blocks; each (set, chunk) is one
 // item, and every member of the set owns one partial-result slot per chunk. The
-// slots of sequence s are slot_indptr[s] .. slot_indptr[s+1]-1.
+// slots of sequence s are slot_indptr[s] .. slot_indptr[s+1]-1. An item also
+// carries the physical ids of its first 32 blocks, so the kernel can start its
+// loads before the block words arrive.
 //
 // Items are ordered by decreasing block count, and otherwise keep the order of
 // the groups, so items of 1, 2 and 4 row tiles stay mixed through the launch (an
@@ -122,6 +124,10 @@ int plan_shared_host(int B, int G, int max_blocks, int num_pool_blocks, int num_
       m[1] = o.b0 + its[i].c0;
       m[2] = next[o.seq]++;
     }
+    const int doc = keys[st.group].first;
+    int32_t* ids = d + 8 + 4 * LAZY_PLAN_MAX_MEMBERS;
+    for (int k = 0; k < its[i].nb && k < LAZY_PLAN_ITEM_BLOCK_IDS; ++k)
+      ids[k] = doc_blocks[doc_block_indptr[doc] + its[i].c0 + k];
   }
   counts[0] = (int32_t)its.size();
   counts[1] = slot_indptr[B];

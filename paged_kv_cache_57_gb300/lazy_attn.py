@@ -37,7 +37,8 @@ EXPORTED = (
     "lazy_attn_materialize",
 )
 PLAN_MAX_MEMBERS = 16
-PLAN_ITEM_INTS = 8 + 4 * PLAN_MAX_MEMBERS
+PLAN_ITEM_BLOCK_IDS = 32
+PLAN_ITEM_INTS = 8 + 4 * PLAN_MAX_MEMBERS + PLAN_ITEM_BLOCK_IDS
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -225,8 +226,8 @@ def decode_noalloc(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: tor
 class SharedPlan:
     """Work list of the shared-run decode: the planner's host arrays and their device copies.
 
-    ``items_host`` is [num_items, PLAN_ITEM_INTS] int32 (header, then members
-    {seq, first block, slot, 0}); ``slot_indptr_host`` is [B+1]."""
+    ``items_host`` is [num_items, PLAN_ITEM_INTS] int32: header, members {seq, first block,
+    slot, 0}, then the physical ids of the item's first blocks; ``slot_indptr_host`` is [B+1]."""
 
     def __init__(self, items: np.ndarray, slot_indptr: np.ndarray, device="cuda"):
         self.items_host, self.slot_indptr_host = items, slot_indptr

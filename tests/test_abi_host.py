@@ -202,11 +202,14 @@ def test_shared_plan_covers_every_block_once(la, w, chunk):
     cost = []
     for it in items:
         src, b0, nb, last, nm = (int(x) for x in it[:5])
-        assert (it[5:8] == 0).all() and (it[8 + 4 * nm:] == 0).all()
+        ids = it[8 + 4 * la.PLAN_MAX_MEMBERS:]
+        assert (it[5:8] == 0).all() and (it[8 + 4 * nm: 8 + 4 * la.PLAN_MAX_MEMBERS] == 0).all()
         assert 1 <= nm <= la.PLAN_MAX_MEMBERS and nm * G <= 64
         cost.append(nb)
         assert nb <= (chunk or 32)
         src_phys = [exp[src][b][0] for b in range(b0, b0 + nb)]
+        nid = min(nb, la.PLAN_ITEM_BLOCK_IDS)  # the record names the item's first blocks
+        assert list(ids[:nid]) == src_phys[:nid] and (ids[nid:] == 0).all()
         assert [exp[src][b][2] for b in range(b0, b0 + nb)] == [16] * (nb - 1) + [last]
         for seq, bm, slot, zero in it[8: 8 + 4 * nm].reshape(nm, 4):
             assert zero == 0

@@ -138,6 +138,24 @@ def test_shared_decode_flags_inconsistent_plan():
     assert torch.isfinite(out.float()).all()
 
 
+def test_shared_decode_flags_record_block_id_mismatch():
+    """A record whose block id disagrees with the block word (inside the pool, or past
+    its end) is flagged; the kernel loads nothing outside the pool."""
+    L = la()
+    w = W.decode_zipf("sbadid", batch=4, hq=8, hkv=2, d=128, docs_per_seq=2, doc_tokens=40, pool_docs=3,
+                      zipf_s=1.0, seed=168)
+    dv = to_device(w)
+    plan = shared_plan(dv)
+    ids0 = 8 + 4 * L.PLAN_MAX_MEMBERS
+    for bad_id in (int(plan.items_host[0, ids0]) ^ 1, w.num_pool_blocks + 5):
+        items = plan.items_host.copy()
+        items[0, ids0] = bad_id
+        out = decode_shared(dv, L.SharedPlan(items, plan.slot_indptr_host))
+        torch.cuda.synchronize()
+        assert L.device_status(clear=True) & L.LAZY_DEV_LAYOUT
+        assert torch.isfinite(out.float()).all()
+
+
 # ---------------------------------------------------------------- full sizes
 
 def test_llama8b_shared_decode_full():
