@@ -42,7 +42,7 @@ WORKLOAD = "llama8b_decode"
 NCU_TRAFFIC = {"sources": ["paged_kv_cache_57_gb300/csrc/decode_shared.cu",
                            "paged_kv_cache_57_gb300/csrc/decode_block.cuh",
                            "paged_kv_cache_57_gb300/csrc/common.cuh"],
-               "sha16": "ef7f182ca364252e", "bytes_per_launch": 301444864 + 25410560}
+               "sha16": "e198b2d4a451028a", "bytes_per_launch": 302095104 + 10525184}
 
 
 def _traffic_if_current():
