@@ -76,42 +76,73 @@ bool encoder_ready() {
   return true;
 }
 
+// cuTensorMapEncodeTiled through a small per-thread cache of the last maps made
+// (bf16, 128-byte swizzle, no interleave, L2 promotion 256 B, no fill): a call with
+// the same pool pointers and shapes as a recent one reuses its maps.
+static bool encode_cached(CUtensorMap* m, cuuint32_t rank, const void* base, const cuuint64_t* dims,
+                          const cuuint64_t* strides, const cuuint32_t* box) {
+  struct Entry {
+    const void* base;
+    cuuint32_t rank;
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3];
+    CUtensorMap map;
+    bool valid;
+  };
+  thread_local Entry cache[8] = {};
+  thread_local int next = 0;
+  Entry key{};
+  key.base = base;
+  key.rank = rank;
+  for (cuuint32_t i = 0; i < rank; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+    if (i + 1 < rank) key.strides[i] = strides[i];
+  }
+  for (Entry& e : cache)
+    if (e.valid && e.base == key.base && e.rank == key.rank && std::memcmp(e.dims, key.dims, sizeof(key.dims)) == 0 &&
+        std::memcmp(e.strides, key.strides, sizeof(key.strides)) == 0 &&
+        std::memcmp(e.box, key.box, sizeof(key.box)) == 0) {
+      *m = e.map;
+      return true;
+    }
+  if (!encoder_ready()) return false;
+  cuuint32_t es[3] = {1, 1, 1};
+  if (g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  key.map = *m;
+  key.valid = true;
+  cache[next] = key;
+  next = (next + 1) % 8;
+  return true;
+}
+
 // 2-D bf16 view [rows][d] with 16-row x 64-column boxes, 128-byte swizzle.
 bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, int d, uint32_t box_rows) {
-  if (!encoder_ready()) return false;
   cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)d * 2};
   cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_cached(m, 2, base, dims, strides, box);
 }
 
 // 3-D bf16 view of the same [rows][d] pool as (column in a 64-column half, row, half):
 // one box of 64 columns x box_rows rows x d/64 halves lands as the d/64 swizzled
 // 64-column boxes of encode_rows_map placed one after the other, in one copy.
 bool encode_block_map(CUtensorMap* m, const void* base, uint64_t rows, int d, uint32_t box_rows) {
-  if (!encoder_ready()) return false;
   cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(d / 64)};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, 128};
   cuuint32_t box[3] = {64, box_rows, (cuuint32_t)(d / 64)};
-  cuuint32_t es[3] = {1, 1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_cached(m, 3, base, dims, strides, box);
 }
 
 // 3-D bf16 view of q [total_q][Hq][d]: boxes of 64 columns x 1 head x box_rows rows.
 bool encode_q_map(CUtensorMap* m, const void* base, uint64_t total_q, int hq, int d, uint32_t box_rows) {
-  if (!encoder_ready()) return false;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hq, (cuuint64_t)total_q};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)hq * d * 2};
   cuuint32_t box[3] = {64, 1, box_rows};
-  cuuint32_t es[3] = {1, 1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_cached(m, 3, base, dims, strides, box);
 }
 
 int check_params(const lazy_attn_params* p, Checked* c) {

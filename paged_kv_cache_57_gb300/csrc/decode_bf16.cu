@@ -485,7 +485,7 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& kmap,
   constexpr int SPT = LAZY_DECODE_SPT;
   using C = DecodeCfg<D, MT, SPT>;
   auto kern = decode_bf16_kernel<D, MT, SPT, LAZY>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = set_smem_once<decode_bf16_kernel<D, MT, SPT, LAZY>>(C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(a.splits, a.Hkv, a.B);
   kern<<<grid, C::NTHREADS, C::SMEM, st>>>(a, kmap, vmap);

@@ -494,7 +494,7 @@ static cudaError_t launch_shared_t(const SharedDecodeArgs& a, const CUtensorMap&
                                    cudaStream_t st) {
   using C = SharedCfg<D>;
   auto kern = decode_shared_kernel<D, LAZY>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = set_smem_once<decode_shared_kernel<D, LAZY>>(C::SMEM);
   if (e != cudaSuccess) return e;
   const long long blocks = (long long)a.num_items * a.Hkv;
   kern<<<(unsigned)blocks, kShThreads, C::SMEM, st>>>(a, kmap, vmap);

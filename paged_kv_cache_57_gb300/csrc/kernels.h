@@ -1,6 +1,8 @@
 // kernels.h -- internal launch interface between the C ABI (api.cu) and the kernels.
 #pragma once
 
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -8,6 +10,22 @@
 #include "../../include/lazy_attn.h"
 
 namespace lazy {
+
+// Raises a kernel's dynamic shared-memory limit once per device (the attribute
+// persists for the process), instead of on every launch.
+template <auto Kern>
+inline cudaError_t set_smem_once(int bytes) {
+  static std::atomic<unsigned long long> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_relaxed);
+  return e;
+}
+
 
 struct DecodeArgs {
   const void* q;             // [B][Hq][D] unrotated

@@ -903,7 +903,7 @@ cudaError_t launch_prefill_stream(const PrefillArgs& a, bool lazy, const CUtenso
   cudaError_t e = cudaMemsetAsync(a.counters, 0, (size_t)(grid + 1) * 2 * BM * sizeof(int), st);
   if (e != cudaSuccess) return e;
   auto kern = lazy ? prefill_stream_kernel<true> : prefill_stream_kernel<false>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  e = lazy ? set_smem_once<prefill_stream_kernel<true>>(SMEM) : set_smem_once<prefill_stream_kernel<false>>(SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, THREADS, SMEM, st>>>(a, qmap, kmap, vmap);
   return cudaGetLastError();

@@ -542,7 +542,7 @@ cudaError_t launch_prefill_tq(const PrefillArgs& a, bool lazy, const CUtensorMap
   if (a.B == 0 || a.max_q_len == 0) return cudaSuccess;
   dim3 grid((a.max_q_len + BM - 1) / BM, a.Hq, a.B);
   auto kern = lazy ? prefill_tq_kernel<true> : prefill_tq_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  cudaError_t e = lazy ? set_smem_once<prefill_tq_kernel<true>>(SMEM) : set_smem_once<prefill_tq_kernel<false>>(SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, THREADS, SMEM, st>>>(a, qmap, kmap, vmap);
   return cudaGetLastError();

@@ -269,9 +269,10 @@ def decode_shared(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torc
     dt = _tdt(p)
     if out is None:
         out = torch.empty_like(q)
-    nws = decode_shared_workspace_bytes(p, plan.num_slots)
-    if workspace is None and nws:
-        workspace = torch.empty(nws, dtype=torch.uint8, device=q.device)
+    if workspace is None:  # the library checks a given workspace's size itself
+        nws = decode_shared_workspace_bytes(p, plan.num_slots)
+        if nws:
+            workspace = torch.empty(nws, dtype=torch.uint8, device=q.device)
     wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
     i32 = torch.int32
     rc = _lib.lazy_attn_decode_shared(ctypes.byref(p), _dptr(q, "q", dt), _dptr(k_pool, "k_pool", dt),
