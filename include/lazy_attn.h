@@ -129,6 +129,31 @@ size_t lazy_attn_rope_table_bytes(const lazy_attn_params *p);
 int lazy_attn_rope_table_init(const lazy_attn_params *p, void *table, size_t table_bytes,
                               lazy_stream_t stream);
 
+/* Frequency scaling of the rotation (not in the pages, which state the method for
+ * RoPE in general): the Llama-3.1 rule changes only the frequencies w_f = theta^(-2f/d),
+ * so every kernel picks it up from the table. With wavelength lambda = 2 pi / w,
+ * lambda_hi = original_max_position / high_freq_factor and lambda_lo =
+ * original_max_position / low_freq_factor, a frequency is kept when lambda < lambda_hi,
+ * divided by `factor` when lambda > lambda_lo, and otherwise interpolated with
+ * s = (original_max_position / lambda - low_freq_factor) / (high_freq_factor - low_freq_factor):
+ * w' = (1 - s) w / factor + s w. lazy_attn_rope_table_init_scaled fills the same table
+ * as lazy_attn_rope_table_init from the scaled frequencies (scaling NULL: unscaled).
+ * Requires factor > 0 and 0 < low_freq_factor < high_freq_factor and
+ * original_max_position > 0, else LAZY_ERR_INVALID_ARG.
+ * Interleaved (GPT-J) pairing (2f, 2f+1) needs no entry point: it is rotate-half
+ * pairing on a head dimension permuted as [0, 2, 4, ..., d-2, 1, 3, ..., d-1]; a
+ * caller that applies that permutation to q and to the stored K rows (V and out are
+ * not rotated and stay as they are) gets the interleaved results, since one common
+ * permutation of q and k leaves every score unchanged. */
+typedef struct {
+  double factor;
+  double low_freq_factor;
+  double high_freq_factor;
+  int32_t original_max_position;
+} lazy_rope_scaling;
+int lazy_attn_rope_table_init_scaled(const lazy_attn_params *p, const lazy_rope_scaling *scaling, void *table,
+                                     size_t table_bytes, lazy_stream_t stream);
+
 /* ---------------------------------------------------------------- block-word packer
  * Builds block_words and seq_lens from per-sequence document lists (CSR):
  *   seg_indptr [B+1]; segment k of sequence s (seg_indptr[s] <= k < seg_indptr[s+1])

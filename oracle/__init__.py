@@ -50,6 +50,9 @@ def lib():
             build()
             L = ctypes.CDLL(_SO)
             L.lo_rope_rotate.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double, _f64p, _f64p]
+            L.lo_rope_rotate_ex.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_void_p, ctypes.c_int,
+                                            ctypes.c_double, _f64p, _f64p]
+            L.lo_llama3_freqs.argtypes = [ctypes.c_int] + [ctypes.c_double] * 5 + [_f64p]
             L.lo_softmax_dot.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, _f64p, _f64p, _f64p]
             L.lo_tiled_softmax_dot.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, _f64p, _f64p,
                                                ctypes.c_int, _f64p]
@@ -62,6 +65,11 @@ def lib():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double,
                 ctypes.c_int, ctypes.c_int, ctypes.c_void_p, _i32p, _i32p, ctypes.c_void_p,
                 ctypes.c_void_p, ctypes.c_int64, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p, _f64p]
+            L.lo_attention_ex.restype = ctypes.c_int
+            L.lo_attention_ex.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_void_p,
+                ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, _i32p, _i32p,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p, _f64p]
             _lib = L
     return _lib
 
@@ -79,6 +87,27 @@ def rope_rotate(x: np.ndarray, n: float, theta: float) -> np.ndarray:
     y = np.empty_like(x)
     lib().lo_rope_rotate(x.shape[-1], float(theta), float(n), x, y)
     return y
+
+
+def rope_rotate_ex(x: np.ndarray, n: float, theta: float, freqs: Optional[np.ndarray] = None,
+                   interleaved: bool = False) -> np.ndarray:
+    """R_n x with explicit frequencies (None: theta^(-2i/d)) and rotate-half or
+    interleaved (2i, 2i+1) pairing."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(x)
+    f = None if freqs is None else np.ascontiguousarray(freqs, dtype=np.float64)
+    lib().lo_rope_rotate_ex(x.shape[-1], float(theta), None if f is None else f.ctypes.data, int(interleaved),
+                            float(n), x, y)
+    return y
+
+
+def llama3_freqs(d: int, theta: float, factor: float, low_freq_factor: float, high_freq_factor: float,
+                 original_max_position: int) -> np.ndarray:
+    """The d/2 rotation frequencies under Llama-3.1 scaling (see lo_llama3_freqs)."""
+    out = np.empty(d // 2, np.float64)
+    lib().lo_llama3_freqs(int(d), float(theta), float(factor), float(low_freq_factor), float(high_freq_factor),
+                          float(original_max_position), out)
+    return out
 
 
 def softmax_dot(q, K, V) -> np.ndarray:
@@ -122,9 +151,10 @@ def query_rows(w):
 
 
 def attention(w, rows: Optional[Sequence[int]] = None, sm_scale: float = 0.0,
-              k_pool=None, v_pool=None) -> np.ndarray:
+              k_pool=None, v_pool=None, freqs: Optional[np.ndarray] = None, interleaved: bool = False) -> np.ndarray:
     """fp64 reference output of workload ``w`` for the query rows ``rows`` (all by
-    default): decode rows are sequences, prefill rows are chunk tokens.
+    default): decode rows are sequences, prefill rows are chunk tokens. ``freqs``
+    replaces theta^(-2i/d); ``interleaved`` pairs dimensions (2i, 2i+1).
     Returns [len(rows), Hq, d]."""
     q_seq, q_m = query_rows(w)
     q = w.q
@@ -137,7 +167,9 @@ def attention(w, rows: Optional[Sequence[int]] = None, sm_scale: float = 0.0,
     assert dt == dk == dv
     nq = qb.shape[0]
     out = np.zeros((nq, w.num_q_heads, w.head_dim), np.float64)
-    rc = lib().lo_attention(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, float(w.rope_theta),
+    f = None if freqs is None else np.ascontiguousarray(freqs, dtype=np.float64)
+    rc = lib().lo_attention_ex(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, float(w.rope_theta),
+                            None if f is None else f.ctypes.data, int(interleaved),
                             float(sm_scale), dt, nq, qb.ctypes.data, np.ascontiguousarray(q_seq, np.int32),
                             np.ascontiguousarray(q_m, np.int32), kb.ctypes.data, vb.ctypes.data,
                             int(kb.shape[0]), np.ascontiguousarray(w.seg_indptr, np.int32),

@@ -9,7 +9,9 @@
  * What it computes, and where the definition comes from:
  *
  *  - Rotary position embedding R_n, rotate-half pairing (i, i+d/2) with
- *    omega_i = theta^(-2i/d):
+ *    omega_i = theta^(-2i/d) (lo_rope_rotate_ex / lo_attention_ex also take an
+ *    explicit frequency vector, e.g. lo_llama3_freqs, and the interleaved pairing
+ *    (2i, 2i+1)):
  *        y_i     = x_i cos(n w_i) - x_{i+h} sin(n w_i)
  *        y_{i+h} = x_{i+h} cos(n w_i) + x_i sin(n w_i)
  *    The LazyAttention technical summary ("Mathematical Equivalence") relies on
@@ -74,15 +76,47 @@ void lo_set_num_threads(int n) {
 #endif
 }
 
-/* y = R_n x. x and y may alias. */
-void lo_rope_rotate(int d, double theta, double n, const double *x, double *y) {
+/* y = R_n x with frequencies w[i] (NULL: theta^(-2i/d)) and pairing (i, i+d/2), or
+ * (2i, 2i+1) when `interleaved` (GPT-J style). x and y may alias. */
+void lo_rope_rotate_ex(int d, double theta, const double *w, int interleaved, double n, const double *x,
+                       double *y) {
   int h = d / 2;
   for (int i = 0; i < h; i++) {
-    double w = pow(theta, -2.0 * (double)i / (double)d);
-    double c = cos(n * w), s = sin(n * w);
-    double a = x[i], b = x[i + h];
-    y[i] = a * c - b * s;
-    y[i + h] = b * c + a * s;
+    double wi = w ? w[i] : pow(theta, -2.0 * (double)i / (double)d);
+    double c = cos(n * wi), s = sin(n * wi);
+    int ia = interleaved ? 2 * i : i, ib = interleaved ? 2 * i + 1 : i + h;
+    double a = x[ia], b = x[ib];
+    y[ia] = a * c - b * s;
+    y[ib] = b * c + a * s;
+  }
+}
+
+/* y = R_n x, rotate-half pairing, omega_i = theta^(-2i/d). x and y may alias. */
+void lo_rope_rotate(int d, double theta, double n, const double *x, double *y) {
+  lo_rope_rotate_ex(d, theta, NULL, 0, n, x, y);
+}
+
+/* Llama-3.1 frequency scaling of omega_i = theta^(-2i/d), i < d/2 (the rule published
+ * with Llama 3.1): with wavelength lambda = 2 pi / omega, lambda_hi = L / high_ff and
+ * lambda_lo = L / low_ff (L the original context length), a frequency is kept when
+ * lambda < lambda_hi, divided by `factor` when lambda > lambda_lo, and otherwise
+ * interpolated: s = (L / lambda - low_ff) / (high_ff - low_ff),
+ * omega' = (1 - s) omega / factor + s omega. */
+void lo_llama3_freqs(int d, double theta, double factor, double low_ff, double high_ff, double orig_max,
+                     double *out) {
+  const double two_pi = 6.283185307179586476925286766559;
+  const double lam_hi = orig_max / high_ff, lam_lo = orig_max / low_ff;
+  for (int i = 0; i < d / 2; i++) {
+    const double w = pow(theta, -2.0 * (double)i / (double)d);
+    const double lam = two_pi / w;
+    if (lam < lam_hi) {
+      out[i] = w;
+    } else if (lam > lam_lo) {
+      out[i] = w / factor;
+    } else {
+      const double s = (orig_max / lam - low_ff) / (high_ff - low_ff);
+      out[i] = (1.0 - s) * w / factor + s * w;
+    }
   }
 }
 
@@ -157,11 +191,11 @@ double lo_kv_cache_bytes(double layers, double heads, double head_dim, double se
  *   out      [nq][hq][d]   fp64
  * Returns 0, or -1 on a malformed layout.
  */
-int lo_attention(int num_seqs, int hq, int hkv, int d, double theta, double sm_scale, int dtype, int nq,
-                 const void *q, const int32_t *q_seq, const int32_t *q_m, const void *k_pool,
-                 const void *v_pool, int64_t num_pool_blocks, const int32_t *seg_indptr,
-                 const int32_t *seg_doc, const int32_t *seg_len, const int32_t *seq_pos0,
-                 const int32_t *doc_block_indptr, const int32_t *doc_blocks, double *out) {
+int lo_attention_ex(int num_seqs, int hq, int hkv, int d, double theta, const double *freqs, int interleaved,
+                    double sm_scale, int dtype, int nq, const void *q, const int32_t *q_seq, const int32_t *q_m,
+                    const void *k_pool, const void *v_pool, int64_t num_pool_blocks, const int32_t *seg_indptr,
+                    const int32_t *seg_doc, const int32_t *seg_len, const int32_t *seq_pos0,
+                    const int32_t *doc_block_indptr, const int32_t *doc_blocks, double *out) {
   if (hkv <= 0 || hq % hkv != 0 || d <= 0 || d % 2 != 0) return -1;
   const int g = hq / hkv;
   if (sm_scale <= 0.0) sm_scale = 1.0 / sqrt((double)d);
@@ -210,7 +244,7 @@ int lo_attention(int num_seqs, int hq, int hkv, int d, double theta, double sm_s
         const int64_t phys = doc_blocks[doc_block_indptr[doc] + j / 16];
         const int64_t base = ((phys * hkv + kvh) * 16 + (j % 16)) * (int64_t)d;
         for (int c = 0; c < d; c++) row[c] = lo_load(k_pool, dtype, base + c);
-        lo_rope_rotate(d, theta, (double)p, row, &Kadj[t * d]);
+        lo_rope_rotate_ex(d, theta, freqs, interleaved, (double)p, row, &Kadj[t * d]);
         for (int c = 0; c < d; c++) V[t * d + c] = lo_load(v_pool, dtype, base + c);
         pos[t] = p + j;
       }
@@ -223,7 +257,7 @@ int lo_attention(int num_seqs, int hq, int hkv, int d, double theta, double sm_s
       const int64_t m = q_m[r];
       for (int h = kvh * g; h < (kvh + 1) * g; h++) {
         for (int c = 0; c < d; c++) row[c] = lo_load(q, dtype, ((int64_t)r * hq + h) * d + c);
-        lo_rope_rotate(d, theta, (double)m, row, qr);
+        lo_rope_rotate_ex(d, theta, freqs, interleaved, (double)m, row, qr);
         double mx = -INFINITY;
         for (int64_t j = 0; j < n; j++) {
           if (pos[j] > m) { sc[j] = -INFINITY; continue; }
@@ -248,4 +282,15 @@ int lo_attention(int num_seqs, int hq, int hkv, int d, double theta, double sm_s
     free(Kadj), free(V), free(pos), free(row), free(qr), free(sc);
   }
   return bad ? -1 : 0;
+}
+
+/* lo_attention_ex with theta^(-2i/d) frequencies and rotate-half pairing. */
+int lo_attention(int num_seqs, int hq, int hkv, int d, double theta, double sm_scale, int dtype, int nq,
+                 const void *q, const int32_t *q_seq, const int32_t *q_m, const void *k_pool,
+                 const void *v_pool, int64_t num_pool_blocks, const int32_t *seg_indptr,
+                 const int32_t *seg_doc, const int32_t *seg_len, const int32_t *seq_pos0,
+                 const int32_t *doc_block_indptr, const int32_t *doc_blocks, double *out) {
+  return lo_attention_ex(num_seqs, hq, hkv, d, theta, NULL, 0, sm_scale, dtype, nq, q, q_seq, q_m, k_pool, v_pool,
+                         num_pool_blocks, seg_indptr, seg_doc, seg_len, seq_pos0, doc_block_indptr, doc_blocks,
+                         out);
 }

@@ -231,7 +231,21 @@ int lazy_attn_rope_table_init(const lazy_attn_params* p, void* table, size_t tab
   if (rc != LAZY_OK) return rc;
   if (!table) return LAZY_ERR_INVALID_ARG;
   if (table_bytes < lazy_attn_rope_table_bytes(p) || !aligned16(table)) return LAZY_ERR_WORKSPACE;
-  return launched(lazy::launch_rope_table(static_cast<float2*>(table), p->head_dim, p->rope_theta,
+  return launched(lazy::launch_rope_table(static_cast<float2*>(table), p->head_dim, p->rope_theta, nullptr,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int lazy_attn_rope_table_init_scaled(const lazy_attn_params* p, const lazy_rope_scaling* scaling, void* table,
+                                     size_t table_bytes, lazy_stream_t stream) {
+  Checked c;
+  int rc = check_params(p, &c);
+  if (rc != LAZY_OK) return rc;
+  if (!table) return LAZY_ERR_INVALID_ARG;
+  if (scaling && !(scaling->factor > 0.0 && scaling->low_freq_factor > 0.0 &&
+                   scaling->high_freq_factor > scaling->low_freq_factor && scaling->original_max_position > 0))
+    return LAZY_ERR_INVALID_ARG;
+  if (table_bytes < lazy_attn_rope_table_bytes(p) || !aligned16(table)) return LAZY_ERR_WORKSPACE;
+  return launched(lazy::launch_rope_table(static_cast<float2*>(table), p->head_dim, p->rope_theta, scaling,
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 

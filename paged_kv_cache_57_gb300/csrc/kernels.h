@@ -127,7 +127,8 @@ int plan_shared_host(int B, int G, int max_blocks, int num_pool_blocks, int num_
                      int32_t* counts);
 
 // Every launcher returns the cudaError_t of its launch.
-cudaError_t launch_rope_table(float2* table, int head_dim, double theta, cudaStream_t st);
+cudaError_t launch_rope_table(float2* table, int head_dim, double theta, const lazy_rope_scaling* scaling,
+                              cudaStream_t st);
 cudaError_t launch_debug_rope(const float2* table, const int32_t* deltas, int n, int head_dim, float2* out,
                               unsigned int* status, cudaStream_t st);
 cudaError_t launch_pack(const PackArgs& a, cudaStream_t st);

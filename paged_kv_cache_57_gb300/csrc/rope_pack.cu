@@ -4,16 +4,32 @@
 
 namespace lazy {
 
-// t_i = w_i / (2 pi), w_i = theta^(-2i/d), in fp64, stored as fp32 (hi, lo).
+// t_i = w_i / (2 pi), w_i = theta^(-2i/d) (with the Llama-3.1 wavelength-band scaling
+// of lazy_attn.h when requested), in fp64, stored as fp32 (hi, lo).
 // Entries [0, half): the turns (hi, lo). Entries half + i * half + f: (cos, sin)(i w_f)
 // for the prefill row offsets i < LAZY_ROPE_ROWS. Everything in fp64, rounded once.
-__global__ void rope_table_kernel(float2* table, int half, int head_dim, double theta) {
+// Scaling parameters of the frequencies; factor <= 0 means none.
+struct FreqScale {
+  double factor, low_ff, high_ff, orig_max;
+};
+
+__global__ void rope_table_kernel(float2* table, int half, int head_dim, double theta, FreqScale sc) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= half * (1 + LAZY_ROPE_ROWS)) return;
   const int f = idx % half, row = idx / half - 1;
-  const double w = pow(theta, -2.0 * (double)f / (double)head_dim);
+  const double two_pi = 6.283185307179586476925286766559;
+  double w = pow(theta, -2.0 * (double)f / (double)head_dim);
+  if (sc.factor > 0.0) {  // wavelength bands: keep, divide by the factor, or blend the two
+    const double lam = two_pi / w;
+    const double lam_short = sc.orig_max / sc.high_ff, lam_long = sc.orig_max / sc.low_ff;
+    if (lam > lam_long) {
+      w = w / sc.factor;
+    } else if (lam >= lam_short) {
+      const double blend = (sc.orig_max / lam - sc.low_ff) / (sc.high_ff - sc.low_ff);
+      w = (1.0 - blend) * (w / sc.factor) + blend * w;
+    }
+  }
   if (row < 0) {
-    const double two_pi = 6.283185307179586476925286766559;
     const double t = w / two_pi;
     const float hi = (float)t;
     table[idx] = make_float2(hi, (float)(t - (double)hi));
@@ -24,10 +40,14 @@ __global__ void rope_table_kernel(float2* table, int half, int head_dim, double 
   }
 }
 
-cudaError_t launch_rope_table(float2* table, int head_dim, double theta, cudaStream_t st) {
+cudaError_t launch_rope_table(float2* table, int head_dim, double theta, const lazy_rope_scaling* scaling,
+                              cudaStream_t st) {
   const int half = head_dim / 2;
   const int total = half * (1 + LAZY_ROPE_ROWS);
-  rope_table_kernel<<<(total + 255) / 256, 256, 0, st>>>(table, half, head_dim, theta);
+  FreqScale sc{0.0, 1.0, 2.0, 1.0};
+  if (scaling) sc = FreqScale{scaling->factor, scaling->low_freq_factor, scaling->high_freq_factor,
+                              (double)scaling->original_max_position};
+  rope_table_kernel<<<(total + 255) / 256, 256, 0, st>>>(table, half, head_dim, theta, sc);
   return cudaGetLastError();
 }
 

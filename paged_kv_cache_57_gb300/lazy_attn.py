@@ -34,7 +34,7 @@ EXPORTED = (
     "lazy_attn_decode", "lazy_attn_prefill_workspace_bytes", "lazy_attn_prefill", "lazy_attn_debug_gather",
     "lazy_attn_device_status", "lazy_attn_launch_count", "lazy_attn_debug_rope", "lazy_attn_decode_noalloc",
     "lazy_attn_plan_shared_host", "lazy_attn_decode_shared_workspace_bytes", "lazy_attn_decode_shared",
-    "lazy_attn_materialize",
+    "lazy_attn_materialize", "lazy_attn_rope_table_init_scaled",
 )
 PLAN_MAX_MEMBERS = 16
 PLAN_ITEM_BLOCK_IDS = 32
@@ -65,6 +65,7 @@ _sig = {
     "lazy_attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "lazy_attn_rope_table_bytes": (_sz, [_P]),
     "lazy_attn_rope_table_init": (ctypes.c_int, [_P, _vp, _sz, _vp]),
+    "lazy_attn_rope_table_init_scaled": (ctypes.c_int, [_P, _vp, _vp, _sz, _vp]),
     "lazy_attn_pack_block_words_host": (ctypes.c_int, [_P, _i32] + [_vp] * 8),
     "lazy_attn_pack_block_words": (ctypes.c_int, [_P, _i32] + [_vp] * 8 + [_vp]),
     "lazy_attn_decode_workspace_bytes": (_sz, [_P]),
@@ -131,15 +132,33 @@ def rope_table_bytes(p: Params) -> int:
     return int(_lib.lazy_attn_rope_table_bytes(ctypes.byref(p)))
 
 
-def rope_table_init(p: Params, table: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+class RopeScaling(ctypes.Structure):
+    """Llama-3.1 frequency scaling (lazy_rope_scaling)."""
+    _fields_ = [("factor", ctypes.c_double), ("low_freq_factor", ctypes.c_double),
+                ("high_freq_factor", ctypes.c_double), ("original_max_position", ctypes.c_int32)]
+
+
+def rope_table_init(p: Params, table: Optional[torch.Tensor] = None, stream=None,
+                    scaling: Optional[RopeScaling] = None) -> torch.Tensor:
     n = rope_table_bytes(p)
     if n == 0:
         raise LazyAttnError(LAZY_ERR_INVALID_ARG, "rope_table_bytes")
     if table is None:
         table = torch.empty(n, dtype=torch.uint8, device="cuda")
-    _check(_lib.lazy_attn_rope_table_init(ctypes.byref(p), _dptr(table, "table"), table.numel() * table.element_size(),
-                                          _stream(stream)), "rope_table_init")
+    nbytes = table.numel() * table.element_size()
+    if scaling is None:
+        rc = _lib.lazy_attn_rope_table_init(ctypes.byref(p), _dptr(table, "table"), nbytes, _stream(stream))
+    else:
+        rc = _lib.lazy_attn_rope_table_init_scaled(ctypes.byref(p), ctypes.addressof(scaling), _dptr(table, "table"),
+                                                   nbytes, _stream(stream))
+    _check(rc, "rope_table_init")
     return table
+
+
+def interleave_perm(d: int) -> np.ndarray:
+    """Head-dimension order [0, 2, ..., d-2, 1, 3, ..., d-1]: q and stored K permuted this
+    way make the interleaved (GPT-J) pairing (2f, 2f+1) the library's (f, f + d/2)."""
+    return np.concatenate([np.arange(0, d, 2), np.arange(1, d, 2)])
 
 
 # ---------------------------------------------------------------- packer

@@ -27,8 +27,9 @@ def _bf16(x):
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
 
 
-def emulate(w, rows, lazy: bool = True, k_pool=None) -> np.ndarray:
-    """[len(rows), Hq, d] for query rows ``rows`` of workload ``w``."""
+def emulate(w, rows, lazy: bool = True, k_pool=None, freqs=None) -> np.ndarray:
+    """[len(rows), Hq, d] for query rows ``rows`` of workload ``w`` (``freqs``: rotation
+    frequencies other than theta^(-2i/d))."""
     kp = (w.k_pool if k_pool is None else k_pool).double().numpy()
     vp = w.v_pool.double().numpy()
     q = w.q.double().numpy()
@@ -61,16 +62,16 @@ def emulate(w, rows, lazy: bool = True, k_pool=None) -> np.ndarray:
         vis = pos <= m
         K, V, P = K[vis], V[vis], P[vis]
         if w.kind == "prefill" and lazy:
-            K = _bf16(rope(K.transpose(1, 0, 2), P, theta).transpose(1, 0, 2))  # one rotation by R_p, bf16
+            K = _bf16(rope(K.transpose(1, 0, 2), P, theta, freqs).transpose(1, 0, 2))  # one rotation by R_p, bf16
         for h in range(w.num_q_heads):
             kh = K[:, h // g]
             # every kernel folds scale * log2(e) into q' before the bf16 rounding
             if w.kind == "decode" and lazy:
                 # q re-rotated by R_{m-p} per document
-                qd = {pp: _bf16(rope(q[r, h], m - pp, theta) * scale) for pp in np.unique(P)}
+                qd = {pp: _bf16(rope(q[r, h], m - pp, theta, freqs) * scale) for pp in np.unique(P)}
                 sc = np.array([qd[P[j]] @ kh[j] for j in range(len(P))])
             else:
-                sc = kh @ _bf16(rope(q[r, h], m, theta) * scale)
+                sc = kh @ _bf16(rope(q[r, h], m, theta, freqs) * scale)
             e = _bf16(np.exp2(sc - sc.max()))
             out[oi, h] = (e[:, None] * V[:, h // g]).sum(0) / e.sum()
     return _bf16(out)

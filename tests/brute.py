@@ -28,10 +28,11 @@ def from_complex(z: np.ndarray) -> np.ndarray:
     return np.concatenate([z.real, z.imag], axis=-1)
 
 
-def rope(x: np.ndarray, n, theta: float) -> np.ndarray:
-    """R_n x for x [..., d]; n broadcasts against x's leading dims."""
+def rope(x: np.ndarray, n, theta: float, freqs=None) -> np.ndarray:
+    """R_n x for x [..., d]; n broadcasts against x's leading dims. ``freqs`` replaces
+    theta^(-2i/d)."""
     d = x.shape[-1]
-    ang = np.asarray(n, dtype=np.float64)[..., None] * _omega(d, theta)
+    ang = np.asarray(n, dtype=np.float64)[..., None] * (_omega(d, theta) if freqs is None else np.asarray(freqs))
     return from_complex(to_complex(x) * np.exp(1j * ang))
 
 

@@ -1,0 +1,97 @@
+"""GPU parity for the positional variants that need no kernel of their own:
+Llama-3.1 frequency scaling (a rotation table built from the scaled frequencies)
+and the interleaved (GPT-J) pairing (q and stored K permuted along the head
+dimension), on the per-sequence decode, the shared-run decode and the prefill,
+against the oracle's explicit-frequency / interleaved rotation."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bf16_model import emulate
+from gpu_util import assert_close, decode, decode_shared, la, prefill, shared_plan, to_device
+from paged_kv_cache_57_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+# A short original context so that all three wavelength bands fall inside these workloads' positions.
+SCALING = dict(factor=8.0, low_freq_factor=1.0, high_freq_factor=4.0, original_max_position=256)
+
+
+@pytest.fixture(autouse=True)
+def _clean_status():
+    la().device_status(clear=True)
+    yield
+    assert la().device_status(clear=True) == 0, "device status word set"
+
+
+def _freqs(w):
+    return oracle.llama3_freqs(w.head_dim, w.rope_theta, SCALING["factor"], SCALING["low_freq_factor"],
+                               SCALING["high_freq_factor"], SCALING["original_max_position"])
+
+
+def _scaled_device(w):
+    L = la()
+    dv = to_device(w)
+    dv.rope = L.rope_table_init(dv.p, scaling=L.RopeScaling(**SCALING))
+    return dv
+
+
+def _interleaved_device(w):
+    perm = la().interleave_perm(w.head_dim)
+    wp = dataclasses.replace(w, q=w.q[..., perm].contiguous(), k_pool=w.k_pool[..., perm].contiguous())
+    return wp, to_device(wp)
+
+
+def test_decode_f32_scaled_frequencies():
+    w = W.decode_zipf("vs32", batch=4, hq=8, hkv=2, d=64, docs_per_seq=4, doc_tokens=300, pool_docs=6, zipf_s=1.0,
+                      suffix_tokens=9, dtype="f32", theta=1e4, seed=301)
+    f = _freqs(w)
+    ref = oracle.attention(w, freqs=f)
+    assert np.abs(ref - oracle.attention(w)).max() > 1e-3  # the scaling changes the result at these positions
+    assert_close(decode(_scaled_device(w)), ref, "f32", "f32 decode, scaled frequencies")
+
+
+def test_shared_decode_bf16_scaled_frequencies():
+    w = W.decode_zipf("vsb", batch=8, hq=32, hkv=8, d=128, docs_per_seq=3, doc_tokens=260, pool_docs=4, zipf_s=1.0,
+                      suffix_tokens=20, seed=302)
+    f = _freqs(w)
+    dv = _scaled_device(w)
+    ref = oracle.attention(w, freqs=f)
+    emu = lambda r: emulate(w, r, freqs=f)
+    assert_close(decode_shared(dv, shared_plan(dv)), ref, "bf16", "shared decode, scaled", emulate=emu)
+    assert_close(decode(dv), ref, "bf16", "per-sequence decode, scaled", emulate=emu)
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (6, 2)])  # even GQA ratio: stream-K kernel; odd: one-tile kernel
+def test_prefill_scaled_frequencies(hq, hkv):
+    w = W.prefill_zipf("psc", batch=2, hq=hq, hkv=hkv, docs_per_seq=3, doc_tokens=300, pool_docs=4, zipf_s=1.2,
+                       chunk_tokens=[150, 70], seed=303)
+    f = _freqs(w)
+    ref = oracle.attention(w, freqs=f)
+    assert_close(prefill(_scaled_device(w)), ref, "bf16", "prefill, scaled",
+                 emulate=lambda r: emulate(w, r, freqs=f))
+
+
+def test_decode_interleaved_pairing():
+    w = W.decode_zipf("vi32", batch=4, hq=8, hkv=2, d=64, docs_per_seq=3, doc_tokens=200, pool_docs=5, zipf_s=1.0,
+                      suffix_tokens=7, dtype="f32", theta=1e4, seed=304)
+    ref = oracle.attention(w, interleaved=True)
+    _, dv = _interleaved_device(w)
+    assert_close(decode(dv), ref, "f32", "f32 decode, interleaved pairing")
+
+
+def test_shared_decode_and_prefill_interleaved_pairing():
+    w = W.decode_zipf("vib", batch=6, hq=16, hkv=4, d=128, docs_per_seq=3, doc_tokens=180, pool_docs=3, zipf_s=1.0,
+                      suffix_tokens=12, seed=305)
+    ref = oracle.attention(w, interleaved=True)
+    wp, dv = _interleaved_device(w)
+    assert_close(decode_shared(dv, shared_plan(dv)), ref, "bf16", "shared decode, interleaved",
+                 emulate=lambda r: emulate(wp, r))
+    wpf = W.prefill_zipf("pint", batch=2, hq=8, hkv=2, docs_per_seq=2, doc_tokens=200, pool_docs=3, zipf_s=1.0,
+                         chunk_tokens=[130, 40], seed=306)
+    ref = oracle.attention(wpf, interleaved=True)
+    wpp, dvp = _interleaved_device(wpf)
+    assert_close(prefill(dvp), ref, "bf16", "prefill, interleaved", emulate=lambda r: emulate(wpp, r))
