@@ -604,6 +604,18 @@ def measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust):
                         "decode_kv_gbs_unique": b5["unique"] / statistics.median(td) / 1e9,
                         "prefill_tflops": f5 / statistics.median(tp) / 1e12,
                         "decode_tokens": int(wd.tokens_per_seq().sum()), "prefill_gflop": f5 / 1e9}
+    # Cache-policy replay (host C++ in the same library): block hit rate of the
+    # position-agnostic, position-aware and prefix policies on a RAG-shaped Zipf trace,
+    # under 1 GiB of Llama-3.1-8B KV (512 blocks) and with an unbounded pool.
+    from paged_kv_cache_57_gb300 import cache as CM
+    cp = {"trace": "3000 requests x 5 of 500 docs (128-512 tokens), 64-token prompt, 4 in flight"}
+    for s in (0.8, 1.2):
+        reqs, pos0 = W.cache_trace(num_requests=3000, pool_docs=500, docs_per_request=5, zipf_s=s,
+                                   doc_tokens=(128, 512), prompt_tokens=64, seed=23)
+        for budget, tag in ((512, "1gib"), (1 << 30, "unbounded")):
+            cp[f"zipf{s}_{tag}"] = {p: round(CM.simulate(p, budget, reqs, pos0, concurrency=4)["hit_rate"], 4)
+                                    for p in ("agnostic", "aware", "prefix")}
+    out["cache_policies"] = cp
     return out
 
 

@@ -44,7 +44,7 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     os.makedirs(OBJ_DIR, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     deps = srcs + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + \
-        [os.path.join(ROOT, "include", "lazy_attn.h"), os.path.abspath(__file__)]
+        glob.glob(os.path.join(ROOT, "include", "*.h")) + [os.path.abspath(__file__)]
     newest = max(os.path.getmtime(p) for p in deps)
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= newest:
         return LIB

@@ -315,6 +315,25 @@ def mixed_mqa(*, n_decode: int = 48, n_prefill: int = 4, chunk: int = 512, hq: i
     return wd, wp
 
 
+def cache_trace(*, num_requests: int, pool_docs: int, docs_per_request: int, zipf_s: float,
+                doc_tokens: Tuple[int, int] = (256, 1024), prompt_tokens: int = 0,
+                seed: int = 20260007) -> Tuple[List[List[Tuple[int, int]]], List[int]]:
+    """Request trace for the cache-policy simulator, RAG-shaped: every request
+    retrieves ``docs_per_request`` distinct documents drawn by finite Zipf(s) over
+    ``pool_docs`` (placed in draw order, i.e. retrieval rank), each at its own
+    fixed length drawn once uniformly in ``doc_tokens`` (inclusive), after a
+    shared prompt of ``prompt_tokens`` tokens. Returns (requests as lists of
+    (doc, len) segments, pos0 of each request)."""
+    rng = np.random.Generator(np.random.PCG64([seed, 7]))
+    p = finite_zipf_probs(pool_docs, zipf_s)
+    lens = rng.integers(doc_tokens[0], doc_tokens[1] + 1, size=pool_docs)
+    reqs = []
+    for _ in range(num_requests):
+        docs = rng.choice(pool_docs, size=docs_per_request, replace=False, p=p)
+        reqs.append([(int(d), int(lens[d])) for d in docs])
+    return reqs, [int(prompt_tokens)] * num_requests
+
+
 # Full-size workloads, by name. Each is a zero-argument constructor.
 FULL = {
     "tiny_fp32": lambda: tiny_fp32(),
