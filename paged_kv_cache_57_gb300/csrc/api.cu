@@ -394,7 +394,8 @@ int lazy_attn_plan_shared_host(const lazy_attn_params* p, int32_t num_docs, cons
     return LAZY_ERR_INVALID_ARG;
   if (c.G > 64) return LAZY_ERR_UNSUPPORTED;
   const int cb = chunk_blocks > 0 ? chunk_blocks : 32;
-  return lazy::plan_shared_host(p->num_seqs, c.G, p->max_blocks_per_seq, p->num_pool_blocks, num_docs, seg_indptr,
+  return lazy::plan_shared_host(p->num_seqs, c.G, lazy::shared_rows_cap(c.G, p->head_dim), p->max_blocks_per_seq,
+                                p->num_pool_blocks, num_docs, seg_indptr,
                                 seg_doc, seg_len, doc_block_indptr, doc_blocks, cb, capacity, items, slot_indptr,
                                 counts);
 }
@@ -458,10 +459,17 @@ int lazy_attn_decode_shared(const lazy_attn_params* p, const void* q, const void
   if (num_items > 0) {
     CUtensorMap kmap, vmap;
     const uint64_t rows = (uint64_t)p->num_pool_blocks * p->num_kv_heads * lazy::kBlock;
-    if (!encode_block_map(&kmap, k_pool, rows, p->head_dim, lazy::kBlock) ||
-        !encode_block_map(&vmap, v_pool, rows, p->head_dim, lazy::kBlock))
-      return LAZY_ERR_CUDA;
-    rc = launched(lazy::launch_decode_shared(a, p->lazy != 0, kmap, vmap, cs));
+    if (lazy::shared_rows_cap(c.G, p->head_dim) == 128) {  // tensor-core kernel: 16-row x 64-column boxes
+      if (!encode_rows_map(&kmap, k_pool, rows, p->head_dim, lazy::kBlock) ||
+          !encode_rows_map(&vmap, v_pool, rows, p->head_dim, lazy::kBlock))
+        return LAZY_ERR_CUDA;
+      rc = launched(lazy::launch_decode_shared_tc(a, p->lazy != 0, kmap, vmap, cs));
+    } else {
+      if (!encode_block_map(&kmap, k_pool, rows, p->head_dim, lazy::kBlock) ||
+          !encode_block_map(&vmap, v_pool, rows, p->head_dim, lazy::kBlock))
+        return LAZY_ERR_CUDA;
+      rc = launched(lazy::launch_decode_shared(a, p->lazy != 0, kmap, vmap, cs));
+    }
     if (rc != LAZY_OK) return rc;
   }
   return launched(lazy::launch_shared_combine(a, cs));

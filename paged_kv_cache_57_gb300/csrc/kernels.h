@@ -120,8 +120,14 @@ struct MaterializeArgs {
 };
 cudaError_t launch_materialize(const MaterializeArgs& a, cudaStream_t st);
 
+// Query rows per shared-run work item: 128 where the tensor-core kernel
+// (decode_shared_tc.cu) serves the call -- at least 16 query heads per KV head and
+// D = 128 -- else 64 (decode_shared.cu). The planner and the decode call both
+// follow it.
+inline int shared_rows_cap(int G, int D) { return (G >= 16 && D == 128) ? 128 : 64; }
+
 // Host planner of the shared-run decode (shared_plan.cu). counts = {items, slots}.
-int plan_shared_host(int B, int G, int max_blocks, int num_pool_blocks, int num_docs, const int32_t* seg_indptr,
+int plan_shared_host(int B, int G, int rows_cap, int max_blocks, int num_pool_blocks, int num_docs, const int32_t* seg_indptr,
                      const int32_t* seg_doc, const int32_t* seg_len, const int32_t* doc_block_indptr,
                      const int32_t* doc_blocks, int chunk_blocks, int capacity, int32_t* items, int32_t* slot_indptr,
                      int32_t* counts);
@@ -157,6 +163,8 @@ cudaError_t launch_prefill_tq(const PrefillArgs& a, bool lazy, const CUtensorMap
 
 cudaError_t launch_decode_shared(const SharedDecodeArgs& a, bool lazy, const CUtensorMap& kmap,
                                  const CUtensorMap& vmap, cudaStream_t st);
+cudaError_t launch_decode_shared_tc(const SharedDecodeArgs& a, bool lazy, const CUtensorMap& kmap,
+                                    const CUtensorMap& vmap, cudaStream_t st);
 cudaError_t launch_shared_combine(const SharedDecodeArgs& a, cudaStream_t st);
 
 // Shared-memory bytes a bf16 decode CTA needs (for occupancy-based split planning).

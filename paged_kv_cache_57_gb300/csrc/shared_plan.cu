@@ -5,8 +5,9 @@
 // identical physical blocks, whatever their offsets ("Metodologia: Codificação
 // Posicional Diferida": the stored keys carry no global position, which is what
 // makes them shareable), so they form one group. A group is split into sets of
-// at most LAZY_PLAN_MAX_MEMBERS members and at most 64 query rows (members x
-// query heads per KV head), i.e. RT = 1, 2 or 4 tiles of 16 rows. A set's blocks
+// at most LAZY_PLAN_MAX_MEMBERS members and at most rows_cap query rows (members x
+// query heads per KV head): 64 (RT = 1, 2 or 4 tiles of 16 rows for the mma.sync
+// kernel) or 128 (one tensor-core tile). A set's blocks
 // are cut into chunks of chunk_blocks logical blocks; each (set, chunk) is one
 // item, and every member of the set owns one partial-result slot per chunk. The
 // slots of sequence s are slot_indptr[s] .. slot_indptr[s+1]-1. An item also
@@ -27,7 +28,7 @@
 
 namespace lazy {
 
-int plan_shared_host(int B, int G, int max_blocks, int num_pool_blocks, int num_docs, const int32_t* seg_indptr,
+int plan_shared_host(int B, int G, int rows_cap, int max_blocks, int num_pool_blocks, int num_docs, const int32_t* seg_indptr,
                      const int32_t* seg_doc, const int32_t* seg_len, const int32_t* doc_block_indptr,
                      const int32_t* doc_blocks, int chunk_blocks, int capacity, int32_t* items, int32_t* slot_indptr,
                      int32_t* counts) {
@@ -70,7 +71,7 @@ int plan_shared_host(int B, int G, int max_blocks, int num_pool_blocks, int num_
     }
   }
   // ---- member sets, their chunk length, and the slots each member needs
-  const int per_set = std::max(1, std::min(LAZY_PLAN_MAX_MEMBERS, 64 / G));
+  const int per_set = std::max(1, std::min(LAZY_PLAN_MAX_MEMBERS, rows_cap / G));
   struct Set {
     int group, first, n, rt, cb;
   };

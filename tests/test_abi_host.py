@@ -185,6 +185,9 @@ def _shared_workloads():
     d, _ = W.mixed_mqa(n_decode=6, n_prefill=1, chunk=40, hq=8, hkv=1, d=64, pool_docs=30, ctx_lo=50,
                        ctx_hi=3000, doc_lo=5, doc_hi=300, seed=17)
     yield d
+    # G = 32, d = 128: the tensor-core kernel's items, up to 4 members (128 rows)
+    yield W.decode_zipf("sdw", batch=12, hq=32, hkv=1, d=128, docs_per_seq=3, doc_tokens=100, pool_docs=2,
+                        zipf_s=1.0, seed=19)
 
 
 @pytest.mark.parametrize("chunk", [0, 1, 3, 32])
@@ -196,6 +199,7 @@ def test_shared_plan_covers_every_block_once(la, w, chunk):
     items, slot_indptr = la.plan_shared_host(p, len(w.doc_len), w.seg_indptr, w.seg_doc, w.seg_len,
                                              w.doc_block_indptr, w.doc_blocks, chunk_blocks=chunk)
     G = w.num_q_heads // w.num_kv_heads
+    rows_cap = 128 if G >= 16 and w.head_dim == 128 else 64  # one tcgen05 tile, or 4 mma.sync row tiles
     exp = {s: expected_blocks(w, s) for s in range(w.num_seqs)}
     cover = {s: np.zeros(len(exp[s]), np.int64) for s in range(w.num_seqs)}
     slots_seen = set()
@@ -204,7 +208,7 @@ def test_shared_plan_covers_every_block_once(la, w, chunk):
         src, b0, nb, last, nm = (int(x) for x in it[:5])
         ids = it[8 + 4 * la.PLAN_MAX_MEMBERS:]
         assert (it[5:8] == 0).all() and (it[8 + 4 * nm: 8 + 4 * la.PLAN_MAX_MEMBERS] == 0).all()
-        assert 1 <= nm <= la.PLAN_MAX_MEMBERS and nm * G <= 64
+        assert 1 <= nm <= la.PLAN_MAX_MEMBERS and nm * G <= rows_cap
         cost.append(nb)
         assert nb <= (chunk or 32)
         src_phys = [exp[src][b][0] for b in range(b0, b0 + nb)]
@@ -221,6 +225,8 @@ def test_shared_plan_covers_every_block_once(la, w, chunk):
             slots_seen.add(slot)
             cover[seq][bm:bm + nb] += 1
     assert (np.diff(cost) <= 0).all()  # longest items first
+    if w.name == "sdw":  # a document shared by more than two sequences fills a 128-row tile
+        assert items[:, 4].max() * G == 128
     assert len(slots_seen) == slot_indptr[-1]
     for s in range(w.num_seqs):
         assert (cover[s] == 1).all(), s

@@ -48,6 +48,24 @@ def test_shared_decode_chunk_sweep(chunk):
     _check(w, chunk=chunk)
 
 
+@pytest.mark.parametrize("chunk", [1, 5, 40])
+@pytest.mark.parametrize("hq", [16, 32, 64])
+def test_shared_decode_tensor_core_path(hq, chunk):
+    # hq query heads on one KV head, d = 128: the tcgen05 kernel, items of up to 128 rows.
+    # 700-token documents end in a partial block; at chunk 40 an item runs past the 32
+    # block ids its record names.
+    w = W.decode_zipf(f"stc{hq}c{chunk}", batch=10, hq=hq, hkv=1, d=128, docs_per_seq=3, doc_tokens=700,
+                      pool_docs=3, zipf_s=0.8, suffix_tokens=23, seed=190 + hq + chunk)
+    dv = to_device(w)
+    plan = shared_plan(dv, chunk)
+    assert plan.items_host[:, 4].max() * hq == 128  # full tensor-core tiles occur
+    _check(w, chunk=chunk)
+
+
+# (query heads, KV heads): the mma.sync kernel (4 per KV head) and the tensor-core one (32)
+EDGE_SHAPES = [(8, 2), (32, 1)]
+
+
 def test_shared_decode_many_members_per_document():
     # 40 sequences all citing one document (repeatedly): groups are split into items of 16 members
     w = W.decode_zipf("smany", batch=40, hq=8, hkv=2, d=128, docs_per_seq=3, doc_tokens=50, pool_docs=1,
@@ -72,8 +90,9 @@ def test_shared_decode_few_keys():
     _check(w)
 
 
-def test_shared_decode_empty_and_one_key_sequences():
-    w = W.decode_zipf("sone", batch=3, hq=8, hkv=2, d=128, docs_per_seq=1, doc_tokens=1, pool_docs=3,
+@pytest.mark.parametrize("hq,hkv", EDGE_SHAPES)
+def test_shared_decode_empty_and_one_key_sequences(hq, hkv):
+    w = W.decode_zipf("sone", batch=3, hq=hq, hkv=hkv, d=128, docs_per_seq=1, doc_tokens=1, pool_docs=3,
                       zipf_s=1.0, seed=64)
     w.seg_indptr = np.array([0, 1, 1, 2], np.int32)  # sequence 1 is empty
     w.seg_doc, w.seg_len = w.seg_doc[:2].copy(), w.seg_len[:2].copy()
@@ -84,8 +103,8 @@ def test_shared_decode_empty_and_one_key_sequences():
     assert (out[1] == 0).all()
     for s, k in ((0, 0), (2, 1)):
         phys = int(w.doc_blocks[w.doc_block_indptr[w.seg_doc[k]]])
-        for h in range(8):
-            assert torch.equal(out[s, h], w.v_pool[phys, h // 4, 0])  # one key: output is v, exactly
+        for h in range(hq):
+            assert torch.equal(out[s, h], w.v_pool[phys, h // (hq // hkv), 0])  # one key: output is v, exactly
 
 
 def test_shared_decode_agrees_with_per_sequence_decode():
@@ -98,8 +117,9 @@ def test_shared_decode_agrees_with_per_sequence_decode():
     assert np.mean(np.abs(a - b) <= 1e-2 * np.abs(a) + 1e-3) > 0.99
 
 
-def test_shared_decode_shift_invariance_is_bitwise():
-    kw = dict(batch=6, hq=32, hkv=8, d=128, docs_per_seq=3, doc_tokens=64, pool_docs=3, zipf_s=1.0,
+@pytest.mark.parametrize("hkv", [8, 1])
+def test_shared_decode_shift_invariance_is_bitwise(hkv):
+    kw = dict(batch=6, hq=32, hkv=hkv, d=128, docs_per_seq=3, doc_tokens=64, pool_docs=3, zipf_s=1.0,
               suffix_tokens=7, seed=166)
     da = to_device(W.decode_zipf("ss0", **kw))
     a = decode_shared(da, shared_plan(da)).cpu()
@@ -109,8 +129,9 @@ def test_shared_decode_shift_invariance_is_bitwise():
         assert torch.equal(a.view(torch.int16), b.view(torch.int16)), c
 
 
-def test_shared_decode_lazy0_control_on_materialised_pool():
-    w = W.decode_zipf("sctl", batch=4, hq=16, hkv=4, d=128, docs_per_seq=3, doc_tokens=48, pool_docs=4,
+@pytest.mark.parametrize("hq,hkv", [(16, 4), (32, 1)])
+def test_shared_decode_lazy0_control_on_materialised_pool(hq, hkv):
+    w = W.decode_zipf("sctl", batch=4, hq=hq, hkv=hkv, d=128, docs_per_seq=3, doc_tokens=48, pool_docs=4,
                       zipf_s=1.0, suffix_tokens=8, share=False, seed=66)
     kabs = w.k_pool.double().clone()
     for s in range(w.num_seqs):
@@ -123,9 +144,10 @@ def test_shared_decode_lazy0_control_on_materialised_pool():
     assert_close(decode_shared(dv, shared_plan(dv)), oracle.attention(w), "bf16", "shared lazy=0 control")
 
 
-def test_shared_decode_flags_inconsistent_plan():
+@pytest.mark.parametrize("hq,hkv", EDGE_SHAPES)
+def test_shared_decode_flags_inconsistent_plan(hq, hkv):
     L = la()
-    w = W.decode_zipf("sbadplan", batch=4, hq=8, hkv=2, d=128, docs_per_seq=2, doc_tokens=40, pool_docs=3,
+    w = W.decode_zipf("sbadplan", batch=4, hq=hq, hkv=hkv, d=128, docs_per_seq=2, doc_tokens=40, pool_docs=3,
                       zipf_s=1.0, seed=167)
     dv = to_device(w)
     plan = shared_plan(dv)
@@ -138,11 +160,12 @@ def test_shared_decode_flags_inconsistent_plan():
     assert torch.isfinite(out.float()).all()
 
 
-def test_shared_decode_flags_record_block_id_mismatch():
+@pytest.mark.parametrize("hq,hkv", EDGE_SHAPES)
+def test_shared_decode_flags_record_block_id_mismatch(hq, hkv):
     """A record whose block id disagrees with the block word (inside the pool, or past
     its end) is flagged; the kernel loads nothing outside the pool."""
     L = la()
-    w = W.decode_zipf("sbadid", batch=4, hq=8, hkv=2, d=128, docs_per_seq=2, doc_tokens=40, pool_docs=3,
+    w = W.decode_zipf("sbadid", batch=4, hq=hq, hkv=hkv, d=128, docs_per_seq=2, doc_tokens=40, pool_docs=3,
                       zipf_s=1.0, seed=168)
     dv = to_device(w)
     plan = shared_plan(dv)
