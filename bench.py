@@ -42,7 +42,7 @@ WORKLOAD = "llama8b_decode"
 NCU_TRAFFIC = {"sources": ["paged_kv_cache_57_gb300/csrc/decode_shared.cu",
                            "paged_kv_cache_57_gb300/csrc/decode_block.cuh",
                            "paged_kv_cache_57_gb300/csrc/common.cuh"],
-               "sha16": "e198b2d4a451028a", "bytes_per_launch": 302095104 + 10525184}
+               "sha16": "9f69530f95703670", "bytes_per_launch": 302118912 + 9891584}
 
 
 def _traffic_if_current():
@@ -323,7 +323,8 @@ def main():
                     help="decode entry point timed by --workload (shared-run or per-sequence)")
     ap.add_argument("--workload", default=None, choices=sorted(["llama8b_decode", "llama8b_decode_noshare",
                                                                 "llama8b_prefill", "llama70b_decode",
-                                                                "llama70b_decode_noshare"]),
+                                                                "llama70b_decode_noshare", "mixed_mqa_decode",
+                                                                "mixed_mqa_prefill"]),
                     help="time one workload alone and print its own line (used for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

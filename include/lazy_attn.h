@@ -215,9 +215,14 @@ int lazy_attn_decode(const lazy_attn_params *p, const void *q, const void *k_poo
  * Plan (host): lazy_attn_plan_shared_host takes the document lists of the
  * block-word packer (same arguments, host memory). Occurrences of one document
  * with the same used length read the same physical blocks; they are grouped,
- * split into sets of at most LAZY_PLAN_MAX_MEMBERS members and 64 query rows
- * (members x query heads per KV head), and each set's blocks are cut into chunks
- * of chunk_blocks logical blocks (0 selects 32). It writes
+ * split into sets of at most LAZY_PLAN_MAX_MEMBERS members and at most R query
+ * rows (members x query heads per KV head), and each set's blocks are cut into
+ * chunks of chunk_blocks logical blocks. R is 128 when a KV head serves at least
+ * 16 query heads and head_dim is 128 (the decode then runs on the 5th-generation
+ * tensor cores, one 128-row tile per item), else 64. chunk_blocks 0 selects 32,
+ * or, for R = 128, about one item per resident CTA (2 x 152 / num_kv_heads items):
+ * the sets' blocks summed, divided by that count, rounded up to a multiple of 4
+ * and kept within 32 .. 256. It writes
  *   items_host [num_items][LAZY_PLAN_ITEM_INTS] int32, one work item each:
  *     [0] src_seq, [1] b0, [2] nblk, [3] last_valid, [4] nmem, [5..7] 0: nblk
  *         logical blocks of sequence src_seq from block b0, all full but the

@@ -393,11 +393,14 @@ int lazy_attn_plan_shared_host(const lazy_attn_params* p, int32_t num_docs, cons
       (!seg_doc || !seg_len || !doc_block_indptr || !doc_blocks || !items))
     return LAZY_ERR_INVALID_ARG;
   if (c.G > 64) return LAZY_ERR_UNSUPPORTED;
-  const int cb = chunk_blocks > 0 ? chunk_blocks : 32;
-  return lazy::plan_shared_host(p->num_seqs, c.G, lazy::shared_rows_cap(c.G, p->head_dim), p->max_blocks_per_seq,
-                                p->num_pool_blocks, num_docs, seg_indptr,
-                                seg_doc, seg_len, doc_block_indptr, doc_blocks, cb, capacity, items, slot_indptr,
-                                counts);
+  const int cap = lazy::shared_rows_cap(c.G, p->head_dim);
+  // 0: 32 blocks for the mma.sync kernel; for the tensor-core kernel, a length that
+  // gives about one item per resident CTA.
+  const int cb = chunk_blocks > 0 ? chunk_blocks : (cap == 128 ? 0 : 32);
+  const int auto_items = std::max(1, lazy::kSharedTcSlots / std::max(1, p->num_kv_heads));
+  return lazy::plan_shared_host(p->num_seqs, c.G, cap, p->max_blocks_per_seq, p->num_pool_blocks, num_docs,
+                                seg_indptr, seg_doc, seg_len, doc_block_indptr, doc_blocks, cb, auto_items, capacity,
+                                items, slot_indptr, counts);
 }
 
 size_t lazy_attn_decode_shared_workspace_bytes(const lazy_attn_params* p, int32_t num_slots) {

@@ -125,12 +125,18 @@ cudaError_t launch_materialize(const MaterializeArgs& a, cudaStream_t st);
 // D = 128 -- else 64 (decode_shared.cu). The planner and the decode call both
 // follow it.
 inline int shared_rows_cap(int G, int D) { return (G >= 16 && D == 128) ? 128 : 64; }
+// Resident CTAs of the tensor-core kernel on a GB300 (2 per SM x 152 SMs): its
+// automatic chunk length aims at about this many CTAs, so that each CTA's fixed
+// cost (record, query rotation, partials) is paid as few times as the machine allows.
+constexpr int kSharedTcSlots = 2 * 152;
 
 // Host planner of the shared-run decode (shared_plan.cu). counts = {items, slots}.
+// chunk_blocks <= 0 picks the chunk from the batch: about auto_items items in all,
+// 32 to 256 blocks in multiples of 4.
 int plan_shared_host(int B, int G, int rows_cap, int max_blocks, int num_pool_blocks, int num_docs, const int32_t* seg_indptr,
                      const int32_t* seg_doc, const int32_t* seg_len, const int32_t* doc_block_indptr,
-                     const int32_t* doc_blocks, int chunk_blocks, int capacity, int32_t* items, int32_t* slot_indptr,
-                     int32_t* counts);
+                     const int32_t* doc_blocks, int chunk_blocks, int auto_items, int capacity, int32_t* items,
+                     int32_t* slot_indptr, int32_t* counts);
 
 // Every launcher returns the cudaError_t of its launch.
 cudaError_t launch_rope_table(float2* table, int head_dim, double theta, const lazy_rope_scaling* scaling,

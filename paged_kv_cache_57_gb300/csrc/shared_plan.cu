@@ -30,8 +30,8 @@ namespace lazy {
 
 int plan_shared_host(int B, int G, int rows_cap, int max_blocks, int num_pool_blocks, int num_docs, const int32_t* seg_indptr,
                      const int32_t* seg_doc, const int32_t* seg_len, const int32_t* doc_block_indptr,
-                     const int32_t* doc_blocks, int chunk_blocks, int capacity, int32_t* items, int32_t* slot_indptr,
-                     int32_t* counts) {
+                     const int32_t* doc_blocks, int chunk_blocks, int auto_items, int capacity, int32_t* items,
+                     int32_t* slot_indptr, int32_t* counts) {
   struct Occ {
     int seq, b0;
   };
@@ -75,6 +75,14 @@ int plan_shared_host(int B, int G, int rows_cap, int max_blocks, int num_pool_bl
   struct Set {
     int group, first, n, rt, cb;
   };
+  int cb = chunk_blocks;
+  if (cb <= 0) {  // about auto_items items: 32 .. 256 blocks, a multiple of 4 (one key tile)
+    int64_t total = 0;
+    for (int gi = 0; gi < (int)groups.size(); ++gi)
+      total += (int64_t)((keys[gi].second + kBlk - 1) / kBlk) * ((groups[gi].size() + per_set - 1) / per_set);
+    const int64_t per = (total + std::max(1, auto_items) - 1) / std::max(1, auto_items);
+    cb = (int)std::min<int64_t>(256, std::max<int64_t>(32, (per + 3) / 4 * 4));
+  }
   std::vector<Set> sets;
   std::vector<int> nslots(B, 0);
   for (int gi = 0; gi < (int)groups.size(); ++gi) {
@@ -83,7 +91,6 @@ int plan_shared_host(int B, int G, int rows_cap, int max_blocks, int num_pool_bl
       const int n = std::min(per_set, (int)groups[gi].size() - j0);
       const int rows = n * G;
       const int rt = rows <= 16 ? 1 : (rows <= 32 ? 2 : 4);
-      const int cb = std::max(1, chunk_blocks);
       sets.push_back(Set{gi, j0, n, rt, cb});
       for (int j = 0; j < n; ++j) nslots[groups[gi][j0 + j].seq] += (nbk + cb - 1) / cb;
     }

@@ -353,6 +353,9 @@ FULL = {
     "llama70b_decode_noshare": lambda: decode_zipf("llama70b_decode_noshare", batch=32, hq=64, hkv=8,
                                                    docs_per_seq=16, doc_tokens=1024, pool_docs=512,
                                                    zipf_s=1.0, share=False, seed=20260004),
+    # the two halves of the mixed continuous batch (one shared pool), each on its own
+    "mixed_mqa_decode": lambda: mixed_mqa()[0],
+    "mixed_mqa_prefill": lambda: mixed_mqa()[1],
 }
 
 

@@ -210,7 +210,7 @@ def test_shared_plan_covers_every_block_once(la, w, chunk):
         assert (it[5:8] == 0).all() and (it[8 + 4 * nm: 8 + 4 * la.PLAN_MAX_MEMBERS] == 0).all()
         assert 1 <= nm <= la.PLAN_MAX_MEMBERS and nm * G <= rows_cap
         cost.append(nb)
-        assert nb <= (chunk or 32)
+        assert nb <= (chunk or (256 if rows_cap == 128 else 32))
         src_phys = [exp[src][b][0] for b in range(b0, b0 + nb)]
         nid = min(nb, la.PLAN_ITEM_BLOCK_IDS)  # the record names the item's first blocks
         assert list(ids[:nid]) == src_phys[:nid] and (ids[nid:] == 0).all()
@@ -232,6 +232,32 @@ def test_shared_plan_covers_every_block_once(la, w, chunk):
         assert (cover[s] == 1).all(), s
     # Loads are shared: no more source blocks than logical ones.
     assert items[:, 2].sum() <= sum(len(e) for e in exp.values())
+
+
+def test_shared_plan_automatic_chunk_for_the_tensor_core_kernel(la):
+    # 0 selects 32 blocks for the mma.sync kernel; for the tensor-core kernel (G >= 16,
+    # d = 128) about one item per resident CTA (2 x 152 over the KV heads): the sum of
+    # the member sets' blocks over that count, rounded up to 4, within 32 .. 256.
+    for hkv, docs in ((1, 6), (2, 40)):
+        w = W.decode_zipf("sauto", batch=24, hq=32 * hkv, hkv=hkv, d=128, docs_per_seq=docs, doc_tokens=1000,
+                          pool_docs=60, zipf_s=0.5, seed=20)
+        p = _params(la, w)
+        items, _ = la.plan_shared_host(p, len(w.doc_len), w.seg_indptr, w.seg_doc, w.seg_len,
+                                       w.doc_block_indptr, w.doc_blocks, chunk_blocks=0)
+        per_set = 128 // 32
+        groups = {}
+        for s_ in range(w.num_seqs):
+            for doc, ln in w.seq_segments(s_):
+                groups[(doc, ln)] = groups.get((doc, ln), 0) + 1
+        total = sum(-(-ln // 16) * -(-n // per_set) for (doc, ln), n in groups.items())
+        want = min(256, max(32, -(-(-(-total // (304 // hkv))) // 4) * 4))
+        assert items[:, 2].max() == min(want, 63)  # 1000-token documents have 63 blocks
+        assert want > 32 or hkv == 1
+    w = W.decode_zipf("sauto8", batch=8, hq=8, hkv=2, d=128, docs_per_seq=4, doc_tokens=2000, pool_docs=30,
+                      zipf_s=0.5, seed=21)
+    items, _ = la.plan_shared_host(_params(la, w), len(w.doc_len), w.seg_indptr, w.seg_doc, w.seg_len,
+                                   w.doc_block_indptr, w.doc_blocks, chunk_blocks=0)
+    assert items[:, 2].max() == 32  # mma.sync kernel: 32 blocks
 
 
 def test_shared_plan_rejects_bad_layouts(la):
