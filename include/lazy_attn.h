@@ -154,6 +154,28 @@ typedef struct {
 int lazy_attn_rope_table_init_scaled(const lazy_attn_params *p, const lazy_rope_scaling *scaling, void *table,
                                      size_t table_bytes, lazy_stream_t stream);
 
+/* Explicit frequencies: fills the same table from freqs_host[head_dim/2], the rate of
+ * pair f (dims f and f + head_dim/2) in radians per position, fp64 host memory read
+ * during the call. Each rate must be finite with 0 <= w <= 4 (RoPE's fastest rate is
+ * 1), else LAZY_ERR_INVALID_ARG. A rate of 0 leaves its pair unrotated, which gives
+ * partial rotary (GPT-NeoX / GPT-J rotary_dim: only the first r dims rotate, pairs
+ * (f, f + r/2) or (2f, 2f+1) at rates theta^(-2f/r)): permute the head dimension of q
+ * and of the stored K rows so that the rotary pairs become pairs (f, f + head_dim/2),
+ * f < r/2, and the other dims fill the remaining pairs; pass theta^(-2f/r) for f < r/2
+ * and 0 beyond. V and out keep their order. Other frequency rules (NTK-aware or YaRN
+ * interpolation, whose temperature is sm_scale) are rate vectors too. */
+int lazy_attn_rope_table_init_freqs(const lazy_attn_params *p, const double *freqs_host, void *table,
+                                    size_t table_bytes, lazy_stream_t stream);
+
+/* Host helper for the layout above: for a head of head_dim dims whose first rot_dims
+ * rotate (rot_dims even, 2 <= rot_dims <= head_dim; rot_dims = head_dim is full
+ * rotary) with rotate-half pairs (f, f + rot_dims/2), or interleaved pairs (2f, 2f+1)
+ * when `interleaved`, writes perm_out[head_dim] (new dim i holds old dim perm_out[i])
+ * and freqs_out[head_dim/2] (theta^(-2f/rot_dims) for f < rot_dims/2, then 0).
+ * Returns LAZY_ERR_INVALID_ARG on bad sizes. */
+int lazy_attn_rotary_layout_host(int32_t head_dim, int32_t rot_dims, int32_t interleaved, double theta,
+                                 int32_t *perm_out, double *freqs_out);
+
 /* ---------------------------------------------------------------- block-word packer
  * Builds block_words and seq_lens from per-sequence document lists (CSR):
  *   seg_indptr [B+1]; segment k of sequence s (seg_indptr[s] <= k < seg_indptr[s+1])

@@ -52,6 +52,8 @@ def lib():
             L.lo_rope_rotate.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double, _f64p, _f64p]
             L.lo_rope_rotate_ex.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_void_p, ctypes.c_int,
                                             ctypes.c_double, _f64p, _f64p]
+            L.lo_rope_rotate_partial.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_void_p,
+                                                 ctypes.c_int, ctypes.c_double, _f64p, _f64p]
             L.lo_llama3_freqs.argtypes = [ctypes.c_int] + [ctypes.c_double] * 5 + [_f64p]
             L.lo_softmax_dot.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, _f64p, _f64p, _f64p]
             L.lo_tiled_softmax_dot.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, _f64p, _f64p,
@@ -70,6 +72,12 @@ def lib():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_void_p,
                 ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, _i32p, _i32p,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p, _f64p]
+            L.lo_attention_partial.restype = ctypes.c_int
+            L.lo_attention_partial.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, _i32p,
+                _i32p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p,
+                _f64p]
             _lib = L
     return _lib
 
@@ -90,14 +98,15 @@ def rope_rotate(x: np.ndarray, n: float, theta: float) -> np.ndarray:
 
 
 def rope_rotate_ex(x: np.ndarray, n: float, theta: float, freqs: Optional[np.ndarray] = None,
-                   interleaved: bool = False) -> np.ndarray:
-    """R_n x with explicit frequencies (None: theta^(-2i/d)) and rotate-half or
-    interleaved (2i, 2i+1) pairing."""
+                   interleaved: bool = False, rot_dims: Optional[int] = None) -> np.ndarray:
+    """R_n x with explicit frequencies (None: theta^(-2i/r)) and rotate-half or
+    interleaved (2i, 2i+1) pairing, on the first ``rot_dims`` dims (None: all)."""
     x = np.ascontiguousarray(x, dtype=np.float64)
     y = np.empty_like(x)
     f = None if freqs is None else np.ascontiguousarray(freqs, dtype=np.float64)
-    lib().lo_rope_rotate_ex(x.shape[-1], float(theta), None if f is None else f.ctypes.data, int(interleaved),
-                            float(n), x, y)
+    d = x.shape[-1]
+    lib().lo_rope_rotate_partial(d, int(rot_dims or d), float(theta), None if f is None else f.ctypes.data,
+                                 int(interleaved), float(n), x, y)
     return y
 
 
@@ -151,10 +160,12 @@ def query_rows(w):
 
 
 def attention(w, rows: Optional[Sequence[int]] = None, sm_scale: float = 0.0,
-              k_pool=None, v_pool=None, freqs: Optional[np.ndarray] = None, interleaved: bool = False) -> np.ndarray:
+              k_pool=None, v_pool=None, freqs: Optional[np.ndarray] = None, interleaved: bool = False,
+              rot_dims: Optional[int] = None) -> np.ndarray:
     """fp64 reference output of workload ``w`` for the query rows ``rows`` (all by
     default): decode rows are sequences, prefill rows are chunk tokens. ``freqs``
-    replaces theta^(-2i/d); ``interleaved`` pairs dimensions (2i, 2i+1).
+    replaces theta^(-2i/r); ``interleaved`` pairs dimensions (2i, 2i+1);
+    ``rot_dims`` rotates only the first r dims (partial rotary; None: all).
     Returns [len(rows), Hq, d]."""
     q_seq, q_m = query_rows(w)
     q = w.q
@@ -168,7 +179,8 @@ def attention(w, rows: Optional[Sequence[int]] = None, sm_scale: float = 0.0,
     nq = qb.shape[0]
     out = np.zeros((nq, w.num_q_heads, w.head_dim), np.float64)
     f = None if freqs is None else np.ascontiguousarray(freqs, dtype=np.float64)
-    rc = lib().lo_attention_ex(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, float(w.rope_theta),
+    rc = lib().lo_attention_partial(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                            int(rot_dims or w.head_dim), float(w.rope_theta),
                             None if f is None else f.ctypes.data, int(interleaved),
                             float(sm_scale), dt, nq, qb.ctypes.data, np.ascontiguousarray(q_seq, np.int32),
                             np.ascontiguousarray(q_m, np.int32), kb.ctypes.data, vb.ctypes.data,

@@ -11,7 +11,8 @@
  *  - Rotary position embedding R_n, rotate-half pairing (i, i+d/2) with
  *    omega_i = theta^(-2i/d) (lo_rope_rotate_ex / lo_attention_ex also take an
  *    explicit frequency vector, e.g. lo_llama3_freqs, and the interleaved pairing
- *    (2i, 2i+1)):
+ *    (2i, 2i+1); lo_rope_rotate_partial / lo_attention_partial rotate only the
+ *    first r dims, as partial-rotary models do):
  *        y_i     = x_i cos(n w_i) - x_{i+h} sin(n w_i)
  *        y_{i+h} = x_{i+h} cos(n w_i) + x_i sin(n w_i)
  *    The LazyAttention technical summary ("Mathematical Equivalence") relies on
@@ -76,19 +77,29 @@ void lo_set_num_threads(int n) {
 #endif
 }
 
-/* y = R_n x with frequencies w[i] (NULL: theta^(-2i/d)) and pairing (i, i+d/2), or
- * (2i, 2i+1) when `interleaved` (GPT-J style). x and y may alias. */
-void lo_rope_rotate_ex(int d, double theta, const double *w, int interleaved, double n, const double *x,
-                       double *y) {
-  int h = d / 2;
+/* Partial rotary (GPT-NeoX / GPT-J rotary_dim): y = R_n x on the first r dims only,
+ * pairs (i, i + r/2) (rotate-half) or (2i, 2i+1) (`interleaved`), i < r/2, with
+ * frequencies w[i] (NULL: theta^(-2i/r), the exponent taken over the rotated dims);
+ * dims r .. d-1 are copied. r = d is the full rotation. x and y may alias. */
+void lo_rope_rotate_partial(int d, int r, double theta, const double *w, int interleaved, double n,
+                            const double *x, double *y) {
+  int h = r / 2;
+  for (int c = r; c < d; c++) y[c] = x[c];
   for (int i = 0; i < h; i++) {
-    double wi = w ? w[i] : pow(theta, -2.0 * (double)i / (double)d);
+    double wi = w ? w[i] : pow(theta, -2.0 * (double)i / (double)r);
     double c = cos(n * wi), s = sin(n * wi);
     int ia = interleaved ? 2 * i : i, ib = interleaved ? 2 * i + 1 : i + h;
     double a = x[ia], b = x[ib];
     y[ia] = a * c - b * s;
     y[ib] = b * c + a * s;
   }
+}
+
+/* y = R_n x with frequencies w[i] (NULL: theta^(-2i/d)) and pairing (i, i+d/2), or
+ * (2i, 2i+1) when `interleaved` (GPT-J style). x and y may alias. */
+void lo_rope_rotate_ex(int d, double theta, const double *w, int interleaved, double n, const double *x,
+                       double *y) {
+  lo_rope_rotate_partial(d, d, theta, w, interleaved, n, x, y);
 }
 
 /* y = R_n x, rotate-half pairing, omega_i = theta^(-2i/d). x and y may alias. */
@@ -191,12 +202,15 @@ double lo_kv_cache_bytes(double layers, double heads, double head_dim, double se
  *   out      [nq][hq][d]   fp64
  * Returns 0, or -1 on a malformed layout.
  */
-int lo_attention_ex(int num_seqs, int hq, int hkv, int d, double theta, const double *freqs, int interleaved,
-                    double sm_scale, int dtype, int nq, const void *q, const int32_t *q_seq, const int32_t *q_m,
-                    const void *k_pool, const void *v_pool, int64_t num_pool_blocks, const int32_t *seg_indptr,
-                    const int32_t *seg_doc, const int32_t *seg_len, const int32_t *seq_pos0,
-                    const int32_t *doc_block_indptr, const int32_t *doc_blocks, double *out) {
+int lo_attention_partial(int num_seqs, int hq, int hkv, int d, int rot_dims, double theta, const double *freqs,
+                         int interleaved, double sm_scale, int dtype, int nq, const void *q, const int32_t *q_seq,
+                         const int32_t *q_m, const void *k_pool, const void *v_pool, int64_t num_pool_blocks,
+                         const int32_t *seg_indptr, const int32_t *seg_doc, const int32_t *seg_len,
+                         const int32_t *seq_pos0, const int32_t *doc_block_indptr, const int32_t *doc_blocks,
+                         double *out) {
   if (hkv <= 0 || hq % hkv != 0 || d <= 0 || d % 2 != 0) return -1;
+  if (rot_dims <= 0) rot_dims = d;
+  if (rot_dims > d || rot_dims % 2 != 0) return -1;
   const int g = hq / hkv;
   if (sm_scale <= 0.0) sm_scale = 1.0 / sqrt((double)d);
   int bad = 0;
@@ -244,7 +258,7 @@ int lo_attention_ex(int num_seqs, int hq, int hkv, int d, double theta, const do
         const int64_t phys = doc_blocks[doc_block_indptr[doc] + j / 16];
         const int64_t base = ((phys * hkv + kvh) * 16 + (j % 16)) * (int64_t)d;
         for (int c = 0; c < d; c++) row[c] = lo_load(k_pool, dtype, base + c);
-        lo_rope_rotate_ex(d, theta, freqs, interleaved, (double)p, row, &Kadj[t * d]);
+        lo_rope_rotate_partial(d, rot_dims, theta, freqs, interleaved, (double)p, row, &Kadj[t * d]);
         for (int c = 0; c < d; c++) V[t * d + c] = lo_load(v_pool, dtype, base + c);
         pos[t] = p + j;
       }
@@ -257,7 +271,7 @@ int lo_attention_ex(int num_seqs, int hq, int hkv, int d, double theta, const do
       const int64_t m = q_m[r];
       for (int h = kvh * g; h < (kvh + 1) * g; h++) {
         for (int c = 0; c < d; c++) row[c] = lo_load(q, dtype, ((int64_t)r * hq + h) * d + c);
-        lo_rope_rotate_ex(d, theta, freqs, interleaved, (double)m, row, qr);
+        lo_rope_rotate_partial(d, rot_dims, theta, freqs, interleaved, (double)m, row, qr);
         double mx = -INFINITY;
         for (int64_t j = 0; j < n; j++) {
           if (pos[j] > m) { sc[j] = -INFINITY; continue; }
@@ -285,6 +299,16 @@ int lo_attention_ex(int num_seqs, int hq, int hkv, int d, double theta, const do
 }
 
 /* lo_attention_ex with theta^(-2i/d) frequencies and rotate-half pairing. */
+int lo_attention_ex(int num_seqs, int hq, int hkv, int d, double theta, const double *freqs, int interleaved,
+                    double sm_scale, int dtype, int nq, const void *q, const int32_t *q_seq, const int32_t *q_m,
+                    const void *k_pool, const void *v_pool, int64_t num_pool_blocks, const int32_t *seg_indptr,
+                    const int32_t *seg_doc, const int32_t *seg_len, const int32_t *seq_pos0,
+                    const int32_t *doc_block_indptr, const int32_t *doc_blocks, double *out) {
+  return lo_attention_partial(num_seqs, hq, hkv, d, d, theta, freqs, interleaved, sm_scale, dtype, nq, q, q_seq, q_m,
+                              k_pool, v_pool, num_pool_blocks, seg_indptr, seg_doc, seg_len, seq_pos0,
+                              doc_block_indptr, doc_blocks, out);
+}
+
 int lo_attention(int num_seqs, int hq, int hkv, int d, double theta, double sm_scale, int dtype, int nq,
                  const void *q, const int32_t *q_seq, const int32_t *q_m, const void *k_pool,
                  const void *v_pool, int64_t num_pool_blocks, const int32_t *seg_indptr,

@@ -231,7 +231,7 @@ int lazy_attn_rope_table_init(const lazy_attn_params* p, void* table, size_t tab
   if (rc != LAZY_OK) return rc;
   if (!table) return LAZY_ERR_INVALID_ARG;
   if (table_bytes < lazy_attn_rope_table_bytes(p) || !aligned16(table)) return LAZY_ERR_WORKSPACE;
-  return launched(lazy::launch_rope_table(static_cast<float2*>(table), p->head_dim, p->rope_theta, nullptr,
+  return launched(lazy::launch_rope_table(static_cast<float2*>(table), p->head_dim, p->rope_theta, nullptr, nullptr,
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -245,8 +245,40 @@ int lazy_attn_rope_table_init_scaled(const lazy_attn_params* p, const lazy_rope_
                    scaling->high_freq_factor > scaling->low_freq_factor && scaling->original_max_position > 0))
     return LAZY_ERR_INVALID_ARG;
   if (table_bytes < lazy_attn_rope_table_bytes(p) || !aligned16(table)) return LAZY_ERR_WORKSPACE;
-  return launched(lazy::launch_rope_table(static_cast<float2*>(table), p->head_dim, p->rope_theta, scaling,
+  return launched(lazy::launch_rope_table(static_cast<float2*>(table), p->head_dim, p->rope_theta, scaling, nullptr,
                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int lazy_attn_rotary_layout_host(int32_t head_dim, int32_t rot_dims, int32_t interleaved, double theta,
+                                 int32_t* perm_out, double* freqs_out) {
+  if (head_dim < 2 || head_dim % 2 || rot_dims < 2 || rot_dims % 2 || rot_dims > head_dim || !(theta > 1.0) ||
+      !perm_out || !freqs_out)
+    return LAZY_ERR_INVALID_ARG;
+  const int h = head_dim / 2, hr = rot_dims / 2, hn = (head_dim - rot_dims) / 2;
+  for (int f = 0; f < hr; ++f) {  // rotary pair f -> new dims (f, f + h)
+    perm_out[f] = interleaved ? 2 * f : f;
+    perm_out[f + h] = interleaved ? 2 * f + 1 : f + hr;
+    freqs_out[f] = std::pow(theta, -2.0 * (double)f / (double)rot_dims);
+  }
+  for (int k = 0; k < hn; ++k) {  // unrotated dims fill the remaining pairs, rate 0
+    perm_out[hr + k] = rot_dims + k;
+    perm_out[hr + k + h] = rot_dims + hn + k;
+    freqs_out[hr + k] = 0.0;
+  }
+  return LAZY_OK;
+}
+
+int lazy_attn_rope_table_init_freqs(const lazy_attn_params* p, const double* freqs_host, void* table,
+                                    size_t table_bytes, lazy_stream_t stream) {
+  Checked c;
+  int rc = check_params(p, &c);
+  if (rc != LAZY_OK) return rc;
+  if (!freqs_host || !table) return LAZY_ERR_INVALID_ARG;
+  for (int f = 0; f < p->head_dim / 2; ++f)
+    if (!(freqs_host[f] >= 0.0 && freqs_host[f] <= 4.0)) return LAZY_ERR_INVALID_ARG;  // also rejects NaN
+  if (table_bytes < lazy_attn_rope_table_bytes(p) || !aligned16(table)) return LAZY_ERR_WORKSPACE;
+  return launched(lazy::launch_rope_table(static_cast<float2*>(table), p->head_dim, p->rope_theta, nullptr,
+                                          freqs_host, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int lazy_attn_pack_block_words_host(const lazy_attn_params* p, int32_t num_docs, const int32_t* seg_indptr,

@@ -139,8 +139,9 @@ int plan_shared_host(int B, int G, int rows_cap, int max_blocks, int num_pool_bl
                      int32_t* slot_indptr, int32_t* counts);
 
 // Every launcher returns the cudaError_t of its launch.
+// explicit_w (host, head_dim/2 rates in radians per position) overrides theta and scaling.
 cudaError_t launch_rope_table(float2* table, int head_dim, double theta, const lazy_rope_scaling* scaling,
-                              cudaStream_t st);
+                              const double* explicit_w, cudaStream_t st);
 cudaError_t launch_debug_rope(const float2* table, const int32_t* deltas, int n, int head_dim, float2* out,
                               unsigned int* status, cudaStream_t st);
 cudaError_t launch_pack(const PackArgs& a, cudaStream_t st);

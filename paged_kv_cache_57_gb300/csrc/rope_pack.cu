@@ -12,14 +12,20 @@ namespace lazy {
 struct FreqScale {
   double factor, low_ff, high_ff, orig_max;
 };
+// Explicit rates (radians per position), passed by value; `on` selects them.
+struct ExplicitRates {
+  double w[64];
+  int on;
+};
 
-__global__ void rope_table_kernel(float2* table, int half, int head_dim, double theta, FreqScale sc) {
+__global__ void rope_table_kernel(float2* table, int half, int head_dim, double theta, FreqScale sc,
+                                  ExplicitRates ex) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= half * (1 + LAZY_ROPE_ROWS)) return;
   const int f = idx % half, row = idx / half - 1;
   const double two_pi = 6.283185307179586476925286766559;
-  double w = pow(theta, -2.0 * (double)f / (double)head_dim);
-  if (sc.factor > 0.0) {  // wavelength bands: keep, divide by the factor, or blend the two
+  double w = ex.on ? ex.w[f] : pow(theta, -2.0 * (double)f / (double)head_dim);
+  if (!ex.on && sc.factor > 0.0) {  // wavelength bands: keep, divide by the factor, or blend the two
     const double lam = two_pi / w;
     const double lam_short = sc.orig_max / sc.high_ff, lam_long = sc.orig_max / sc.low_ff;
     if (lam > lam_long) {
@@ -41,13 +47,19 @@ __global__ void rope_table_kernel(float2* table, int half, int head_dim, double 
 }
 
 cudaError_t launch_rope_table(float2* table, int head_dim, double theta, const lazy_rope_scaling* scaling,
-                              cudaStream_t st) {
+                              const double* explicit_w, cudaStream_t st) {
   const int half = head_dim / 2;
+  if (half > 64) return cudaErrorInvalidValue;
   const int total = half * (1 + LAZY_ROPE_ROWS);
   FreqScale sc{0.0, 1.0, 2.0, 1.0};
   if (scaling) sc = FreqScale{scaling->factor, scaling->low_freq_factor, scaling->high_freq_factor,
                               (double)scaling->original_max_position};
-  rope_table_kernel<<<(total + 255) / 256, 256, 0, st>>>(table, half, head_dim, theta, sc);
+  ExplicitRates ex{};
+  if (explicit_w) {
+    ex.on = 1;
+    for (int f = 0; f < half; ++f) ex.w[f] = explicit_w[f];
+  }
+  rope_table_kernel<<<(total + 255) / 256, 256, 0, st>>>(table, half, head_dim, theta, sc, ex);
   return cudaGetLastError();
 }
 

@@ -34,7 +34,8 @@ EXPORTED = (
     "lazy_attn_decode", "lazy_attn_prefill_workspace_bytes", "lazy_attn_prefill", "lazy_attn_debug_gather",
     "lazy_attn_device_status", "lazy_attn_launch_count", "lazy_attn_debug_rope", "lazy_attn_decode_noalloc",
     "lazy_attn_plan_shared_host", "lazy_attn_decode_shared_workspace_bytes", "lazy_attn_decode_shared",
-    "lazy_attn_materialize", "lazy_attn_rope_table_init_scaled",
+    "lazy_attn_materialize", "lazy_attn_rope_table_init_scaled", "lazy_attn_rope_table_init_freqs",
+    "lazy_attn_rotary_layout_host",
 )
 PLAN_MAX_MEMBERS = 16
 PLAN_ITEM_BLOCK_IDS = 32
@@ -66,6 +67,8 @@ _sig = {
     "lazy_attn_rope_table_bytes": (_sz, [_P]),
     "lazy_attn_rope_table_init": (ctypes.c_int, [_P, _vp, _sz, _vp]),
     "lazy_attn_rope_table_init_scaled": (ctypes.c_int, [_P, _vp, _vp, _sz, _vp]),
+    "lazy_attn_rope_table_init_freqs": (ctypes.c_int, [_P, _vp, _vp, _sz, _vp]),
+    "lazy_attn_rotary_layout_host": (ctypes.c_int, [_i32, _i32, _i32, ctypes.c_double, _vp, _vp]),
     "lazy_attn_pack_block_words_host": (ctypes.c_int, [_P, _i32] + [_vp] * 8),
     "lazy_attn_pack_block_words": (ctypes.c_int, [_P, _i32] + [_vp] * 8 + [_vp]),
     "lazy_attn_decode_workspace_bytes": (_sz, [_P]),
@@ -139,20 +142,39 @@ class RopeScaling(ctypes.Structure):
 
 
 def rope_table_init(p: Params, table: Optional[torch.Tensor] = None, stream=None,
-                    scaling: Optional[RopeScaling] = None) -> torch.Tensor:
+                    scaling: Optional[RopeScaling] = None, freqs: Optional[np.ndarray] = None) -> torch.Tensor:
+    """Rotation table from theta (default), the Llama-3.1 scaling, or explicit rates
+    ``freqs`` [head_dim/2] in radians per position (see rotary_layout)."""
     n = rope_table_bytes(p)
     if n == 0:
         raise LazyAttnError(LAZY_ERR_INVALID_ARG, "rope_table_bytes")
     if table is None:
         table = torch.empty(n, dtype=torch.uint8, device="cuda")
     nbytes = table.numel() * table.element_size()
-    if scaling is None:
+    if freqs is not None:
+        f = np.ascontiguousarray(freqs, dtype=np.float64)
+        if f.shape != (p.head_dim // 2,):
+            raise ValueError(f"freqs must have shape ({p.head_dim // 2},)")
+        rc = _lib.lazy_attn_rope_table_init_freqs(ctypes.byref(p), f.ctypes.data, _dptr(table, "table"), nbytes,
+                                                  _stream(stream))
+    elif scaling is None:
         rc = _lib.lazy_attn_rope_table_init(ctypes.byref(p), _dptr(table, "table"), nbytes, _stream(stream))
     else:
         rc = _lib.lazy_attn_rope_table_init_scaled(ctypes.byref(p), ctypes.addressof(scaling), _dptr(table, "table"),
                                                    nbytes, _stream(stream))
     _check(rc, "rope_table_init")
     return table
+
+
+def rotary_layout(d: int, rot_dims: int, theta: float, interleaved: bool = False):
+    """(perm [d], freqs [d/2]) of lazy_attn_rotary_layout_host: permute q and the stored
+    K rows by ``perm`` and build the table with ``freqs`` to rotate only the first
+    ``rot_dims`` dims (partial rotary), rotate-half or interleaved."""
+    perm = np.empty(d, np.int32)
+    freqs = np.empty(d // 2, np.float64)
+    _check(_lib.lazy_attn_rotary_layout_host(int(d), int(rot_dims), int(bool(interleaved)), float(theta),
+                                             perm.ctypes.data, freqs.ctypes.data), "rotary_layout")
+    return perm.astype(np.int64), freqs
 
 
 def interleave_perm(d: int) -> np.ndarray:

@@ -95,3 +95,46 @@ def test_shared_decode_and_prefill_interleaved_pairing():
     ref = oracle.attention(wpf, interleaved=True)
     wpp, dvp = _interleaved_device(wpf)
     assert_close(prefill(dvp), ref, "bf16", "prefill, interleaved", emulate=lambda r: emulate(wpp, r))
+
+
+# ---------------------------------------------------------------- partial rotary
+# Only the first r dims rotate: q and stored K permuted by the library's layout, the
+# table built from its rates (0 for the unrotated pairs); the oracle rotates the first
+# r dims of the unpermuted inputs directly.
+
+def _partial_device(w, r, interleaved=False):
+    L = la()
+    perm, freqs = L.rotary_layout(w.head_dim, r, w.rope_theta, interleaved)
+    wp = dataclasses.replace(w, q=w.q[..., perm].contiguous(), k_pool=w.k_pool[..., perm].contiguous())
+    dv = to_device(wp)
+    dv.rope = L.rope_table_init(dv.p, freqs=freqs)
+    return wp, dv, freqs
+
+
+def test_decode_f32_partial_rotary():
+    w = W.decode_zipf("vp32", batch=4, hq=8, hkv=2, d=64, docs_per_seq=3, doc_tokens=150, pool_docs=5, zipf_s=1.0,
+                      suffix_tokens=11, dtype="f32", theta=1e4, seed=307)
+    ref = oracle.attention(w, rot_dims=16)
+    _, dv, _ = _partial_device(w, 16)
+    assert_close(decode(dv), ref, "f32", "f32 decode, partial rotary")
+
+
+@pytest.mark.parametrize("hq,hkv,interleaved", [(16, 4, False), (32, 1, False), (32, 1, True)])
+def test_shared_and_per_sequence_decode_partial_rotary(hq, hkv, interleaved):
+    # 4 query heads per KV head: mma.sync shared-run kernel; 32: the tensor-core one
+    w = W.decode_zipf(f"vpb{hq}", batch=8, hq=hq, hkv=hkv, d=128, docs_per_seq=3, doc_tokens=230, pool_docs=3,
+                      zipf_s=1.0, suffix_tokens=17, seed=308 + hq)
+    ref = oracle.attention(w, rot_dims=32, interleaved=interleaved)
+    wp, dv, freqs = _partial_device(w, 32, interleaved)
+    emu = lambda r: emulate(wp, r, freqs=freqs)
+    assert_close(decode_shared(dv, shared_plan(dv)), ref, "bf16", "shared decode, partial rotary", emulate=emu)
+    assert_close(decode(dv), ref, "bf16", "per-sequence decode, partial rotary", emulate=emu)
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (6, 2)])  # stream-K and one-tile prefill kernels
+def test_prefill_partial_rotary(hq, hkv):
+    w = W.prefill_zipf("ppart", batch=2, hq=hq, hkv=hkv, docs_per_seq=3, doc_tokens=260, pool_docs=4, zipf_s=1.2,
+                       chunk_tokens=[140, 60], seed=310)
+    ref = oracle.attention(w, rot_dims=64)
+    wp, dv, freqs = _partial_device(w, 64)
+    assert_close(prefill(dv), ref, "bf16", "prefill, partial rotary", emulate=lambda r: emulate(wp, r, freqs=freqs))

@@ -122,3 +122,83 @@ def test_scaled_table_rejects_bad_scaling_without_cuda():
         assert rc == L.LAZY_ERR_INVALID_ARG, bad
     perm = L.interleave_perm(8)
     assert list(perm) == [0, 2, 4, 6, 1, 3, 5, 7]
+
+
+# ---------------------------------------------------------------- partial rotary
+
+def test_partial_rotary_full_width_is_the_full_rotation():
+    x = np.random.default_rng(4).standard_normal(64)
+    for n in (0.0, 5.0, -123.0):
+        assert np.array_equal(oracle.rope_rotate_ex(x, n, 1e4, rot_dims=64), oracle.rope_rotate(x, n, 1e4))
+
+
+def test_partial_rotary_two_dims_is_one_plane_rotation():
+    # r = 2: one pair (0, 1) at rate theta^0 = 1; every other dim passes through.
+    x = np.random.default_rng(5).standard_normal(16)
+    for interleaved in (False, True):
+        for n in (0.75, -3.0, 40.0):
+            y = oracle.rope_rotate_ex(x, n, 1e4, interleaved=interleaved, rot_dims=2)
+            c, s = math.cos(n), math.sin(n)
+            assert np.allclose(y[:2], [c * x[0] - s * x[1], s * x[0] + c * x[1]], atol=1e-14)
+            assert np.array_equal(y[2:], x[2:])
+
+
+def test_partial_rotary_head_is_an_r_dim_rotation_and_tail_passes():
+    x = np.random.default_rng(6).standard_normal(128)
+    for r in (32, 64):
+        for n in (7.0, -1000.0):
+            y = oracle.rope_rotate_ex(x, n, 1e4, rot_dims=r)
+            assert np.array_equal(y[r:], x[r:])
+            # rates theta^(-2i/r): the r-dim vector rotated on its own (rates given
+            # explicitly from numpy, so the check does not share the oracle's rate code)
+            w = 1e4 ** (-2.0 * np.arange(r // 2) / r)
+            half = r // 2
+            a, b = x[:half], x[half:r]
+            want = np.concatenate([a * np.cos(n * w) - b * np.sin(n * w), b * np.cos(n * w) + a * np.sin(n * w)])
+            assert np.allclose(y[:r], want, atol=1e-12)
+            assert np.isclose(np.linalg.norm(y), np.linalg.norm(x), rtol=1e-14)
+
+
+@pytest.mark.parametrize("interleaved", [False, True])
+def test_partial_rotary_relative_offset_property(interleaved):
+    rng = np.random.default_rng(7)
+    q, k = rng.standard_normal(128), rng.standard_normal(128)
+    for m, p in ((50, 10), (9000, 8999), (3, 300)):
+        lhs = oracle.rope_rotate_ex(q, m, 1e4, None, interleaved, 32) @ oracle.rope_rotate_ex(k, p, 1e4, None,
+                                                                                              interleaved, 32)
+        rhs = oracle.rope_rotate_ex(q, m - p, 1e4, None, interleaved, 32) @ k
+        assert abs(lhs - rhs) < 1e-10
+
+
+@pytest.mark.parametrize("interleaved", [False, True])
+def test_library_layout_reproduces_partial_rotary_in_the_oracle(interleaved):
+    """The library's layout (permutation + rates, zero for the unrotated pairs) turned
+    into a full-width rotate-half attention on permuted inputs equals the oracle's
+    partial rotary on the original inputs: two independent code paths of the oracle."""
+    from paged_kv_cache_57_gb300 import lazy_attn as L
+    w = W.decode_zipf("rpart", batch=3, hq=4, hkv=2, d=64, docs_per_seq=3, doc_tokens=40, pool_docs=5,
+                      zipf_s=1.0, suffix_tokens=5, dtype="f32", theta=1e4, seed=212)
+    perm, freqs = L.rotary_layout(64, 16, 1e4, interleaved)
+    assert sorted(perm) == list(range(64)) and (freqs[8:] == 0).all()
+    wp = dataclasses.replace(w, q=w.q[..., perm].contiguous(), k_pool=w.k_pool[..., perm].contiguous())
+    a = oracle.attention(w, rot_dims=16, interleaved=interleaved)
+    b = oracle.attention(wp, freqs=freqs)
+    assert np.allclose(a, b, atol=1e-12)
+    assert np.abs(oracle.attention(w) - a).max() > 1e-3  # rotating only 16 of 64 dims changes the result
+
+
+def test_rotary_layout_and_explicit_rates_argument_checks():
+    from paged_kv_cache_57_gb300 import lazy_attn as L
+    for bad in ((64, 0), (64, 3), (64, 66), (63, 32)):
+        with pytest.raises(L.LazyAttnError):
+            L.rotary_layout(bad[0], bad[1], 1e4)
+    w = W.tiny_fp32()
+    p = L.make_params(num_seqs=w.num_seqs, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                      head_dim=w.head_dim, num_pool_blocks=w.num_pool_blocks, max_blocks_per_seq=w.max_blocks_per_seq,
+                      dtype=w.dtype, rope_theta=w.rope_theta)
+    fake = ctypes.c_void_p(4096)  # never dereferenced: the rates are rejected first
+    for bad in (-1e-3, 4.5, float("nan"), float("inf")):
+        f = np.full(w.head_dim // 2, 0.5)
+        f[3] = bad
+        rc = L._lib.lazy_attn_rope_table_init_freqs(ctypes.byref(p), f.ctypes.data, fake, 1 << 20, None)
+        assert rc == L.LAZY_ERR_INVALID_ARG, bad
