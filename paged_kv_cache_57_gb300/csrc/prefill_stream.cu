@@ -503,16 +503,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         (void)u;
         (void)un;
         (void)U0;
-        // The segment's first S pair: its Q is rotated; S_t overwrites P_t of the previous tile.
+        // The segment's first S pair: its Q is rotated. S_t overwrites P_t of the previous
+        // tile, whose P V was issued earlier by this thread: one thread's MMAs execute in
+        // issue order, so that P V has read P_t before S_t writes the columns.
         ok = mbar_wait(q_ready, sg & 1, a.status) && mbar_wait(&k_ready[g % NK], (g / NK) & 1, a.status);
-        for (int t = 0; ok && t < 2; ++t) {
-          if (g > 0) ok = mbar_wait(&pv_done[t], (g - 1) & 1, a.status);
-          if (ok) {
-            tc_fence_after();
-            issue_s(g, t);
-          }
-        }
         if (!ok) return false;
+        tc_fence_after();
+        issue_s(g, 0);
+        issue_s(g, 1);
         LAZY_PF_TRACE_IF(true, sg, 7, global_timer_ns());
         tc_commit(&k_empty[g % NK]);
         if (j1 - j0 == 1) tc_commit(q_empty);  // the segment's last S product is issued
@@ -523,9 +521,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!ok) return false;
           tc_fence_after();
           issue_pv(g, 0, j > j0);
-          if (more) {  // S_A(g+1) overwrites P_A(g): wait for PV_A(g)
-            ok = mbar_wait(&k_ready[(g + 1) % NK], ((g + 1) / NK) & 1, a.status) &&
-                 mbar_wait(&pv_done[0], g & 1, a.status);
+          if (more) {  // S_A(g+1) overwrites P_A(g), read by PV_A(g) issued just above (in order)
+            ok = mbar_wait(&k_ready[(g + 1) % NK], ((g + 1) / NK) & 1, a.status);
             if (!ok) return false;
             tc_fence_after();
             issue_s(g + 1, 0);
@@ -536,9 +533,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           issue_pv(g, 1, j > j0);
           tc_commit(&v_empty[g % NV]);
           if (more) {
-            ok = mbar_wait(&pv_done[1], g & 1, a.status);
-            if (!ok) return false;
-            tc_fence_after();
             issue_s(g + 1, 1);
             tc_commit(&k_empty[(g + 1) % NK]);
             if (j + 2 == j1) tc_commit(q_empty);  // the segment's last S product is issued
