@@ -414,12 +414,12 @@ __global__ void __launch_bounds__(kShThreads, 3)
 // out[s][h] = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k over the sequence's
 // slots k in [slot_indptr[s], slot_indptr[s+1]); a sequence without slots gets 0.
 // One warp per (sequence, query head), D/32 output columns per lane. Slots are
-// taken eight at a time with all their loads issued together (one memory round
-// trip per eight slots), folded in with the online rescale of the running
+// taken BATCH (8 or 16) at a time with all their loads issued together (one
+// memory round trip per batch), folded in with the online rescale of the running
 // maximum. Launched as a programmatic dependent of the decode kernel: its CTAs
 // may become resident while the decode kernel's last CTAs run, and wait for the
 // decode grid's completion (and its partials) before reading anything.
-template <int D>
+template <int D, int BATCH>
 __global__ void shared_combine_kernel(const SharedDecodeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int wg = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -432,7 +432,6 @@ __global__ void shared_combine_kernel(const SharedDecodeArgs a) {
     k0 = k1 = 0;
   }
   constexpr int PER = D / 32;
-  constexpr int BATCH = 8;
   const float2* ml = reinterpret_cast<const float2*>(a.ws_ml);
   float M = -INFINITY, L = 0.f;
   float acc[PER];
@@ -521,8 +520,14 @@ cudaError_t launch_shared_combine(const SharedDecodeArgs& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (a.D == 128) return cudaLaunchKernelEx(&cfg, shared_combine_kernel<128>, a);
-  return cudaLaunchKernelEx(&cfg, shared_combine_kernel<64>, a);
+  // Slots per round trip: 16 when sequences hold many slots (fewer round trips), else
+  // 8 (fewer registers: two CTAs per SM).
+  const bool wide = (long long)a.num_slots > 12LL * a.B;
+  if (a.D == 128)
+    return wide ? cudaLaunchKernelEx(&cfg, shared_combine_kernel<128, 16>, a)
+                : cudaLaunchKernelEx(&cfg, shared_combine_kernel<128, 8>, a);
+  return wide ? cudaLaunchKernelEx(&cfg, shared_combine_kernel<64, 16>, a)
+              : cudaLaunchKernelEx(&cfg, shared_combine_kernel<64, 8>, a);
 }
 
 }  // namespace lazy
