@@ -148,10 +148,21 @@ static_assert(OFF_SCHED % 16 == 0 && OFF_TMEM % 16 == 0, "shared-memory slots ar
       reinterpret_cast<unsigned long long*>(a.partials + (size_t)2 * gridDim.x * 2 * PARTIAL_TILE_FLOATS) \
           [((size_t)blockIdx.x * 8 + (sg)) * 8 + (i)] = (v);                                            \
   } while (0)
+// After the timestamps, 8 cycle totals per CTA over its tiles: softmax of tile A,
+// row 0: [0] waiting for S and V, [1] first pass, [2] second pass and P, [3] rescale
+// and hand-off, [4] tiles; MMA warp: [5] waiting for P_A and V, [6] for P_B, [7] for K.
+#define LAZY_PF_COUNT(i, v)                                                                             \
+  (reinterpret_cast<unsigned long long*>(a.partials + (size_t)2 * gridDim.x * 2 * PARTIAL_TILE_FLOATS) \
+       [(size_t)gridDim.x * 64 + (size_t)blockIdx.x * 8 + (i)] += (v))
+#define LAZY_PF_CLK(var) const long long var = clock64()
 #else
 #define LAZY_PF_TRACE_IF(cond, sg, i, v) \
   do {                                   \
   } while (0)
+#define LAZY_PF_COUNT(i, v) \
+  do {                      \
+  } while (0)
+#define LAZY_PF_CLK(var)
 #endif
 #define LAZY_PF_TRACE(sg, i, v) LAZY_PF_TRACE_IF(threadIdx.x == 0, sg, i, v)
 
@@ -516,18 +527,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (j1 - j0 == 1) tc_commit(q_empty);  // the segment's last S product is issued
         for (int j = j0; j < j1; ++j, ++g) {
           const bool more = j + 1 < j1;
+          LAZY_PF_CLK(c0);
           ok = mbar_wait(&p_full[0], g & 1, a.status) && mbar_wait(&v_full[g % NV], (g / NV) & 1, a.status) &&
                mbar_wait(&v_ready[g % NV], (g / NV) & 1, a.status);
+          LAZY_PF_CLK(c1);
+          LAZY_PF_COUNT(5, c1 - c0);
           if (!ok) return false;
           tc_fence_after();
           issue_pv(g, 0, j > j0);
           if (more) {  // S_A(g+1) overwrites P_A(g), read by PV_A(g) issued just above (in order)
+            LAZY_PF_CLK(c2);
             ok = mbar_wait(&k_ready[(g + 1) % NK], ((g + 1) / NK) & 1, a.status);
+            LAZY_PF_CLK(c3);
+            LAZY_PF_COUNT(7, c3 - c2);
             if (!ok) return false;
             tc_fence_after();
             issue_s(g + 1, 0);
           }
+          LAZY_PF_CLK(c4);
           ok = mbar_wait(&p_full[1], g & 1, a.status);
+          LAZY_PF_CLK(c5);
+          LAZY_PF_COUNT(6, c5 - c4);
           if (!ok) return false;
           tc_fence_after();
           issue_pv(g, 1, j > j0);
@@ -768,7 +788,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = j0; j < j1; ++j, ++g) {
         const int vs = g % NV;
+        LAZY_PF_CLK(k0);
         ok = warp_wait(&s_full[t], g & 1, a.status) && warp_wait(&v_full[vs], (g / NV) & 1, a.status);
+        LAZY_PF_CLK(k1);
         if (!ok) return false;
         if (j == j0) LAZY_PF_TRACE(sg, 0, global_timer_ns());
         tc_fence_after();
@@ -809,6 +831,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           m_run = mx;
         }
         const float m_use = m_run == -INFINITY ? 0.f : m_run;
+        LAZY_PF_CLK(k2);
         // Pass 2: weights -> bf16 P over S's first 64 columns (chunk q's 16 words land on
         // columns already read), row sum in fp32.
         const uint64_t mm = f2(m_use, m_use);
@@ -835,6 +858,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         const float2 sa = f2_split(acc);
         l_run = l_run * alpha + (sa.x + sa.y);
+        LAZY_PF_CLK(k3);
         // Rescale the running output when this row's maximum was refreshed (warp-uniform);
         // PV_t(g-1) has completed, since S_t(g) was issued after it.
         if (j > j0 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -851,6 +875,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&p_full[t]);
+#ifdef LAZY_PREFILL_TRACE
+        if (threadIdx.x == 0) {
+          LAZY_PF_CLK(k4);
+          LAZY_PF_COUNT(0, k1 - k0);
+          LAZY_PF_COUNT(1, k2 - k1);
+          LAZY_PF_COUNT(2, k3 - k2);
+          LAZY_PF_COUNT(3, k4 - k3);
+          LAZY_PF_COUNT(4, 1);
+        }
+#endif
       }
       pend = Pend{un, j0, j1, U0, g - 1, sg, m_run, l_run, true};
       return true;
@@ -885,7 +919,7 @@ size_t prefill_stream_counter_bytes(int grid) {
 size_t prefill_stream_workspace_bytes(int grid) {
   size_t bytes = prefill_stream_counter_bytes(grid) + (size_t)2 * grid * 2 * PARTIAL_TILE_FLOATS * sizeof(float);
 #ifdef LAZY_PREFILL_TRACE
-  bytes += (size_t)grid * 8 * 8 * 8;
+  bytes += (size_t)grid * 9 * 8 * 8;
 #endif
   return bytes;
 }
