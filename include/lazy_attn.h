@@ -240,7 +240,7 @@ int lazy_attn_decode(const lazy_attn_params *p, const void *q, const void *k_poo
  * split into sets of at most LAZY_PLAN_MAX_MEMBERS members and at most R query
  * rows (members x query heads per KV head), and each set's blocks are cut into
  * chunks of chunk_blocks logical blocks. R is 128 when a KV head serves at least
- * 16 query heads and head_dim is 128 (the decode then runs on the 5th-generation
+ * 8 query heads and head_dim is 128 (the decode then runs on the 5th-generation
  * tensor cores, one 128-row tile per item), else 64. chunk_blocks 0 selects 32,
  * or, for R = 128, about one item per resident CTA (2 x 152 / num_kv_heads items):
  * the sets' blocks summed, divided by that count, rounded up to a multiple of 4

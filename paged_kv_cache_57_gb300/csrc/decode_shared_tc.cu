@@ -4,9 +4,9 @@
 // The work items, slots and partial results of decode_shared.cu ("Resumo Técnico:
 // LazyAttention", "Implementação Técnica", item 2: each member's query is rotated
 // once by its relative offset R_{m-p}; the stored keys are read as they are),
-// computed with tcgen05. When one KV head serves G >= 16 query heads (MQA, wide
-// GQA), an item's rows (members x G, at most 128) fill the M = 128 rows of one
-// tensor-core tile, and a 64-key tile costs 12 MMA instructions issued by one
+// computed with tcgen05. When one KV head serves G >= 8 query heads (MQA, wide
+// GQA such as Llama-3.1-70B's 64/8), an item's rows (members x G, at most 128)
+// fill the M = 128 rows of one tensor-core tile, and a 64-key tile costs 12 MMA instructions issued by one
 // thread instead of hundreds of dependent mma.sync per warp.
 //
 //   warps 0-3  prologue (member checks, R_{m-p} q pre-scaled -> shared memory),
@@ -45,7 +45,7 @@ constexpr int kTcTile = 2 * kTcHalf;          // K or V of one tile: 16 KiB
 constexpr int kTcQHalf = kTcRows * 128;       // one 64-column half of the Q tile: 16 KiB
 constexpr int kTcNS = 2;                      // stages of each ring
 constexpr int kTcThreads = 224;               // 7 warps
-constexpr int kTcMembers = kTcRows / 16;      // G >= 16: at most 8 members
+constexpr int kTcMembers = kTcRows / 8;       // G >= 8: at most 16 members
 constexpr uint32_t kTcCols = 256;
 constexpr uint32_t kColS = 0, kColO = 128;    // S buffer b at kColS + 64 b
 constexpr int kItemInts = LAZY_PLAN_ITEM_INTS;

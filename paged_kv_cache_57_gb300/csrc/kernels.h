@@ -121,10 +121,12 @@ struct MaterializeArgs {
 cudaError_t launch_materialize(const MaterializeArgs& a, cudaStream_t st);
 
 // Query rows per shared-run work item: 128 where the tensor-core kernel
-// (decode_shared_tc.cu) serves the call -- at least 16 query heads per KV head and
+// (decode_shared_tc.cu) serves the call -- at least 8 query heads per KV head and
 // D = 128 -- else 64 (decode_shared.cu). The planner and the decode call both
-// follow it.
-inline int shared_rows_cap(int G, int D) { return (G >= 16 && D == 128) ? 128 : 64; }
+// follow it. (Measured: at 8 query heads per KV head, items of 16 members on the
+// tensor cores beat items of 8 on mma.sync; at 4, 16-member items fill only half
+// a tile and mma.sync stays ahead.)
+inline int shared_rows_cap(int G, int D) { return (G >= 8 && D == 128) ? 128 : 64; }
 // Resident CTAs of the tensor-core kernel on a GB300 (2 per SM x 152 SMs): its
 // automatic chunk length aims at about this many CTAs, so that each CTA's fixed
 // cost (record, query rotation, partials) is paid as few times as the machine allows.

@@ -199,7 +199,7 @@ def test_shared_plan_covers_every_block_once(la, w, chunk):
     items, slot_indptr = la.plan_shared_host(p, len(w.doc_len), w.seg_indptr, w.seg_doc, w.seg_len,
                                              w.doc_block_indptr, w.doc_blocks, chunk_blocks=chunk)
     G = w.num_q_heads // w.num_kv_heads
-    rows_cap = 128 if G >= 16 and w.head_dim == 128 else 64  # one tcgen05 tile, or 4 mma.sync row tiles
+    rows_cap = 128 if G >= 8 and w.head_dim == 128 else 64  # one tcgen05 tile, or 4 mma.sync row tiles
     exp = {s: expected_blocks(w, s) for s in range(w.num_seqs)}
     cover = {s: np.zeros(len(exp[s]), np.int64) for s in range(w.num_seqs)}
     slots_seen = set()
@@ -235,7 +235,7 @@ def test_shared_plan_covers_every_block_once(la, w, chunk):
 
 
 def test_shared_plan_automatic_chunk_for_the_tensor_core_kernel(la):
-    # 0 selects 32 blocks for the mma.sync kernel; for the tensor-core kernel (G >= 16,
+    # 0 selects 32 blocks for the mma.sync kernel; for the tensor-core kernel (G >= 8,
     # d = 128) about one item per resident CTA (2 x 152 over the KV heads): the sum of
     # the member sets' blocks over that count, rounded up to 4, within 32 .. 256.
     for hkv, docs in ((1, 6), (2, 40)):

@@ -49,13 +49,13 @@ def test_shared_decode_chunk_sweep(chunk):
 
 
 @pytest.mark.parametrize("chunk", [1, 5, 40])
-@pytest.mark.parametrize("hq", [16, 32, 64])
+@pytest.mark.parametrize("hq", [8, 16, 32, 64])
 def test_shared_decode_tensor_core_path(hq, chunk):
-    # hq query heads on one KV head, d = 128: the tcgen05 kernel, items of up to 128 rows.
-    # 700-token documents end in a partial block; at chunk 40 an item runs past the 32
-    # block ids its record names.
-    w = W.decode_zipf(f"stc{hq}c{chunk}", batch=10, hq=hq, hkv=1, d=128, docs_per_seq=3, doc_tokens=700,
-                      pool_docs=3, zipf_s=0.8, suffix_tokens=23, seed=190 + hq + chunk)
+    # hq query heads on one KV head, d = 128: the tcgen05 kernel, items of up to 128 rows
+    # (16 members at 8 heads). 700-token documents end in a partial block; at chunk 40 an
+    # item runs past the 32 block ids its record names.
+    w = W.decode_zipf(f"stc{hq}c{chunk}", batch=max(10, 128 // hq + 4), hq=hq, hkv=1, d=128, docs_per_seq=3,
+                      doc_tokens=700, pool_docs=3, zipf_s=0.8, suffix_tokens=23, seed=190 + hq + chunk)
     dv = to_device(w)
     plan = shared_plan(dv, chunk)
     assert plan.items_host[:, 4].max() * hq == 128  # full tensor-core tiles occur
