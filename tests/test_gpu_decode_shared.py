@@ -48,6 +48,10 @@ def test_shared_decode_chunk_sweep(chunk):
     _check(w, chunk=chunk)
 
 
+# (query heads, KV heads): the mma.sync kernel (4 per KV head) and the tensor-core one (32)
+EDGE_SHAPES = [(8, 2), (32, 1)]
+
+
 @pytest.mark.parametrize("chunk", [1, 5, 40])
 @pytest.mark.parametrize("hq", [8, 16, 32, 64])
 def test_shared_decode_tensor_core_path(hq, chunk):
@@ -62,17 +66,16 @@ def test_shared_decode_tensor_core_path(hq, chunk):
     _check(w, chunk=chunk)
 
 
-# (query heads, KV heads): the mma.sync kernel (4 per KV head) and the tensor-core one (32)
-EDGE_SHAPES = [(8, 2), (32, 1)]
 
-
-def test_shared_decode_many_members_per_document():
-    # 40 sequences all citing one document (repeatedly): groups are split into items of 16 members
-    w = W.decode_zipf("smany", batch=40, hq=8, hkv=2, d=128, docs_per_seq=3, doc_tokens=50, pool_docs=1,
+@pytest.mark.parametrize("hq,hkv,cap", [(8, 2, 16), (16, 2, 16), (32, 1, 4)])
+def test_shared_decode_many_members_per_document(hq, hkv, cap):
+    # 40 sequences all citing one document (repeatedly): groups are split into items of at
+    # most 16 members and at most 64 (mma.sync) or 128 (tcgen05) rows
+    w = W.decode_zipf("smany", batch=40, hq=hq, hkv=hkv, d=128, docs_per_seq=3, doc_tokens=50, pool_docs=1,
                       zipf_s=1.0, suffix_tokens=5, seed=162)
     dv = to_device(w)
     plan = shared_plan(dv)
-    assert plan.items_host[:, 4].max() == 16 and plan.num_items < int(plan.items_host[:, 4].sum())
+    assert plan.items_host[:, 4].max() == cap and plan.num_items < int(plan.items_host[:, 4].sum())
     _check(w)
 
 
@@ -83,8 +86,9 @@ def test_shared_decode_holes_and_partial_blocks():
     _check(d, chunk=4)
 
 
-def test_shared_decode_few_keys():
-    w = W.decode_zipf("sfew", batch=6, hq=8, hkv=2, d=128, docs_per_seq=1, doc_tokens=3, pool_docs=2,
+@pytest.mark.parametrize("hq,hkv", EDGE_SHAPES)
+def test_shared_decode_few_keys(hq, hkv):
+    w = W.decode_zipf("sfew", batch=6, hq=hq, hkv=hkv, d=128, docs_per_seq=1, doc_tokens=3, pool_docs=2,
                       zipf_s=1.0, seed=164)
     w.seg_len[:] = np.array([2, 3, 2, 3, 1, 2], np.int32)
     _check(w)
