@@ -246,9 +246,11 @@ int lazy_attn_decode(const lazy_attn_params *p, const void *q, const void *k_poo
  * the sets' blocks summed, divided by that count, rounded up to a multiple of 4
  * and kept within 32 .. 256. It writes
  *   items_host [num_items][LAZY_PLAN_ITEM_INTS] int32, one work item each:
- *     [0] src_seq, [1] b0, [2] nblk, [3] last_valid, [4] nmem, [5..7] 0: nblk
- *         logical blocks of sequence src_seq from block b0, all full but the
- *         last (last_valid slots), computed for nmem members;
+ *     [0] src_seq, [1] b0, [2] nblk, [3] last_valid, [4] nmem, [5] c0, [6..7] 0:
+ *         nblk logical blocks of sequence src_seq from block b0, all full but
+ *         the last (last_valid slots), computed for nmem members; they are the
+ *         blocks c0 .. c0+nblk-1 of their document (key k of block c0 + i is the
+ *         document's key 16 (c0 + i) + k);
  *     [8 + 4j ..] member j < nmem: {seq, b0, slot, 0}: sequence seq holds the
  *         same physical blocks at its logical blocks b0 .. b0+nblk-1 and its
  *         partial result goes to `slot`; unused member entries are 0;
@@ -284,6 +286,31 @@ int lazy_attn_decode_shared(const lazy_attn_params *p, const void *q, const void
                             const uint32_t *block_words, const int32_t *q_pos, const void *rope_table,
                             int32_t num_items, const int32_t *items, int32_t num_slots, const int32_t *slot_indptr,
                             void *out, void *workspace, size_t workspace_bytes, lazy_stream_t stream);
+
+/* ALiBi ("Resumo Técnico: LazyAttention", "Principais Contribuições", item 4: the
+ * mechanism carries over to relative position encodings such as ALiBi): the same
+ * call with every score of query head h also biased by -alibi_slopes[h] * (m - n)
+ * before the softmax, for a key at absolute position n (its document's start p plus
+ * its index within the document) and the query at m = q_pos. Stored keys carry no
+ * position, and the bias is formed on the fly from p (the block words), the item's
+ * first block within its document (record field [5]) and the slot. ALiBi models do
+ * not rotate q or k: pass a table built by lazy_attn_rope_table_init_freqs from zero
+ * rates, which makes every rotation the identity. alibi_slopes: device fp32 [Hq],
+ * 4-byte aligned; requires p->lazy = 1, else LAZY_ERR_INVALID_ARG. Only this
+ * shared-run entry point takes ALiBi: the per-sequence decode and the prefill read
+ * key positions from the block words, which do not carry a block's index within its
+ * document. */
+int lazy_attn_decode_shared_alibi(const lazy_attn_params *p, const void *q, const void *k_pool, const void *v_pool,
+                                  const uint32_t *block_words, const int32_t *q_pos, const void *rope_table,
+                                  int32_t num_items, const int32_t *items, int32_t num_slots,
+                                  const int32_t *slot_indptr, const float *alibi_slopes, void *out, void *workspace,
+                                  size_t workspace_bytes, lazy_stream_t stream);
+
+/* The usual ALiBi slopes for num_heads heads (host, out[num_heads]): 2^(-8 i / n),
+ * i = 1..n, when n is a power of two; otherwise the slopes of the largest power of
+ * two n' below n, followed by the odd-indexed slopes 2^(-8 (2k+1) / (2 n')) for the
+ * remaining heads. LAZY_ERR_INVALID_ARG for num_heads outside 1..4096. */
+int lazy_attn_alibi_slopes_host(int32_t num_heads, float *out);
 
 /* ---------------------------------------------------------------- decode without allocation
  * The pages have no counterpart for this entry point; it exists for callers that

@@ -77,7 +77,7 @@ def lib():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                 ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, _i32p,
                 _i32p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p,
-                _f64p]
+                ctypes.c_void_p, _f64p]
             _lib = L
     return _lib
 
@@ -161,11 +161,12 @@ def query_rows(w):
 
 def attention(w, rows: Optional[Sequence[int]] = None, sm_scale: float = 0.0,
               k_pool=None, v_pool=None, freqs: Optional[np.ndarray] = None, interleaved: bool = False,
-              rot_dims: Optional[int] = None) -> np.ndarray:
+              rot_dims: Optional[int] = None, alibi: Optional[np.ndarray] = None) -> np.ndarray:
     """fp64 reference output of workload ``w`` for the query rows ``rows`` (all by
     default): decode rows are sequences, prefill rows are chunk tokens. ``freqs``
     replaces theta^(-2i/r); ``interleaved`` pairs dimensions (2i, 2i+1);
-    ``rot_dims`` rotates only the first r dims (partial rotary; None: all).
+    ``rot_dims`` rotates only the first r dims (partial rotary; None: all);
+    ``alibi`` [Hq] adds the bias -alibi[h] (m - n) to every score (ALiBi).
     Returns [len(rows), Hq, d]."""
     q_seq, q_m = query_rows(w)
     q = w.q
@@ -179,6 +180,9 @@ def attention(w, rows: Optional[Sequence[int]] = None, sm_scale: float = 0.0,
     nq = qb.shape[0]
     out = np.zeros((nq, w.num_q_heads, w.head_dim), np.float64)
     f = None if freqs is None else np.ascontiguousarray(freqs, dtype=np.float64)
+    al = None if alibi is None else np.ascontiguousarray(alibi, dtype=np.float64)
+    if al is not None and al.shape != (w.num_q_heads,):
+        raise ValueError("alibi needs one slope per query head")
     rc = lib().lo_attention_partial(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
                             int(rot_dims or w.head_dim), float(w.rope_theta),
                             None if f is None else f.ctypes.data, int(interleaved),
@@ -188,7 +192,8 @@ def attention(w, rows: Optional[Sequence[int]] = None, sm_scale: float = 0.0,
                             np.ascontiguousarray(w.seg_doc, np.int32), np.ascontiguousarray(w.seg_len, np.int32),
                             np.ascontiguousarray(w.seq_pos0, np.int32),
                             np.ascontiguousarray(w.doc_block_indptr, np.int32),
-                            np.ascontiguousarray(w.doc_blocks, np.int32), out)
+                            np.ascontiguousarray(w.doc_blocks, np.int32),
+                            None if al is None else al.ctypes.data, out)
     if rc != 0:
         raise ValueError("oracle: malformed layout")
     return out

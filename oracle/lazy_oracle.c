@@ -12,7 +12,8 @@
  *    omega_i = theta^(-2i/d) (lo_rope_rotate_ex / lo_attention_ex also take an
  *    explicit frequency vector, e.g. lo_llama3_freqs, and the interleaved pairing
  *    (2i, 2i+1); lo_rope_rotate_partial / lo_attention_partial rotate only the
- *    first r dims, as partial-rotary models do):
+ *    first r dims, as partial-rotary models do, and lo_attention_partial adds an
+ *    optional ALiBi bias):
  *        y_i     = x_i cos(n w_i) - x_{i+h} sin(n w_i)
  *        y_{i+h} = x_{i+h} cos(n w_i) + x_i sin(n w_i)
  *    The LazyAttention technical summary ("Mathematical Equivalence") relies on
@@ -202,12 +203,15 @@ double lo_kv_cache_bytes(double layers, double heads, double head_dim, double se
  *   out      [nq][hq][d]   fp64
  * Returns 0, or -1 on a malformed layout.
  */
+/* ALiBi: with alibi[hq] given, every score of q-head h also gets the linear bias
+ * -alibi[h] * (m - n) for a key at absolute position n and a query at m (the bias is
+ * added to the scaled score, before the softmax). NULL: no bias. */
 int lo_attention_partial(int num_seqs, int hq, int hkv, int d, int rot_dims, double theta, const double *freqs,
                          int interleaved, double sm_scale, int dtype, int nq, const void *q, const int32_t *q_seq,
                          const int32_t *q_m, const void *k_pool, const void *v_pool, int64_t num_pool_blocks,
                          const int32_t *seg_indptr, const int32_t *seg_doc, const int32_t *seg_len,
                          const int32_t *seq_pos0, const int32_t *doc_block_indptr, const int32_t *doc_blocks,
-                         double *out) {
+                         const double *alibi, double *out) {
   if (hkv <= 0 || hq % hkv != 0 || d <= 0 || d % 2 != 0) return -1;
   if (rot_dims <= 0) rot_dims = d;
   if (rot_dims > d || rot_dims % 2 != 0) return -1;
@@ -278,6 +282,7 @@ int lo_attention_partial(int num_seqs, int hq, int hkv, int d, int rot_dims, dou
           double acc = 0.0;
           for (int c = 0; c < d; c++) acc += qr[c] * Kadj[j * d + c];
           sc[j] = acc * sm_scale;
+          if (alibi) sc[j] -= alibi[h] * (double)(m - pos[j]);
           if (sc[j] > mx) mx = sc[j];
         }
         double *o = &out[((int64_t)r * hq + h) * d];
@@ -306,7 +311,7 @@ int lo_attention_ex(int num_seqs, int hq, int hkv, int d, double theta, const do
                     const int32_t *doc_block_indptr, const int32_t *doc_blocks, double *out) {
   return lo_attention_partial(num_seqs, hq, hkv, d, d, theta, freqs, interleaved, sm_scale, dtype, nq, q, q_seq, q_m,
                               k_pool, v_pool, num_pool_blocks, seg_indptr, seg_doc, seg_len, seq_pos0,
-                              doc_block_indptr, doc_blocks, out);
+                              doc_block_indptr, doc_blocks, NULL, out);
 }
 
 int lo_attention(int num_seqs, int hq, int hkv, int d, double theta, double sm_scale, int dtype, int nq,

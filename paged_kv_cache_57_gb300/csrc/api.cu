@@ -445,13 +445,15 @@ size_t lazy_attn_decode_shared_workspace_bytes(const lazy_attn_params* p, int32_
   return bytes;
 }
 
-int lazy_attn_decode_shared(const lazy_attn_params* p, const void* q, const void* k_pool, const void* v_pool,
-                            const uint32_t* block_words, const int32_t* q_pos, const void* rope_table,
-                            int32_t num_items, const int32_t* items, int32_t num_slots, const int32_t* slot_indptr,
-                            void* out, void* workspace, size_t workspace_bytes, lazy_stream_t stream) {
+static int decode_shared_impl(const lazy_attn_params* p, const void* q, const void* k_pool, const void* v_pool,
+                              const uint32_t* block_words, const int32_t* q_pos, const void* rope_table,
+                              int32_t num_items, const int32_t* items, int32_t num_slots, const int32_t* slot_indptr,
+                              const float* alibi, void* out, void* workspace, size_t workspace_bytes,
+                              lazy_stream_t stream) {
   Checked c;
   int rc = check_params(p, &c);
   if (rc != LAZY_OK) return rc;
+  if (alibi && (!p->lazy || (reinterpret_cast<uintptr_t>(alibi) & 3u))) return LAZY_ERR_INVALID_ARG;
   if (p->dtype != LAZY_BF16) return LAZY_ERR_UNSUPPORTED;
   if (c.G > 64) return LAZY_ERR_UNSUPPORTED;
   if (num_items < 0 || num_slots < 0) return LAZY_ERR_INVALID_ARG;
@@ -498,16 +500,47 @@ int lazy_attn_decode_shared(const lazy_attn_params* p, const void* q, const void
       if (!encode_rows_map(&kmap, k_pool, rows, p->head_dim, lazy::kBlock) ||
           !encode_rows_map(&vmap, v_pool, rows, p->head_dim, lazy::kBlock))
         return LAZY_ERR_CUDA;
-      rc = launched(lazy::launch_decode_shared_tc(a, p->lazy != 0, kmap, vmap, cs));
+      rc = launched(lazy::launch_decode_shared_tc(a, alibi, p->lazy != 0, kmap, vmap, cs));
     } else {
       if (!encode_block_map(&kmap, k_pool, rows, p->head_dim, lazy::kBlock) ||
           !encode_block_map(&vmap, v_pool, rows, p->head_dim, lazy::kBlock))
         return LAZY_ERR_CUDA;
-      rc = launched(lazy::launch_decode_shared(a, p->lazy != 0, kmap, vmap, cs));
+      rc = launched(lazy::launch_decode_shared(a, alibi, p->lazy != 0, kmap, vmap, cs));
     }
     if (rc != LAZY_OK) return rc;
   }
   return launched(lazy::launch_shared_combine(a, cs));
+}
+
+int lazy_attn_decode_shared(const lazy_attn_params* p, const void* q, const void* k_pool, const void* v_pool,
+                            const uint32_t* block_words, const int32_t* q_pos, const void* rope_table,
+                            int32_t num_items, const int32_t* items, int32_t num_slots, const int32_t* slot_indptr,
+                            void* out, void* workspace, size_t workspace_bytes, lazy_stream_t stream) {
+  return decode_shared_impl(p, q, k_pool, v_pool, block_words, q_pos, rope_table, num_items, items, num_slots,
+                            slot_indptr, nullptr, out, workspace, workspace_bytes, stream);
+}
+
+int lazy_attn_decode_shared_alibi(const lazy_attn_params* p, const void* q, const void* k_pool, const void* v_pool,
+                                  const uint32_t* block_words, const int32_t* q_pos, const void* rope_table,
+                                  int32_t num_items, const int32_t* items, int32_t num_slots,
+                                  const int32_t* slot_indptr, const float* alibi_slopes, void* out, void* workspace,
+                                  size_t workspace_bytes, lazy_stream_t stream) {
+  if (!alibi_slopes) return LAZY_ERR_INVALID_ARG;
+  return decode_shared_impl(p, q, k_pool, v_pool, block_words, q_pos, rope_table, num_items, items, num_slots,
+                            slot_indptr, alibi_slopes, out, workspace, workspace_bytes, stream);
+}
+
+int lazy_attn_alibi_slopes_host(int32_t num_heads, float* out) {
+  if (num_heads < 1 || num_heads > 4096 || !out) return LAZY_ERR_INVALID_ARG;
+  // Geometric slopes 2^(-8 i / n), i = 1..n, for n a power of two; otherwise those of
+  // the largest power of two n' below num_heads, then every other slope of 2 n'
+  // (the odd-indexed ones) for the remaining heads.
+  int np2 = 1;
+  while (2 * np2 <= num_heads) np2 *= 2;
+  for (int i = 0; i < np2; ++i) out[i] = (float)std::exp2(-8.0 * (double)(i + 1) / (double)np2);
+  for (int k = 0; np2 + k < num_heads; ++k)
+    out[np2 + k] = (float)std::exp2(-8.0 * (double)(2 * k + 1) / (double)(2 * np2));
+  return LAZY_OK;
 }
 
 // The two-tile prefill (even GQA ratio) runs one persistent CTA per SM and needs a

@@ -70,10 +70,12 @@ constexpr float kDecodeRescaleLog2 = 8.f;
 // layout). The query fragments carry the softmax scale and log2(e), so scores
 // come out in log2 units. Only the first `nvalid` slots of the block are keys;
 // the others (holes, an unloaded block) get weight 0 and their V rows are masked
-// out of the product.
-template <int D>
-__device__ __forceinline__ void attend_block(uint32_t kbase, LdsmLane ln, const uint32_t (&qa)[D / 16][4], int nvalid,
-                                             float (&o)[D / 8][4], float (&m_r)[2], float (&l_r)[2], int lane) {
+// out of the product. With BIAS, row g + 8 rr's score of key k also gets
+// bias0[rr] + slope[rr] * k (log2 units; the ALiBi bias of the shared-run decode).
+template <int D, bool BIAS>
+__device__ __forceinline__ void attend_block_impl(uint32_t kbase, LdsmLane ln, const uint32_t (&qa)[D / 16][4],
+                                                  int nvalid, float (&o)[D / 8][4], float (&m_r)[2], float (&l_r)[2],
+                                                  int lane, const float* bias0, const float* slope) {
   using G = BlockGeom<D>;
   const int t = lane & 3;
   const uint32_t ka = kbase + ln.k;
@@ -98,6 +100,12 @@ __device__ __forceinline__ void attend_block(uint32_t kbase, LdsmLane ln, const 
   for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
     for (int e = 0; e < 4; ++e) sv[rr][e] = sc[e >> 1][0][2 * rr + (e & 1)] + sc[e >> 1][1][2 * rr + (e & 1)];
+  if constexpr (BIAS) {
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sv[rr][e] += fmaf(slope[rr], (float)((e >> 1) * 8 + 2 * t + (e & 1)), bias0[rr]);
+  }
   const bool partial = nvalid < kBlock;  // warp-uniform
   if (partial) {
 #pragma unroll
@@ -152,6 +160,19 @@ __device__ __forceinline__ void attend_block(uint32_t kbase, LdsmLane ln, const 
       mma_16816(o[2 * c + 1], pa, r[2] & m0, r[3] & m1);
     }
   }
+}
+
+template <int D>
+__device__ __forceinline__ void attend_block(uint32_t kbase, LdsmLane ln, const uint32_t (&qa)[D / 16][4], int nvalid,
+                                             float (&o)[D / 8][4], float (&m_r)[2], float (&l_r)[2], int lane) {
+  attend_block_impl<D, false>(kbase, ln, qa, nvalid, o, m_r, l_r, lane, nullptr, nullptr);
+}
+
+template <int D>
+__device__ __forceinline__ void attend_block_bias(uint32_t kbase, LdsmLane ln, const uint32_t (&qa)[D / 16][4],
+                                                  int nvalid, float (&o)[D / 8][4], float (&m_r)[2], float (&l_r)[2],
+                                                  int lane, const float (&bias0)[2], const float (&slope)[2]) {
+  attend_block_impl<D, true>(kbase, ln, qa, nvalid, o, m_r, l_r, lane, bias0, slope);
 }
 
 // Per-lane description of one logical block: physical id (num_pool_blocks for a

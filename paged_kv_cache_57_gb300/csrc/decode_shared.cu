@@ -19,6 +19,7 @@
 // (member, query head) writes one fp32 partial (m, l, o) to its slot; the
 // combine kernel merges a sequence's slots with the online-softmax rescale.
 #include <cfloat>
+#include <type_traits>
 
 #include "decode_block.cuh"
 #include "kernels.h"
@@ -90,10 +91,10 @@ __device__ __forceinline__ void load_block_3d(uint8_t* stage, uint64_t* bar, int
   } while (0)
 #endif
 
-template <int D, bool LAZY>
+template <int D, bool LAZY, bool ALIBI>
 __global__ void __launch_bounds__(kShThreads, 3)
-    decode_shared_kernel(const SharedDecodeArgs a, const __grid_constant__ CUtensorMap kmap,
-                         const __grid_constant__ CUtensorMap vmap) {
+    decode_shared_kernel(const std::conditional_t<ALIBI, SharedAlibiArgs, SharedDecodeArgs> a,
+                         const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
   using C = SharedCfg<D>;
   using G = BlockGeom<D>;
   constexpr int HALF = D / 2;
@@ -278,6 +279,23 @@ __global__ void __launch_bounds__(kShThreads, 3)
       }
   }
   LAZY_TRACE(2, global_timer_ns());
+  // ALiBi: row r's scores get slope_r (n - m) in log2 units, n = p + j the key's
+  // position, m the query's: slope_r (j - delta_r) with j = 16 (c0 + kb) + k for key k
+  // of the item's block kb (c0: the item's first block within its document).
+  float ab_slope[2] = {0.f, 0.f};
+  int ab_delta[2] = {0, 0}, item_c0 = 0;
+  if constexpr (ALIBI) {
+    item_c0 = rec[5];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int r = rt * 16 + g + 8 * rr;
+      const int m = r / a.G, h = r - m * a.G;
+      if (r < rows && m_ok[m]) {
+        ab_slope[rr] = __ldg(&a.alibi[kvh * a.G + h]) * 1.4426950408889634f;
+        ab_delta[rr] = m_delta[m];
+      }
+    }
+  }
 
   // ------------------------------------------------------------ main loop
   float o[D / 8][4];
@@ -296,7 +314,15 @@ __global__ void __launch_bounds__(kShThreads, 3)
     const int slot = k % NS;
     const int nvalid = __shfl_sync(0xffffffffu, cur_nv, k & 31);
     bool ok = warp_wait(&tfull[slot], (k / NS) & 1, a.status);
-    if (ok) attend_block<D>(smem_u32(tst + slot * G::STAGE_BYTES), ln, qa, nvalid, o, m_r, l_r, lane);
+    if (ok) {
+      if constexpr (ALIBI) {
+        const int j0 = kBlock * (item_c0 + kb0 + k);
+        const float b0[2] = {ab_slope[0] * (float)(j0 - ab_delta[0]), ab_slope[1] * (float)(j0 - ab_delta[1])};
+        attend_block_bias<D>(smem_u32(tst + slot * G::STAGE_BYTES), ln, qa, nvalid, o, m_r, l_r, lane, b0, ab_slope);
+      } else {
+        attend_block<D>(smem_u32(tst + slot * G::STAGE_BYTES), ln, qa, nvalid, o, m_r, l_r, lane);
+      }
+    }
     // The team's warps are all done with this stage (and agree to go on) before it is refilled.
     if (RT > 1) ok = team_and(team, 32 * RT, ok);
     if (!ok) {
@@ -488,23 +514,39 @@ __global__ void shared_combine_kernel(const SharedDecodeArgs a) {
 
 // ------------------------------------------------------------------ launchers
 
-template <int D, bool LAZY>
-static cudaError_t launch_shared_t(const SharedDecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                   cudaStream_t st) {
+template <int D, bool LAZY, bool ALIBI>
+static cudaError_t launch_shared_t(const SharedDecodeArgs& a, const float* alibi, const CUtensorMap& kmap,
+                                   const CUtensorMap& vmap, cudaStream_t st) {
   using C = SharedCfg<D>;
-  auto kern = decode_shared_kernel<D, LAZY>;
-  cudaError_t e = set_smem_once<decode_shared_kernel<D, LAZY>>(C::SMEM);
+  auto kern = decode_shared_kernel<D, LAZY, ALIBI>;
+  cudaError_t e = set_smem_once<decode_shared_kernel<D, LAZY, ALIBI>>(C::SMEM);
   if (e != cudaSuccess) return e;
   const long long blocks = (long long)a.num_items * a.Hkv;
-  kern<<<(unsigned)blocks, kShThreads, C::SMEM, st>>>(a, kmap, vmap);
+  if constexpr (ALIBI) {
+    SharedAlibiArgs aa;
+    static_cast<SharedDecodeArgs&>(aa) = a;
+    aa.alibi = alibi;
+    kern<<<(unsigned)blocks, kShThreads, C::SMEM, st>>>(aa, kmap, vmap);
+  } else {
+    (void)alibi;
+    kern<<<(unsigned)blocks, kShThreads, C::SMEM, st>>>(a, kmap, vmap);
+  }
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode_shared(const SharedDecodeArgs& a, bool lazy, const CUtensorMap& kmap,
+cudaError_t launch_decode_shared(const SharedDecodeArgs& a, const float* alibi, bool lazy, const CUtensorMap& kmap,
                                  const CUtensorMap& vmap, cudaStream_t st) {
   if (a.num_items == 0) return cudaSuccess;
-  if (a.D == 128) return lazy ? launch_shared_t<128, true>(a, kmap, vmap, st) : launch_shared_t<128, false>(a, kmap, vmap, st);
-  return lazy ? launch_shared_t<64, true>(a, kmap, vmap, st) : launch_shared_t<64, false>(a, kmap, vmap, st);
+  if (alibi) {  // ALiBi needs the members' positions: lazy mode only
+    if (!lazy) return cudaErrorInvalidValue;
+    return a.D == 128 ? launch_shared_t<128, true, true>(a, alibi, kmap, vmap, st)
+                      : launch_shared_t<64, true, true>(a, alibi, kmap, vmap, st);
+  }
+  if (a.D == 128)
+    return lazy ? launch_shared_t<128, true, false>(a, nullptr, kmap, vmap, st)
+                : launch_shared_t<128, false, false>(a, nullptr, kmap, vmap, st);
+  return lazy ? launch_shared_t<64, true, false>(a, nullptr, kmap, vmap, st)
+              : launch_shared_t<64, false, false>(a, nullptr, kmap, vmap, st);
 }
 
 cudaError_t launch_shared_combine(const SharedDecodeArgs& a, cudaStream_t st) {

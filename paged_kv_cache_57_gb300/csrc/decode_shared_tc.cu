@@ -29,6 +29,7 @@
 // disagrees with the item record, get weight 0 and their V rows are zeroed (a
 // pool slot that holds no key may hold anything, NaN included).
 #include <cfloat>
+#include <type_traits>
 
 #include "prefill_common.cuh"
 
@@ -91,10 +92,10 @@ static_assert(kItemInts % 4 == 0 && kItemInts / 4 <= kTcThreads, "item record la
 #define LAZY_TC_ACC(acc, a0, a1)
 #endif
 
-template <bool LAZY>
+template <bool LAZY, bool ALIBI>
 __global__ void __launch_bounds__(kTcThreads, 2)
-    decode_shared_tc_kernel(const SharedDecodeArgs a, const __grid_constant__ CUtensorMap kmap,
-                            const __grid_constant__ CUtensorMap vmap) {
+    decode_shared_tc_kernel(const std::conditional_t<ALIBI, SharedAlibiArgs, SharedDecodeArgs> a,
+                            const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = pf::align1024(smem_raw);
   uint8_t* sQ = base + OFF_Q;
@@ -334,6 +335,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (i == 0) LAZY_TC_TRACE(1, global_timer_ns());
 
     const uint32_t tO = tmem + kColO + lane_base;
+    // ALiBi: this row's scores get slope (n - m) in log2 units, n = p + j the key's
+    // position, m the query's: slope (j - delta) with j = 16 (c0 + 4 jt) + c for column
+    // c of tile jt (c0: the item's first block within its document).
+    float ab_slope = 0.f;
+    int ab_delta = 0;
+    if constexpr (ALIBI) {
+      if (row_in && m_ok[m]) {
+        ab_slope = __ldg(&a.alibi[kvh * a.G + hh]) * 1.4426950408889634f;
+        ab_delta = m_delta[m];
+      }
+    }
+    const int item_c0 = rec[5];
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     long long c_s = 0, c_c = 0, c_pv = 0, c_st = 0;
@@ -381,6 +394,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         tmem_ld32(tS, sv[0]);
         tmem_ld32(tS + 32, sv[1]);
         tmem_ld_wait(sv[0], sv[1]);
+        if constexpr (ALIBI) {
+          const float base = ab_slope * (float)(kBlock * (item_c0 + kTcBlocks * j) - ab_delta);
+#pragma unroll
+          for (int c = 0; c < kTcKeys; ++c) sv[c >> 5][c & 31] += fmaf(ab_slope, (float)c, base);
+        }
         if (!full_tile) {
 #pragma unroll
           for (int c = 0; c < kTcKeys; ++c)
@@ -523,15 +541,25 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   }
 }
 
-cudaError_t launch_decode_shared_tc(const SharedDecodeArgs& a, bool lazy, const CUtensorMap& kmap,
-                                    const CUtensorMap& vmap, cudaStream_t st) {
+cudaError_t launch_decode_shared_tc(const SharedDecodeArgs& a, const float* alibi, bool lazy,
+                                    const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t st) {
   if (a.D != kTcD) return cudaErrorNotSupported;
   if (a.num_items == 0) return cudaSuccess;
-  cudaError_t e = lazy ? set_smem_once<decode_shared_tc_kernel<true>>(SMEM)
-                       : set_smem_once<decode_shared_tc_kernel<false>>(SMEM);
-  if (e != cudaSuccess) return e;
   const long long blocks = (long long)a.num_items * a.Hkv;
-  auto kern = lazy ? decode_shared_tc_kernel<true> : decode_shared_tc_kernel<false>;
+  if (alibi) {
+    if (!lazy) return cudaErrorInvalidValue;  // ALiBi needs the members' positions
+    cudaError_t e = set_smem_once<decode_shared_tc_kernel<true, true>>(SMEM);
+    if (e != cudaSuccess) return e;
+    SharedAlibiArgs aa;
+    static_cast<SharedDecodeArgs&>(aa) = a;
+    aa.alibi = alibi;
+    decode_shared_tc_kernel<true, true><<<(unsigned)blocks, kTcThreads, SMEM, st>>>(aa, kmap, vmap);
+    return cudaGetLastError();
+  }
+  cudaError_t e = lazy ? set_smem_once<decode_shared_tc_kernel<true, false>>(SMEM)
+                       : set_smem_once<decode_shared_tc_kernel<false, false>>(SMEM);
+  if (e != cudaSuccess) return e;
+  auto kern = lazy ? decode_shared_tc_kernel<true, false> : decode_shared_tc_kernel<false, false>;
   kern<<<(unsigned)blocks, kTcThreads, SMEM, st>>>(a, kmap, vmap);
   return cudaGetLastError();
 }

@@ -104,6 +104,11 @@ struct SharedDecodeArgs {
   int num_items, num_slots;
   float scale_log2;
 };
+// The ALiBi variants' arguments: the same and the slopes. (A separate type keeps the
+// other kernels' argument block, and so their register allocation, unchanged.)
+struct SharedAlibiArgs : SharedDecodeArgs {
+  const float* alibi;  // [Hq] slopes
+};
 
 // Eager materialisation (materialize.cu): per-sequence copies with K at absolute positions.
 struct MaterializeArgs {
@@ -170,10 +175,11 @@ int prefill_stream_grid();
 cudaError_t launch_prefill_tq(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
                               const CUtensorMap& vmap, cudaStream_t st);
 
-cudaError_t launch_decode_shared(const SharedDecodeArgs& a, bool lazy, const CUtensorMap& kmap,
+// alibi: null, or [Hq] ALiBi slopes (lazy mode only).
+cudaError_t launch_decode_shared(const SharedDecodeArgs& a, const float* alibi, bool lazy, const CUtensorMap& kmap,
                                  const CUtensorMap& vmap, cudaStream_t st);
-cudaError_t launch_decode_shared_tc(const SharedDecodeArgs& a, bool lazy, const CUtensorMap& kmap,
-                                    const CUtensorMap& vmap, cudaStream_t st);
+cudaError_t launch_decode_shared_tc(const SharedDecodeArgs& a, const float* alibi, bool lazy,
+                                    const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t st);
 cudaError_t launch_shared_combine(const SharedDecodeArgs& a, cudaStream_t st);
 
 // Shared-memory bytes a bf16 decode CTA needs (for occupancy-based split planning).

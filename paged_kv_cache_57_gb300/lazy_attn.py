@@ -35,7 +35,7 @@ EXPORTED = (
     "lazy_attn_device_status", "lazy_attn_launch_count", "lazy_attn_debug_rope", "lazy_attn_decode_noalloc",
     "lazy_attn_plan_shared_host", "lazy_attn_decode_shared_workspace_bytes", "lazy_attn_decode_shared",
     "lazy_attn_materialize", "lazy_attn_rope_table_init_scaled", "lazy_attn_rope_table_init_freqs",
-    "lazy_attn_rotary_layout_host",
+    "lazy_attn_rotary_layout_host", "lazy_attn_decode_shared_alibi", "lazy_attn_alibi_slopes_host",
 )
 PLAN_MAX_MEMBERS = 16
 PLAN_ITEM_BLOCK_IDS = 32
@@ -84,6 +84,9 @@ _sig = {
     "lazy_attn_decode_shared_workspace_bytes": (_sz, [_P, _i32]),
     "lazy_attn_materialize": (ctypes.c_int, [_P] + [_vp] * 8 + [_vp]),
     "lazy_attn_decode_shared": (ctypes.c_int, [_P] + [_vp] * 6 + [_i32, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "lazy_attn_decode_shared_alibi": (ctypes.c_int,
+                                      [_P] + [_vp] * 6 + [_i32, _vp, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "lazy_attn_alibi_slopes_host": (ctypes.c_int, [_i32, _vp]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -306,7 +309,9 @@ def decode_shared_workspace_bytes(p: Params, num_slots: int) -> int:
 
 def decode_shared(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, block_words: torch.Tensor,
                   q_pos: torch.Tensor, rope_table: torch.Tensor, plan: SharedPlan, out: Optional[torch.Tensor] = None,
-                  workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                  workspace: Optional[torch.Tensor] = None, stream=None,
+                  alibi_slopes: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Shared-run decode; ``alibi_slopes`` (device fp32 [Hq]) selects the ALiBi call."""
     dt = _tdt(p)
     if out is None:
         out = torch.empty_like(q)
@@ -316,13 +321,25 @@ def decode_shared(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torc
             workspace = torch.empty(nws, dtype=torch.uint8, device=q.device)
     wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
     i32 = torch.int32
-    rc = _lib.lazy_attn_decode_shared(ctypes.byref(p), _dptr(q, "q", dt), _dptr(k_pool, "k_pool", dt),
-                                      _dptr(v_pool, "v_pool", dt), _dptr(block_words, "block_words"),
-                                      _dptr(q_pos, "q_pos", i32), _dptr(rope_table, "rope_table"), plan.num_items,
-                                      _dptr(plan.items, "items", i32), plan.num_slots,
-                                      _dptr(plan.slot_indptr, "slot_indptr", i32), _dptr(out, "out", dt),
-                                      _dptr(workspace, "workspace"), wsz, _stream(stream))
+    args = (ctypes.byref(p), _dptr(q, "q", dt), _dptr(k_pool, "k_pool", dt), _dptr(v_pool, "v_pool", dt),
+            _dptr(block_words, "block_words"), _dptr(q_pos, "q_pos", i32), _dptr(rope_table, "rope_table"),
+            plan.num_items, _dptr(plan.items, "items", i32), plan.num_slots,
+            _dptr(plan.slot_indptr, "slot_indptr", i32))
+    tail = (_dptr(out, "out", dt), _dptr(workspace, "workspace"), wsz, _stream(stream))
+    if alibi_slopes is None:
+        rc = _lib.lazy_attn_decode_shared(*args, *tail)
+    else:
+        if alibi_slopes.numel() != p.num_q_heads:
+            raise ValueError("alibi_slopes needs one slope per query head")
+        rc = _lib.lazy_attn_decode_shared_alibi(*args, _dptr(alibi_slopes, "alibi_slopes", torch.float32), *tail)
     _check(rc, "decode_shared")
+    return out
+
+
+def alibi_slopes(num_heads: int) -> np.ndarray:
+    """The usual ALiBi slopes (lazy_attn_alibi_slopes_host), fp32 [num_heads]."""
+    out = np.empty(num_heads, np.float32)
+    _check(_lib.lazy_attn_alibi_slopes_host(int(num_heads), out.ctypes.data), "alibi_slopes")
     return out
 
 

@@ -27,9 +27,10 @@ def _bf16(x):
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
 
 
-def emulate(w, rows, lazy: bool = True, k_pool=None, freqs=None) -> np.ndarray:
+def emulate(w, rows, lazy: bool = True, k_pool=None, freqs=None, alibi=None) -> np.ndarray:
     """[len(rows), Hq, d] for query rows ``rows`` of workload ``w`` (``freqs``: rotation
-    frequencies other than theta^(-2i/d))."""
+    frequencies other than theta^(-2i/d); ``alibi``: per-head slopes of the bias
+    -slope (m - n), added in fp32 to the scores before the exponentials)."""
     kp = (w.k_pool if k_pool is None else k_pool).double().numpy()
     vp = w.v_pool.double().numpy()
     q = w.q.double().numpy()
@@ -72,6 +73,8 @@ def emulate(w, rows, lazy: bool = True, k_pool=None, freqs=None) -> np.ndarray:
                 sc = np.array([qd[P[j]] @ kh[j] for j in range(len(P))])
             else:
                 sc = kh @ _bf16(rope(q[r, h], m, theta, freqs) * scale)
+            if alibi is not None:
+                sc = sc - float(alibi[h]) * np.log2(np.e) * (m - pos[vis])
             e = _bf16(np.exp2(sc - sc.max()))
             out[oi, h] = (e[:, None] * V[:, h // g]).sum(0) / e.sum()
     return _bf16(out)

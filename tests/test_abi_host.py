@@ -207,7 +207,16 @@ def test_shared_plan_covers_every_block_once(la, w, chunk):
     for it in items:
         src, b0, nb, last, nm = (int(x) for x in it[:5])
         ids = it[8 + 4 * la.PLAN_MAX_MEMBERS:]
-        assert (it[5:8] == 0).all() and (it[8 + 4 * nm: 8 + 4 * la.PLAN_MAX_MEMBERS] == 0).all()
+        assert (it[6:8] == 0).all() and (it[8 + 4 * nm: 8 + 4 * la.PLAN_MAX_MEMBERS] == 0).all()
+        # [5]: the item's first block within its document, whose start is the member's segment start
+        seg_first = {}
+        bpos = 0
+        for doc, ln in w.seq_segments(src):
+            nbk = -(-ln // 16)
+            for q in range(nbk):
+                seg_first[bpos + q] = bpos
+            bpos += nbk
+        assert int(it[5]) == b0 - seg_first[b0]
         assert 1 <= nm <= la.PLAN_MAX_MEMBERS and nm * G <= rows_cap
         cost.append(nb)
         assert nb <= (chunk or (256 if rows_cap == 128 else 32))

@@ -138,3 +138,27 @@ def test_prefill_partial_rotary(hq, hkv):
     ref = oracle.attention(w, rot_dims=64)
     wp, dv, freqs = _partial_device(w, 64)
     assert_close(prefill(dv), ref, "bf16", "prefill, partial rotary", emulate=lambda r: emulate(wp, r, freqs=freqs))
+
+
+# ---------------------------------------------------------------- ALiBi
+# No rotation (a zero-rate table) and the bias -slope_h (m - n) formed in the
+# shared-run kernels from the members' document starts and the items' first blocks.
+
+@pytest.mark.parametrize("hq,hkv,chunk", [(8, 8, 0), (8, 2, 3), (16, 2, 0), (32, 1, 5)])
+def test_shared_decode_alibi(hq, hkv, chunk):
+    # 1 and 4 query heads per KV head: the mma.sync kernel; 8 and 32: the tcgen05 one.
+    # Chunks of 3 or 5 blocks start items inside documents (c0 > 0).
+    L = la()
+    w = W.decode_zipf(f"valibi{hq}", batch=8, hq=hq, hkv=hkv, d=128, docs_per_seq=3, doc_tokens=170, pool_docs=3,
+                      zipf_s=1.0, suffix_tokens=13, seed=320 + hq)
+    slopes = L.alibi_slopes(hq)
+    ref = oracle.attention(w, freqs=np.zeros(64), alibi=slopes.astype(np.float64))
+    dv = to_device(w)
+    dv.rope = L.rope_table_init(dv.p, freqs=np.zeros(64))
+    plan = shared_plan(dv, chunk)
+    out = L.decode_shared(dv.p, dv.q, dv.k_pool, dv.v_pool, dv.words, dv.q_pos, dv.rope, plan,
+                          alibi_slopes=torch.from_numpy(slopes).cuda())
+    assert_close(out, ref, "bf16", f"shared decode, ALiBi, {hq}/{hkv}",
+                 emulate=lambda r: emulate(w, r, freqs=np.zeros(64), alibi=slopes))
+    # the bias matters at these positions
+    assert np.abs(ref - oracle.attention(w, freqs=np.zeros(64))).max() > 1e-2

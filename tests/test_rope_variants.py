@@ -202,3 +202,64 @@ def test_rotary_layout_and_explicit_rates_argument_checks():
         f[3] = bad
         rc = L._lib.lazy_attn_rope_table_init_freqs(ctypes.byref(p), f.ctypes.data, fake, 1 << 20, None)
         assert rc == L.LAZY_ERR_INVALID_ARG, bad
+
+
+# ---------------------------------------------------------------- ALiBi
+
+def _alibi_w(shift=0, hq=4, hkv=2):
+    return W.decode_zipf("ralibi", batch=3, hq=hq, hkv=hkv, d=64, docs_per_seq=3, doc_tokens=40, pool_docs=4,
+                         zipf_s=1.0, suffix_tokens=5, dtype="f32", theta=1e4, seed=213, shift=shift)
+
+
+def test_alibi_zero_slopes_is_no_bias():
+    w = _alibi_w()
+    zero = np.zeros(w.head_dim // 2)
+    assert np.array_equal(oracle.attention(w, freqs=zero, alibi=np.zeros(w.num_q_heads)),
+                          oracle.attention(w, freqs=zero))
+
+
+def test_alibi_depends_only_on_relative_positions():
+    slopes = np.array([0.5, 0.25, 0.125, 0.0625])
+    zero = np.zeros(32)
+    a = oracle.attention(_alibi_w(), freqs=zero, alibi=slopes)
+    b = oracle.attention(_alibi_w(shift=777), freqs=zero, alibi=slopes)
+    assert np.allclose(a, b, atol=1e-12)
+    assert np.abs(a - oracle.attention(_alibi_w(), freqs=zero)).max() > 1e-3
+
+
+def test_alibi_steep_slope_selects_the_most_recent_key():
+    # slope -> infinity: all weight on the key nearest the query (position m - 1 in decode)
+    w = _alibi_w()
+    out = oracle.attention(w, freqs=np.zeros(32), alibi=np.full(w.num_q_heads, 1e4))
+    for s in range(w.num_seqs):
+        doc, ln = w.seq_segments(s)[-1]
+        phys = int(w.doc_blocks[w.doc_block_indptr[doc] + (ln - 1) // 16])
+        for h in range(w.num_q_heads):
+            v_last = w.v_pool[phys, h // (w.num_q_heads // w.num_kv_heads), (ln - 1) % 16].double().numpy()
+            assert np.allclose(out[s, h], v_last, atol=1e-12)
+
+
+def test_alibi_slopes_closed_form():
+    from paged_kv_cache_57_gb300 import lazy_attn as L
+    assert np.array_equal(L.alibi_slopes(8), np.float32(2.0) ** -np.arange(1, 9, dtype=np.float32))
+    s12 = L.alibi_slopes(12)  # 8 of the 8-head sequence, then the odd-indexed slopes of 16 heads
+    assert np.array_equal(s12[:8], L.alibi_slopes(8))
+    assert np.allclose(s12[8:], 2.0 ** -(np.arange(4) + 0.5), rtol=1e-7)
+    with pytest.raises(L.LazyAttnError):
+        L.alibi_slopes(0)
+
+
+def test_alibi_decode_rejects_the_control_path_without_cuda():
+    from paged_kv_cache_57_gb300 import lazy_attn as L
+    w = _alibi_w()
+    p = L.make_params(num_seqs=w.num_seqs, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                      head_dim=w.head_dim, num_pool_blocks=w.num_pool_blocks, max_blocks_per_seq=w.max_blocks_per_seq,
+                      dtype="bf16", rope_theta=w.rope_theta, lazy=False)
+    fake = ctypes.c_void_p(4096)  # never dereferenced: the arguments are rejected first
+    rc = L._lib.lazy_attn_decode_shared_alibi(ctypes.byref(p), *([fake] * 6), 1, fake, 1, fake, fake, fake, fake,
+                                              1 << 20, None)
+    assert rc == L.LAZY_ERR_INVALID_ARG
+    p.lazy = 1
+    rc = L._lib.lazy_attn_decode_shared_alibi(ctypes.byref(p), *([fake] * 6), 1, fake, 1, fake, None, fake, fake,
+                                              1 << 20, None)
+    assert rc == L.LAZY_ERR_INVALID_ARG  # no slopes
