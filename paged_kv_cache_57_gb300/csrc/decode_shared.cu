@@ -440,7 +440,7 @@ __global__ void __launch_bounds__(kShThreads, 3)
 // out[s][h] = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k over the sequence's
 // slots k in [slot_indptr[s], slot_indptr[s+1]); a sequence without slots gets 0.
 // One warp per (sequence, query head), D/32 output columns per lane. Slots are
-// taken BATCH (8 or 16) at a time with all their loads issued together (one
+// taken BATCH (12 or 16) at a time with all their loads issued together (one
 // memory round trip per batch), folded in with the online rescale of the running
 // maximum. Launched as a programmatic dependent of the decode kernel: its CTAs
 // may become resident while the decode kernel's last CTAs run, and wait for the
@@ -562,14 +562,14 @@ cudaError_t launch_shared_combine(const SharedDecodeArgs& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // Slots per round trip: 16 when sequences hold many slots (fewer round trips), else
-  // 8 (fewer registers: two CTAs per SM).
+  // Slots per round trip: 12 when sequences hold at most 12 slots on average (one
+  // round trip for most, two CTAs per SM), else 16 (fewer round trips).
   const bool wide = (long long)a.num_slots > 12LL * a.B;
   if (a.D == 128)
     return wide ? cudaLaunchKernelEx(&cfg, shared_combine_kernel<128, 16>, a)
-                : cudaLaunchKernelEx(&cfg, shared_combine_kernel<128, 8>, a);
+                : cudaLaunchKernelEx(&cfg, shared_combine_kernel<128, 12>, a);
   return wide ? cudaLaunchKernelEx(&cfg, shared_combine_kernel<64, 16>, a)
-              : cudaLaunchKernelEx(&cfg, shared_combine_kernel<64, 8>, a);
+              : cudaLaunchKernelEx(&cfg, shared_combine_kernel<64, 12>, a);
 }
 
 }  // namespace lazy
