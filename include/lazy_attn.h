@@ -104,6 +104,12 @@ typedef struct {
   double rope_theta;          /* 1e4, 5e5, ... */
   float sm_scale;             /* softmax scale; 0 selects 1/sqrt(head_dim) */
   int32_t num_splits;         /* decode split-K factor; 0 = choose from the shapes and SM count */
+  int32_t key_positions;      /* 0: a block word's offset is taken from its document's start p
+                                 (RoPE). 1: from the position of the block's first key, so every
+                                 key's absolute position is the word's position plus its slot
+                                 (ALiBi). The packers write either form; the ALiBi calls require
+                                 1, every other attention call and the materialiser require 0
+                                 (LAZY_ERR_INVALID_ARG) */
 } lazy_attn_params;
 
 /* Human-readable name of a lazy_status value. Never NULL. */
@@ -289,17 +295,19 @@ int lazy_attn_decode_shared(const lazy_attn_params *p, const void *q, const void
 
 /* ALiBi ("Resumo Técnico: LazyAttention", "Principais Contribuições", item 4: the
  * mechanism carries over to relative position encodings such as ALiBi): the same
- * call with every score of query head h also biased by -alibi_slopes[h] * (m - n)
- * before the softmax, for a key at absolute position n (its document's start p plus
- * its index within the document) and the query at m = q_pos. Stored keys carry no
- * position, and the bias is formed on the fly from p (the block words), the item's
- * first block within its document (record field [5]) and the slot. ALiBi models do
- * not rotate q or k: pass a table built by lazy_attn_rope_table_init_freqs from zero
- * rates, which makes every rotation the identity. alibi_slopes: device fp32 [Hq],
- * 4-byte aligned; requires p->lazy = 1, else LAZY_ERR_INVALID_ARG. Only this
- * shared-run entry point takes ALiBi: the per-sequence decode and the prefill read
- * key positions from the block words, which do not carry a block's index within its
- * document. */
+ * calls with every score of query head h also biased by -alibi_slopes[h] * (m - n)
+ * before the softmax, for a key at absolute position n and the query at m = q_pos.
+ * Stored keys carry no position; n comes from the block words packed with
+ * p->key_positions = 1 (a block's word gives the position of its first key; n is
+ * that plus the slot), and the bias is formed on the fly. ALiBi models do not rotate
+ * q or k: pass a table built by lazy_attn_rope_table_init_freqs from zero rates (the
+ * calls do not rotate, whatever p->lazy says). alibi_slopes: device fp32 [Hq], 4-byte
+ * aligned; p->key_positions must be 1, else LAZY_ERR_INVALID_ARG. bf16 only. The
+ * prefill has no ALiBi form. */
+int lazy_attn_decode_alibi(const lazy_attn_params *p, const void *q, const void *k_pool, const void *v_pool,
+                           const uint32_t *block_words, const int32_t *seq_lens, const int32_t *q_pos,
+                           const void *rope_table, const float *alibi_slopes, void *out, void *workspace,
+                           size_t workspace_bytes, lazy_stream_t stream);
 int lazy_attn_decode_shared_alibi(const lazy_attn_params *p, const void *q, const void *k_pool, const void *v_pool,
                                   const uint32_t *block_words, const int32_t *q_pos, const void *rope_table,
                                   int32_t num_items, const int32_t *items, int32_t num_slots,

@@ -158,6 +158,7 @@ int check_params(const lazy_attn_params* p, Checked* c) {
   if (!(p->rope_theta > 0.0) || !std::isfinite(p->rope_theta)) return LAZY_ERR_INVALID_ARG;
   if (!(p->sm_scale >= 0.f) || !std::isfinite(p->sm_scale)) return LAZY_ERR_INVALID_ARG;
   if (p->num_splits < 0) return LAZY_ERR_INVALID_ARG;
+  if (p->key_positions != 0 && p->key_positions != 1) return LAZY_ERR_INVALID_ARG;
   c->id_bits = p->id_bits ? p->id_bits : kDefaultIdBits;
   if (c->id_bits < 8 || c->id_bits > 24) return LAZY_ERR_INVALID_ARG;
   if ((int64_t)p->num_pool_blocks > ((int64_t)1 << c->id_bits)) return LAZY_ERR_INVALID_ARG;
@@ -310,7 +311,8 @@ int lazy_attn_pack_block_words_host(const lazy_attn_params* p, int32_t num_docs,
       if (blk + nbk > MB) return LAZY_ERR_LAYOUT;
       for (int q = 0; q < nbk; ++q) {
         const int phys = doc_blocks[doc_block_indptr[doc] + q];
-        const int64_t off = (int64_t)lazy::kBlock * (blk + q) - pos;
+        // offset from the document's start, or (key_positions) from the block's first key
+        const int64_t off = (int64_t)lazy::kBlock * (blk + q) - pos - (p->key_positions ? (int64_t)lazy::kBlock * q : 0);
         if (phys < 0 || phys >= p->num_pool_blocks || (uint32_t)phys > id_mask || off < off_lo || off > off_hi)
           return LAZY_ERR_LAYOUT;
         wrow[blk + q] = ((uint32_t)(int32_t)off << c.id_bits) | ((uint32_t)phys & id_mask);
@@ -340,7 +342,7 @@ int lazy_attn_pack_block_words(const lazy_attn_params* p, int32_t num_docs, cons
   unsigned int* st = status_ptr();
   if (!st) return LAZY_ERR_CUDA;
   lazy::PackArgs a{seg_indptr, seg_doc, seg_len, seq_pos0, doc_block_indptr, doc_blocks, block_words, seq_lens, st,
-                   p->num_seqs, num_docs, p->max_blocks_per_seq, c.id_bits, p->num_pool_blocks};
+                   p->num_seqs, num_docs, p->max_blocks_per_seq, c.id_bits, p->num_pool_blocks, p->key_positions};
   return launched(lazy::launch_pack(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -352,13 +354,16 @@ size_t lazy_attn_decode_workspace_bytes(const lazy_attn_params* p) {
   return decode_ws_bytes(p, splits);
 }
 
-int lazy_attn_decode(const lazy_attn_params* p, const void* q, const void* k_pool, const void* v_pool,
-                     const uint32_t* block_words, const int32_t* seq_lens, const int32_t* q_pos,
-                     const void* rope_table, void* out, void* workspace, size_t workspace_bytes,
-                     lazy_stream_t stream) {
+static int decode_impl(const lazy_attn_params* p, const void* q, const void* k_pool, const void* v_pool,
+                       const uint32_t* block_words, const int32_t* seq_lens, const int32_t* q_pos,
+                       const void* rope_table, const float* alibi, void* out, void* workspace,
+                       size_t workspace_bytes, lazy_stream_t stream) {
   Checked c;
   int rc = check_params(p, &c);
   if (rc != LAZY_OK) return rc;
+  // key-position words carry no document start: only the ALiBi form reads them
+  if (!alibi != !p->key_positions || (reinterpret_cast<uintptr_t>(alibi) & 3u)) return LAZY_ERR_INVALID_ARG;
+  if (alibi && p->dtype != LAZY_BF16) return LAZY_ERR_UNSUPPORTED;
   if (p->num_seqs == 0) return LAZY_OK;
   if (!q || !k_pool || !v_pool || !block_words || !seq_lens || !q_pos || !rope_table || !out)
     return LAZY_ERR_INVALID_ARG;
@@ -406,10 +411,27 @@ int lazy_attn_decode(const lazy_attn_params* p, const void* q, const void* k_poo
     if (!encode_rows_map(&kmap, k_pool, rows, p->head_dim, lazy::kBlock) ||
         !encode_rows_map(&vmap, v_pool, rows, p->head_dim, lazy::kBlock))
       return LAZY_ERR_CUDA;
-    rc = launched(lazy::launch_decode_bf16(a, p->lazy != 0, kmap, vmap, cs));
+    rc = launched(lazy::launch_decode_bf16(a, alibi, p->lazy != 0, kmap, vmap, cs));
   }
   if (rc != LAZY_OK || splits == 1) return rc;
   return launched(lazy::launch_combine(a, p->dtype == LAZY_BF16, cs));
+}
+
+int lazy_attn_decode(const lazy_attn_params* p, const void* q, const void* k_pool, const void* v_pool,
+                     const uint32_t* block_words, const int32_t* seq_lens, const int32_t* q_pos,
+                     const void* rope_table, void* out, void* workspace, size_t workspace_bytes,
+                     lazy_stream_t stream) {
+  return decode_impl(p, q, k_pool, v_pool, block_words, seq_lens, q_pos, rope_table, nullptr, out, workspace,
+                     workspace_bytes, stream);
+}
+
+int lazy_attn_decode_alibi(const lazy_attn_params* p, const void* q, const void* k_pool, const void* v_pool,
+                           const uint32_t* block_words, const int32_t* seq_lens, const int32_t* q_pos,
+                           const void* rope_table, const float* alibi_slopes, void* out, void* workspace,
+                           size_t workspace_bytes, lazy_stream_t stream) {
+  if (!alibi_slopes) return LAZY_ERR_INVALID_ARG;
+  return decode_impl(p, q, k_pool, v_pool, block_words, seq_lens, q_pos, rope_table, alibi_slopes, out, workspace,
+                     workspace_bytes, stream);
 }
 
 int lazy_attn_plan_shared_host(const lazy_attn_params* p, int32_t num_docs, const int32_t* seg_indptr,
@@ -453,7 +475,7 @@ static int decode_shared_impl(const lazy_attn_params* p, const void* q, const vo
   Checked c;
   int rc = check_params(p, &c);
   if (rc != LAZY_OK) return rc;
-  if (alibi && (!p->lazy || (reinterpret_cast<uintptr_t>(alibi) & 3u))) return LAZY_ERR_INVALID_ARG;
+  if (!alibi != !p->key_positions || (reinterpret_cast<uintptr_t>(alibi) & 3u)) return LAZY_ERR_INVALID_ARG;
   if (p->dtype != LAZY_BF16) return LAZY_ERR_UNSUPPORTED;
   if (c.G > 64) return LAZY_ERR_UNSUPPORTED;
   if (num_items < 0 || num_slots < 0) return LAZY_ERR_INVALID_ARG;
@@ -500,12 +522,12 @@ static int decode_shared_impl(const lazy_attn_params* p, const void* q, const vo
       if (!encode_rows_map(&kmap, k_pool, rows, p->head_dim, lazy::kBlock) ||
           !encode_rows_map(&vmap, v_pool, rows, p->head_dim, lazy::kBlock))
         return LAZY_ERR_CUDA;
-      rc = launched(lazy::launch_decode_shared_tc(a, alibi, p->lazy != 0, kmap, vmap, cs));
+      rc = launched(lazy::launch_decode_shared_tc(a, alibi, alibi || p->lazy != 0, kmap, vmap, cs));
     } else {
       if (!encode_block_map(&kmap, k_pool, rows, p->head_dim, lazy::kBlock) ||
           !encode_block_map(&vmap, v_pool, rows, p->head_dim, lazy::kBlock))
         return LAZY_ERR_CUDA;
-      rc = launched(lazy::launch_decode_shared(a, alibi, p->lazy != 0, kmap, vmap, cs));
+      rc = launched(lazy::launch_decode_shared(a, alibi, alibi || p->lazy != 0, kmap, vmap, cs));
     }
     if (rc != LAZY_OK) return rc;
   }
@@ -565,7 +587,7 @@ int lazy_attn_prefill(const lazy_attn_params* p, const void* q, const int32_t* c
   int rc = check_params(p, &c);
   if (rc != LAZY_OK) return rc;
   if (p->dtype != LAZY_BF16 || p->head_dim != 128) return LAZY_ERR_UNSUPPORTED;
-  if (total_q < 0 || max_q_len < 0) return LAZY_ERR_INVALID_ARG;
+  if (total_q < 0 || max_q_len < 0 || p->key_positions) return LAZY_ERR_INVALID_ARG;
   if (p->num_seqs == 0 || total_q == 0 || max_q_len == 0) return LAZY_OK;
   if (!q || !cu_seqlens_q || !q_start || !k_pool || !v_pool || !block_words || !seq_lens || !rope_table || !out)
     return LAZY_ERR_INVALID_ARG;
@@ -621,6 +643,7 @@ int lazy_attn_materialize(const lazy_attn_params* p, const void* k_pool, const v
   int rc = check_params(p, &c);
   if (rc != LAZY_OK) return rc;
   if (p->dtype != LAZY_BF16) return LAZY_ERR_UNSUPPORTED;
+  if (p->key_positions) return LAZY_ERR_INVALID_ARG;
   if (p->num_seqs == 0) return LAZY_OK;
   if (!k_pool || !v_pool || !block_words || !seq_lens || !rope_table || !k_out || !v_out || !block_words_out)
     return LAZY_ERR_INVALID_ARG;

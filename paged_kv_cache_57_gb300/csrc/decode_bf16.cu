@@ -27,6 +27,7 @@
 // output) and decode_combine merges the splits.
 #include <cfloat>
 #include <climits>
+#include <type_traits>
 
 #include "decode_block.cuh"
 #include "kernels.h"
@@ -121,10 +122,14 @@ __device__ __forceinline__ void build_q_frags(uint32_t (&qa)[D / 16][4], const f
   }
 }
 
-template <int D, int MT, int SPT, bool LAZY>
+// ALIBI (with LAZY = false, key-position words): q is built once (the caller's table
+// has zero rates: no rotation), and every score of row r gets slope_r (n - m) in log2
+// units, n = the block word's position + slot, m = q_pos.
+template <int D, int MT, int SPT, bool LAZY, bool ALIBI = false>
 __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS, MT == 1 ? 3 : 1)
-    decode_bf16_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
-                       const __grid_constant__ CUtensorMap vmap) {
+    decode_bf16_kernel(const std::conditional_t<ALIBI, DecodeAlibiArgs, DecodeArgs> a,
+                       const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
+  static_assert(!(ALIBI && LAZY), "the ALiBi variant does not rotate");
   using C = DecodeCfg<D, MT, SPT>;
   constexpr int HALF = C::HALF, CPL = (HALF + 31) / 32;
   extern __shared__ uint8_t smem_raw[];
@@ -210,6 +215,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS, MT == 1 ? 3 :
     });
   };
   if constexpr (!LAZY) rebuild(m_pos);  // control: pool holds absolute-position keys, rotate q once by R_m
+  float ab_slope[2] = {0.f, 0.f};
+  if constexpr (ALIBI) {
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int row = mt * 16 + g + 8 * rr;
+      if (row < a.G) ab_slope[rr] = __ldg(&a.alibi[kvh * a.G + row]) * 1.4426950408889634f;
+    }
+  }
 
   float o[D / 8][4];
 #pragma unroll
@@ -242,7 +255,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS, MT == 1 ? 3 :
       }
     }
     bool ok = warp_wait(&tfull[slot], (k / SPT) & 1, a.status);
-    if (ok) attend_block<D>(smem_u32(tst + slot * C::STAGE_BYTES), ln, qa, nvalid, o, m_r, l_r, lane);
+    if constexpr (ALIBI) {
+      const int pk = __shfl_sync(0xffffffffu, cur.p, k & 31);  // this block's first key position
+      const float b0[2] = {ab_slope[0] * (float)(pk - m_pos), ab_slope[1] * (float)(pk - m_pos)};
+      if (ok) attend_block_bias<D>(smem_u32(tst + slot * C::STAGE_BYTES), ln, qa, nvalid, o, m_r, l_r, lane, b0, ab_slope);
+    } else {
+      if (ok) attend_block<D>(smem_u32(tst + slot * C::STAGE_BYTES), ln, qa, nvalid, o, m_r, l_r, lane);
+    }
     // The team's warps are all done with this stage (and agree to go on) before it is refilled.
     if constexpr (MT > 1) ok = team_and(team, 32 * MT, ok);
     if (!ok) {
@@ -479,25 +498,33 @@ __global__ void __launch_bounds__(64) gather_bf16_kernel(const GatherArgs a, con
 
 // ------------------------------------------------------------------ launchers
 
-template <int D, int MT, bool LAZY>
-static cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                   cudaStream_t st) {
+template <int D, int MT, bool LAZY, bool ALIBI>
+static cudaError_t launch_decode_t(const DecodeArgs& a, const float* alibi, const CUtensorMap& kmap,
+                                   const CUtensorMap& vmap, cudaStream_t st) {
   constexpr int SPT = LAZY_DECODE_SPT;
   using C = DecodeCfg<D, MT, SPT>;
-  auto kern = decode_bf16_kernel<D, MT, SPT, LAZY>;
-  cudaError_t e = set_smem_once<decode_bf16_kernel<D, MT, SPT, LAZY>>(C::SMEM);
+  auto kern = decode_bf16_kernel<D, MT, SPT, LAZY, ALIBI>;
+  cudaError_t e = set_smem_once<decode_bf16_kernel<D, MT, SPT, LAZY, ALIBI>>(C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(a.splits, a.Hkv, a.B);
-  kern<<<grid, C::NTHREADS, C::SMEM, st>>>(a, kmap, vmap);
+  if constexpr (ALIBI) {
+    DecodeAlibiArgs aa;
+    static_cast<DecodeArgs&>(aa) = a;
+    aa.alibi = alibi;
+    kern<<<grid, C::NTHREADS, C::SMEM, st>>>(aa, kmap, vmap);
+  } else {
+    (void)alibi;
+    kern<<<grid, C::NTHREADS, C::SMEM, st>>>(a, kmap, vmap);
+  }
   return cudaGetLastError();
 }
 
-template <int D, bool LAZY>
-static cudaError_t dispatch_mt(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                               cudaStream_t st) {
-  if (a.G <= 16) return launch_decode_t<D, 1, LAZY>(a, kmap, vmap, st);
-  if (a.G <= 32) return launch_decode_t<D, 2, LAZY>(a, kmap, vmap, st);
-  return launch_decode_t<D, 4, LAZY>(a, kmap, vmap, st);
+template <int D, bool LAZY, bool ALIBI>
+static cudaError_t dispatch_mt(const DecodeArgs& a, const float* alibi, const CUtensorMap& kmap,
+                               const CUtensorMap& vmap, cudaStream_t st) {
+  if (a.G <= 16) return launch_decode_t<D, 1, LAZY, ALIBI>(a, alibi, kmap, vmap, st);
+  if (a.G <= 32) return launch_decode_t<D, 2, LAZY, ALIBI>(a, alibi, kmap, vmap, st);
+  return launch_decode_t<D, 4, LAZY, ALIBI>(a, alibi, kmap, vmap, st);
 }
 
 int decode_bf16_smem_bytes(int D, int G) {
@@ -507,10 +534,16 @@ int decode_bf16_smem_bytes(int D, int G) {
   return G <= 16 ? DecodeCfg<128, 1, S>::SMEM : G <= 32 ? DecodeCfg<128, 2, S>::SMEM : DecodeCfg<128, 4, S>::SMEM;
 }
 
-cudaError_t launch_decode_bf16(const DecodeArgs& a, bool lazy, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                               cudaStream_t st) {
-  if (a.D == 128) return lazy ? dispatch_mt<128, true>(a, kmap, vmap, st) : dispatch_mt<128, false>(a, kmap, vmap, st);
-  return lazy ? dispatch_mt<64, true>(a, kmap, vmap, st) : dispatch_mt<64, false>(a, kmap, vmap, st);
+cudaError_t launch_decode_bf16(const DecodeArgs& a, const float* alibi, bool lazy, const CUtensorMap& kmap,
+                               const CUtensorMap& vmap, cudaStream_t st) {
+  if (alibi)
+    return a.D == 128 ? dispatch_mt<128, false, true>(a, alibi, kmap, vmap, st)
+                      : dispatch_mt<64, false, true>(a, alibi, kmap, vmap, st);
+  if (a.D == 128)
+    return lazy ? dispatch_mt<128, true, false>(a, nullptr, kmap, vmap, st)
+                : dispatch_mt<128, false, false>(a, nullptr, kmap, vmap, st);
+  return lazy ? dispatch_mt<64, true, false>(a, nullptr, kmap, vmap, st)
+              : dispatch_mt<64, false, false>(a, nullptr, kmap, vmap, st);
 }
 
 cudaError_t launch_combine(const DecodeArgs& a, bool out_bf16, cudaStream_t st) {

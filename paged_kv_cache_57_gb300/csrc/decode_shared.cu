@@ -279,13 +279,12 @@ __global__ void __launch_bounds__(kShThreads, 3)
       }
   }
   LAZY_TRACE(2, global_timer_ns());
-  // ALiBi: row r's scores get slope_r (n - m) in log2 units, n = p + j the key's
-  // position, m the query's: slope_r (j - delta_r) with j = 16 (c0 + kb) + k for key k
-  // of the item's block kb (c0: the item's first block within its document).
+  // ALiBi (key-position words): a member's word gives the position of its first item
+  // block, so delta_r = m - that position and key k of item block kb sits at
+  // n - m = 16 kb + k - delta_r; row r's scores get slope_r (n - m) in log2 units.
   float ab_slope[2] = {0.f, 0.f};
-  int ab_delta[2] = {0, 0}, item_c0 = 0;
+  int ab_delta[2] = {0, 0};
   if constexpr (ALIBI) {
-    item_c0 = rec[5];
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       const int r = rt * 16 + g + 8 * rr;
@@ -316,7 +315,7 @@ __global__ void __launch_bounds__(kShThreads, 3)
     bool ok = warp_wait(&tfull[slot], (k / NS) & 1, a.status);
     if (ok) {
       if constexpr (ALIBI) {
-        const int j0 = kBlock * (item_c0 + kb0 + k);
+        const int j0 = kBlock * (kb0 + k);
         const float b0[2] = {ab_slope[0] * (float)(j0 - ab_delta[0]), ab_slope[1] * (float)(j0 - ab_delta[1])};
         attend_block_bias<D>(smem_u32(tst + slot * G::STAGE_BYTES), ln, qa, nvalid, o, m_r, l_r, lane, b0, ab_slope);
       } else {

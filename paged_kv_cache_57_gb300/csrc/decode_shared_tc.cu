@@ -335,9 +335,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (i == 0) LAZY_TC_TRACE(1, global_timer_ns());
 
     const uint32_t tO = tmem + kColO + lane_base;
-    // ALiBi: this row's scores get slope (n - m) in log2 units, n = p + j the key's
-    // position, m the query's: slope (j - delta) with j = 16 (c0 + 4 jt) + c for column
-    // c of tile jt (c0: the item's first block within its document).
+    // ALiBi (key-position words): the member's word gives the position of its first
+    // item block, delta = m - that position, and column c of tile jt sits at
+    // n - m = 16 (4 jt) + c - delta; the row's scores get slope (n - m) in log2 units.
     float ab_slope = 0.f;
     int ab_delta = 0;
     if constexpr (ALIBI) {
@@ -346,7 +346,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         ab_delta = m_delta[m];
       }
     }
-    const int item_c0 = rec[5];
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     long long c_s = 0, c_c = 0, c_pv = 0, c_st = 0;
@@ -395,7 +394,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         tmem_ld32(tS + 32, sv[1]);
         tmem_ld_wait(sv[0], sv[1]);
         if constexpr (ALIBI) {
-          const float base = ab_slope * (float)(kBlock * (item_c0 + kTcBlocks * j) - ab_delta);
+          const float base = ab_slope * (float)(kBlock * kTcBlocks * j - ab_delta);
 #pragma unroll
           for (int c = 0; c < kTcKeys; ++c) sv[c >> 5][c & 31] += fmaf(ab_slope, (float)c, base);
         }

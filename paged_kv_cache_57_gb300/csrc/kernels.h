@@ -43,6 +43,11 @@ struct DecodeArgs {
   int splits, bps;           // split-K factor and logical blocks per split
   float scale_log2;          // softmax scale * log2(e)
 };
+// The ALiBi variants' arguments (a separate type keeps the other kernels' argument
+// block unchanged).
+struct DecodeAlibiArgs : DecodeArgs {
+  const float* alibi;  // [Hq] slopes
+};
 
 struct GatherArgs {
   const uint32_t* words;
@@ -67,6 +72,7 @@ struct PackArgs {
   int32_t* seq_lens;
   unsigned int* status;
   int B, num_docs, max_blocks, id_bits, num_pool_blocks;
+  int key_positions;         // offsets from each block's first key instead of its document's start
 };
 
 struct PrefillArgs {
@@ -153,7 +159,9 @@ cudaError_t launch_debug_rope(const float2* table, const int32_t* deltas, int n,
                               unsigned int* status, cudaStream_t st);
 cudaError_t launch_pack(const PackArgs& a, cudaStream_t st);
 cudaError_t launch_decode_f32(const DecodeArgs& a, bool lazy, cudaStream_t st);
-cudaError_t launch_decode_bf16(const DecodeArgs& a, bool lazy, const CUtensorMap& kmap, const CUtensorMap& vmap,
+// alibi: null, or [Hq] ALiBi slopes (key-position words; no rotation).
+cudaError_t launch_decode_bf16(const DecodeArgs& a, const float* alibi, bool lazy, const CUtensorMap& kmap,
+                               const CUtensorMap& vmap,
                                cudaStream_t st);
 cudaError_t launch_combine(const DecodeArgs& a, bool out_bf16, cudaStream_t st);
 cudaError_t launch_gather_bf16(const GatherArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,

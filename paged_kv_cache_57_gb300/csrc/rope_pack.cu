@@ -133,7 +133,7 @@ __global__ void pack_words_kernel(const PackArgs a) {
       bool e2 = false;
       for (int q = lane; q < nj; q += 32) {
         const int phys = ids[q];
-        const long long off = (long long)kBlock * (bj + q) - pj;
+        const long long off = (long long)kBlock * (bj + q) - pj - (a.key_positions ? (long long)kBlock * q : 0);
         e2 |= phys < 0 || phys >= a.num_pool_blocks || (uint32_t)phys > id_mask || off < off_lo || off > off_hi;
         wrow[bj + q] = ((uint32_t)(int)off << a.id_bits) | ((uint32_t)phys & id_mask);
       }

@@ -125,7 +125,7 @@ int plan_shared_host(int B, int G, int rows_cap, int max_blocks, int num_pool_bl
     d[2] = its[i].nb;
     d[3] = its[i].last;
     d[4] = st.n;
-    d[5] = its[i].c0;  // the item's first block within its document (key positions for ALiBi)
+    d[5] = its[i].c0;  // the item's first block within its document
     for (int j = 0; j < st.n; ++j) {
       const Occ& o = occ[st.first + j];
       int32_t* m = d + 8 + 4 * j;

@@ -36,6 +36,7 @@ EXPORTED = (
     "lazy_attn_plan_shared_host", "lazy_attn_decode_shared_workspace_bytes", "lazy_attn_decode_shared",
     "lazy_attn_materialize", "lazy_attn_rope_table_init_scaled", "lazy_attn_rope_table_init_freqs",
     "lazy_attn_rotary_layout_host", "lazy_attn_decode_shared_alibi", "lazy_attn_alibi_slopes_host",
+    "lazy_attn_decode_alibi",
 )
 PLAN_MAX_MEMBERS = 16
 PLAN_ITEM_BLOCK_IDS = 32
@@ -50,7 +51,7 @@ class Params(ctypes.Structure):
         ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32), ("num_pool_blocks", ctypes.c_int32),
         ("max_blocks_per_seq", ctypes.c_int32), ("id_bits", ctypes.c_int32), ("dtype", ctypes.c_int32),
         ("lazy", ctypes.c_int32), ("rope_theta", ctypes.c_double), ("sm_scale", ctypes.c_float),
-        ("num_splits", ctypes.c_int32),
+        ("num_splits", ctypes.c_int32), ("key_positions", ctypes.c_int32),
     ]
 
 
@@ -87,6 +88,7 @@ _sig = {
     "lazy_attn_decode_shared_alibi": (ctypes.c_int,
                                       [_P] + [_vp] * 6 + [_i32, _vp, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "lazy_attn_alibi_slopes_host": (ctypes.c_int, [_i32, _vp]),
+    "lazy_attn_decode_alibi": (ctypes.c_int, [_P] + [_vp] * 9 + [_vp, _sz, _vp]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -104,10 +106,10 @@ def _check(rc: int, where: str) -> None:
 
 def make_params(*, num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int, num_pool_blocks: int,
                 max_blocks_per_seq: int, dtype: str = "bf16", rope_theta: float = 5e5, lazy: bool = True,
-                sm_scale: float = 0.0, id_bits: int = 0, num_splits: int = 0) -> Params:
+                sm_scale: float = 0.0, id_bits: int = 0, num_splits: int = 0, key_positions: bool = False) -> Params:
     return Params(num_seqs, num_q_heads, num_kv_heads, head_dim, BLOCK, num_pool_blocks, max_blocks_per_seq,
                   id_bits, LAZY_BF16 if dtype == "bf16" else LAZY_F32, int(bool(lazy)), float(rope_theta),
-                  float(sm_scale), num_splits)
+                  float(sm_scale), num_splits, int(bool(key_positions)))
 
 
 def _dptr(t: Optional[torch.Tensor], name: str, dtype=None, device_required=True):
@@ -235,7 +237,9 @@ def decode_workspace_bytes(p: Params) -> int:
 
 def decode(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, block_words: torch.Tensor,
            seq_lens: torch.Tensor, q_pos: torch.Tensor, rope_table: torch.Tensor, out: Optional[torch.Tensor] = None,
-           workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+           workspace: Optional[torch.Tensor] = None, stream=None,
+           alibi_slopes: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """alibi_slopes (fp32 [Hq]) selects lazy_attn_decode_alibi: words packed with key_positions=True."""
     dt = _tdt(p)
     if out is None:
         out = torch.empty_like(q)
@@ -243,11 +247,14 @@ def decode(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tenso
     if workspace is None and nws:
         workspace = torch.empty(nws, dtype=torch.uint8, device=q.device)
     wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = _lib.lazy_attn_decode(ctypes.byref(p), _dptr(q, "q", dt), _dptr(k_pool, "k_pool", dt),
-                               _dptr(v_pool, "v_pool", dt), _dptr(block_words, "block_words"),
-                               _dptr(seq_lens, "seq_lens", torch.int32), _dptr(q_pos, "q_pos", torch.int32),
-                               _dptr(rope_table, "rope_table"), _dptr(out, "out", dt),
-                               _dptr(workspace, "workspace"), wsz, _stream(stream))
+    head = (ctypes.byref(p), _dptr(q, "q", dt), _dptr(k_pool, "k_pool", dt), _dptr(v_pool, "v_pool", dt),
+            _dptr(block_words, "block_words"), _dptr(seq_lens, "seq_lens", torch.int32),
+            _dptr(q_pos, "q_pos", torch.int32), _dptr(rope_table, "rope_table"))
+    tail = (_dptr(out, "out", dt), _dptr(workspace, "workspace"), wsz, _stream(stream))
+    if alibi_slopes is None:
+        rc = _lib.lazy_attn_decode(*head, *tail)
+    else:
+        rc = _lib.lazy_attn_decode_alibi(*head, _dptr(alibi_slopes, "alibi_slopes", torch.float32), *tail)
     _check(rc, "decode")
     return out
 

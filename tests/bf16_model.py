@@ -27,10 +27,22 @@ def _bf16(x):
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
 
 
-def emulate(w, rows, lazy: bool = True, k_pool=None, freqs=None, alibi=None) -> np.ndarray:
+# Unit roundoff of bf16 (8 significand bits): round-to-nearest moves a value by at
+# most this fraction of itself.
+BF16_U = 2.0 ** -8
+
+
+def emulate(w, rows, lazy: bool = True, k_pool=None, freqs=None, alibi=None, weight_bound: bool = False):
     """[len(rows), Hq, d] for query rows ``rows`` of workload ``w`` (``freqs``: rotation
     frequencies other than theta^(-2i/d); ``alibi``: per-head slopes of the bias
-    -slope (m - n), added in fp32 to the scores before the exponentials)."""
+    -slope (m - n), added in fp32 to the scores before the exponentials).
+
+    The weights here are rounded to bf16 relative to the row's global maximum; a
+    split-K kernel rounds each one relative to the running maximum of its own split,
+    a different but equally valid bf16 value within BF16_U of the exact weight. With
+    ``weight_bound`` the call also returns, per element, the first-order bound on what
+    two such roundings can change in the output, 2 BF16_U sum_j p_j |v_j - o| (exact
+    weights p, output o), as a second array of the same shape."""
     kp = (w.k_pool if k_pool is None else k_pool).double().numpy()
     vp = w.v_pool.double().numpy()
     q = w.q.double().numpy()
@@ -45,6 +57,7 @@ def emulate(w, rows, lazy: bool = True, k_pool=None, freqs=None, alibi=None) -> 
     d, theta = w.head_dim, w.rope_theta
     scale = np.log2(np.e) / np.sqrt(d)
     out = np.zeros((len(rows), w.num_q_heads, d))
+    bound = np.zeros_like(out)
     for oi, r in enumerate(np.asarray(rows)):
         s, m = int(q_seq[r]), int(q_m[r])
         Ks, Vs, Ps, pos = [], [], [], []
@@ -77,4 +90,9 @@ def emulate(w, rows, lazy: bool = True, k_pool=None, freqs=None, alibi=None) -> 
                 sc = sc - float(alibi[h]) * np.log2(np.e) * (m - pos[vis])
             e = _bf16(np.exp2(sc - sc.max()))
             out[oi, h] = (e[:, None] * V[:, h // g]).sum(0) / e.sum()
-    return _bf16(out)
+            if weight_bound:
+                pw = np.exp2(sc - sc.max())
+                pw /= pw.sum()
+                o = pw @ V[:, h // g]
+                bound[oi, h] = 2 * BF16_U * (pw[:, None] * np.abs(V[:, h // g] - o)).sum(0)
+    return (_bf16(out), bound) if weight_bound else _bf16(out)

@@ -114,6 +114,31 @@ def test_host_packer_round_trip(la, w):
         assert (words[s, nb:] == 0).all()
 
 
+@pytest.mark.parametrize("w", list(_workloads())[2:], ids=lambda w: f"{w.name}-{w.num_seqs}")
+def test_host_packer_key_position_words(la, w):
+    # key_positions = 1: a word's position is that of its block's first key (the
+    # document start plus 16 per earlier block of the document); ids, sequence
+    # lengths and the valid-count rule are those of the document-start form.
+    words0, lens0 = la.pack_block_words_host(_params(la, w), len(w.doc_len), w.seg_indptr, w.seg_doc, w.seg_len,
+                                             w.seq_pos0, w.doc_block_indptr, w.doc_blocks)
+    words, seq_lens = la.pack_block_words_host(_params(la, w, key_positions=True), len(w.doc_len), w.seg_indptr,
+                                               w.seg_doc, w.seg_len, w.seq_pos0, w.doc_block_indptr, w.doc_blocks)
+    assert np.array_equal(seq_lens, lens0)
+    id_bits = 18
+    for s in range(w.num_seqs):
+        first_keys, p = [], int(w.seq_pos0[s])
+        for doc, L in w.seq_segments(s):
+            first_keys += [p + 16 * j for j in range((L + 15) // 16)]
+            p += L
+        nb = len(first_keys)
+        got = [unpack(words[s, b], b, id_bits) for b in range(nb)]
+        assert [g[1] for g in got] == first_keys
+        assert [g[0] for g in got] == [unpack(words0[s, b], b, id_bits)[0] for b in range(nb)]
+        assert [valid_by_rule(first_keys, b, nb, int(seq_lens[s])) for b in range(nb)] == \
+            [e[2] for e in expected_blocks(w, s)]
+        assert (words[s, nb:] == 0).all()
+
+
 def test_host_packer_rejects_bad_layouts(la):
     w = W.decode_zipf("bad", batch=2, hq=4, hkv=2, d=64, docs_per_seq=2, doc_tokens=20, pool_docs=3, zipf_s=1.0,
                       seed=8)

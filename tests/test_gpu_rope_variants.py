@@ -141,24 +141,54 @@ def test_prefill_partial_rotary(hq, hkv):
 
 
 # ---------------------------------------------------------------- ALiBi
-# No rotation (a zero-rate table) and the bias -slope_h (m - n) formed in the
-# shared-run kernels from the members' document starts and the items' first blocks.
+# No rotation (a zero-rate table) and the bias -slope_h (m - n), formed in the
+# kernels from key-position words (each word gives its block's first key).
+# The steepest slopes put most of a row's weight on two or three keys, where the
+# bf16 rounding of those weights alone (relative to each split's running maximum
+# in the kernels, to the row maximum in the emulation) can exceed 2e-3; the
+# emulation check then allows that rounding's first-order bound. A wrong key
+# position moves such a row by about a tenth of |v|, far outside it.
+
+def _alibi_device(w, pack_on_device=True):
+    L = la()
+    dv = to_device(w, key_positions=True, pack_on_device=pack_on_device)
+    dv.rope = L.rope_table_init(dv.p, freqs=np.zeros(w.head_dim // 2))
+    return dv
+
 
 @pytest.mark.parametrize("hq,hkv,chunk", [(8, 8, 0), (8, 2, 3), (16, 2, 0), (32, 1, 5)])
 def test_shared_decode_alibi(hq, hkv, chunk):
     # 1 and 4 query heads per KV head: the mma.sync kernel; 8 and 32: the tcgen05 one.
-    # Chunks of 3 or 5 blocks start items inside documents (c0 > 0).
+    # Chunks of 3 or 5 blocks start items inside documents.
     L = la()
     w = W.decode_zipf(f"valibi{hq}", batch=8, hq=hq, hkv=hkv, d=128, docs_per_seq=3, doc_tokens=170, pool_docs=3,
                       zipf_s=1.0, suffix_tokens=13, seed=320 + hq)
     slopes = L.alibi_slopes(hq)
     ref = oracle.attention(w, freqs=np.zeros(64), alibi=slopes.astype(np.float64))
-    dv = to_device(w)
-    dv.rope = L.rope_table_init(dv.p, freqs=np.zeros(64))
+    dv = _alibi_device(w)
     plan = shared_plan(dv, chunk)
     out = L.decode_shared(dv.p, dv.q, dv.k_pool, dv.v_pool, dv.words, dv.q_pos, dv.rope, plan,
                           alibi_slopes=torch.from_numpy(slopes).cuda())
     assert_close(out, ref, "bf16", f"shared decode, ALiBi, {hq}/{hkv}",
-                 emulate=lambda r: emulate(w, r, freqs=np.zeros(64), alibi=slopes))
+                 emulate=lambda r: emulate(w, r, freqs=np.zeros(64), alibi=slopes, weight_bound=True))
     # the bias matters at these positions
     assert np.abs(ref - oracle.attention(w, freqs=np.zeros(64))).max() > 1e-2
+
+
+@pytest.mark.parametrize("hq,hkv,d,splits,host_pack", [(8, 8, 128, 0, False), (8, 2, 128, 3, True),
+                                                       (32, 1, 128, 0, False), (4, 2, 64, 1, False)])
+def test_per_sequence_decode_alibi(hq, hkv, d, splits, host_pack):
+    # the split-K per-sequence kernel: 1, 4 and 32 query heads per KV head, d 64 and 128,
+    # one split, three and the automatic count; words from the device and the host packer
+    L = la()
+    w = W.decode_zipf(f"vpsalibi{hq}", batch=6, hq=hq, hkv=hkv, d=d, docs_per_seq=4, doc_tokens=150, pool_docs=5,
+                      zipf_s=1.0, suffix_tokens=21, seed=340 + hq + d)
+    slopes = L.alibi_slopes(hq)
+    ref = oracle.attention(w, freqs=np.zeros(d // 2), alibi=slopes.astype(np.float64))
+    dv = _alibi_device(w, pack_on_device=not host_pack)
+    dv.p.num_splits = splits
+    out = L.decode(dv.p, dv.q, dv.k_pool, dv.v_pool, dv.words, dv.seq_lens, dv.q_pos, dv.rope,
+                   alibi_slopes=torch.from_numpy(slopes).cuda())
+    assert_close(out, ref, "bf16", f"per-sequence decode, ALiBi, {hq}/{hkv} d{d}",
+                 emulate=lambda r: emulate(w, r, freqs=np.zeros(d // 2), alibi=slopes, weight_bound=True))
+    assert np.abs(ref - oracle.attention(w, freqs=np.zeros(d // 2))).max() > 1e-2

@@ -249,17 +249,38 @@ def test_alibi_slopes_closed_form():
         L.alibi_slopes(0)
 
 
-def test_alibi_decode_rejects_the_control_path_without_cuda():
+def test_alibi_calls_and_key_position_words_go_together_without_cuda():
+    # The ALiBi calls read key positions from words packed with key_positions = 1;
+    # every other call reads document starts and must refuse such words.
     from paged_kv_cache_57_gb300 import lazy_attn as L
     w = _alibi_w()
-    p = L.make_params(num_seqs=w.num_seqs, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
-                      head_dim=w.head_dim, num_pool_blocks=w.num_pool_blocks, max_blocks_per_seq=w.max_blocks_per_seq,
-                      dtype="bf16", rope_theta=w.rope_theta, lazy=False)
     fake = ctypes.c_void_p(4096)  # never dereferenced: the arguments are rejected first
-    rc = L._lib.lazy_attn_decode_shared_alibi(ctypes.byref(p), *([fake] * 6), 1, fake, 1, fake, fake, fake, fake,
-                                              1 << 20, None)
-    assert rc == L.LAZY_ERR_INVALID_ARG
-    p.lazy = 1
-    rc = L._lib.lazy_attn_decode_shared_alibi(ctypes.byref(p), *([fake] * 6), 1, fake, 1, fake, None, fake, fake,
-                                              1 << 20, None)
-    assert rc == L.LAZY_ERR_INVALID_ARG  # no slopes
+
+    def params(key_positions, dtype="bf16"):
+        return L.make_params(num_seqs=w.num_seqs, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                             head_dim=w.head_dim, num_pool_blocks=w.num_pool_blocks,
+                             max_blocks_per_seq=w.max_blocks_per_seq, dtype=dtype, rope_theta=w.rope_theta,
+                             key_positions=key_positions)
+
+    def shared_alibi(p, slopes):
+        return L._lib.lazy_attn_decode_shared_alibi(ctypes.byref(p), *([fake] * 6), 1, fake, 1, fake, slopes,
+                                                    fake, fake, 1 << 20, None)
+
+    def decode_alibi(p, slopes):
+        return L._lib.lazy_attn_decode_alibi(ctypes.byref(p), *([fake] * 7), slopes, fake, fake, 1 << 20, None)
+
+    doc_words, key_words = params(False), params(True)
+    bad = L.LAZY_ERR_INVALID_ARG
+    assert shared_alibi(doc_words, fake) == bad and decode_alibi(doc_words, fake) == bad
+    assert shared_alibi(key_words, None) == bad and decode_alibi(key_words, None) == bad
+    assert shared_alibi(key_words, ctypes.c_void_p(4098)) == bad  # slopes not 4-byte aligned
+    assert decode_alibi(params(True, "f32"), fake) == L.LAZY_ERR_UNSUPPORTED
+    assert L._lib.lazy_attn_decode(ctypes.byref(key_words), *([fake] * 8), fake, 1 << 20, None) == bad
+    assert L._lib.lazy_attn_decode_shared(ctypes.byref(key_words), *([fake] * 6), 1, fake, 1, fake, fake, fake,
+                                          1 << 20, None) == bad
+    p = params(True)
+    p.head_dim = 128  # the prefill's only head size
+    assert L._lib.lazy_attn_prefill(ctypes.byref(p), fake, fake, fake, 1, 1, *([fake] * 7), 1 << 20, None) == bad
+    p = params(True)
+    p.key_positions = 2
+    assert decode_alibi(p, fake) == bad
