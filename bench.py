@@ -518,6 +518,31 @@ def measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust):
                                 "decode_ms_prerotated": 1e3 * sh0,
                                 "decode_per_sequence_path": 100.0 * (sq1 / sq0 - 1.0),
                                 "pages_h100_context": {"decode_latency": 0.13, "prefill_flops_m128": 0.59}}
+    # ALiBi on both decode paths: the same pool, plan and queries, block words in the
+    # key-position form, a zero-rate table and the usual slopes, against the rotating
+    # decode just timed.
+    try:
+        pa = L.make_params(num_seqs=w.num_seqs, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                           head_dim=w.head_dim, num_pool_blocks=w.num_pool_blocks,
+                           max_blocks_per_seq=d["p"].max_blocks_per_seq, dtype=w.dtype, rope_theta=w.rope_theta,
+                           key_positions=True)
+        c = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+        wa, _ = L.pack_block_words(pa, len(w.doc_len), c(w.seg_indptr), c(w.seg_doc), c(w.seg_len),
+                                   c(w.seq_pos0), c(w.doc_block_indptr), c(w.doc_blocks))
+        ra = L.rope_table_init(pa, freqs=np.zeros(w.head_dim // 2))
+        sl = torch.from_numpy(L.alibi_slopes(w.num_q_heads)).cuda()
+        ta = statistics.median(time_steps(lambda: L.decode_shared(
+            pa, d["q"], d["k"], d["v"], wa, d["q_pos"], ra, d["plan"], out=d["out"], workspace=d["ws_sh"],
+            alibi_slopes=sl), n, 3, flush))
+        tq = statistics.median(time_steps(lambda: L.decode(
+            pa, d["q"], d["k"], d["v"], wa, d["seq_lens"], d["q_pos"], ra, out=d["out"], workspace=d["ws"],
+            alibi_slopes=sl), n, 3, flush))
+        out["alibi_decode"] = {"shared_ms": 1e3 * ta, "shared_vs_rope_pct": 100.0 * (ta / sh1 - 1.0),
+                               "per_sequence_ms": 1e3 * tq, "per_sequence_vs_rope_pct": 100.0 * (tq / sq1 - 1.0),
+                               "kv_gbs_unique_shared": nb8["unique"] / ta / 1e9}
+        del wa, ra, sl
+    except L.LazyAttnError as e:
+        out["alibi_decode"] = {"unavailable": str(e)}
     # The per-sequence path (lazy_attn_decode) on the same workload, for comparison.
     out["decode_per_sequence_path"] = {"ms_median": 1e3 * sq1, "kv_gbs_logical": nb8["kv_logical"] / sq1 / 1e9,
                                        "kv_gbs_unique": nb8["unique"] / sq1 / 1e9,

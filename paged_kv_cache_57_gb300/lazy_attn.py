@@ -254,6 +254,8 @@ def decode(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tenso
     if alibi_slopes is None:
         rc = _lib.lazy_attn_decode(*head, *tail)
     else:
+        if alibi_slopes.numel() != p.num_q_heads:
+            raise ValueError("alibi_slopes needs one slope per query head")
         rc = _lib.lazy_attn_decode_alibi(*head, _dptr(alibi_slopes, "alibi_slopes", torch.float32), *tail)
     _check(rc, "decode")
     return out
