@@ -580,6 +580,25 @@ def measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust):
         ctl.update({key + "gbs": gbs, key + "frac_of_measured": gbs / hbm, key + "frac_of_8tbs": gbs / 8000.0,
                     key + "ms_median": 1e3 * tc})
     out["noshare_control"] = ctl
+    # FP8 KV (e4m3 codes, per-tensor scales) on the per-sequence decode, the headline
+    # and the no-sharing workloads, against the bf16 pools on the same path.
+    fp8 = {}
+    for tag, ww, dd in (("llama8b_decode", w, d), ("llama8b_decode_noshare", wc, dc)):
+        k8, v8, ks, vs = W.fp8_pools(ww)
+        k8, v8 = k8.cuda(), v8.cuda()
+        p8 = L.make_params(num_seqs=ww.num_seqs, num_q_heads=ww.num_q_heads, num_kv_heads=ww.num_kv_heads,
+                           head_dim=ww.head_dim, num_pool_blocks=ww.num_pool_blocks,
+                           max_blocks_per_seq=dd["p"].max_blocks_per_seq, dtype=ww.dtype, rope_theta=ww.rope_theta,
+                           kv_dtype="fp8_e4m3", k_scale=ks, v_scale=vs)
+        t8 = statistics.median(time_steps(lambda: L.decode(p8, dd["q"], k8, v8, dd["words"], dd["seq_lens"],
+                                                           dd["q_pos"], dd["rope"], out=dd["out"], workspace=dd["ws"]),
+                                          n, 3, flush))
+        t16 = statistics.median(time_steps(lambda: run_decode(dd, path="seq"), n, 3, flush))
+        ub = decode_bytes(ww)["unique"]
+        fp8[tag] = {"fp8_ms": 1e3 * t8, "bf16_ms": 1e3 * t16, "fp8_unique_gbs": ub / 2 / t8 / 1e9,
+                    "fp8_frac_of_measured": ub / 2 / t8 / 1e9 / hbm, "kv_bytes_ratio": 0.5}
+        del k8, v8
+    out["fp8_kv_decode"] = fp8
     del dc
     # Prefill (Llama-3.1-8B-shaped, 8 x (6 x 1024 docs + 256-token chunk)).
     try:

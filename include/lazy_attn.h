@@ -27,6 +27,9 @@
  *    word and returns. Outputs are then unspecified.
  *  - Numerics: dtype LAZY_F32 computes in fp32; LAZY_BF16 multiplies bf16
  *    operands on the tensor cores with fp32 accumulation and fp32 softmax.
+ *    With kv_dtype LAZY_FP8_E4M3 (lazy_attn_decode only) the pools hold OCP
+ *    e4m3 codes and the products take f16 operands (every e4m3 value is exact
+ *    in f16), with fp32 accumulation and softmax.
  *
  * Layout (one layer)
  * ------------------
@@ -77,7 +80,7 @@ typedef enum {
   LAZY_ERR_DEVICE = 6       /* the device status word reported a fault */
 } lazy_status;
 
-typedef enum { LAZY_F32 = 0, LAZY_BF16 = 1 } lazy_dtype;
+typedef enum { LAZY_F32 = 0, LAZY_BF16 = 1, LAZY_FP8_E4M3 = 2 } lazy_dtype;
 
 /* Bits of the per-device status word. */
 #define LAZY_DEV_BAD_BLOCK_ID 0x1u /* a word's phys_id >= num_pool_blocks (block skipped) */
@@ -110,6 +113,14 @@ typedef struct {
                                  (ALiBi). The packers write either form; the ALiBi calls require
                                  1, every other attention call and the materialiser require 0
                                  (LAZY_ERR_INVALID_ARG) */
+  int32_t kv_dtype;           /* 0: the pools have `dtype`. LAZY_FP8_E4M3: the pools hold one
+                                 e4m3 byte per element (same [block][head][16][d] layout), a
+                                 key's value is code * k_scale and a value's code * v_scale.
+                                 Only lazy_attn_decode (and _noalloc) with dtype LAZY_BF16 and
+                                 head_dim 128 take it; the other attention calls and the
+                                 materialiser return LAZY_ERR_UNSUPPORTED. Pools 16-byte aligned. */
+  float k_scale;              /* FP8 dequantisation scales: finite, > 0; 0 selects 1 */
+  float v_scale;
 } lazy_attn_params;
 
 /* Human-readable name of a lazy_status value. Never NULL. */

@@ -148,6 +148,30 @@ def _bits(t) -> tuple:
     raise TypeError(f"oracle reads fp32 or bf16 stored tensors, not {t.dtype}")
 
 
+def e4m3_decode(codes) -> np.ndarray:
+    """Values of OCP FP8 E4M3 codes (uint8 array), fp64, from the format's definition:
+    sign bit 7, exponent bits 6..3 with bias 7, mantissa bits 2..0; exponent 0 encodes
+    subnormals (-1)^s 2^-6 (m / 8); S.1111.111 is NaN; there are no infinities."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    s = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    val = np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1.0 + m / 8.0, (e - 7).astype(np.int64)))
+    val = s * val
+    return np.where((c & 0x7F) == 0x7F, np.nan, val)
+
+
+def fp8_pool_as_bf16(pool):
+    """An e4m3 pool (torch.float8_e4m3fn, CPU) as a bf16 tensor of the same values.
+    Every e4m3 value has at most 4 significant bits and an exponent in [-9, 8], so it
+    is exact in bf16; the conversion is checked."""
+    import torch
+    vals = e4m3_decode(pool.contiguous().view(torch.uint8).numpy())
+    out = torch.from_numpy(vals).to(torch.bfloat16)
+    assert np.array_equal(out.double().numpy(), vals, equal_nan=True)
+    return out
+
+
 def query_rows(w):
     """(q_seq, q_m) for every query row of a workload."""
     if w.kind == "decode":
@@ -161,13 +185,24 @@ def query_rows(w):
 
 def attention(w, rows: Optional[Sequence[int]] = None, sm_scale: float = 0.0,
               k_pool=None, v_pool=None, freqs: Optional[np.ndarray] = None, interleaved: bool = False,
-              rot_dims: Optional[int] = None, alibi: Optional[np.ndarray] = None) -> np.ndarray:
+              rot_dims: Optional[int] = None, alibi: Optional[np.ndarray] = None, k_scale: float = 1.0,
+              v_scale: float = 1.0) -> np.ndarray:
     """fp64 reference output of workload ``w`` for the query rows ``rows`` (all by
     default): decode rows are sequences, prefill rows are chunk tokens. ``freqs``
     replaces theta^(-2i/r); ``interleaved`` pairs dimensions (2i, 2i+1);
     ``rot_dims`` rotates only the first r dims (partial rotary; None: all);
     ``alibi`` [Hq] adds the bias -alibi[h] (m - n) to every score (ALiBi).
+    Pools of e4m3 codes (torch.float8_e4m3fn) hold keys code * k_scale and values
+    code * v_scale: the scores scale by k_scale (folded into the softmax scale) and
+    the output, linear in V, by v_scale.
     Returns [len(rows), Hq, d]."""
+    import torch
+    kp = w.k_pool if k_pool is None else k_pool
+    vp = w.v_pool if v_pool is None else v_pool
+    if kp.dtype == torch.float8_e4m3fn or vp.dtype == torch.float8_e4m3fn:
+        base = sm_scale if sm_scale > 0 else 1.0 / np.sqrt(w.head_dim)
+        return v_scale * attention(w, rows, base * k_scale, fp8_pool_as_bf16(kp), fp8_pool_as_bf16(vp), freqs,
+                                   interleaved, rot_dims, alibi)
     q_seq, q_m = query_rows(w)
     q = w.q
     if rows is not None:

@@ -80,9 +80,11 @@ bool encoder_ready() {
 // (bf16, 128-byte swizzle, no interleave, L2 promotion 256 B, no fill): a call with
 // the same pool pointers and shapes as a recent one reuses its maps.
 static bool encode_cached(CUtensorMap* m, cuuint32_t rank, const void* base, const cuuint64_t* dims,
-                          const cuuint64_t* strides, const cuuint32_t* box) {
+                          const cuuint64_t* strides, const cuuint32_t* box,
+                          CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   struct Entry {
     const void* base;
+    CUtensorMapDataType dtype;
     cuuint32_t rank;
     cuuint64_t dims[3], strides[2];
     cuuint32_t box[3];
@@ -93,6 +95,7 @@ static bool encode_cached(CUtensorMap* m, cuuint32_t rank, const void* base, con
   thread_local int next = 0;
   Entry key{};
   key.base = base;
+  key.dtype = dtype;
   key.rank = rank;
   for (cuuint32_t i = 0; i < rank; ++i) {
     key.dims[i] = dims[i];
@@ -100,7 +103,7 @@ static bool encode_cached(CUtensorMap* m, cuuint32_t rank, const void* base, con
     if (i + 1 < rank) key.strides[i] = strides[i];
   }
   for (Entry& e : cache)
-    if (e.valid && e.base == key.base && e.rank == key.rank && std::memcmp(e.dims, key.dims, sizeof(key.dims)) == 0 &&
+    if (e.valid && e.base == key.base && e.dtype == key.dtype && e.rank == key.rank && std::memcmp(e.dims, key.dims, sizeof(key.dims)) == 0 &&
         std::memcmp(e.strides, key.strides, sizeof(key.strides)) == 0 &&
         std::memcmp(e.box, key.box, sizeof(key.box)) == 0) {
       *m = e.map;
@@ -108,7 +111,7 @@ static bool encode_cached(CUtensorMap* m, cuuint32_t rank, const void* base, con
     }
   if (!encoder_ready()) return false;
   cuuint32_t es[3] = {1, 1, 1};
-  if (g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
+  if (g_encode(m, dtype, rank, const_cast<void*>(base), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
@@ -125,6 +128,14 @@ bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, int d, uin
   cuuint64_t strides[1] = {(cuuint64_t)d * 2};
   cuuint32_t box[2] = {64, box_rows};
   return encode_cached(m, 2, base, dims, strides, box);
+}
+
+// 2-D e4m3 view [rows][128] with 16-row x 128-byte boxes, 128-byte swizzle.
+bool encode_rows_map_fp8(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, box_rows};
+  return encode_cached(m, 2, base, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8);
 }
 
 // 3-D bf16 view of the same [rows][d] pool as (column in a 64-column half, row, half):
@@ -145,6 +156,9 @@ bool encode_q_map(CUtensorMap* m, const void* base, uint64_t total_q, int hq, in
   return encode_cached(m, 3, base, dims, strides, box);
 }
 
+// The pools hold e4m3 codes (FP8 KV; only the per-sequence decode reads them).
+static bool kv_fp8(const lazy_attn_params* p) { return p->kv_dtype == LAZY_FP8_E4M3 && p->dtype != LAZY_FP8_E4M3; }
+
 int check_params(const lazy_attn_params* p, Checked* c) {
   if (!p) return LAZY_ERR_INVALID_ARG;
   if (p->num_seqs < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 || p->num_q_heads % p->num_kv_heads != 0)
@@ -159,6 +173,9 @@ int check_params(const lazy_attn_params* p, Checked* c) {
   if (!(p->sm_scale >= 0.f) || !std::isfinite(p->sm_scale)) return LAZY_ERR_INVALID_ARG;
   if (p->num_splits < 0) return LAZY_ERR_INVALID_ARG;
   if (p->key_positions != 0 && p->key_positions != 1) return LAZY_ERR_INVALID_ARG;
+  if (p->kv_dtype != 0 && p->kv_dtype != p->dtype && p->kv_dtype != LAZY_FP8_E4M3) return LAZY_ERR_UNSUPPORTED;
+  if (!(p->k_scale >= 0.f) || !std::isfinite(p->k_scale) || !(p->v_scale >= 0.f) || !std::isfinite(p->v_scale))
+    return LAZY_ERR_INVALID_ARG;
   c->id_bits = p->id_bits ? p->id_bits : kDefaultIdBits;
   if (c->id_bits < 8 || c->id_bits > 24) return LAZY_ERR_INVALID_ARG;
   if ((int64_t)p->num_pool_blocks > ((int64_t)1 << c->id_bits)) return LAZY_ERR_INVALID_ARG;
@@ -364,6 +381,8 @@ static int decode_impl(const lazy_attn_params* p, const void* q, const void* k_p
   // key-position words carry no document start: only the ALiBi form reads them
   if (!alibi != !p->key_positions || (reinterpret_cast<uintptr_t>(alibi) & 3u)) return LAZY_ERR_INVALID_ARG;
   if (alibi && p->dtype != LAZY_BF16) return LAZY_ERR_UNSUPPORTED;
+  const bool fp8 = kv_fp8(p);
+  if (fp8 && (p->dtype != LAZY_BF16 || p->head_dim != 128 || alibi)) return LAZY_ERR_UNSUPPORTED;
   if (p->num_seqs == 0) return LAZY_OK;
   if (!q || !k_pool || !v_pool || !block_words || !seq_lens || !q_pos || !rope_table || !out)
     return LAZY_ERR_INVALID_ARG;
@@ -405,6 +424,13 @@ static int decode_impl(const lazy_attn_params* p, const void* q, const void* k_p
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (p->dtype == LAZY_F32) {
     rc = launched(lazy::launch_decode_f32(a, p->lazy != 0, cs));
+  } else if (fp8) {
+    CUtensorMap kmap, vmap;
+    const uint64_t rows = (uint64_t)p->num_pool_blocks * p->num_kv_heads * lazy::kBlock;
+    if (!encode_rows_map_fp8(&kmap, k_pool, rows, lazy::kBlock) || !encode_rows_map_fp8(&vmap, v_pool, rows, lazy::kBlock))
+      return LAZY_ERR_CUDA;
+    rc = launched(lazy::launch_decode_fp8(a, p->k_scale > 0.f ? p->k_scale : 1.f, p->v_scale > 0.f ? p->v_scale : 1.f,
+                                          p->lazy != 0, kmap, vmap, cs));
   } else {
     CUtensorMap kmap, vmap;
     const uint64_t rows = (uint64_t)p->num_pool_blocks * p->num_kv_heads * lazy::kBlock;
@@ -476,7 +502,7 @@ static int decode_shared_impl(const lazy_attn_params* p, const void* q, const vo
   int rc = check_params(p, &c);
   if (rc != LAZY_OK) return rc;
   if (!alibi != !p->key_positions || (reinterpret_cast<uintptr_t>(alibi) & 3u)) return LAZY_ERR_INVALID_ARG;
-  if (p->dtype != LAZY_BF16) return LAZY_ERR_UNSUPPORTED;
+  if (p->dtype != LAZY_BF16 || kv_fp8(p)) return LAZY_ERR_UNSUPPORTED;
   if (c.G > 64) return LAZY_ERR_UNSUPPORTED;
   if (num_items < 0 || num_slots < 0) return LAZY_ERR_INVALID_ARG;
   if (p->num_seqs == 0) return LAZY_OK;
@@ -586,7 +612,7 @@ int lazy_attn_prefill(const lazy_attn_params* p, const void* q, const int32_t* c
   Checked c;
   int rc = check_params(p, &c);
   if (rc != LAZY_OK) return rc;
-  if (p->dtype != LAZY_BF16 || p->head_dim != 128) return LAZY_ERR_UNSUPPORTED;
+  if (p->dtype != LAZY_BF16 || p->head_dim != 128 || kv_fp8(p)) return LAZY_ERR_UNSUPPORTED;
   if (total_q < 0 || max_q_len < 0 || p->key_positions) return LAZY_ERR_INVALID_ARG;
   if (p->num_seqs == 0 || total_q == 0 || max_q_len == 0) return LAZY_OK;
   if (!q || !cu_seqlens_q || !q_start || !k_pool || !v_pool || !block_words || !seq_lens || !rope_table || !out)
@@ -642,7 +668,7 @@ int lazy_attn_materialize(const lazy_attn_params* p, const void* k_pool, const v
   Checked c;
   int rc = check_params(p, &c);
   if (rc != LAZY_OK) return rc;
-  if (p->dtype != LAZY_BF16) return LAZY_ERR_UNSUPPORTED;
+  if (p->dtype != LAZY_BF16 || kv_fp8(p)) return LAZY_ERR_UNSUPPORTED;
   if (p->key_positions) return LAZY_ERR_INVALID_ARG;
   if (p->num_seqs == 0) return LAZY_OK;
   if (!k_pool || !v_pool || !block_words || !seq_lens || !rope_table || !k_out || !v_out || !block_words_out)
@@ -665,6 +691,7 @@ int lazy_attn_debug_gather(const lazy_attn_params* p, const void* k_pool, const 
   Checked c;
   int rc = check_params(p, &c);
   if (rc != LAZY_OK) return rc;
+  if (kv_fp8(p)) return LAZY_ERR_UNSUPPORTED;
   if (p->num_seqs == 0) return LAZY_OK;
   if (!k_pool || !v_pool || !block_words || !seq_lens || !k_out || !v_out) return LAZY_ERR_INVALID_ARG;
   if (p->num_pool_blocks == 0 || p->max_blocks_per_seq == 0) return LAZY_ERR_INVALID_ARG;

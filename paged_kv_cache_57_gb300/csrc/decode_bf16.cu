@@ -38,7 +38,10 @@
 
 namespace lazy {
 
-template <int D, int MT, int SPT>
+// FP8: each ring stage holds one block's e4m3 K and V (one 16-row x 128-byte box each),
+// and every team has one more buffer where the block is converted to f16 in the
+// bf16 path's tile layout.
+template <int D, int MT, int SPT, bool FP8 = false>
 struct DecodeCfg {
   static constexpr int TEAMS = (MT >= 4) ? 2 : 4;
   static constexpr int CW = TEAMS * MT;  // warps
@@ -47,11 +50,13 @@ struct DecodeCfg {
   static constexpr int NBOX = D / 64;  // 64-column (128-byte) TMA boxes per row
   static constexpr int BOX_BYTES = kBlock * 128;
   static constexpr int KV_BYTES = NBOX * BOX_BYTES;
-  static constexpr int STAGE_BYTES = 2 * KV_BYTES;
+  static constexpr int STAGE_BYTES = FP8 ? 2 * kBlock * D : 2 * KV_BYTES;
+  static constexpr int CONV_BYTES = FP8 ? 2 * KV_BYTES : 0;
+  static constexpr int TEAM_BYTES = SPT * STAGE_BYTES + CONV_BYTES;
   static constexpr int ROWS = MT * 16;
   static constexpr int QS_STRIDE = D + 8;  // fp32 q rows, padded against bank conflicts
   static constexpr int MERGE_BYTES = TEAMS * ROWS * (D + 2) * 4;
-  static constexpr int RING_BYTES = TEAMS * SPT * STAGE_BYTES;
+  static constexpr int RING_BYTES = TEAMS * TEAM_BYTES;
   static constexpr int STAGES_BYTES =
       ((RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES) + 1023) / 1024 * 1024;
   static constexpr int QS_BYTES = ROWS * QS_STRIDE * 4;
@@ -82,7 +87,7 @@ __device__ __forceinline__ LaneBlock describe_block(bool live, int b, int nb, in
 // halves of the same rotate-half pairs, so each pair is rotated by one thread.
 // cs_of(ks, i) returns (cos, sin) for frequency i and is called by all lanes
 // with the same ks sequence (it may shuffle).
-template <int D, int QS_STRIDE, typename CsFn>
+template <int D, int QS_STRIDE, bool F16 = false, typename CsFn>
 __device__ __forceinline__ void build_q_frags(uint32_t (&qa)[D / 16][4], const float* __restrict__ qs, int mt,
                                               int lane, float scale, CsFn cs_of) {
   constexpr int HALF = D / 2;
@@ -111,26 +116,69 @@ __device__ __forceinline__ void build_q_frags(uint32_t (&qa)[D / 16][4], const f
       yr[1][2 * e2] = fmaf(y1.x, c0.x, x1.x * c0.y);
       yr[1][2 * e2 + 1] = fmaf(y1.y, c1.x, x1.y * c1.y);
     }
-    qa[ks][0] = pack_bf16x2(xr[0][0], xr[0][1]);
-    qa[ks][1] = pack_bf16x2(xr[1][0], xr[1][1]);
-    qa[ks][2] = pack_bf16x2(xr[0][2], xr[0][3]);
-    qa[ks][3] = pack_bf16x2(xr[1][2], xr[1][3]);
-    qa[ks + D / 32][0] = pack_bf16x2(yr[0][0], yr[0][1]);
-    qa[ks + D / 32][1] = pack_bf16x2(yr[1][0], yr[1][1]);
-    qa[ks + D / 32][2] = pack_bf16x2(yr[0][2], yr[0][3]);
-    qa[ks + D / 32][3] = pack_bf16x2(yr[1][2], yr[1][3]);
+    qa[ks][0] = pack_op2<F16>(xr[0][0], xr[0][1]);
+    qa[ks][1] = pack_op2<F16>(xr[1][0], xr[1][1]);
+    qa[ks][2] = pack_op2<F16>(xr[0][2], xr[0][3]);
+    qa[ks][3] = pack_op2<F16>(xr[1][2], xr[1][3]);
+    qa[ks + D / 32][0] = pack_op2<F16>(yr[0][0], yr[0][1]);
+    qa[ks + D / 32][1] = pack_op2<F16>(yr[1][0], yr[1][1]);
+    qa[ks + D / 32][2] = pack_op2<F16>(yr[0][2], yr[0][3]);
+    qa[ks + D / 32][3] = pack_op2<F16>(yr[1][2], yr[1][3]);
   }
 }
 
 // ALIBI (with LAZY = false, key-position words): q is built once (the caller's table
 // has zero rates: no rotation), and every score of row r gets slope_r (n - m) in log2
 // units, n = the block word's position + slot, m = q_pos.
-template <int D, int MT, int SPT, bool LAZY, bool ALIBI = false>
+// Issues the TMA loads of one block's e4m3 K and V rows (kv head kvh, d = 128: one
+// 16-row x 128-byte box each) into `stage`; an id outside the pool is not loaded.
+__device__ __forceinline__ void load_block_fp8(uint8_t* stage, uint64_t* bar, int phys, int num_pool_blocks, int hkv,
+                                               int kvh, const CUtensorMap* kmap, const CUtensorMap* vmap) {
+  if (phys < num_pool_blocks) {
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, 2 * kBlock * 128);
+    const int y = (phys * hkv + kvh) * kBlock;
+    tma_load_2d(stage, kmap, bar, 0, y);
+    tma_load_2d(stage + kBlock * 128, vmap, bar, 0, y);
+  } else {
+    mbar_arrive(bar);
+  }
+}
+
+// Converts one landed e4m3 block (K box then V box, 16 rows x 128 bytes, 128-byte
+// swizzle: 16-byte chunk c of row r at r * 128 + ((c ^ r) & 7) * 16) into f16 tiles
+// laid out as the bf16 path's (per 64-column box of 2048 bytes, the same swizzle),
+// so that the ldmatrix fragments of attend_block_impl read them unchanged. Thread
+// tid of nt; a chunk of 16 codes becomes two 16-byte f16 chunks.
+__device__ __forceinline__ void convert_fp8_block(const uint8_t* src, uint8_t* dst, int tid, int nt) {
+  using G = BlockGeom<128>;
+  for (int it = tid; it < 2 * kBlock * 8; it += nt) {
+    const int kv = it >> 7, r = (it >> 3) & 15, c = it & 7;
+    const uint4 x = *reinterpret_cast<const uint4*>(src + kv * (kBlock * 128) + r * 128 + (((c ^ r) & 7) << 4));
+    uint4 lo, hi;
+    e4m3x4_to_f16x4(x.x, lo.x, lo.y);
+    e4m3x4_to_f16x4(x.y, lo.z, lo.w);
+    e4m3x4_to_f16x4(x.z, hi.x, hi.y);
+    e4m3x4_to_f16x4(x.w, hi.z, hi.w);
+    uint8_t* row = dst + kv * G::KV_BYTES + (c >> 2) * G::BOX_BYTES + r * 128;
+    const int ch = 2 * (c & 3);  // f16 columns 16c .. 16c + 15: chunks ch, ch + 1 of box c / 4
+    *reinterpret_cast<uint4*>(row + (((ch ^ r) & 7) << 4)) = lo;
+    *reinterpret_cast<uint4*>(row + ((((ch + 1) ^ r) & 7) << 4)) = hi;
+  }
+}
+
+// FP8 (D = 128): the pools hold e4m3 codes. Each block lands in the ring as codes,
+// the team converts it (exactly) to f16 in its conversion buffer, and the block is
+// attended with f16 operands, scores scaled by k_scale; the output is scaled by
+// v_scale.
+template <int D, int MT, int SPT, bool LAZY, bool ALIBI = false, bool FP8 = false>
 __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS, MT == 1 ? 3 : 1)
-    decode_bf16_kernel(const std::conditional_t<ALIBI, DecodeAlibiArgs, DecodeArgs> a,
+    decode_bf16_kernel(const std::conditional_t<ALIBI, DecodeAlibiArgs,
+                                                std::conditional_t<FP8, DecodeFp8Args, DecodeArgs>> a,
                        const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
   static_assert(!(ALIBI && LAZY), "the ALiBi variant does not rotate");
-  using C = DecodeCfg<D, MT, SPT>;
+  static_assert(!(ALIBI && FP8) && (!FP8 || D == 128), "FP8 KV: d = 128, no ALiBi");
+  using C = DecodeCfg<D, MT, SPT, FP8>;
   constexpr int HALF = C::HALF, CPL = (HALF + 31) / 32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stages = align1024(smem_raw);
@@ -172,9 +220,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS, MT == 1 ? 3 :
   const int per_team = (n + C::TEAMS - 1) / C::TEAMS;
   const int kb0 = team * per_team;
   const int nk = max(0, min(n, kb0 + per_team) - kb0);  // blocks of this team
-  uint8_t* tst = stages + team * SPT * C::STAGE_BYTES;
+  uint8_t* tst = stages + team * C::TEAM_BYTES;
+  const uint32_t conv = smem_u32(tst + SPT * C::STAGE_BYTES);  // FP8: the f16 tile buffer
   uint64_t* tfull = full + team * SPT;
   const bool leader = (mt == 0 && lane == 0);
+  auto issue_load = [&](uint8_t* stage, uint64_t* bar, int phys) {
+    if constexpr (FP8) load_block_fp8(stage, bar, phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
+    else load_block<D>(stage, bar, phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
+  };
   auto block_of = [&](int k) { return b0 + kb0 + k; };
   auto load_words = [&](int kc, uint32_t& w, uint32_t& wn) {
     const int k = kc + lane, b = block_of(k);
@@ -195,7 +248,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS, MT == 1 ? 3 :
     const int pro = min(SPT, nk);
     for (int k = 0; k < pro; ++k) {
       const int phys = __shfl_sync(0xffffffffu, cur.phys, k);
-      if (leader) load_block<D>(tst + k * C::STAGE_BYTES, &tfull[k], phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
+      if (leader) issue_load(tst + k * C::STAGE_BYTES, &tfull[k], phys);
     }
     issued = pro;
   }
@@ -209,7 +262,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS, MT == 1 ? 3 :
   auto rebuild = [&](int delta) {
 #pragma unroll
     for (int j = 0; j < CPL; ++j) cs[j] = rope_cs(tr[j], delta, a.status);
-    build_q_frags<D, C::QS_STRIDE>(qa, qs, mt, lane, a.scale_log2, [&](int ks, int i) {
+    build_q_frags<D, C::QS_STRIDE, FP8>(qa, qs, mt, lane, a.scale_log2, [&](int ks, int i) {
       const float2 v = cs[(16 * ks) >> 5];
       return make_float2(__shfl_sync(0xffffffffu, v.x, i & 31), __shfl_sync(0xffffffffu, v.y, i & 31));
     });
@@ -259,6 +312,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS, MT == 1 ? 3 :
       const int pk = __shfl_sync(0xffffffffu, cur.p, k & 31);  // this block's first key position
       const float b0[2] = {ab_slope[0] * (float)(pk - m_pos), ab_slope[1] * (float)(pk - m_pos)};
       if (ok) attend_block_bias<D>(smem_u32(tst + slot * C::STAGE_BYTES), ln, qa, nvalid, o, m_r, l_r, lane, b0, ab_slope);
+    } else if constexpr (FP8) {
+      if (ok) convert_fp8_block(tst + slot * C::STAGE_BYTES, tst + SPT * C::STAGE_BYTES, 32 * mt + lane, 32 * MT);
+      // the team's f16 tiles are complete before any warp reads them
+      if constexpr (MT > 1) ok = team_and(team, 32 * MT, ok);
+      else __syncwarp();
+      if (ok) attend_block_f16<D>(conv, ln, qa, nvalid, o, m_r, l_r, lane, a.k_scale);
     } else {
       if (ok) attend_block<D>(smem_u32(tst + slot * C::STAGE_BYTES), ln, qa, nvalid, o, m_r, l_r, lane);
     }
@@ -283,8 +342,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS, MT == 1 ? 3 :
         }
         phys = __shfl_sync(0xffffffffu, nxt.phys, kn & 31);
       }
-      if (leader) load_block<D>(tst + slot * C::STAGE_BYTES, &tfull[slot], phys, a.num_pool_blocks, a.Hkv, kvh, &kmap,
-                                &vmap);
+      if (leader) issue_load(tst + slot * C::STAGE_BYTES, &tfull[slot], phys);
       issued = kn + 1;
     }
   }
@@ -307,10 +365,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS, MT == 1 ? 3 :
       const int row = mt * 16 + g + 8 * rr;
       if (row < a.G) {
         float* dst = red + ((size_t)team * C::ROWS + row) * (D + 2);
+        float vs = 1.f;
+        if constexpr (FP8) vs = a.v_scale;
 #pragma unroll
         for (int j = 0; j < D / 8; ++j) {
-          dst[8 * j + 2 * t] = o[j][2 * rr];
-          dst[8 * j + 2 * t + 1] = o[j][2 * rr + 1];
+          dst[8 * j + 2 * t] = o[j][2 * rr] * vs;
+          dst[8 * j + 2 * t + 1] = o[j][2 * rr + 1] * vs;
         }
         if (t == 0) {
           dst[D] = m_r[rr];
@@ -498,16 +558,24 @@ __global__ void __launch_bounds__(64) gather_bf16_kernel(const GatherArgs a, con
 
 // ------------------------------------------------------------------ launchers
 
-template <int D, int MT, bool LAZY, bool ALIBI>
+template <int D, int MT, bool LAZY, bool ALIBI, bool FP8 = false>
 static cudaError_t launch_decode_t(const DecodeArgs& a, const float* alibi, const CUtensorMap& kmap,
-                                   const CUtensorMap& vmap, cudaStream_t st) {
+                                   const CUtensorMap& vmap, cudaStream_t st, float k_scale = 1.f,
+                                   float v_scale = 1.f) {
   constexpr int SPT = LAZY_DECODE_SPT;
-  using C = DecodeCfg<D, MT, SPT>;
-  auto kern = decode_bf16_kernel<D, MT, SPT, LAZY, ALIBI>;
-  cudaError_t e = set_smem_once<decode_bf16_kernel<D, MT, SPT, LAZY, ALIBI>>(C::SMEM);
+  using C = DecodeCfg<D, MT, SPT, FP8>;
+  auto kern = decode_bf16_kernel<D, MT, SPT, LAZY, ALIBI, FP8>;
+  cudaError_t e = set_smem_once<decode_bf16_kernel<D, MT, SPT, LAZY, ALIBI, FP8>>(C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(a.splits, a.Hkv, a.B);
-  if constexpr (ALIBI) {
+  if constexpr (FP8) {
+    (void)alibi;
+    DecodeFp8Args fa;
+    static_cast<DecodeArgs&>(fa) = a;
+    fa.k_scale = k_scale;
+    fa.v_scale = v_scale;
+    kern<<<grid, C::NTHREADS, C::SMEM, st>>>(fa, kmap, vmap);
+  } else if constexpr (ALIBI) {
     DecodeAlibiArgs aa;
     static_cast<DecodeArgs&>(aa) = a;
     aa.alibi = alibi;
@@ -544,6 +612,21 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, const float* alibi, bool laz
                 : dispatch_mt<128, false, false>(a, nullptr, kmap, vmap, st);
   return lazy ? dispatch_mt<64, true, false>(a, nullptr, kmap, vmap, st)
               : dispatch_mt<64, false, false>(a, nullptr, kmap, vmap, st);
+}
+
+template <bool LAZY>
+static cudaError_t dispatch_fp8(const DecodeArgs& a, float ks, float vs, const CUtensorMap& kmap,
+                                const CUtensorMap& vmap, cudaStream_t st) {
+  if (a.G <= 16) return launch_decode_t<128, 1, LAZY, false, true>(a, nullptr, kmap, vmap, st, ks, vs);
+  if (a.G <= 32) return launch_decode_t<128, 2, LAZY, false, true>(a, nullptr, kmap, vmap, st, ks, vs);
+  return launch_decode_t<128, 4, LAZY, false, true>(a, nullptr, kmap, vmap, st, ks, vs);
+}
+
+cudaError_t launch_decode_fp8(const DecodeArgs& a, float k_scale, float v_scale, bool lazy, const CUtensorMap& kmap,
+                              const CUtensorMap& vmap, cudaStream_t st) {
+  if (a.D != 128) return cudaErrorInvalidValue;
+  return lazy ? dispatch_fp8<true>(a, k_scale, v_scale, kmap, vmap, st)
+              : dispatch_fp8<false>(a, k_scale, v_scale, kmap, vmap, st);
 }
 
 cudaError_t launch_combine(const DecodeArgs& a, bool out_bf16, cudaStream_t st) {

@@ -71,11 +71,19 @@ constexpr float kDecodeRescaleLog2 = 8.f;
 // come out in log2 units. Only the first `nvalid` slots of the block are keys;
 // the others (holes, an unloaded block) get weight 0 and their V rows are masked
 // out of the product. With BIAS, row g + 8 rr's score of key k also gets
-// bias0[rr] + slope[rr] * k (log2 units; the ALiBi bias of the shared-run decode).
-template <int D, bool BIAS>
+// bias0[rr] + slope[rr] * k (log2 units; the ALiBi bias). With F16 the operands
+// (q fragments, the K/V tiles, P) are f16 instead of bf16 and every score is
+// multiplied by sscale first (the FP8-KV decode: the tiles hold unscaled e4m3
+// values, sscale is the K scale).
+template <int D, bool BIAS, bool F16 = false>
 __device__ __forceinline__ void attend_block_impl(uint32_t kbase, LdsmLane ln, const uint32_t (&qa)[D / 16][4],
                                                   int nvalid, float (&o)[D / 8][4], float (&m_r)[2], float (&l_r)[2],
-                                                  int lane, const float* bias0, const float* slope) {
+                                                  int lane, const float* bias0, const float* slope,
+                                                  float sscale = 1.f) {
+  auto mma = [](float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    if constexpr (F16) mma_16816_f16(d, a, b0, b1);
+    else mma_16816(d, a, b0, b1);
+  };
   using G = BlockGeom<D>;
   const int t = lane & 3;
   const uint32_t ka = kbase + ln.k;
@@ -91,8 +99,8 @@ __device__ __forceinline__ void attend_block_impl(uint32_t kbase, LdsmLane ln, c
   for (int ks = 0; ks < D / 16; ++ks) {
     uint32_t r[4];
     ldsm_x4(r, (ka ^ (uint32_t)(((2 * ks) & 7) << 4)) + (ks >> 2) * G::BOX_BYTES);
-    mma_16816(sc[0][ks & 1], qa[ks], r[0], r[1]);
-    mma_16816(sc[1][ks & 1], qa[ks], r[2], r[3]);
+    mma(sc[0][ks & 1], qa[ks], r[0], r[1]);
+    mma(sc[1][ks & 1], qa[ks], r[2], r[3]);
   }
   // sv[rr][e]: row g + 8 rr, key (e >> 1) * 8 + 2t + (e & 1).
   float sv[2][4];
@@ -100,6 +108,12 @@ __device__ __forceinline__ void attend_block_impl(uint32_t kbase, LdsmLane ln, c
   for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
     for (int e = 0; e < 4; ++e) sv[rr][e] = sc[e >> 1][0][2 * rr + (e & 1)] + sc[e >> 1][1][2 * rr + (e & 1)];
+  if constexpr (F16) {
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sv[rr][e] *= sscale;
+  }
   if constexpr (BIAS) {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr)
@@ -131,13 +145,12 @@ __device__ __forceinline__ void attend_block_impl(uint32_t kbase, LdsmLane ln, c
       }
     }
     const float mu = m_r[rr] == -INFINITY ? 0.f : m_r[rr];
-    const uint32_t lo = pack_bf16x2(fast_ex2(sv[rr][0] - mu), fast_ex2(sv[rr][1] - mu));
-    const uint32_t hi = pack_bf16x2(fast_ex2(sv[rr][2] - mu), fast_ex2(sv[rr][3] - mu));
+    const uint32_t lo = pack_op2<F16>(fast_ex2(sv[rr][0] - mu), fast_ex2(sv[rr][1] - mu));
+    const uint32_t hi = pack_op2<F16>(fast_ex2(sv[rr][2] - mu), fast_ex2(sv[rr][3] - mu));
     pa[rr] = lo;      // keys 2t, 2t+1     (a0 / a1)
     pa[2 + rr] = hi;  // keys 8+2t, 8+2t+1 (a2 / a3)
-    // The row sum uses the same bf16-rounded weights as the product.
-    l_r[rr] += (__uint_as_float(lo << 16) + __uint_as_float(lo & 0xffff0000u)) +
-               (__uint_as_float(hi << 16) + __uint_as_float(hi & 0xffff0000u));
+    // The row sum uses the same rounded weights as the product.
+    l_r[rr] += sum_op2<F16>(lo) + sum_op2<F16>(hi);
   }
   // O += P V: V^T fragments via ldmatrix.trans, two d-tiles per load.
   if (!partial) {
@@ -145,8 +158,8 @@ __device__ __forceinline__ void attend_block_impl(uint32_t kbase, LdsmLane ln, c
     for (int c = 0; c < D / 16; ++c) {
       uint32_t r[4];
       ldsm_x4_trans(r, (va ^ (uint32_t)(((2 * c) & 7) << 4)) + (c >> 2) * G::BOX_BYTES);
-      mma_16816(o[2 * c], pa, r[0], r[1]);
-      mma_16816(o[2 * c + 1], pa, r[2], r[3]);
+      mma(o[2 * c], pa, r[0], r[1]);
+      mma(o[2 * c + 1], pa, r[2], r[3]);
     }
   } else {  // hole slots may hold anything (even NaN): zero their V
     const int k0 = 2 * t;
@@ -156,8 +169,8 @@ __device__ __forceinline__ void attend_block_impl(uint32_t kbase, LdsmLane ln, c
     for (int c = 0; c < D / 16; ++c) {
       uint32_t r[4];
       ldsm_x4_trans(r, (va ^ (uint32_t)(((2 * c) & 7) << 4)) + (c >> 2) * G::BOX_BYTES);
-      mma_16816(o[2 * c], pa, r[0] & m0, r[1] & m1);
-      mma_16816(o[2 * c + 1], pa, r[2] & m0, r[3] & m1);
+      mma(o[2 * c], pa, r[0] & m0, r[1] & m1);
+      mma(o[2 * c + 1], pa, r[2] & m0, r[3] & m1);
     }
   }
 }
@@ -173,6 +186,14 @@ __device__ __forceinline__ void attend_block_bias(uint32_t kbase, LdsmLane ln, c
                                                   int nvalid, float (&o)[D / 8][4], float (&m_r)[2], float (&l_r)[2],
                                                   int lane, const float (&bias0)[2], const float (&slope)[2]) {
   attend_block_impl<D, true>(kbase, ln, qa, nvalid, o, m_r, l_r, lane, bias0, slope);
+}
+
+// f16 operands, scores scaled by kscale (the FP8-KV decode).
+template <int D>
+__device__ __forceinline__ void attend_block_f16(uint32_t kbase, LdsmLane ln, const uint32_t (&qa)[D / 16][4],
+                                                 int nvalid, float (&o)[D / 8][4], float (&m_r)[2], float (&l_r)[2],
+                                                 int lane, float kscale) {
+  attend_block_impl<D, false, true>(kbase, ln, qa, nvalid, o, m_r, l_r, lane, nullptr, nullptr, kscale);
 }
 
 // Per-lane description of one logical block: physical id (num_pool_blocks for a

@@ -49,6 +49,12 @@ struct DecodeAlibiArgs : DecodeArgs {
   const float* alibi;  // [Hq] slopes
 };
 
+// FP8-KV decode: pools hold e4m3 codes; a key's value is code * k_scale, a value
+// row's code * v_scale.
+struct DecodeFp8Args : DecodeArgs {
+  float k_scale, v_scale;
+};
+
 struct GatherArgs {
   const uint32_t* words;
   const int32_t* seq_lens;
@@ -163,6 +169,10 @@ cudaError_t launch_decode_f32(const DecodeArgs& a, bool lazy, cudaStream_t st);
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const float* alibi, bool lazy, const CUtensorMap& kmap,
                                const CUtensorMap& vmap,
                                cudaStream_t st);
+// FP8-KV form of launch_decode_bf16 (D = 128): kmap / vmap are e4m3 [rows][128] maps
+// with 16-row x 128-byte boxes.
+cudaError_t launch_decode_fp8(const DecodeArgs& a, float k_scale, float v_scale, bool lazy, const CUtensorMap& kmap,
+                              const CUtensorMap& vmap, cudaStream_t st);
 cudaError_t launch_combine(const DecodeArgs& a, bool out_bf16, cudaStream_t st);
 cudaError_t launch_gather_bf16(const GatherArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                cudaStream_t st);

@@ -24,7 +24,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 LAZY_OK, LAZY_ERR_INVALID_ARG, LAZY_ERR_UNSUPPORTED, LAZY_ERR_WORKSPACE, LAZY_ERR_LAYOUT, LAZY_ERR_CUDA, \
     LAZY_ERR_DEVICE = range(7)
-LAZY_F32, LAZY_BF16 = 0, 1
+LAZY_F32, LAZY_BF16, LAZY_FP8_E4M3 = 0, 1, 2
 LAZY_DEV_BAD_BLOCK_ID, LAZY_DEV_POS_RANGE, LAZY_DEV_TIMEOUT, LAZY_DEV_LAYOUT, LAZY_DEV_BAD_LEN = 1, 2, 4, 8, 16
 BLOCK = 16
 
@@ -51,7 +51,8 @@ class Params(ctypes.Structure):
         ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32), ("num_pool_blocks", ctypes.c_int32),
         ("max_blocks_per_seq", ctypes.c_int32), ("id_bits", ctypes.c_int32), ("dtype", ctypes.c_int32),
         ("lazy", ctypes.c_int32), ("rope_theta", ctypes.c_double), ("sm_scale", ctypes.c_float),
-        ("num_splits", ctypes.c_int32), ("key_positions", ctypes.c_int32),
+        ("num_splits", ctypes.c_int32), ("key_positions", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
+        ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
     ]
 
 
@@ -106,10 +107,13 @@ def _check(rc: int, where: str) -> None:
 
 def make_params(*, num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int, num_pool_blocks: int,
                 max_blocks_per_seq: int, dtype: str = "bf16", rope_theta: float = 5e5, lazy: bool = True,
-                sm_scale: float = 0.0, id_bits: int = 0, num_splits: int = 0, key_positions: bool = False) -> Params:
+                sm_scale: float = 0.0, id_bits: int = 0, num_splits: int = 0, key_positions: bool = False,
+                kv_dtype: Optional[str] = None, k_scale: float = 0.0, v_scale: float = 0.0) -> Params:
+    """kv_dtype "fp8_e4m3": pools of e4m3 codes (torch.float8_e4m3fn), values code * k_scale / v_scale."""
+    kv = 0 if kv_dtype is None else {"fp8_e4m3": LAZY_FP8_E4M3}[kv_dtype]
     return Params(num_seqs, num_q_heads, num_kv_heads, head_dim, BLOCK, num_pool_blocks, max_blocks_per_seq,
                   id_bits, LAZY_BF16 if dtype == "bf16" else LAZY_F32, int(bool(lazy)), float(rope_theta),
-                  float(sm_scale), num_splits, int(bool(key_positions)))
+                  float(sm_scale), num_splits, int(bool(key_positions)), kv, float(k_scale), float(v_scale))
 
 
 def _dptr(t: Optional[torch.Tensor], name: str, dtype=None, device_required=True):
@@ -132,6 +136,11 @@ def _stream(stream) -> int:
 
 def _tdt(p: Params):
     return torch.bfloat16 if p.dtype == LAZY_BF16 else torch.float32
+
+
+def _kvdt(p: Params):
+    """torch dtype of the pools."""
+    return torch.float8_e4m3fn if p.kv_dtype == LAZY_FP8_E4M3 else _tdt(p)
 
 
 # ---------------------------------------------------------------- rotation table
@@ -247,7 +256,7 @@ def decode(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tenso
     if workspace is None and nws:
         workspace = torch.empty(nws, dtype=torch.uint8, device=q.device)
     wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    head = (ctypes.byref(p), _dptr(q, "q", dt), _dptr(k_pool, "k_pool", dt), _dptr(v_pool, "v_pool", dt),
+    head = (ctypes.byref(p), _dptr(q, "q", dt), _dptr(k_pool, "k_pool", _kvdt(p)), _dptr(v_pool, "v_pool", _kvdt(p)),
             _dptr(block_words, "block_words"), _dptr(seq_lens, "seq_lens", torch.int32),
             _dptr(q_pos, "q_pos", torch.int32), _dptr(rope_table, "rope_table"))
     tail = (_dptr(out, "out", dt), _dptr(workspace, "workspace"), wsz, _stream(stream))
@@ -268,8 +277,8 @@ def decode_noalloc(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: tor
     that cannot allocate a workspace). ``out`` is required: the call allocates nothing.
     Calls that overlap on the GPU share that array and must not run concurrently."""
     dt = _tdt(p)
-    rc = _lib.lazy_attn_decode_noalloc(ctypes.byref(p), _dptr(q, "q", dt), _dptr(k_pool, "k_pool", dt),
-                                       _dptr(v_pool, "v_pool", dt), _dptr(block_words, "block_words"),
+    rc = _lib.lazy_attn_decode_noalloc(ctypes.byref(p), _dptr(q, "q", dt), _dptr(k_pool, "k_pool", _kvdt(p)),
+                                       _dptr(v_pool, "v_pool", _kvdt(p)), _dptr(block_words, "block_words"),
                                        _dptr(seq_lens, "seq_lens", torch.int32), _dptr(q_pos, "q_pos", torch.int32),
                                        _dptr(rope_table, "rope_table"), _dptr(out, "out", dt), _stream(stream))
     _check(rc, "decode_noalloc")

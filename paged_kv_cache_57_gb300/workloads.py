@@ -375,3 +375,17 @@ def kv_bytes_unique(w: Workload) -> int:
     """K+V bytes of the distinct physical blocks touched: the lower bound on DRAM reads."""
     elt = 4 if w.dtype == "f32" else 2
     return w.unique_blocks() * BLOCK * w.num_kv_heads * w.head_dim * 2 * elt
+
+
+def fp8_pools(w: Workload):
+    """e4m3 copies of a workload's pools for the FP8-KV decode: per-tensor scales
+    amax / 448 (the largest e4m3 value; amax over the finite entries, hole slots keep
+    their non-finite filler as NaN codes), codes = round-to-nearest-even of x / scale.
+    Returns (k_codes, v_codes, k_scale, v_scale); codes are torch.float8_e4m3fn."""
+    out = []
+    for pool in (w.k_pool, w.v_pool):
+        x = pool.float()
+        fin = x[torch.isfinite(x)]
+        scale = (float(fin.abs().max()) / 448.0 if fin.numel() else 0.0) or 1.0
+        out.append(((x / scale).to(torch.float8_e4m3fn), scale))
+    return out[0][0], out[1][0], out[0][1], out[1][1]
