@@ -130,6 +130,41 @@ __device__ __forceinline__ void build_q_frags(uint32_t (&qa)[D / 16][4], const f
 // ALIBI (with LAZY = false, key-position words): q is built once (the caller's table
 // has zero rates: no rotation), and every score of row r gets slope_r (n - m) in log2
 // units, n = the block word's position + slot, m = q_pos.
+// f16 A fragments of scale * R_delta q (D = 128) in the permuted head-dimension order
+// of the FP8 decode's K fragments: k-step ks, columns 2t + {0,1} and 2t + 8 + {0,1}
+// hold dimensions 32t + 4ks + {0,1} and {2,3} (t = lane & 3), so lanes t = 0, 1 hold
+// first halves of rotate-half pairs and t = 2, 3 second halves. cs[j] is this lane's
+// (cos, sin) of frequency lane + 32 j.
+template <int QS_STRIDE>
+__device__ __forceinline__ void build_q_frags_perm(uint32_t (&qa)[8][4], const float* __restrict__ qs, int mt,
+                                                   int lane, float scale, const float2 (&cs)[2]) {
+  const int g = lane >> 2, t = lane & 3;
+  const bool second = t >= 2;
+  const float* r0 = qs + (mt * 16 + g) * QS_STRIDE;
+  const float* r1 = r0 + 8 * QS_STRIDE;
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    float v0[4], v1[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = 4 * ks + e;
+      const int d = 32 * t + i, dp = second ? d - 64 : d + 64;  // own dimension and its pair partner
+      // frequency d mod 64 = 32 (t & 1) + i: lane i's cs[t & 1]
+      const float2 ca = make_float2(__shfl_sync(0xffffffffu, cs[0].x, i), __shfl_sync(0xffffffffu, cs[0].y, i));
+      const float2 cb = make_float2(__shfl_sync(0xffffffffu, cs[1].x, i), __shfl_sync(0xffffffffu, cs[1].y, i));
+      const float c = ((t & 1) ? cb.x : ca.x) * scale;
+      const float sn = ((t & 1) ? cb.y : ca.y) * scale;
+      // first half: x c - y s; second half: y c + x s (own value times c, partner times s)
+      v0[e] = fmaf(r0[d], c, (second ? r0[dp] : -r0[dp]) * sn);
+      v1[e] = fmaf(r1[d], c, (second ? r1[dp] : -r1[dp]) * sn);
+    }
+    qa[ks][0] = pack_f16x2(v0[0], v0[1]);
+    qa[ks][1] = pack_f16x2(v1[0], v1[1]);
+    qa[ks][2] = pack_f16x2(v0[2], v0[3]);
+    qa[ks][3] = pack_f16x2(v1[2], v1[3]);
+  }
+}
+
 // Issues the TMA loads of one block's e4m3 K and V rows (kv head kvh, d = 128: one
 // 16-row x 128-byte box each) into `stage`; an id outside the pool is not loaded.
 __device__ __forceinline__ void load_block_fp8(uint8_t* stage, uint64_t* bar, int phys, int num_pool_blocks, int hkv,
@@ -148,11 +183,12 @@ __device__ __forceinline__ void load_block_fp8(uint8_t* stage, uint64_t* bar, in
 // Converts one landed e4m3 block (K box then V box, 16 rows x 128 bytes, 128-byte
 // swizzle: 16-byte chunk c of row r at r * 128 + ((c ^ r) & 7) * 16) into f16 tiles
 // laid out as the bf16 path's (per 64-column box of 2048 bytes, the same swizzle),
-// so that the ldmatrix fragments of attend_block_impl read them unchanged. Thread
-// tid of nt; a chunk of 16 codes becomes two 16-byte f16 chunks.
+// so that the ldmatrix fragments of attend_block_impl read them unchanged. Only the
+// V box is converted (K fragments come from the codes directly). Thread tid of nt; a
+// chunk of 16 codes becomes two 16-byte f16 chunks.
 __device__ __forceinline__ void convert_fp8_block(const uint8_t* src, uint8_t* dst, int tid, int nt) {
   using G = BlockGeom<128>;
-  for (int it = tid; it < 2 * kBlock * 8; it += nt) {
+  for (int it = kBlock * 8 + tid; it < 2 * kBlock * 8; it += nt) {  // V only: K fragments read the codes
     const int kv = it >> 7, r = (it >> 3) & 15, c = it & 7;
     const uint4 x = *reinterpret_cast<const uint4*>(src + kv * (kBlock * 128) + r * 128 + (((c ^ r) & 7) << 4));
     uint4 lo, hi;
@@ -262,10 +298,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS, MT == 1 ? 3 :
   auto rebuild = [&](int delta) {
 #pragma unroll
     for (int j = 0; j < CPL; ++j) cs[j] = rope_cs(tr[j], delta, a.status);
-    build_q_frags<D, C::QS_STRIDE, FP8>(qa, qs, mt, lane, a.scale_log2, [&](int ks, int i) {
-      const float2 v = cs[(16 * ks) >> 5];
-      return make_float2(__shfl_sync(0xffffffffu, v.x, i & 31), __shfl_sync(0xffffffffu, v.y, i & 31));
-    });
+    if constexpr (FP8) {
+      build_q_frags_perm<C::QS_STRIDE>(qa, qs, mt, lane, a.scale_log2, cs);
+    } else {
+      build_q_frags<D, C::QS_STRIDE>(qa, qs, mt, lane, a.scale_log2, [&](int ks, int i) {
+        const float2 v = cs[(16 * ks) >> 5];
+        return make_float2(__shfl_sync(0xffffffffu, v.x, i & 31), __shfl_sync(0xffffffffu, v.y, i & 31));
+      });
+    }
   };
   if constexpr (!LAZY) rebuild(m_pos);  // control: pool holds absolute-position keys, rotate q once by R_m
   float ab_slope[2] = {0.f, 0.f};
@@ -317,7 +357,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS, MT == 1 ? 3 :
       // the team's f16 tiles are complete before any warp reads them
       if constexpr (MT > 1) ok = team_and(team, 32 * MT, ok);
       else __syncwarp();
-      if (ok) attend_block_f16<D>(conv, ln, qa, nvalid, o, m_r, l_r, lane, a.k_scale);
+      if constexpr (FP8) {  // always true here; keeps the D = 128 call out of other instantiations
+        if (ok)
+          attend_block_fp8(smem_u32(tst + slot * C::STAGE_BYTES), conv + C::KV_BYTES, ln, qa, nvalid, o, m_r, l_r,
+                           lane, a.k_scale);
+      }
     } else {
       if (ok) attend_block<D>(smem_u32(tst + slot * C::STAGE_BYTES), ln, qa, nvalid, o, m_r, l_r, lane);
     }

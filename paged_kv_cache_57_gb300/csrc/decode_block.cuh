@@ -75,11 +75,19 @@ constexpr float kDecodeRescaleLog2 = 8.f;
 // (q fragments, the K/V tiles, P) are f16 instead of bf16 and every score is
 // multiplied by sscale first (the FP8-KV decode: the tiles hold unscaled e4m3
 // values, sscale is the K scale).
-template <int D, bool BIAS, bool F16 = false>
+//
+// With KFP8 (D = 128, implies F16) kbase is the block's e4m3 K box (16 rows x 128
+// bytes, 128-byte swizzle) and the K fragments are converted from it directly; the
+// q fragments then follow the permuted head-dimension order of build_q_frags_perm
+// (k-step ks, fragment column 2t + {0,1} / 2t + 8 + {0,1} is dimension
+// 32t + 4ks + {0,1} / {2,3}), so each lane's four codes of a k-step are one word. V
+// comes from the f16 tile at vbase.
+template <int D, bool BIAS, bool F16 = false, bool KFP8 = false>
 __device__ __forceinline__ void attend_block_impl(uint32_t kbase, LdsmLane ln, const uint32_t (&qa)[D / 16][4],
                                                   int nvalid, float (&o)[D / 8][4], float (&m_r)[2], float (&l_r)[2],
                                                   int lane, const float* bias0, const float* slope,
-                                                  float sscale = 1.f) {
+                                                  float sscale = 1.f, uint32_t vbase = 0) {
+  static_assert(!KFP8 || (F16 && D == 128), "e4m3 K fragments: f16 operands, d = 128");
   auto mma = [](float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     if constexpr (F16) mma_16816_f16(d, a, b0, b1);
     else mma_16816(d, a, b0, b1);
@@ -87,7 +95,7 @@ __device__ __forceinline__ void attend_block_impl(uint32_t kbase, LdsmLane ln, c
   using G = BlockGeom<D>;
   const int t = lane & 3;
   const uint32_t ka = kbase + ln.k;
-  const uint32_t va = kbase + G::KV_BYTES + ln.v;
+  const uint32_t va = (KFP8 ? vbase : kbase + G::KV_BYTES) + ln.v;
   // S = q' K^T for the 16 keys: two n-tiles of 8 keys, each summed in two
   // independent chains (even and odd k-steps) to halve the dependent MMA latency.
   float sc[2][2][4];
@@ -95,12 +103,32 @@ __device__ __forceinline__ void attend_block_impl(uint32_t kbase, LdsmLane ln, c
   for (int n = 0; n < 2; ++n)
 #pragma unroll
     for (int c = 0; c < 2; ++c) sc[n][c][0] = sc[n][c][1] = sc[n][c][2] = sc[n][c][3] = 0.f;
+  if constexpr (KFP8) {
+    // keys g and g + 8 (rows of the box; (g + 8) & 7 == g), 16-byte chunks 2t and 2t + 1
+    const int g8 = lane >> 2;
 #pragma unroll
-  for (int ks = 0; ks < D / 16; ++ks) {
-    uint32_t r[4];
-    ldsm_x4(r, (ka ^ (uint32_t)(((2 * ks) & 7) << 4)) + (ks >> 2) * G::BOX_BYTES);
-    mma(sc[0][ks & 1], qa[ks], r[0], r[1]);
-    mma(sc[1][ks & 1], qa[ks], r[2], r[3]);
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t sw = (uint32_t)(((2 * t + h) ^ g8) & 7) << 4;
+      const uint4 k0 = lds_v4(kbase + g8 * 128 + sw), k1 = lds_v4(kbase + (g8 + 8) * 128 + sw);
+      const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w}, w1[4] = {k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int ks = 4 * h + e;
+        uint32_t b0, b1, c0, c1;
+        e4m3x4_to_f16x4(w0[e], b0, b1);
+        e4m3x4_to_f16x4(w1[e], c0, c1);
+        mma(sc[0][ks & 1], qa[ks], b0, b1);
+        mma(sc[1][ks & 1], qa[ks], c0, c1);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t r[4];
+      ldsm_x4(r, (ka ^ (uint32_t)(((2 * ks) & 7) << 4)) + (ks >> 2) * G::BOX_BYTES);
+      mma(sc[0][ks & 1], qa[ks], r[0], r[1]);
+      mma(sc[1][ks & 1], qa[ks], r[2], r[3]);
+    }
   }
   // sv[rr][e]: row g + 8 rr, key (e >> 1) * 8 + 2t + (e & 1).
   float sv[2][4];
@@ -188,12 +216,13 @@ __device__ __forceinline__ void attend_block_bias(uint32_t kbase, LdsmLane ln, c
   attend_block_impl<D, true>(kbase, ln, qa, nvalid, o, m_r, l_r, lane, bias0, slope);
 }
 
-// f16 operands, scores scaled by kscale (the FP8-KV decode).
-template <int D>
-__device__ __forceinline__ void attend_block_f16(uint32_t kbase, LdsmLane ln, const uint32_t (&qa)[D / 16][4],
-                                                 int nvalid, float (&o)[D / 8][4], float (&m_r)[2], float (&l_r)[2],
-                                                 int lane, float kscale) {
-  attend_block_impl<D, false, true>(kbase, ln, qa, nvalid, o, m_r, l_r, lane, nullptr, nullptr, kscale);
+// The FP8-KV decode: K fragments from the e4m3 box at kcodes, V from the f16 tile at
+// vbase, f16 operands, scores scaled by kscale.
+__device__ __forceinline__ void attend_block_fp8(uint32_t kcodes, uint32_t vbase, LdsmLane ln,
+                                                 const uint32_t (&qa)[8][4], int nvalid, float (&o)[16][4],
+                                                 float (&m_r)[2], float (&l_r)[2], int lane, float kscale) {
+  attend_block_impl<128, false, true, true>(kcodes, ln, qa, nvalid, o, m_r, l_r, lane, nullptr, nullptr, kscale,
+                                            vbase);
 }
 
 // Per-lane description of one logical block: physical id (num_pool_blocks for a
