@@ -55,3 +55,21 @@ def test_fp8_decode_noalloc_and_empty_sequences():
     assert torch.count_nonzero(out[1]) == 0
     keep = [0, 2, 3]
     assert_close(out[keep], ref[keep], "bf16", "fp8 decode beside an empty sequence")
+
+
+def test_fp8_decode_control_path_with_identity_rotation():
+    # lazy = 0 (the pool holds absolute-position keys; q rotated once by R_m) with a
+    # zero-rate table, where every rotation is the identity: the control kernel's
+    # permuted q fragments and its single-pass loop against the oracle on the codes.
+    L = la()
+    w = W.decode_zipf("fp8ctl", batch=5, hq=32, hkv=8, d=128, docs_per_seq=3, doc_tokens=90, pool_docs=4,
+                      zipf_s=1.0, suffix_tokens=11, share=False, seed=540)
+    k8, v8, ks, vs = W.fp8_pools(w)
+    zero = np.zeros(64)
+    ref = oracle.attention(w, freqs=zero, k_pool=k8, v_pool=v8, k_scale=ks, v_scale=vs)
+    dv = to_device(w, lazy=False)
+    p = dv.p
+    p.kv_dtype, p.k_scale, p.v_scale = L.LAZY_FP8_E4M3, ks, vs
+    rope = L.rope_table_init(p, freqs=zero)
+    out = L.decode(p, dv.q, k8.cuda(), v8.cuda(), dv.words, dv.seq_lens, dv.q_pos, rope)
+    assert_close(out, ref, "bf16", "fp8 decode, lazy=0 control")
