@@ -326,6 +326,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="headline decode only (used for ncu launch lists)")
     ap.add_argument("--decode-path", default="shared", choices=["shared", "seq"],
                     help="decode entry point timed by --workload (shared-run or per-sequence)")
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8_e4m3"],
+                    help="pools timed by --workload with --decode-path seq (fp8_e4m3: quantised copies)")
     ap.add_argument("--workload", default=None, choices=sorted(["llama8b_decode", "llama8b_decode_noshare",
                                                                 "llama8b_prefill", "llama70b_decode",
                                                                 "llama70b_decode_noshare", "mixed_mqa_decode",
@@ -441,7 +443,18 @@ def single_workload(args):
     w = W.FULL[args.workload]()
     d = build_device(w)
     flush = L2Flush(0)
-    if w.kind == "decode":
+    if w.kind == "decode" and args.kv_dtype == "fp8_e4m3":
+        from paged_kv_cache_57_gb300 import lazy_attn as L
+        k8, v8, ks, vs = W.fp8_pools(w)
+        k8, v8 = k8.cuda(), v8.cuda()
+        p8 = L.make_params(num_seqs=w.num_seqs, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                           head_dim=w.head_dim, num_pool_blocks=w.num_pool_blocks,
+                           max_blocks_per_seq=d["p"].max_blocks_per_seq, dtype=w.dtype, rope_theta=w.rope_theta,
+                           kv_dtype="fp8_e4m3", k_scale=ks, v_scale=vs)
+        t = time_steps(lambda: L.decode(p8, d["q"], k8, v8, d["words"], d["seq_lens"], d["q_pos"], d["rope"],
+                                        out=d["out"], workspace=d["ws"]), args.steps, args.warmup, flush)
+        v, unit = decode_bytes(w)["kv_logical"] / 2 / statistics.median(t) / 1e9, "GB/s"  # e4m3 bytes
+    elif w.kind == "decode":
         t = time_steps(lambda: run_decode(d, lazy=True, path=args.decode_path), args.steps, args.warmup, flush)
         v, unit = decode_bytes(w)["kv_logical"] / statistics.median(t) / 1e9, "GB/s"
     else:
