@@ -346,7 +346,10 @@ int lazy_attn_alibi_slopes_host(int32_t num_heads, float *out);
  *    tells the need; setting p->num_splits lower reduces it, and 1 needs none).
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any stream
- *    capture.
+ *    capture. The address is kept with the unique id of the context it was found
+ *    in, and looked up again on the first call after that context changed (after
+ *    cudaDeviceReset, or with another context made current); that call too should
+ *    come before any stream capture.
  *  - Every call shares the one array: calls that overlap on the GPU (other
  *    streams, other threads) race on it and must be serialised by the caller. */
 #define LAZY_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB */
@@ -411,6 +414,21 @@ int lazy_attn_materialize(const lazy_attn_params *p, const void *k_pool, const v
 int lazy_attn_debug_gather(const lazy_attn_params *p, const void *k_pool, const void *v_pool,
                            const uint32_t *block_words, const int32_t *seq_lens, void *k_out, void *v_out,
                            int32_t *pos_out, lazy_stream_t stream);
+
+/* Failure-path test of the bounded waits: lazy_attn_debug_gather (bf16 pools) with
+ * the TMA copies of logical block `withhold_block` of sequence 0, KV head 0 never
+ * issued, and every pipeline wait of the launch limited to wait_limit_us
+ * microseconds (1 .. 2,000,000) instead of 2 s. The withheld block's stage never
+ * completes and no copy of it is in flight: the copying warp's wait runs out, sets
+ * LAZY_DEV_TIMEOUT and stops; the loading warp's next wait on that stage runs out
+ * too, it waits (bounded) for the copies it did issue, and the CTA exits. Other
+ * (sequence, head) pairs are gathered as usual. The call returns LAZY_OK after the
+ * launch; read the status word to see the timeout. LAZY_ERR_INVALID_ARG for
+ * withhold_block < 0 or a limit outside the range, LAZY_ERR_UNSUPPORTED for fp32. */
+int lazy_attn_debug_gather_withheld(const lazy_attn_params *p, const void *k_pool, const void *v_pool,
+                                    const uint32_t *block_words, const int32_t *seq_lens, void *k_out, void *v_out,
+                                    int32_t *pos_out, int32_t withhold_block, uint32_t wait_limit_us,
+                                    lazy_stream_t stream);
 
 /* Evaluates the kernels' rotation for n offsets: cs_out[k][i] = (cos, sin) of
  * deltas[k] * w_i, i < head_dim/2, with the device function the attention

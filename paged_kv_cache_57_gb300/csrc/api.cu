@@ -685,9 +685,9 @@ int lazy_attn_materialize(const lazy_attn_params* p, const void* k_pool, const v
   return launched(lazy::launch_materialize(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int lazy_attn_debug_gather(const lazy_attn_params* p, const void* k_pool, const void* v_pool,
-                           const uint32_t* block_words, const int32_t* seq_lens, void* k_out, void* v_out,
-                           int32_t* pos_out, lazy_stream_t stream) {
+static int debug_gather_impl(const lazy_attn_params* p, const void* k_pool, const void* v_pool,
+                             const uint32_t* block_words, const int32_t* seq_lens, void* k_out, void* v_out,
+                             int32_t* pos_out, int32_t withhold_block, uint64_t wait_ns, lazy_stream_t stream) {
   Checked c;
   int rc = check_params(p, &c);
   if (rc != LAZY_OK) return rc;
@@ -700,15 +700,35 @@ int lazy_attn_debug_gather(const lazy_attn_params* p, const void* k_pool, const 
   if (!st) return LAZY_ERR_CUDA;
   lazy::GatherArgs a{block_words, seq_lens, k_pool, v_pool, k_out, v_out, pos_out, st,
                      p->num_seqs, p->num_kv_heads, p->head_dim, p->max_blocks_per_seq, c.id_bits,
-                     p->num_pool_blocks};
+                     p->num_pool_blocks, withhold_block, wait_ns};
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (p->dtype == LAZY_F32) return launched(lazy::launch_gather_f32(a, cs));
+  if (p->dtype == LAZY_F32) {
+    if (withhold_block >= 0) return LAZY_ERR_UNSUPPORTED;  // the fp32 gather has no pipeline to stall
+    return launched(lazy::launch_gather_f32(a, cs));
+  }
   CUtensorMap kmap, vmap;
   const uint64_t rows = (uint64_t)p->num_pool_blocks * p->num_kv_heads * lazy::kBlock;
   if (!encode_rows_map(&kmap, k_pool, rows, p->head_dim, lazy::kBlock) ||
       !encode_rows_map(&vmap, v_pool, rows, p->head_dim, lazy::kBlock))
     return LAZY_ERR_CUDA;
   return launched(lazy::launch_gather_bf16(a, kmap, vmap, cs));
+}
+
+int lazy_attn_debug_gather(const lazy_attn_params* p, const void* k_pool, const void* v_pool,
+                           const uint32_t* block_words, const int32_t* seq_lens, void* k_out, void* v_out,
+                           int32_t* pos_out, lazy_stream_t stream) {
+  return debug_gather_impl(p, k_pool, v_pool, block_words, seq_lens, k_out, v_out, pos_out, -1, lazy::kWaitLimitNs,
+                           stream);
+}
+
+int lazy_attn_debug_gather_withheld(const lazy_attn_params* p, const void* k_pool, const void* v_pool,
+                                    const uint32_t* block_words, const int32_t* seq_lens, void* k_out, void* v_out,
+                                    int32_t* pos_out, int32_t withhold_block, uint32_t wait_limit_us,
+                                    lazy_stream_t stream) {
+  if (withhold_block < 0 || wait_limit_us == 0 || (uint64_t)wait_limit_us * 1000u > lazy::kWaitLimitNs)
+    return LAZY_ERR_INVALID_ARG;
+  return debug_gather_impl(p, k_pool, v_pool, block_words, seq_lens, k_out, v_out, pos_out, withhold_block,
+                           (uint64_t)wait_limit_us * 1000u, stream);
 }
 
 int lazy_attn_debug_rope(const lazy_attn_params* p, const void* rope_table, const int32_t* deltas, int32_t n,

@@ -84,13 +84,15 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete. Gives up after
-// kWaitLimitNs, sets LAZY_DEV_TIMEOUT and returns false: callers then skip the
-// rest of their work, so the kernel always terminates.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status) {
+// limit_ns (kWaitLimitNs unless a test asks for less), sets LAZY_DEV_TIMEOUT and
+// returns false: callers then skip the rest of their work, so the kernel always
+// terminates.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       raise_status(status, LAZY_DEV_TIMEOUT);
       return false;
     }

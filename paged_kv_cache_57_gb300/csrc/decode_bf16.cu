@@ -552,11 +552,14 @@ __global__ void __launch_bounds__(64) gather_bf16_kernel(const GatherArgs a, con
         const int phys = __shfl_sync(0xffffffffu, lb.phys, j);
         const int p = __shfl_sync(0xffffffffu, lb.p, j);
         const int nv = __shfl_sync(0xffffffffu, lb.nv, j);
-        if (i >= NS && !warp_wait(&empty[st], ((i / NS) & 1) ^ 1, a.status)) {
+        if (i >= NS && !warp_wait(&empty[st], ((i / NS) & 1) ^ 1, a.status, a.wait_ns)) {
           ok = false;
           break;
         }
-        if (lane == 0) {
+        // A withheld block (failure-path test) gets neither its copies nor the arrival
+        // that expects them: its stage's phase never completes and no copy is in flight.
+        const bool withhold = i == a.withhold_block && s == 0 && kvh == 0;
+        if (lane == 0 && !withhold) {
           meta[2 * st] = p;
           meta[2 * st + 1] = nv;
           load_block<D>(stages + st * 2 * KV_BYTES, &full[st], phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
@@ -565,11 +568,11 @@ __global__ void __launch_bounds__(64) gather_bf16_kernel(const GatherArgs a, con
       }
     }
     if (lane == 0)
-      for (int i = max(0, issued - NS); i < issued; ++i) mbar_wait(&full[i % NS], (i / NS) & 1, a.status);
+      for (int i = max(0, issued - NS); i < issued; ++i) mbar_wait(&full[i % NS], (i / NS) & 1, a.status, a.wait_ns);
   } else {
     for (int i = 0; i < nb; ++i) {
       const int st = i % NS;
-      if (!warp_wait(&full[st], (i / NS) & 1, a.status)) break;
+      if (!warp_wait(&full[st], (i / NS) & 1, a.status, a.wait_ns)) break;
       const int p = meta[2 * st], nvalid = meta[2 * st + 1];
       const uint8_t* kb = stages + st * 2 * KV_BYTES;
       const uint8_t* vb = kb + KV_BYTES;

@@ -236,8 +236,9 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 // Warp-uniform bounded wait: every lane polls, and the warp gives up together.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* status) {
-  const bool ok = mbar_wait(bar, parity, status);
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+  const bool ok = mbar_wait(bar, parity, status, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -65,6 +65,10 @@ struct GatherArgs {
   int32_t* pos_out;          // [B][16*max_blocks] or null
   unsigned int* status;
   int B, Hkv, D, max_blocks, id_bits, num_pool_blocks;
+  // Failure-path test only: logical block `withhold_block` of sequence 0, KV head 0
+  // is never loaded (-1: none), and every wait gives up after wait_ns.
+  int withhold_block;
+  uint64_t wait_ns;
 };
 
 struct PackArgs {

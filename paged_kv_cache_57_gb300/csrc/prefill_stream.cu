@@ -86,7 +86,10 @@ __device__ __forceinline__ UnitDesc unit_desc(const PrefillArgs& a, int u, int P
   d.seq_len = d.nb = d.b_chunk = d.n = 0;
   if (d.C <= 0 || d.row0 >= d.C) return d;
   int seq_len = __ldg(&a.seq_lens[d.s]);
-  if (seq_len < 0 || seq_len > kBlock * a.max_blocks) seq_len = seq_len < 0 ? 0 : kBlock * a.max_blocks;
+  if (seq_len < 0 || seq_len > kBlock * a.max_blocks) {
+    raise_status(a.status, LAZY_DEV_BAD_LEN);
+    seq_len = seq_len < 0 ? 0 : kBlock * a.max_blocks;
+  }
   d.seq_len = seq_len;
   d.nb = (seq_len + kBlock - 1) / kBlock;
   d.b_chunk = max(0, d.nb - (d.C + kBlock - 1) / kBlock);  // the chunk's own keys are the last segment

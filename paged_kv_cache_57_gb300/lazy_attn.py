@@ -36,7 +36,7 @@ EXPORTED = (
     "lazy_attn_plan_shared_host", "lazy_attn_decode_shared_workspace_bytes", "lazy_attn_decode_shared",
     "lazy_attn_materialize", "lazy_attn_rope_table_init_scaled", "lazy_attn_rope_table_init_freqs",
     "lazy_attn_rotary_layout_host", "lazy_attn_decode_shared_alibi", "lazy_attn_alibi_slopes_host",
-    "lazy_attn_decode_alibi",
+    "lazy_attn_decode_alibi", "lazy_attn_debug_gather_withheld",
 )
 PLAN_MAX_MEMBERS = 16
 PLAN_ITEM_BLOCK_IDS = 32
@@ -78,6 +78,7 @@ _sig = {
     "lazy_attn_prefill_workspace_bytes": (_sz, [_P, _i32]),
     "lazy_attn_prefill": (ctypes.c_int, [_P, _vp, _vp, _vp, _i32, _i32] + [_vp] * 7 + [_sz, _vp]),
     "lazy_attn_debug_gather": (ctypes.c_int, [_P] + [_vp] * 7 + [_vp]),
+    "lazy_attn_debug_gather_withheld": (ctypes.c_int, [_P] + [_vp] * 7 + [_i32, ctypes.c_uint32, _vp]),
     "lazy_attn_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "lazy_attn_launch_count": (_u64, []),
     "lazy_attn_debug_rope": (ctypes.c_int, [_P, _vp, _vp, _i32, _vp, _vp]),
@@ -404,16 +405,23 @@ def prefill(p: Params, q: torch.Tensor, cu_seqlens_q: torch.Tensor, q_start: tor
 
 
 def debug_gather(p: Params, k_pool: torch.Tensor, v_pool: torch.Tensor, block_words: torch.Tensor,
-                 seq_lens: torch.Tensor, with_pos: bool = True, stream=None):
+                 seq_lens: torch.Tensor, with_pos: bool = True, stream=None, withhold_block: int = -1,
+                 wait_limit_us: int = 0):
+    """Dense copies of every logical K/V slot through the decode load path. With
+    ``withhold_block >= 0`` (failure-path test) that block of sequence 0, KV head 0 is
+    never loaded and every wait gives up after ``wait_limit_us``."""
     dt = _tdt(p)
     rows = BLOCK * p.max_blocks_per_seq
     k_out = torch.empty((p.num_seqs, p.num_kv_heads, rows, p.head_dim), dtype=dt, device=k_pool.device)
     v_out = torch.empty_like(k_out)
     pos = torch.empty((p.num_seqs, rows), dtype=torch.int32, device=k_pool.device) if with_pos else None
-    rc = _lib.lazy_attn_debug_gather(ctypes.byref(p), _dptr(k_pool, "k_pool", dt), _dptr(v_pool, "v_pool", dt),
-                                     _dptr(block_words, "block_words"), _dptr(seq_lens, "seq_lens", torch.int32),
-                                     _dptr(k_out, "k_out"), _dptr(v_out, "v_out"), _dptr(pos, "pos_out"),
-                                     _stream(stream))
+    args = (ctypes.byref(p), _dptr(k_pool, "k_pool", dt), _dptr(v_pool, "v_pool", dt),
+            _dptr(block_words, "block_words"), _dptr(seq_lens, "seq_lens", torch.int32),
+            _dptr(k_out, "k_out"), _dptr(v_out, "v_out"), _dptr(pos, "pos_out"))
+    if withhold_block >= 0:
+        rc = _lib.lazy_attn_debug_gather_withheld(*args, int(withhold_block), int(wait_limit_us), _stream(stream))
+    else:
+        rc = _lib.lazy_attn_debug_gather(*args, _stream(stream))
     _check(rc, "debug_gather")
     return k_out, v_out, pos
 

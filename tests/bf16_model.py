@@ -32,10 +32,12 @@ def _bf16(x):
 BF16_U = 2.0 ** -8
 
 
-def emulate(w, rows, lazy: bool = True, k_pool=None, freqs=None, alibi=None, weight_bound: bool = False):
+def emulate(w, rows, lazy: bool = True, k_pool=None, freqs=None, alibi=None, weight_bound: bool = False,
+            sm_scale: float = 0.0):
     """[len(rows), Hq, d] for query rows ``rows`` of workload ``w`` (``freqs``: rotation
     frequencies other than theta^(-2i/d); ``alibi``: per-head slopes of the bias
-    -slope (m - n), added in fp32 to the scores before the exponentials).
+    -slope (m - n), added in fp32 to the scores before the exponentials; ``sm_scale``:
+    softmax scale, 0 for 1/sqrt(d)).
 
     The weights here are rounded to bf16 relative to the row's global maximum; a
     split-K kernel rounds each one relative to the running maximum of its own split,
@@ -55,7 +57,7 @@ def emulate(w, rows, lazy: bool = True, k_pool=None, freqs=None, alibi=None, wei
         q_m = np.concatenate([w.q_start[s] + np.arange(cu[s + 1] - cu[s]) for s in range(w.num_seqs)])
     g = w.num_q_heads // w.num_kv_heads
     d, theta = w.head_dim, w.rope_theta
-    scale = np.log2(np.e) / np.sqrt(d)
+    scale = np.log2(np.e) * (sm_scale if sm_scale > 0 else 1.0 / np.sqrt(d))
     out = np.zeros((len(rows), w.num_q_heads, d))
     bound = np.zeros_like(out)
     for oi, r in enumerate(np.asarray(rows)):

@@ -85,11 +85,27 @@ def visible_keys(w, rows=None) -> np.ndarray:
     return n if rows is None else n[np.asarray(rows)]
 
 
-def assert_close(got: torch.Tensor, ref: np.ndarray, dtype: str, what: str = "", emulate=None) -> float:
-    """Elementwise |gpu - ref| <= atol + rtol |ref| against the fp64 oracle. For bf16,
-    an element outside that bound passes only if it is within the same bound of the
-    bf16-operand emulation (tests/bf16_model.py) for its row: the deviation is then
-    the rounding of the tensor-core operands, not a wrong key, mask or rotation.
+# Elements that pass only through the bf16-operand emulation, per test: filled by
+# assert_close, printed by the terminal-summary hook in conftest.py.
+FALLBACK_LOG: list = []
+
+# Cap on emulation-only elements for the named few-key edge cases (contexts of 1-3
+# keys, causal chunk rows near their start, the steepest ALiBi slopes): a fraction of
+# the compared elements. Every other test passes against the oracle alone (cap 0).
+FEW_KEY_FALLBACK_FRAC = 0.01
+
+
+def assert_close(got: torch.Tensor, ref: np.ndarray, dtype: str, what: str = "", emulate=None,
+                 fallback_frac: float = 0.0) -> float:
+    """Elementwise |gpu - ref| <= atol + rtol |ref| against the fp64 oracle.
+
+    By default every element must meet that bound (``fallback_frac = 0``). Tests of
+    the named few-key edge cases pass ``fallback_frac`` (at most FEW_KEY_FALLBACK_FRAC):
+    then an element outside the bound may pass if it is within the same bound of the
+    bf16-operand emulation (tests/bf16_model.py) for its row -- the deviation is the
+    rounding of the tensor-core operands, not a wrong key, mask or rotation -- and the
+    number of such elements must stay within ``fallback_frac`` of the compared
+    elements. The count is recorded (FALLBACK_LOG) whatever the outcome.
     ``emulate(local_rows)`` returns the emulation for those rows of ``ref``, or a pair
     (emulation, per-element bound on the bf16 rounding of the softmax weights), whose
     bound then widens that second comparison."""
@@ -98,21 +114,23 @@ def assert_close(got: torch.Tensor, ref: np.ndarray, dtype: str, what: str = "",
     err = np.abs(g - ref)
     bad = err > atol + rtol * np.abs(ref)
     assert np.isfinite(g).all(), f"{what}: non-finite output"
+    n_fb = 0
     if bad.any() and emulate is not None:
         rows = np.unique(np.nonzero(bad)[0])
         emu = emulate(rows)
         emu, wb = emu if isinstance(emu, tuple) else (emu, 0.0)
         still = bad[rows] & (np.abs(g[rows] - emu) > atol + rtol * np.abs(emu) + wb)
-        if not still.any():
-            print(f"{what}: {int(bad.sum())} element(s) outside the oracle tolerance, all within it of the "
-                  f"bf16-operand emulation")
-            return float(err.max())
+        n_fb = int(bad.sum()) - int(still.sum())
         bad = np.zeros_like(bad)
         bad[rows] = still
+    FALLBACK_LOG.append((what, n_fb, int(bad.size), fallback_frac))
     if bad.any():
         i = np.unravel_index(np.argmax(np.where(bad, err, -1.0)), err.shape)
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements outside tolerance; worst at {i}: "
                              f"gpu={g[i]!r} ref={ref[i]!r}")
+    cap = int(fallback_frac * bad.size)
+    assert n_fb <= cap, (f"{what}: {n_fb} of {bad.size} elements are outside the oracle tolerance and within it "
+                         f"only of the bf16-operand emulation (allowed here: {cap})")
     return float(err.max())
 
 

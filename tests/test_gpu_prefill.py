@@ -6,7 +6,7 @@ import torch
 import oracle
 from brute import rope
 from bf16_model import emulate
-from gpu_util import assert_close, la, prefill, to_device
+from gpu_util import FEW_KEY_FALLBACK_FRAC, assert_close, la, prefill, to_device
 from paged_kv_cache_57_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -19,14 +19,14 @@ def _clean_status():
     assert la().device_status(clear=True) == 0, "device status word set"
 
 
-def _check(w, rows=None, lazy=True, k_pool=None):
+def _check(w, rows=None, lazy=True, k_pool=None, fallback_frac=0.0):
     dv = to_device(w, lazy=lazy, k_pool=k_pool)
     out = prefill(dv)
     ref = oracle.attention(w, rows=rows)
     got = out if rows is None else out[torch.as_tensor(rows, device=out.device)]
     sel = np.arange(ref.shape[0]) if rows is None else np.asarray(rows)
     return assert_close(got, ref, w.dtype, w.name,
-                        emulate=lambda r: emulate(w, sel[r], lazy=lazy, k_pool=k_pool))
+                        emulate=lambda r: emulate(w, sel[r], lazy=lazy, k_pool=k_pool), fallback_frac=fallback_frac)
 
 
 def test_prefill_single_tile():
@@ -45,7 +45,8 @@ def test_prefill_varlen_chunks(chunks):
 def test_prefill_chunk_only_is_causal():
     w = W.prefill_zipf("pc", batch=2, hq=4, hkv=4, docs_per_seq=0, doc_tokens=16, pool_docs=1, zipf_s=1.0,
                        chunk_tokens=[300, 45], seed=74)
-    _check(w)
+    # the first rows of a chunk with no cached context see 1, 2, 3 ... keys: few-key edge case (capped)
+    _check(w, fallback_frac=FEW_KEY_FALLBACK_FRAC)
 
 
 @pytest.mark.parametrize("hq,hkv", [(32, 8), (32, 1), (8, 8)])
@@ -159,3 +160,15 @@ def test_llama8b_prefill_split_units_sampled():
         lo, hi = int(cu[s]) + 128 * tile, min(int(cu[s + 1]), int(cu[s]) + 128 * tile + 128)
         rows.update(int(x) for x in rng.choice(np.arange(lo, hi), 4, replace=False))
     _check(w, rows=sorted(rows))
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (6, 2)])
+def test_prefill_non_default_sm_scale(hq, hkv):
+    # even GQA ratio: the stream-K kernel; odd (3 per KV head): the TMEM-Q kernel
+    w = W.prefill_zipf("pscale", batch=2, hq=hq, hkv=hkv, docs_per_seq=2, doc_tokens=150, pool_docs=3,
+                       zipf_s=1.0, chunk_tokens=[140, 33], seed=79 + hq)
+    dv = to_device(w)
+    dv.p.sm_scale = 0.05
+    ref = oracle.attention(w, sm_scale=0.05)
+    assert_close(prefill(dv), ref, "bf16", f"prefill {hq}/{hkv}, sm_scale 0.05")
+    assert np.abs(ref - oracle.attention(w)).max() > 1e-2

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from bf16_model import emulate
-from gpu_util import assert_close, decode, decode_shared, la, prefill, shared_plan, to_device
+from gpu_util import FEW_KEY_FALLBACK_FRAC, assert_close, decode, decode_shared, la, prefill, shared_plan, to_device
 from paged_kv_cache_57_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -170,7 +170,8 @@ def test_shared_decode_alibi(hq, hkv, chunk):
     out = L.decode_shared(dv.p, dv.q, dv.k_pool, dv.v_pool, dv.words, dv.q_pos, dv.rope, plan,
                           alibi_slopes=torch.from_numpy(slopes).cuda())
     assert_close(out, ref, "bf16", f"shared decode, ALiBi, {hq}/{hkv}",
-                 emulate=lambda r: emulate(w, r, freqs=np.zeros(64), alibi=slopes, weight_bound=True))
+                 emulate=lambda r: emulate(w, r, freqs=np.zeros(64), alibi=slopes, weight_bound=True),
+                 fallback_frac=FEW_KEY_FALLBACK_FRAC)
     # the bias matters at these positions
     assert np.abs(ref - oracle.attention(w, freqs=np.zeros(64))).max() > 1e-2
 
@@ -190,5 +191,6 @@ def test_per_sequence_decode_alibi(hq, hkv, d, splits, host_pack):
     out = L.decode(dv.p, dv.q, dv.k_pool, dv.v_pool, dv.words, dv.seq_lens, dv.q_pos, dv.rope,
                    alibi_slopes=torch.from_numpy(slopes).cuda())
     assert_close(out, ref, "bf16", f"per-sequence decode, ALiBi, {hq}/{hkv} d{d}",
-                 emulate=lambda r: emulate(w, r, freqs=np.zeros(d // 2), alibi=slopes, weight_bound=True))
+                 emulate=lambda r: emulate(w, r, freqs=np.zeros(d // 2), alibi=slopes, weight_bound=True),
+                 fallback_frac=FEW_KEY_FALLBACK_FRAC)
     assert np.abs(ref - oracle.attention(w, freqs=np.zeros(d // 2))).max() > 1e-2

@@ -11,7 +11,8 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import TOL, decode, la, to_device
+import oracle
+from gpu_util import assert_close, decode, la, to_device
 from paged_kv_cache_57_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -21,12 +22,6 @@ def _workload(seed):
     # 64 sequences x 32/8 heads x ~1.7k tokens: the split plan needs a few MiB of partials
     return W.decode_zipf("noalloc", batch=64, hq=32, hkv=8, d=128, docs_per_seq=6, doc_tokens=272, pool_docs=40,
                          zipf_s=1.0, suffix_tokens=33, seed=seed)
-
-
-def _close(a, b):
-    atol, rtol = TOL["bf16"]
-    a, b = a.float().cpu().numpy(), b.float().cpu().numpy()
-    return np.all(np.abs(a - b) <= atol + rtol * np.abs(b))
 
 
 def test_decode_noalloc_matches_decode_on_two_calls():
@@ -41,7 +36,11 @@ def test_decode_noalloc_matches_decode_on_two_calls():
         L.decode_noalloc(dv.p, dv.q, dv.k_pool, dv.v_pool, dv.words, dv.seq_lens, dv.q_pos, dv.rope, out)
         torch.cuda.synchronize()
         assert torch.isfinite(out.float()).all()
-        assert _close(out, ref)
+        # the same kernels on the same inputs and split plan: only where the partials
+        # live differs, so the outputs must agree bit for bit (a partial overwrite of
+        # the shared array would show here), and both must match the oracle
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+        assert_close(out, oracle.attention(dv.w), "bf16", f"decode_noalloc, call {seed - 90}")
     assert L.device_status(clear=True) == 0
 
 
