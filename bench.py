@@ -327,7 +327,7 @@ def main():
     ap.add_argument("--decode-path", default="shared", choices=["shared", "seq"],
                     help="decode entry point timed by --workload (shared-run or per-sequence)")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8_e4m3"],
-                    help="pools timed by --workload with --decode-path seq (fp8_e4m3: quantised copies)")
+                    help="pools timed by --workload (fp8_e4m3: quantised copies)")
     ap.add_argument("--workload", default=None, choices=sorted(["llama8b_decode", "llama8b_decode_noshare",
                                                                 "llama8b_prefill", "llama70b_decode",
                                                                 "llama70b_decode_noshare", "mixed_mqa_decode",
@@ -451,8 +451,18 @@ def single_workload(args):
                            head_dim=w.head_dim, num_pool_blocks=w.num_pool_blocks,
                            max_blocks_per_seq=d["p"].max_blocks_per_seq, dtype=w.dtype, rope_theta=w.rope_theta,
                            kv_dtype="fp8_e4m3", k_scale=ks, v_scale=vs)
-        t = time_steps(lambda: L.decode(p8, d["q"], k8, v8, d["words"], d["seq_lens"], d["q_pos"], d["rope"],
-                                        out=d["out"], workspace=d["ws"]), args.steps, args.warmup, flush)
+        if args.decode_path == "shared":  # planned for e4m3 pools (items of at most 64 rows)
+            items, slot_indptr = L.plan_shared_host(p8, len(w.doc_len), w.seg_indptr, w.seg_doc, w.seg_len,
+                                                    w.doc_block_indptr, w.doc_blocks)
+            plan8 = L.SharedPlan(items, slot_indptr)
+            ws8 = torch.empty(max(1, L.decode_shared_workspace_bytes(p8, plan8.num_slots)), dtype=torch.uint8,
+                              device="cuda")
+            fn = lambda: L.decode_shared(p8, d["q"], k8, v8, d["words"], d["q_pos"], d["rope"], plan8, out=d["out"],
+                                         workspace=ws8)
+        else:
+            fn = lambda: L.decode(p8, d["q"], k8, v8, d["words"], d["seq_lens"], d["q_pos"], d["rope"], out=d["out"],
+                                  workspace=d["ws"])
+        t = time_steps(fn, args.steps, args.warmup, flush)
         v, unit = decode_bytes(w)["kv_logical"] / 2 / statistics.median(t) / 1e9, "GB/s"  # e4m3 bytes
     elif w.kind == "decode":
         t = time_steps(lambda: run_decode(d, lazy=True, path=args.decode_path), args.steps, args.warmup, flush)

@@ -27,9 +27,10 @@
  *    word and returns. Outputs are then unspecified.
  *  - Numerics: dtype LAZY_F32 computes in fp32; LAZY_BF16 multiplies bf16
  *    operands on the tensor cores with fp32 accumulation and fp32 softmax.
- *    With kv_dtype LAZY_FP8_E4M3 (lazy_attn_decode only) the pools hold OCP
- *    e4m3 codes and the products take f16 operands (every e4m3 value is exact
- *    in f16), with fp32 accumulation and softmax.
+ *    With kv_dtype LAZY_FP8_E4M3 (the decodes: lazy_attn_decode, _noalloc and
+ *    lazy_attn_decode_shared) the pools hold OCP e4m3 codes and the products take
+ *    f16 operands (every e4m3 value is exact in f16), with fp32 accumulation and
+ *    softmax.
  *
  * Layout (one layer)
  * ------------------
@@ -116,9 +117,10 @@ typedef struct {
   int32_t kv_dtype;           /* 0: the pools have `dtype`. LAZY_FP8_E4M3: the pools hold one
                                  e4m3 byte per element (same [block][head][16][d] layout), a
                                  key's value is code * k_scale and a value's code * v_scale.
-                                 Only lazy_attn_decode (and _noalloc) with dtype LAZY_BF16 and
-                                 head_dim 128 take it; the other attention calls and the
-                                 materialiser return LAZY_ERR_UNSUPPORTED. Pools 16-byte aligned. */
+                                 Only lazy_attn_decode (and _noalloc) and lazy_attn_decode_shared
+                                 with dtype LAZY_BF16 and head_dim 128 take it; the ALiBi calls,
+                                 the prefill and the materialiser return LAZY_ERR_UNSUPPORTED.
+                                 Pools 16-byte aligned. */
   float k_scale;              /* FP8 dequantisation scales: finite, > 0; 0 selects 1 */
   float v_scale;
 } lazy_attn_params;
@@ -257,8 +259,9 @@ int lazy_attn_decode(const lazy_attn_params *p, const void *q, const void *k_poo
  * split into sets of at most LAZY_PLAN_MAX_MEMBERS members and at most R query
  * rows (members x query heads per KV head), and each set's blocks are cut into
  * chunks of chunk_blocks logical blocks. R is 128 when a KV head serves at least
- * 8 query heads and head_dim is 128 (the decode then runs on the 5th-generation
- * tensor cores, one 128-row tile per item), else 64. chunk_blocks 0 selects 32,
+ * 8 query heads, head_dim is 128 and the pools are not e4m3 (the decode then runs
+ * on the 5th-generation tensor cores, one 128-row tile per item), else 64 (plan
+ * with the kv_dtype the decode will use). chunk_blocks 0 selects 32,
  * or, for R = 128, about one item per resident CTA (2 x 152 / num_kv_heads items):
  * the sets' blocks summed, divided by that count, rounded up to a multiple of 4
  * and kept within 32 .. 256. It writes
@@ -287,7 +290,9 @@ int lazy_attn_decode(const lazy_attn_params *p, const void *q, const void *k_poo
  * Decode: items and slot_indptr copied to device memory unchanged (items 16-byte
  * aligned), block_words packed from the same document lists. workspace: at least
  * lazy_attn_decode_shared_workspace_bytes(p, num_slots) bytes, 16-byte aligned.
- * bf16 only; at most 64 query heads per KV head. A member whose first block does
+ * dtype bf16 only; at most 64 query heads per KV head. kv_dtype LAZY_FP8_E4M3
+ * (head_dim 128): pools of e4m3 codes, read as 16-row x 128-byte boxes, on the
+ * mma.sync kernel at every ratio (items of at most 64 rows). A member whose first block does
  * not hold the item's physical block, or an item outside the table, sets
  * LAZY_DEV_LAYOUT and is skipped. */
 #define LAZY_PLAN_MAX_MEMBERS 16

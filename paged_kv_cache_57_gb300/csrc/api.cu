@@ -473,7 +473,8 @@ int lazy_attn_plan_shared_host(const lazy_attn_params* p, int32_t num_docs, cons
       (!seg_doc || !seg_len || !doc_block_indptr || !doc_blocks || !items))
     return LAZY_ERR_INVALID_ARG;
   if (c.G > 64) return LAZY_ERR_UNSUPPORTED;
-  const int cap = lazy::shared_rows_cap(c.G, p->head_dim);
+  // e4m3 pools run on the mma.sync kernel (items of at most 64 rows) at every ratio
+  const int cap = kv_fp8(p) ? 64 : lazy::shared_rows_cap(c.G, p->head_dim);
   // 0: 32 blocks for the mma.sync kernel; for the tensor-core kernel, a length that
   // gives about one item per resident CTA.
   const int cb = chunk_blocks > 0 ? chunk_blocks : (cap == 128 ? 0 : 32);
@@ -502,7 +503,9 @@ static int decode_shared_impl(const lazy_attn_params* p, const void* q, const vo
   int rc = check_params(p, &c);
   if (rc != LAZY_OK) return rc;
   if (!alibi != !p->key_positions || (reinterpret_cast<uintptr_t>(alibi) & 3u)) return LAZY_ERR_INVALID_ARG;
-  if (p->dtype != LAZY_BF16 || kv_fp8(p)) return LAZY_ERR_UNSUPPORTED;
+  if (p->dtype != LAZY_BF16) return LAZY_ERR_UNSUPPORTED;
+  const bool fp8 = kv_fp8(p);
+  if (fp8 && (p->head_dim != 128 || alibi)) return LAZY_ERR_UNSUPPORTED;
   if (c.G > 64) return LAZY_ERR_UNSUPPORTED;
   if (num_items < 0 || num_slots < 0) return LAZY_ERR_INVALID_ARG;
   if (p->num_seqs == 0) return LAZY_OK;
@@ -544,7 +547,13 @@ static int decode_shared_impl(const lazy_attn_params* p, const void* q, const vo
   if (num_items > 0) {
     CUtensorMap kmap, vmap;
     const uint64_t rows = (uint64_t)p->num_pool_blocks * p->num_kv_heads * lazy::kBlock;
-    if (lazy::shared_rows_cap(c.G, p->head_dim) == 128) {  // tensor-core kernel: 16-row x 64-column boxes
+    if (fp8) {  // e4m3 codes: one 16-row x 128-byte box per block (mma.sync kernel at every ratio)
+      if (!encode_rows_map_fp8(&kmap, k_pool, rows, lazy::kBlock) ||
+          !encode_rows_map_fp8(&vmap, v_pool, rows, lazy::kBlock))
+        return LAZY_ERR_CUDA;
+      rc = launched(lazy::launch_decode_shared_fp8(a, p->k_scale > 0.f ? p->k_scale : 1.f,
+                                                   p->v_scale > 0.f ? p->v_scale : 1.f, p->lazy != 0, kmap, vmap, cs));
+    } else if (lazy::shared_rows_cap(c.G, p->head_dim) == 128) {  // tensor-core kernel: 16-row x 64-column boxes
       if (!encode_rows_map(&kmap, k_pool, rows, p->head_dim, lazy::kBlock) ||
           !encode_rows_map(&vmap, v_pool, rows, p->head_dim, lazy::kBlock))
         return LAZY_ERR_CUDA;

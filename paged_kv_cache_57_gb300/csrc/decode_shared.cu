@@ -18,6 +18,14 @@
 // are those of decode_bf16.cu). Teams merge in shared memory, and every
 // (member, query head) writes one fp32 partial (m, l, o) to its slot; the
 // combine kernel merges a sequence's slots with the online-softmax rescale.
+//
+// FP8 (d = 128): the pools hold e4m3 codes (one 16-row x 128-byte box per block for
+// K and for V, half the bytes). A team converts each landed V box exactly to f16 in
+// its own tile buffer; the K fragments are converted from the codes directly, the
+// query fragments are f16 in the permuted head-dimension order of those K fragments,
+// scores are scaled by k_scale and the partial outputs by v_scale. (Converting K
+// into the team's tile too, once for all of its row tiles, measured slower: the
+// tile's stores, barrier and reloads cost more than each warp's own conversion.)
 #include <cfloat>
 #include <type_traits>
 
@@ -39,13 +47,17 @@ constexpr int kRecBlocks = LAZY_PLAN_ITEM_BLOCK_IDS;
 static_assert(kItemInts == kRecIds + kRecBlocks && kItemInts % 4 == 0 && kItemInts / 4 <= kShThreads,
               "item record layout");
 
-template <int D>
+template <int D, bool FP8 = false>
 struct SharedCfg {
   using G = BlockGeom<D>;
   static constexpr int RED_STRIDE = D + 4;  // merge rows: o[D], m, l, padding to 16 bytes
-  static constexpr int RING_BYTES = kShStages * G::STAGE_BYTES;
+  static constexpr int STAGE_BYTES = FP8 ? 2 * kBlock * D : G::STAGE_BYTES;  // e4m3: one byte per element
+  static constexpr int RING_BYTES = kShStages * STAGE_BYTES;
+  // FP8: one f16 tile buffer per team (at most kShWarps teams), the bf16 tile layout
+  static constexpr int CONV_BYTES = FP8 ? kShWarps * G::STAGE_BYTES : 0;
   static constexpr int MERGE_BYTES = kShRows * RED_STRIDE * 4;
-  static constexpr int BUF_BYTES = ((RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES) + 1023) / 1024 * 1024;
+  static constexpr int BUF_BYTES =
+      ((RING_BYTES + CONV_BYTES > MERGE_BYTES ? RING_BYTES + CONV_BYTES : MERGE_BYTES) + 1023) / 1024 * 1024;
   static constexpr int CS_BYTES = kShMembers * (D / 2) * 8;  // (cos, sin) per member and frequency
   static constexpr int BAR_BYTES = kShStages * 8;
   static constexpr int REC_BYTES = kItemInts * 4;
@@ -91,11 +103,13 @@ __device__ __forceinline__ void load_block_3d(uint8_t* stage, uint64_t* bar, int
   } while (0)
 #endif
 
-template <int D, bool LAZY, bool ALIBI>
+template <int D, bool LAZY, bool ALIBI, bool FP8 = false>
 __global__ void __launch_bounds__(kShThreads, 3)
-    decode_shared_kernel(const std::conditional_t<ALIBI, SharedAlibiArgs, SharedDecodeArgs> a,
+    decode_shared_kernel(const std::conditional_t<ALIBI, SharedAlibiArgs,
+                                                  std::conditional_t<FP8, SharedFp8Args, SharedDecodeArgs>> a,
                          const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
-  using C = SharedCfg<D>;
+  static_assert(!FP8 || (D == 128 && !ALIBI), "FP8 KV: d = 128, no ALiBi");
+  using C = SharedCfg<D, FP8>;
   using G = BlockGeom<D>;
   constexpr int HALF = D / 2;
   constexpr int NQ = D / 32;  // k-step pairs of a fragment row
@@ -162,7 +176,11 @@ __global__ void __launch_bounds__(kShThreads, 3)
   const int RT = rows <= 16 ? 1 : (rows <= 32 ? 2 : 4);
   const int rt = warp % RT;
   const int g = lane >> 2, t = lane & 3;
+  // FP8 (permuted order): dims 32t .. 32t + 31 of each row and their rotate-half
+  // partners, as 16-byte vectors.
+  constexpr int QV = FP8 ? 4 : 1;
   uint32_t qx[2][NQ][2], qy[2][NQ][2];
+  uint4 qo[2][QV], qp[2][QV];
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
     const int r = rt * 16 + g + 8 * rr;
@@ -171,14 +189,24 @@ __global__ void __launch_bounds__(kShThreads, 3)
     const uint32_t* qrow = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.q) +
                                                              ((size_t)(live ? mem_seq(m) : 0) * a.Hq +
                                                               (size_t)kvh * a.G + (live ? h : 0)) * D);
+    if constexpr (FP8) {
+      const uint4* own = reinterpret_cast<const uint4*>(qrow + 16 * t);        // dims 32t ..
+      const uint4* par = reinterpret_cast<const uint4*>(qrow + 16 * (t ^ 2));  // dims (32t) ^ 64 ..
 #pragma unroll
-    for (int ks = 0; ks < NQ; ++ks)
-#pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        const int i = 16 * ks + 2 * t + 8 * e2;
-        qx[rr][ks][e2] = live ? __ldg(qrow + i / 2) : 0u;
-        qy[rr][ks][e2] = live ? __ldg(qrow + (i + HALF) / 2) : 0u;
+      for (int v = 0; v < QV; ++v) {
+        qo[rr][v] = live ? __ldg(own + v) : make_uint4(0, 0, 0, 0);
+        qp[rr][v] = live ? __ldg(par + v) : make_uint4(0, 0, 0, 0);
       }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < NQ; ++ks)
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int i = 16 * ks + 2 * t + 8 * e2;
+          qx[rr][ks][e2] = live ? __ldg(qrow + i / 2) : 0u;
+          qy[rr][ks][e2] = live ? __ldg(qrow + (i + HALF) / 2) : 0u;
+        }
+    }
   }
 
   // ------------------------------------------------------------ teams and first loads
@@ -188,7 +216,12 @@ __global__ void __launch_bounds__(kShThreads, 3)
   const int per_team = (nblk + TEAMS - 1) / TEAMS;
   const int kb0 = team * per_team;
   const int nk = max(0, min(nblk, kb0 + per_team) - kb0);  // blocks of this team
-  uint8_t* tst = ring + team * NS * G::STAGE_BYTES;
+  uint8_t* tst = ring + team * NS * C::STAGE_BYTES;
+  uint8_t* tconv = ring + C::RING_BYTES + team * G::STAGE_BYTES;  // FP8: the team's f16 tile buffer
+  auto issue = [&](uint8_t* stage, uint64_t* bar, int phys) {
+    if constexpr (FP8) load_block_fp8(stage, bar, phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
+    else load_block_3d<D>(stage, bar, phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
+  };
   uint64_t* tfull = full + team * NS;
   const bool leader = (rt == 0 && lane == 0);
   const uint32_t* wrow = a.words + (size_t)src * a.max_blocks + b0 + kb0;  // the team's block words
@@ -223,7 +256,7 @@ __global__ void __launch_bounds__(kShThreads, 3)
     for (int k = 0; k < pro; ++k) {
       const int rid = rec_id(kb0 + k);
       const int phys = (rid >= 0 && rid < a.num_pool_blocks) ? rid : a.num_pool_blocks;
-      load_block_3d<D>(tst + k * G::STAGE_BYTES, &tfull[k], phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
+      issue(tst + k * C::STAGE_BYTES, &tfull[k], phys);
     }
   int cur_phys, cur_nv, nxt_phys = a.num_pool_blocks, nxt_nv = 0;
   describe(0, cur_phys, cur_nv);
@@ -231,7 +264,7 @@ __global__ void __launch_bounds__(kShThreads, 3)
   if (!rec_first)
     for (int k = 0; k < pro; ++k) {
       const int phys = __shfl_sync(0xffffffffu, cur_phys, k);
-      if (leader) load_block_3d<D>(tst + k * G::STAGE_BYTES, &tfull[k], phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
+      if (leader) issue(tst + k * C::STAGE_BYTES, &tfull[k], phys);
     }
   int issued = pro;
   LAZY_TRACE(1, global_timer_ns());
@@ -265,6 +298,31 @@ __global__ void __launch_bounds__(kShThreads, 3)
     const int m = r / a.G;
     const float2* cs = cs_tab + (r < rows ? m : 0) * HALF;
     const float sc = (r < rows && m_ok[r < rows ? m : 0]) ? a.scale_log2 : 0.f;  // a failed member's rows are 0
+    if constexpr (FP8) {
+      // f16 fragments in the permuted order: k-step ks, columns 2t + {0,1} / 2t + 8 + {0,1}
+      // hold dims 32t + 4ks + {0,1} / {2,3}; lanes t = 0, 1 hold first halves of
+      // rotate-half pairs (x c - y s), t = 2, 3 second halves (y c + x s).
+      const bool second = t >= 2;
+      const uint32_t* ow = reinterpret_cast<const uint32_t*>(qo[rr]);
+      const uint32_t* pw = reinterpret_cast<const uint32_t*>(qp[rr]);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        float v[4];
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[2 * ks + e2]));
+          const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pw[2 * ks + e2]));
+          const int f = (32 * t + 4 * ks + 2 * e2) & (HALF - 1);
+          const float2 c0 = cs[f], c1 = cs[f + 1];
+          const float s0 = second ? c0.y : -c0.y, s1 = second ? c1.y : -c1.y;
+          v[2 * e2] = fmaf(x.x, c0.x * sc, y.x * (s0 * sc));
+          v[2 * e2 + 1] = fmaf(x.y, c1.x * sc, y.y * (s1 * sc));
+        }
+        qa[ks][rr] = pack_f16x2(v[0], v[1]);
+        qa[ks][rr + 2] = pack_f16x2(v[2], v[3]);
+      }
+      continue;
+    }
 #pragma unroll
     for (int ks = 0; ks < NQ; ++ks)
 #pragma unroll
@@ -313,7 +371,16 @@ __global__ void __launch_bounds__(kShThreads, 3)
     const int slot = k % NS;
     const int nvalid = __shfl_sync(0xffffffffu, cur_nv, k & 31);
     bool ok = warp_wait(&tfull[slot], (k / NS) & 1, a.status);
-    if (ok) {
+    if constexpr (FP8) {
+      uint8_t* stage = tst + slot * C::STAGE_BYTES;
+      if (ok) convert_fp8_block(stage, tconv, 32 * rt + lane, 32 * RT);
+      // the team's f16 V tile is complete before any of its warps reads it
+      if (RT > 1) ok = team_and(team, 32 * RT, ok);
+      else __syncwarp();
+      if (ok)
+        attend_block_fp8(smem_u32(stage), smem_u32(tconv) + G::KV_BYTES, ln, qa, nvalid, o, m_r, l_r, lane,
+                         a.k_scale);
+    } else if (ok) {
       if constexpr (ALIBI) {
         const int j0 = kBlock * (kb0 + k);
         const float b0[2] = {ab_slope[0] * (float)(j0 - ab_delta[0]), ab_slope[1] * (float)(j0 - ab_delta[1])};
@@ -342,8 +409,7 @@ __global__ void __launch_bounds__(kShThreads, 3)
         }
         phys = __shfl_sync(0xffffffffu, nxt_phys, kn & 31);
       }
-      if (leader)
-        load_block_3d<D>(tst + slot * G::STAGE_BYTES, &tfull[slot], phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
+      if (leader) issue(tst + slot * C::STAGE_BYTES, &tfull[slot], phys);
       issued = kn + 1;
     }
   }
@@ -362,6 +428,8 @@ __global__ void __launch_bounds__(kShThreads, 3)
   __syncthreads();  // every team is done with its ring (the merge reuses it)
   LAZY_TRACE(3, global_timer_ns());
   if (abort_flag) return;
+  float vsc = 1.f;  // FP8: values are code * v_scale, and the output is linear in them
+  if constexpr (FP8) vsc = a.v_scale;
   if (TEAMS == 1) {  // one team: write straight from the accumulators
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
@@ -375,7 +443,7 @@ __global__ void __launch_bounds__(kShThreads, 3)
 #pragma unroll
       for (int j = 0; j < D / 8; ++j)
         *reinterpret_cast<float2*>(dst + 8 * j) =
-            good ? make_float2(o[j][2 * rr], o[j][2 * rr + 1]) : make_float2(0.f, 0.f);
+            good ? make_float2(o[j][2 * rr] * vsc, o[j][2 * rr + 1] * vsc) : make_float2(0.f, 0.f);
       if (t == 0) *reinterpret_cast<float2*>(a.ws_ml + 2 * pidx) = good ? make_float2(m_r[rr], l_r[rr])
                                                                          : make_float2(-INFINITY, 0.f);
     }
@@ -389,7 +457,7 @@ __global__ void __launch_bounds__(kShThreads, 3)
         float* dst = red + ((size_t)team * trows + row) * C::RED_STRIDE;
 #pragma unroll
         for (int j = 0; j < D / 8; ++j)
-          *reinterpret_cast<float2*>(dst + 8 * j + 2 * t) = make_float2(o[j][2 * rr], o[j][2 * rr + 1]);
+          *reinterpret_cast<float2*>(dst + 8 * j + 2 * t) = make_float2(o[j][2 * rr] * vsc, o[j][2 * rr + 1] * vsc);
         if (t == 0) *reinterpret_cast<float2*>(dst + D) = make_float2(m_r[rr], l_r[rr]);
       }
     }
@@ -513,12 +581,13 @@ __global__ void shared_combine_kernel(const SharedDecodeArgs a) {
 
 // ------------------------------------------------------------------ launchers
 
-template <int D, bool LAZY, bool ALIBI>
+template <int D, bool LAZY, bool ALIBI, bool FP8 = false>
 static cudaError_t launch_shared_t(const SharedDecodeArgs& a, const float* alibi, const CUtensorMap& kmap,
-                                   const CUtensorMap& vmap, cudaStream_t st) {
-  using C = SharedCfg<D>;
-  auto kern = decode_shared_kernel<D, LAZY, ALIBI>;
-  cudaError_t e = set_smem_once<decode_shared_kernel<D, LAZY, ALIBI>>(C::SMEM);
+                                   const CUtensorMap& vmap, cudaStream_t st, float k_scale = 1.f,
+                                   float v_scale = 1.f) {
+  using C = SharedCfg<D, FP8>;
+  auto kern = decode_shared_kernel<D, LAZY, ALIBI, FP8>;
+  cudaError_t e = set_smem_once<decode_shared_kernel<D, LAZY, ALIBI, FP8>>(C::SMEM);
   if (e != cudaSuccess) return e;
   const long long blocks = (long long)a.num_items * a.Hkv;
   if constexpr (ALIBI) {
@@ -526,6 +595,13 @@ static cudaError_t launch_shared_t(const SharedDecodeArgs& a, const float* alibi
     static_cast<SharedDecodeArgs&>(aa) = a;
     aa.alibi = alibi;
     kern<<<(unsigned)blocks, kShThreads, C::SMEM, st>>>(aa, kmap, vmap);
+  } else if constexpr (FP8) {
+    (void)alibi;
+    SharedFp8Args fa;
+    static_cast<SharedDecodeArgs&>(fa) = a;
+    fa.k_scale = k_scale;
+    fa.v_scale = v_scale;
+    kern<<<(unsigned)blocks, kShThreads, C::SMEM, st>>>(fa, kmap, vmap);
   } else {
     (void)alibi;
     kern<<<(unsigned)blocks, kShThreads, C::SMEM, st>>>(a, kmap, vmap);
@@ -546,6 +622,14 @@ cudaError_t launch_decode_shared(const SharedDecodeArgs& a, const float* alibi, 
                 : launch_shared_t<128, false, false>(a, nullptr, kmap, vmap, st);
   return lazy ? launch_shared_t<64, true, false>(a, nullptr, kmap, vmap, st)
               : launch_shared_t<64, false, false>(a, nullptr, kmap, vmap, st);
+}
+
+cudaError_t launch_decode_shared_fp8(const SharedDecodeArgs& a, float k_scale, float v_scale, bool lazy,
+                                     const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t st) {
+  if (a.num_items == 0) return cudaSuccess;
+  if (a.D != 128) return cudaErrorNotSupported;
+  return lazy ? launch_shared_t<128, true, false, true>(a, nullptr, kmap, vmap, st, k_scale, v_scale)
+              : launch_shared_t<128, false, false, true>(a, nullptr, kmap, vmap, st, k_scale, v_scale);
 }
 
 cudaError_t launch_shared_combine(const SharedDecodeArgs& a, cudaStream_t st) {

@@ -126,6 +126,11 @@ struct SharedAlibiArgs : SharedDecodeArgs {
   const float* alibi;  // [Hq] slopes
 };
 
+// FP8 (e4m3) pools on the shared-run decode: keys code * k_scale, values code * v_scale.
+struct SharedFp8Args : SharedDecodeArgs {
+  float k_scale, v_scale;
+};
+
 // Eager materialisation (materialize.cu): per-sequence copies with K at absolute positions.
 struct MaterializeArgs {
   const void* k_pool;        // [NB][Hkv][16][D]
@@ -200,6 +205,10 @@ cudaError_t launch_prefill_tq(const PrefillArgs& a, bool lazy, const CUtensorMap
 // alibi: null, or [Hq] ALiBi slopes (lazy mode only).
 cudaError_t launch_decode_shared(const SharedDecodeArgs& a, const float* alibi, bool lazy, const CUtensorMap& kmap,
                                  const CUtensorMap& vmap, cudaStream_t st);
+// The same kernel on e4m3 pools (d = 128; every query-head count up to 64 per KV head,
+// items of at most 64 rows).
+cudaError_t launch_decode_shared_fp8(const SharedDecodeArgs& a, float k_scale, float v_scale, bool lazy,
+                                     const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t st);
 cudaError_t launch_decode_shared_tc(const SharedDecodeArgs& a, const float* alibi, bool lazy,
                                     const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t st);
 cudaError_t launch_shared_combine(const SharedDecodeArgs& a, cudaStream_t st);

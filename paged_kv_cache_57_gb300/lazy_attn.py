@@ -340,7 +340,7 @@ def decode_shared(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torc
             workspace = torch.empty(nws, dtype=torch.uint8, device=q.device)
     wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
     i32 = torch.int32
-    args = (ctypes.byref(p), _dptr(q, "q", dt), _dptr(k_pool, "k_pool", dt), _dptr(v_pool, "v_pool", dt),
+    args = (ctypes.byref(p), _dptr(q, "q", dt), _dptr(k_pool, "k_pool", _kvdt(p)), _dptr(v_pool, "v_pool", _kvdt(p)),
             _dptr(block_words, "block_words"), _dptr(q_pos, "q_pos", i32), _dptr(rope_table, "rope_table"),
             plan.num_items, _dptr(plan.items, "items", i32), plan.num_slots,
             _dptr(plan.slot_indptr, "slot_indptr", i32))

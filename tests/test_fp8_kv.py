@@ -81,9 +81,14 @@ def test_fp8_argument_rules_without_cuda():
     p = params()
     p.kv_dtype = 7
     assert decode(p) == un
-    p = params()
+    # the shared-run decode takes e4m3 pools at d = 128 only, and not with ALiBi
+    p = params(head_dim=64)
     assert L._lib.lazy_attn_decode_shared(ctypes.byref(p), *([fake] * 6), 1, fake, 1, fake, fake, fake, 1 << 20,
                                           None) == un
+    p = params(key_positions=True)
+    assert L._lib.lazy_attn_decode_shared_alibi(ctypes.byref(p), *([fake] * 6), 1, fake, 1, fake, fake, fake, fake,
+                                                1 << 20, None) == un
+    p = params()
     assert L._lib.lazy_attn_prefill(ctypes.byref(p), fake, fake, fake, 1, 1, *([fake] * 7), 1 << 20, None) == un
     assert L._lib.lazy_attn_materialize(ctypes.byref(p), *([fake] * 8), None) == un
     assert L._lib.lazy_attn_decode_alibi(ctypes.byref(params(key_positions=True)), *([fake] * 7), fake, fake, fake,
