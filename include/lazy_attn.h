@@ -319,7 +319,7 @@ int lazy_attn_decode_shared(const lazy_attn_params *p, const void *q, const void
  * q or k: pass a table built by lazy_attn_rope_table_init_freqs from zero rates (the
  * calls do not rotate, whatever p->lazy says). alibi_slopes: device fp32 [Hq], 4-byte
  * aligned; p->key_positions must be 1, else LAZY_ERR_INVALID_ARG. bf16 only. The
- * prefill has no ALiBi form. */
+ * prefill's ALiBi form, lazy_attn_prefill_alibi, is declared after lazy_attn_prefill. */
 int lazy_attn_decode_alibi(const lazy_attn_params *p, const void *q, const void *k_pool, const void *v_pool,
                            const uint32_t *block_words, const int32_t *seq_lens, const int32_t *q_pos,
                            const void *rope_table, const float *alibi_slopes, void *out, void *workspace,
@@ -390,6 +390,22 @@ int lazy_attn_prefill(const lazy_attn_params *p, const void *q, const int32_t *c
                       const void *v_pool, const uint32_t *block_words, const int32_t *seq_lens,
                       const void *rope_table, void *out, void *workspace, size_t workspace_bytes,
                       lazy_stream_t stream);
+
+/* ALiBi prefill ("Resumo Técnico: LazyAttention", "Principais Contribuições", item 4):
+ * the same call with every score of query head h biased by
+ * -alibi_slopes[h] * (m_i - n) before the softmax, for query row i at m_i =
+ * q_start[s] + i and a key at absolute position n (the chunk's own keys included).
+ * The block words must be packed with p->key_positions = 1 (a block's word gives the
+ * position of its first key; n is that plus the slot) and the rope table built from
+ * zero rates (ALiBi models do not rotate; the call never rotates K, and rotates Q
+ * only by that table). alibi_slopes: device fp32 [Hq], 4-byte aligned. Both prefill
+ * kernels take it (every GQA ratio, MHA included). LAZY_ERR_INVALID_ARG without
+ * slopes or with p->key_positions = 0; lazy_attn_prefill refuses key-position words. */
+int lazy_attn_prefill_alibi(const lazy_attn_params *p, const void *q, const int32_t *cu_seqlens_q,
+                            const int32_t *q_start, int32_t total_q, int32_t max_q_len, const void *k_pool,
+                            const void *v_pool, const uint32_t *block_words, const int32_t *seq_lens,
+                            const void *rope_table, const float *alibi_slopes, void *out, void *workspace,
+                            size_t workspace_bytes, lazy_stream_t stream);
 
 /* ---------------------------------------------------------------- eager materialisation (baseline)
  * The alternative the lazy method avoids ("Declaração do Problema"): a reused

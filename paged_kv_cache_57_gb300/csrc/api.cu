@@ -614,15 +614,17 @@ size_t lazy_attn_prefill_workspace_bytes(const lazy_attn_params* p, int32_t tota
   return lazy::prefill_stream_workspace_bytes(current_device() >= 0 ? lazy::prefill_stream_grid() : kDefaultSmCount);
 }
 
-int lazy_attn_prefill(const lazy_attn_params* p, const void* q, const int32_t* cu_seqlens_q, const int32_t* q_start,
-                      int32_t total_q, int32_t max_q_len, const void* k_pool, const void* v_pool,
-                      const uint32_t* block_words, const int32_t* seq_lens, const void* rope_table, void* out,
-                      void* workspace, size_t workspace_bytes, lazy_stream_t stream) {
+static int prefill_impl(const lazy_attn_params* p, const void* q, const int32_t* cu_seqlens_q, const int32_t* q_start,
+                        int32_t total_q, int32_t max_q_len, const void* k_pool, const void* v_pool,
+                        const uint32_t* block_words, const int32_t* seq_lens, const void* rope_table,
+                        const float* alibi, void* out, void* workspace, size_t workspace_bytes, lazy_stream_t stream) {
   Checked c;
   int rc = check_params(p, &c);
   if (rc != LAZY_OK) return rc;
   if (p->dtype != LAZY_BF16 || p->head_dim != 128 || kv_fp8(p)) return LAZY_ERR_UNSUPPORTED;
-  if (total_q < 0 || max_q_len < 0 || p->key_positions) return LAZY_ERR_INVALID_ARG;
+  // key-position words carry no document start: only the ALiBi form reads them
+  if (total_q < 0 || max_q_len < 0 || !alibi != !p->key_positions || (reinterpret_cast<uintptr_t>(alibi) & 3u))
+    return LAZY_ERR_INVALID_ARG;
   if (p->num_seqs == 0 || total_q == 0 || max_q_len == 0) return LAZY_OK;
   if (!q || !cu_seqlens_q || !q_start || !k_pool || !v_pool || !block_words || !seq_lens || !rope_table || !out)
     return LAZY_ERR_INVALID_ARG;
@@ -665,10 +667,28 @@ int lazy_attn_prefill(const lazy_attn_params* p, const void* q, const int32_t* c
     a.counters = static_cast<int*>(workspace);
     a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + lazy::prefill_stream_counter_bytes(grid));
   }
-  cudaError_t e =
-      lazy::launch_prefill(a, p->lazy != 0, qmap, kmap, vmap, grid, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = lazy::launch_prefill(a, alibi ? false : p->lazy != 0, qmap, kmap, vmap, grid,
+                                       reinterpret_cast<cudaStream_t>(stream), alibi);
   if (e == cudaErrorNotSupported) return LAZY_ERR_UNSUPPORTED;
   return launched(e);
+}
+
+int lazy_attn_prefill(const lazy_attn_params* p, const void* q, const int32_t* cu_seqlens_q, const int32_t* q_start,
+                      int32_t total_q, int32_t max_q_len, const void* k_pool, const void* v_pool,
+                      const uint32_t* block_words, const int32_t* seq_lens, const void* rope_table, void* out,
+                      void* workspace, size_t workspace_bytes, lazy_stream_t stream) {
+  return prefill_impl(p, q, cu_seqlens_q, q_start, total_q, max_q_len, k_pool, v_pool, block_words, seq_lens,
+                      rope_table, nullptr, out, workspace, workspace_bytes, stream);
+}
+
+int lazy_attn_prefill_alibi(const lazy_attn_params* p, const void* q, const int32_t* cu_seqlens_q,
+                            const int32_t* q_start, int32_t total_q, int32_t max_q_len, const void* k_pool,
+                            const void* v_pool, const uint32_t* block_words, const int32_t* seq_lens,
+                            const void* rope_table, const float* alibi_slopes, void* out, void* workspace,
+                            size_t workspace_bytes, lazy_stream_t stream) {
+  if (!alibi_slopes) return LAZY_ERR_INVALID_ARG;
+  return prefill_impl(p, q, cu_seqlens_q, q_start, total_q, max_q_len, k_pool, v_pool, block_words, seq_lens,
+                      rope_table, alibi_slopes, out, workspace, workspace_bytes, stream);
 }
 
 int lazy_attn_materialize(const lazy_attn_params* p, const void* k_pool, const void* v_pool,

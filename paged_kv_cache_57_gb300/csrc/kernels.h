@@ -101,6 +101,11 @@ struct PrefillArgs {
   int* counters;
   float* partials;
 };
+// ALiBi prefill: no rotation (key-position words), score of query head h and a key
+// at position n biased by slope_h (n - m) for the query at m.
+struct PrefillAlibiArgs : PrefillArgs {
+  const float* alibi;  // [Hq] slopes
+};
 constexpr int PREFILL_PARTIAL_ROW_FLOATS = 128 + 4;
 constexpr int pf_tile_rows = 128;  // query rows per prefill tile
 
@@ -190,17 +195,17 @@ cudaError_t launch_gather_f32(const GatherArgs& a, cudaStream_t st);
 // needs a.counters / a.partials and `grid` = prefill_stream_grid()), else the
 // TMEM-Q one-tile kernel.
 cudaError_t launch_prefill(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, int grid, cudaStream_t st);
+                           const CUtensorMap& vmap, int grid, cudaStream_t st, const float* alibi = nullptr);
 // Two query tiles per CTA, one CTA per SM, stream-K over (unit, K tile); even GQA ratio.
 cudaError_t launch_prefill_stream(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                                  const CUtensorMap& vmap, int grid, cudaStream_t st);
+                                  const CUtensorMap& vmap, int grid, cudaStream_t st, const float* alibi = nullptr);
 size_t prefill_stream_workspace_bytes(int grid);  // counters, then partials
 size_t prefill_stream_counter_bytes(int grid);
 int prefill_stream_grid();
 
 // One query tile per CTA with the rotated Q tile in tensor memory; any GQA ratio.
 cudaError_t launch_prefill_tq(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                              const CUtensorMap& vmap, cudaStream_t st);
+                              const CUtensorMap& vmap, cudaStream_t st, const float* alibi = nullptr);
 
 // alibi: null, or [Hq] ALiBi slopes (lazy mode only).
 cudaError_t launch_decode_shared(const SharedDecodeArgs& a, const float* alibi, bool lazy, const CUtensorMap& kmap,

@@ -16,16 +16,21 @@
 //                      needs an even GQA ratio.
 //   prefill_tq.cu      one query tile per CTA with Q' held in tensor memory; any
 //                      GQA ratio.
+// With ALiBi ("Principais Contribuições", item 4: the mechanism carries over to
+// relative encodings such as ALiBi) both run without rotation on key-position block
+// words, and the softmax adds slope_h (n - m) to each score from the block's first
+// key position and the slot.
 #include "kernels.h"
 
 namespace lazy {
 
 cudaError_t launch_prefill(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, int grid, cudaStream_t st) {
+                           const CUtensorMap& vmap, int grid, cudaStream_t st, const float* alibi) {
   if (a.D != 128) return cudaErrorNotSupported;
+  if (alibi && lazy) return cudaErrorInvalidValue;  // ALiBi: key-position words, no rotation
   if (a.B == 0 || a.max_q_len == 0) return cudaSuccess;
-  if (a.G % 2 == 0) return launch_prefill_stream(a, lazy, qmap, kmap, vmap, grid, st);
-  return launch_prefill_tq(a, lazy, qmap, kmap, vmap, st);
+  if (a.G % 2 == 0) return launch_prefill_stream(a, lazy, qmap, kmap, vmap, grid, st, alibi);
+  return launch_prefill_tq(a, lazy, qmap, kmap, vmap, st, alibi);
 }
 
 }  // namespace lazy

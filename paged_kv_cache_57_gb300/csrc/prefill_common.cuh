@@ -24,6 +24,8 @@ struct KMeta {
 struct VMeta {
   int nvalid;
   int chunk_j0;  // chunk-local index of the block's first key, or -1 for cached documents
+  int pos;       // the position the block word gives (ALiBi: that of the block's first key)
+  int pad;
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {

@@ -30,6 +30,7 @@
 // so the pipeline runs on across segment boundaries: the producers load the next
 // segment's Q and K/V tiles while the current one drains.
 #include <climits>
+#include <type_traits>
 
 #include "prefill_common.cuh"
 
@@ -169,10 +170,12 @@ static_assert(OFF_SCHED % 16 == 0 && OFF_TMEM % 16 == 0, "shared-memory slots ar
 #endif
 #define LAZY_PF_TRACE(sg, i, v) LAZY_PF_TRACE_IF(threadIdx.x == 0, sg, i, v)
 
-template <bool LAZY>
+template <bool LAZY, bool ALIBI = false>
 __global__ void __launch_bounds__(THREADS, 1)
-    prefill_stream_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
-                          const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
+    prefill_stream_kernel(const std::conditional_t<ALIBI, PrefillAlibiArgs, PrefillArgs> a,
+                          const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                          const __grid_constant__ CUtensorMap vmap) {
+  static_assert(!(ALIBI && LAZY), "the ALiBi prefill does not rotate");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   uint8_t* sQ[2] = {base + OFF_QA, base + OFF_QB};
@@ -465,7 +468,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (g >= ns && !warp_wait(&emp_ring[st], ((g / ns) & 1) ^ 1, a.status)) return ok = false;
         if (lane < BLOCKS) {
           if (is_v)
-            vmeta[st * BLOCKS + lane] = VMeta{nv, b >= un.b_chunk ? kBlock * (b - un.b_chunk) : -1};
+            vmeta[st * BLOCKS + lane] = VMeta{nv, b >= un.b_chunk ? kBlock * (b - un.b_chunk) : -1, bi.p, 0};
           else
             kmeta[st * BLOCKS + lane] = KMeta{bi.p, nv};
         }
@@ -772,6 +775,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                      const UnitDesc& next_un) {
       (void)u;
       const int iq = un.row0 + i;  // query index within the chunk
+      // ALiBi: slope of this tile's query head in log2 units and the row's position m_i.
+      float slope2 = 0.f;
+      int m_row = 0;
+      if constexpr (ALIBI) {
+        slope2 = __ldg(&a.alibi[2 * un.hp + t]) * 1.4426950408889634f;
+        m_row = __ldg(&a.q_start[un.s]) + iq;
+      }
       // Q prologue: R_{m_i} of row i of tile t, m_i = q_start + row0 + i, pre-scaled by
       // sm_scale * log2(e).
       if (sg == 0) make_bq(un, 0);
@@ -799,13 +809,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         // Per-block key limits for this row (holes; causal inside the chunk).
         int lim[BLOCKS];
+        float bias0[ALIBI ? BLOCKS : 1];  // ALiBi: slope (n0 - m_i) of each block's first key
         bool full_tile = true;
 #pragma unroll
         for (int bl = 0; bl < BLOCKS; ++bl) {
           const VMeta m = vmeta[vs * BLOCKS + bl];
           full_tile &= (m.nvalid == kBlock) & (m.chunk_j0 < 0);
           lim[bl] = m.chunk_j0 >= 0 ? max(0, min(m.nvalid, iq - m.chunk_j0 + 1)) : m.nvalid;
+          if constexpr (ALIBI) bias0[bl] = slope2 * (float)(m.pos - m_row);
         }
+        // Scores of chunk q (32 keys: blocks 2q, 2q + 1) plus the ALiBi bias.
+        auto add_bias = [&](float (&sv)[32], int q) {
+          if constexpr (ALIBI) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) sv[k] = fmaf(slope2, (float)(k & 15), sv[k] + bias0[2 * q + (k >> 4)]);
+          }
+        };
         // Pass 1: row maximum.
         float mx = -INFINITY;
 #pragma unroll 1
@@ -813,6 +832,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           float sv[32];
           tmem_ld32(tS + lane_base + 32 * q, sv);
           tmem_ld_wait(sv);
+          add_bias(sv, q);
           if (full_tile) {
             float m2[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -844,6 +864,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           float sv[32];
           tmem_ld32(tS + lane_base + 32 * q, sv);
           tmem_ld_wait(sv);
+          add_bias(sv, q);
           if (!full_tile) {
 #pragma unroll
             for (int k = 0; k < 32; ++k)
@@ -928,11 +949,20 @@ size_t prefill_stream_workspace_bytes(int grid) {
 }
 
 cudaError_t launch_prefill_stream(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                                  const CUtensorMap& vmap, int grid, cudaStream_t st) {
+                                  const CUtensorMap& vmap, int grid, cudaStream_t st, const float* alibi) {
   if (a.D != D || a.G % 2 != 0) return cudaErrorNotSupported;
   if (a.B == 0 || a.max_q_len == 0 || grid <= 0) return cudaSuccess;
   cudaError_t e = cudaMemsetAsync(a.counters, 0, (size_t)(grid + 1) * 2 * BM * sizeof(int), st);
   if (e != cudaSuccess) return e;
+  if (alibi) {
+    e = set_smem_once<prefill_stream_kernel<false, true>>(SMEM);
+    if (e != cudaSuccess) return e;
+    PrefillAlibiArgs aa;
+    static_cast<PrefillArgs&>(aa) = a;
+    aa.alibi = alibi;
+    prefill_stream_kernel<false, true><<<grid, THREADS, SMEM, st>>>(aa, qmap, kmap, vmap);
+    return cudaGetLastError();
+  }
   auto kern = lazy ? prefill_stream_kernel<true> : prefill_stream_kernel<false>;
   e = lazy ? set_smem_once<prefill_stream_kernel<true>>(SMEM) : set_smem_once<prefill_stream_kernel<false>>(SMEM);
   if (e != cudaSuccess) return e;

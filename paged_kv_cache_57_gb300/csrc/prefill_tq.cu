@@ -27,6 +27,7 @@
 // Barriers that could be passed twice before their consumer looks (S ready) come one
 // per buffer; the epilogue waits on a barrier with a single phase.
 #include <climits>
+#include <type_traits>
 
 #include "prefill_common.cuh"
 
@@ -77,10 +78,12 @@ __device__ __forceinline__ void store_rotated_q(const uint8_t* sQ, int i, int c0
 
 }  // namespace
 
-template <bool LAZY>
+template <bool LAZY, bool ALIBI = false>
 __global__ void __launch_bounds__(THREADS, 1)
-    prefill_tq_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
-                      const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
+    prefill_tq_kernel(const std::conditional_t<ALIBI, PrefillAlibiArgs, PrefillArgs> a,
+                      const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap) {
+  static_assert(!(ALIBI && LAZY), "the ALiBi prefill does not rotate");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   uint8_t* sQ = base + OFF_Q;
@@ -218,7 +221,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (lane < BLOCKS) {
         if (is_v)
-          vmeta[st * BLOCKS + lane] = VMeta{nv, b >= b_chunk ? kBlock * (b - b_chunk) : -1};
+          vmeta[st * BLOCKS + lane] = VMeta{nv, b >= b_chunk ? kBlock * (b - b_chunk) : -1, bi.p, 0};
         else
           kmeta[st * BLOCKS + lane] = KMeta{bi.p, nv};
       }
@@ -386,6 +389,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int i = threadIdx.x & 127;            // query row within the tile == TMEM lane
     const int iq = row0 + i;                    // query index within the chunk
     const int pair_bar = BAR_PAIR0 + quad;
+    // ALiBi: slope of the query head in log2 units and the row's position m_i.
+    float slope2 = 0.f;
+    int m_row = 0;
+    if constexpr (ALIBI) {
+      slope2 = __ldg(&a.alibi[h]) * 1.4426950408889634f;
+      m_row = a.q_start[s] + iq;
+    }
     const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
     const uint32_t tO = tmem + COL_O + lane_base + 64 * hc;  // this thread's 64 columns of O
     const uint32_t tP = tmem + COL_P + lane_base + 32 * hc;  // and its 32 columns of P
@@ -428,6 +438,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           lim[k] = m.chunk_j0 >= 0 ? max(0, min(m.nvalid, iq - m.chunk_j0 + 1)) : m.nvalid;
         }
         tmem_ld_wait(sv[0], sv[1]);
+        if constexpr (ALIBI) {  // + slope (n - m_i), n = the block's first key position + slot
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const float b0 = slope2 * (float)(vmeta[vs * BLOCKS + 4 * hc + k4].pos - m_row);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              float& x = sv[k4 >> 1][16 * (k4 & 1) + k];
+              x = fmaf(slope2, (float)k, x + b0);
+            }
+          }
+        }
         if (!full_half) {
 #pragma unroll
           for (int k = 0; k < 64; ++k)
@@ -537,10 +558,19 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 cudaError_t launch_prefill_tq(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                              const CUtensorMap& vmap, cudaStream_t st) {
+                              const CUtensorMap& vmap, cudaStream_t st, const float* alibi) {
   if (a.D != D) return cudaErrorNotSupported;
   if (a.B == 0 || a.max_q_len == 0) return cudaSuccess;
   dim3 grid((a.max_q_len + BM - 1) / BM, a.Hq, a.B);
+  if (alibi) {
+    cudaError_t e = set_smem_once<prefill_tq_kernel<false, true>>(SMEM);
+    if (e != cudaSuccess) return e;
+    PrefillAlibiArgs aa;
+    static_cast<PrefillArgs&>(aa) = a;
+    aa.alibi = alibi;
+    prefill_tq_kernel<false, true><<<grid, THREADS, SMEM, st>>>(aa, qmap, kmap, vmap);
+    return cudaGetLastError();
+  }
   auto kern = lazy ? prefill_tq_kernel<true> : prefill_tq_kernel<false>;
   cudaError_t e = lazy ? set_smem_once<prefill_tq_kernel<true>>(SMEM) : set_smem_once<prefill_tq_kernel<false>>(SMEM);
   if (e != cudaSuccess) return e;

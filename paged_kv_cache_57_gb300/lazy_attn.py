@@ -36,7 +36,7 @@ EXPORTED = (
     "lazy_attn_plan_shared_host", "lazy_attn_decode_shared_workspace_bytes", "lazy_attn_decode_shared",
     "lazy_attn_materialize", "lazy_attn_rope_table_init_scaled", "lazy_attn_rope_table_init_freqs",
     "lazy_attn_rotary_layout_host", "lazy_attn_decode_shared_alibi", "lazy_attn_alibi_slopes_host",
-    "lazy_attn_decode_alibi", "lazy_attn_debug_gather_withheld",
+    "lazy_attn_decode_alibi", "lazy_attn_debug_gather_withheld", "lazy_attn_prefill_alibi",
 )
 PLAN_MAX_MEMBERS = 16
 PLAN_ITEM_BLOCK_IDS = 32
@@ -77,6 +77,7 @@ _sig = {
     "lazy_attn_decode": (ctypes.c_int, [_P] + [_vp] * 9 + [_sz, _vp]),
     "lazy_attn_prefill_workspace_bytes": (_sz, [_P, _i32]),
     "lazy_attn_prefill": (ctypes.c_int, [_P, _vp, _vp, _vp, _i32, _i32] + [_vp] * 7 + [_sz, _vp]),
+    "lazy_attn_prefill_alibi": (ctypes.c_int, [_P, _vp, _vp, _vp, _i32, _i32] + [_vp] * 8 + [_sz, _vp]),
     "lazy_attn_debug_gather": (ctypes.c_int, [_P] + [_vp] * 7 + [_vp]),
     "lazy_attn_debug_gather_withheld": (ctypes.c_int, [_P] + [_vp] * 7 + [_i32, ctypes.c_uint32, _vp]),
     "lazy_attn_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
@@ -386,7 +387,8 @@ def prefill_workspace_bytes(p: Params, total_q: int) -> int:
 def prefill(p: Params, q: torch.Tensor, cu_seqlens_q: torch.Tensor, q_start: torch.Tensor, max_q_len: int,
             k_pool: torch.Tensor, v_pool: torch.Tensor, block_words: torch.Tensor, seq_lens: torch.Tensor,
             rope_table: torch.Tensor, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-            stream=None) -> torch.Tensor:
+            stream=None, alibi_slopes: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Prefill; ``alibi_slopes`` (device fp32 [Hq]) selects the ALiBi call."""
     dt = _tdt(p)
     if out is None:
         out = torch.empty_like(q)
@@ -394,12 +396,17 @@ def prefill(p: Params, q: torch.Tensor, cu_seqlens_q: torch.Tensor, q_start: tor
     if workspace is None and nws:
         workspace = torch.empty(nws, dtype=torch.uint8, device=q.device)
     wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = _lib.lazy_attn_prefill(ctypes.byref(p), _dptr(q, "q", dt), _dptr(cu_seqlens_q, "cu_seqlens_q", torch.int32),
-                                _dptr(q_start, "q_start", torch.int32), int(q.shape[0]), int(max_q_len),
-                                _dptr(k_pool, "k_pool", dt), _dptr(v_pool, "v_pool", dt),
-                                _dptr(block_words, "block_words"), _dptr(seq_lens, "seq_lens", torch.int32),
-                                _dptr(rope_table, "rope_table"), _dptr(out, "out", dt), _dptr(workspace, "workspace"),
-                                wsz, _stream(stream))
+    head = (ctypes.byref(p), _dptr(q, "q", dt), _dptr(cu_seqlens_q, "cu_seqlens_q", torch.int32),
+            _dptr(q_start, "q_start", torch.int32), int(q.shape[0]), int(max_q_len),
+            _dptr(k_pool, "k_pool", dt), _dptr(v_pool, "v_pool", dt),
+            _dptr(block_words, "block_words"), _dptr(seq_lens, "seq_lens", torch.int32), _dptr(rope_table, "rope_table"))
+    tail = (_dptr(out, "out", dt), _dptr(workspace, "workspace"), wsz, _stream(stream))
+    if alibi_slopes is None:
+        rc = _lib.lazy_attn_prefill(*head, *tail)
+    else:
+        if alibi_slopes.numel() != p.num_q_heads:
+            raise ValueError("alibi_slopes needs one slope per query head")
+        rc = _lib.lazy_attn_prefill_alibi(*head, _dptr(alibi_slopes, "alibi_slopes", torch.float32), *tail)
     _check(rc, "prefill")
     return out
 

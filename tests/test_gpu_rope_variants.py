@@ -194,3 +194,26 @@ def test_per_sequence_decode_alibi(hq, hkv, d, splits, host_pack):
                  emulate=lambda r: emulate(w, r, freqs=np.zeros(d // 2), alibi=slopes, weight_bound=True),
                  fallback_frac=FEW_KEY_FALLBACK_FRAC)
     assert np.abs(ref - oracle.attention(w, freqs=np.zeros(d // 2))).max() > 1e-2
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (32, 1), (8, 8), (6, 2)])
+def test_prefill_alibi(hq, hkv):
+    # even GQA ratios (4, 32 per KV head): the stream-K kernel; odd (MHA, 3): the
+    # TMEM-Q kernel. Chunks of 140 and 33 rows over two 150-token documents: the
+    # bias reaches the cached keys and the chunk's own causal keys.
+    L = la()
+    w = W.prefill_zipf(f"palibi{hq}", batch=2, hq=hq, hkv=hkv, docs_per_seq=2, doc_tokens=150, pool_docs=3,
+                       zipf_s=1.0, chunk_tokens=[140, 33], seed=360 + hq + hkv)
+    slopes = L.alibi_slopes(hq)
+    ref = oracle.attention(w, freqs=np.zeros(64), alibi=slopes.astype(np.float64))
+    dv = _alibi_device(w)
+    out = L.prefill(dv.p, dv.q, dv.cu_seqlens_q, dv.q_start, dv.max_q_len, dv.k_pool, dv.v_pool, dv.words,
+                    dv.seq_lens, dv.rope, alibi_slopes=torch.from_numpy(slopes).cuda())
+    assert_close(out, ref, "bf16", f"prefill, ALiBi, {hq}/{hkv}",
+                 emulate=lambda r: emulate(w, r, freqs=np.zeros(64), alibi=slopes, weight_bound=True),
+                 fallback_frac=FEW_KEY_FALLBACK_FRAC)
+    assert np.abs(ref - oracle.attention(w, freqs=np.zeros(64))).max() > 1e-2
+    # the rotating call refuses key-position words
+    with pytest.raises(L.LazyAttnError):
+        L.prefill(dv.p, dv.q, dv.cu_seqlens_q, dv.q_start, dv.max_q_len, dv.k_pool, dv.v_pool, dv.words,
+                  dv.seq_lens, dv.rope)
