@@ -309,6 +309,29 @@ int lazy_attn_decode_shared(const lazy_attn_params *p, const void *q, const void
                             int32_t num_items, const int32_t *items, int32_t num_slots, const int32_t *slot_indptr,
                             void *out, void *workspace, size_t workspace_bytes, lazy_stream_t stream);
 
+/* The two halves of lazy_attn_decode_shared as separate calls (same arguments and
+ * checks). The split-K decode is two passes: partial results per document chunk,
+ * then their merge ("KV Cache, Flash Attention & Otimização de Inferência",
+ * "Flash Attention -- tiling": the running-maximum rescale). Keeping the partials
+ * lets a caller merge chunks computed elsewhere (another stream, or another GPU's
+ * share of the documents, gathered first), or time the two passes apart.
+ * lazy_attn_decode_shared_partials runs the work-item kernel only and leaves in
+ * `workspace`: fp32 o[num_slots][Hq][head_dim] (unnormalised weighted values, in
+ * log2 units of the running maximum), then fp32 (m, l)[num_slots][Hq] (running
+ * maximum in log2 units and weight sum; (-inf, 0) for an empty slot).
+ * lazy_attn_decode_shared_combine merges each sequence's slots of such a workspace
+ * into out [B][Hq][head_dim] bf16: out = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k
+ * over the slots k of slot_indptr, M = max_k m_k; 0 for a sequence without slots.
+ * lazy_attn_decode_shared = partials, then combine (launched so that the combine's
+ * start overlaps the work-item kernel's last CTAs). */
+int lazy_attn_decode_shared_partials(const lazy_attn_params *p, const void *q, const void *k_pool,
+                                     const void *v_pool, const uint32_t *block_words, const int32_t *q_pos,
+                                     const void *rope_table, int32_t num_items, const int32_t *items,
+                                     int32_t num_slots, void *workspace, size_t workspace_bytes,
+                                     lazy_stream_t stream);
+int lazy_attn_decode_shared_combine(const lazy_attn_params *p, int32_t num_slots, const int32_t *slot_indptr,
+                                    const void *workspace, size_t workspace_bytes, void *out, lazy_stream_t stream);
+
 /* ALiBi ("Resumo Técnico: LazyAttention", "Principais Contribuições", item 4: the
  * mechanism carries over to relative position encodings such as ALiBi): the same
  * calls with every score of query head h also biased by -alibi_slopes[h] * (m - n)

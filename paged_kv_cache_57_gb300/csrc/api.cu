@@ -494,11 +494,15 @@ size_t lazy_attn_decode_shared_workspace_bytes(const lazy_attn_params* p, int32_
   return bytes;
 }
 
+// phase: kSharedBoth (work-item kernel, then the combine as its programmatic
+// dependent), kSharedPartials (work-item kernel only), kSharedCombine (combine only).
+enum { kSharedBoth = 0, kSharedPartials = 1, kSharedCombine = 2 };
+
 static int decode_shared_impl(const lazy_attn_params* p, const void* q, const void* k_pool, const void* v_pool,
                               const uint32_t* block_words, const int32_t* q_pos, const void* rope_table,
                               int32_t num_items, const int32_t* items, int32_t num_slots, const int32_t* slot_indptr,
                               const float* alibi, void* out, void* workspace, size_t workspace_bytes,
-                              lazy_stream_t stream) {
+                              lazy_stream_t stream, int phase = kSharedBoth) {
   Checked c;
   int rc = check_params(p, &c);
   if (rc != LAZY_OK) return rc;
@@ -509,14 +513,16 @@ static int decode_shared_impl(const lazy_attn_params* p, const void* q, const vo
   if (c.G > 64) return LAZY_ERR_UNSUPPORTED;
   if (num_items < 0 || num_slots < 0) return LAZY_ERR_INVALID_ARG;
   if (p->num_seqs == 0) return LAZY_OK;
-  if (!q || !k_pool || !v_pool || !block_words || !q_pos || !rope_table || !slot_indptr || !out)
-    return LAZY_ERR_INVALID_ARG;
-  if (num_items > 0 && (!items || num_slots == 0)) return LAZY_ERR_INVALID_ARG;
-  if ((int64_t)num_items * p->num_kv_heads > INT32_MAX) return LAZY_ERR_UNSUPPORTED;
-  if (p->num_pool_blocks == 0 || p->max_blocks_per_seq == 0) return LAZY_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) || !aligned16(rope_table) ||
-      (items && !aligned16(items)))
-    return LAZY_ERR_INVALID_ARG;
+  if (phase != kSharedCombine) {
+    if (!q || !k_pool || !v_pool || !block_words || !q_pos || !rope_table) return LAZY_ERR_INVALID_ARG;
+    if (num_items > 0 && (!items || num_slots == 0)) return LAZY_ERR_INVALID_ARG;
+    if ((int64_t)num_items * p->num_kv_heads > INT32_MAX) return LAZY_ERR_UNSUPPORTED;
+    if (p->num_pool_blocks == 0 || p->max_blocks_per_seq == 0) return LAZY_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(rope_table) ||
+        (items && !aligned16(items)))
+      return LAZY_ERR_INVALID_ARG;
+  }
+  if (phase != kSharedPartials && (!slot_indptr || !out || !aligned16(out))) return LAZY_ERR_INVALID_ARG;
   const size_t need = lazy_attn_decode_shared_workspace_bytes(p, num_slots);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return LAZY_ERR_WORKSPACE;
   unsigned int* st = status_ptr();
@@ -544,6 +550,7 @@ static int decode_shared_impl(const lazy_attn_params* p, const void* q, const vo
   a.num_slots = num_slots;
   a.scale_log2 = scale_log2(p);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (phase == kSharedCombine) return launched(lazy::launch_shared_combine(a, cs));
   if (num_items > 0) {
     CUtensorMap kmap, vmap;
     const uint64_t rows = (uint64_t)p->num_pool_blocks * p->num_kv_heads * lazy::kBlock;
@@ -566,7 +573,24 @@ static int decode_shared_impl(const lazy_attn_params* p, const void* q, const vo
     }
     if (rc != LAZY_OK) return rc;
   }
+  if (phase == kSharedPartials) return LAZY_OK;
   return launched(lazy::launch_shared_combine(a, cs));
+}
+
+int lazy_attn_decode_shared_partials(const lazy_attn_params* p, const void* q, const void* k_pool,
+                                     const void* v_pool, const uint32_t* block_words, const int32_t* q_pos,
+                                     const void* rope_table, int32_t num_items, const int32_t* items,
+                                     int32_t num_slots, void* workspace, size_t workspace_bytes,
+                                     lazy_stream_t stream) {
+  return decode_shared_impl(p, q, k_pool, v_pool, block_words, q_pos, rope_table, num_items, items, num_slots,
+                            nullptr, nullptr, nullptr, workspace, workspace_bytes, stream, kSharedPartials);
+}
+
+int lazy_attn_decode_shared_combine(const lazy_attn_params* p, int32_t num_slots, const int32_t* slot_indptr,
+                                    const void* workspace, size_t workspace_bytes, void* out, lazy_stream_t stream) {
+  return decode_shared_impl(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr, num_slots,
+                            slot_indptr, nullptr, out, const_cast<void*>(workspace), workspace_bytes, stream,
+                            kSharedCombine);
 }
 
 int lazy_attn_decode_shared(const lazy_attn_params* p, const void* q, const void* k_pool, const void* v_pool,

@@ -20,7 +20,6 @@
 // group stay adjacent, so the CTAs that read the same blocks run at about the
 // same time.
 #include <algorithm>
-#include <map>
 #include <utility>
 #include <vector>
 
@@ -36,10 +35,13 @@ int plan_shared_host(int B, int G, int rows_cap, int max_blocks, int num_pool_bl
     int seq, b0;
   };
   const int kBlk = 16;
-  // ---- group the occurrences by (document, used length)
-  std::map<std::pair<int, int>, int> group_of;
+  // ---- group the occurrences by (document, used length): the groups of document d
+  // form a list from doc_head[d] (a document is rarely used at two lengths); each
+  // occurrence is tagged with its group, then the groups are laid out contiguously.
+  std::vector<int> doc_head(std::max(0, num_docs), -1), group_next;
   std::vector<std::pair<int, int>> keys;  // (doc, len)
-  std::vector<std::vector<Occ>> groups;
+  std::vector<int> occ_group;
+  std::vector<Occ> occ_all;
   for (int s = 0; s < B; ++s) {
     const int k0 = seg_indptr[s], k1 = seg_indptr[s + 1];
     if (k1 < k0) return LAZY_ERR_LAYOUT;
@@ -55,21 +57,30 @@ int plan_shared_host(int B, int G, int rows_cap, int max_blocks, int num_pool_bl
         const int phys = doc_blocks[doc_block_indptr[doc] + q];
         if (phys < 0 || phys >= num_pool_blocks) return LAZY_ERR_LAYOUT;
       }
-      const std::pair<int, int> key{doc, len};
-      auto f = group_of.find(key);
-      int gi;
-      if (f == group_of.end()) {
-        gi = (int)groups.size();
-        group_of.emplace(key, gi);
-        keys.push_back(key);
-        groups.emplace_back();
-      } else {
-        gi = f->second;
+      int gi = doc_head[doc];
+      while (gi >= 0 && keys[gi].second != len) gi = group_next[gi];
+      if (gi < 0) {
+        gi = (int)keys.size();
+        keys.emplace_back(doc, len);
+        group_next.push_back(doc_head[doc]);
+        doc_head[doc] = gi;
       }
-      groups[gi].push_back(Occ{s, (int)blk});
+      occ_group.push_back(gi);
+      occ_all.push_back(Occ{s, (int)blk});
       blk += nbk;
     }
   }
+  // Occurrences of group gi: occ[gstart[gi] .. gstart[gi + 1]), in input order.
+  const int ng = (int)keys.size();
+  std::vector<int> gstart(ng + 1, 0);
+  for (int g : occ_group) ++gstart[g + 1];
+  for (int g = 0; g < ng; ++g) gstart[g + 1] += gstart[g];
+  std::vector<Occ> occ(occ_all.size());
+  {
+    std::vector<int> fill(gstart.begin(), gstart.end() - 1);
+    for (size_t k = 0; k < occ_all.size(); ++k) occ[fill[occ_group[k]]++] = occ_all[k];
+  }
+  auto gsize = [&](int gi) { return gstart[gi + 1] - gstart[gi]; };
   // ---- member sets, their chunk length, and the slots each member needs
   const int per_set = std::max(1, std::min(LAZY_PLAN_MAX_MEMBERS, rows_cap / G));
   struct Set {
@@ -78,21 +89,21 @@ int plan_shared_host(int B, int G, int rows_cap, int max_blocks, int num_pool_bl
   int cb = chunk_blocks;
   if (cb <= 0) {  // about auto_items items: 32 .. 256 blocks, a multiple of 4 (one key tile)
     int64_t total = 0;
-    for (int gi = 0; gi < (int)groups.size(); ++gi)
-      total += (int64_t)((keys[gi].second + kBlk - 1) / kBlk) * ((groups[gi].size() + per_set - 1) / per_set);
+    for (int gi = 0; gi < ng; ++gi)
+      total += (int64_t)((keys[gi].second + kBlk - 1) / kBlk) * ((gsize(gi) + per_set - 1) / per_set);
     const int64_t per = (total + std::max(1, auto_items) - 1) / std::max(1, auto_items);
     cb = (int)std::min<int64_t>(256, std::max<int64_t>(32, (per + 3) / 4 * 4));
   }
   std::vector<Set> sets;
   std::vector<int> nslots(B, 0);
-  for (int gi = 0; gi < (int)groups.size(); ++gi) {
+  for (int gi = 0; gi < ng; ++gi) {
     const int nbk = (keys[gi].second + kBlk - 1) / kBlk;
-    for (int j0 = 0; j0 < (int)groups[gi].size(); j0 += per_set) {
-      const int n = std::min(per_set, (int)groups[gi].size() - j0);
+    for (int j0 = 0; j0 < gsize(gi); j0 += per_set) {
+      const int n = std::min(per_set, gsize(gi) - j0);
       const int rows = n * G;
       const int rt = rows <= 16 ? 1 : (rows <= 32 ? 2 : 4);
-      sets.push_back(Set{gi, j0, n, rt, cb});
-      for (int j = 0; j < n; ++j) nslots[groups[gi][j0 + j].seq] += (nbk + cb - 1) / cb;
+      sets.push_back(Set{gi, gstart[gi] + j0, n, rt, cb});
+      for (int j = 0; j < n; ++j) nslots[occ[gstart[gi] + j0 + j].seq] += (nbk + cb - 1) / cb;
     }
   }
   slot_indptr[0] = 0;
@@ -117,7 +128,6 @@ int plan_shared_host(int B, int G, int rows_cap, int max_blocks, int num_pool_bl
   std::vector<int> next(slot_indptr, slot_indptr + B);
   for (size_t i = 0; i < its.size(); ++i) {
     const Set& st = sets[its[i].set];
-    const std::vector<Occ>& occ = groups[st.group];
     int32_t* d = items + (size_t)LAZY_PLAN_ITEM_INTS * i;
     std::fill(d, d + LAZY_PLAN_ITEM_INTS, 0);
     d[0] = occ[st.first].seq;

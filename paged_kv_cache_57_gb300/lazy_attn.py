@@ -37,6 +37,7 @@ EXPORTED = (
     "lazy_attn_materialize", "lazy_attn_rope_table_init_scaled", "lazy_attn_rope_table_init_freqs",
     "lazy_attn_rotary_layout_host", "lazy_attn_decode_shared_alibi", "lazy_attn_alibi_slopes_host",
     "lazy_attn_decode_alibi", "lazy_attn_debug_gather_withheld", "lazy_attn_prefill_alibi",
+    "lazy_attn_decode_shared_partials", "lazy_attn_decode_shared_combine",
 )
 PLAN_MAX_MEMBERS = 16
 PLAN_ITEM_BLOCK_IDS = 32
@@ -91,6 +92,8 @@ _sig = {
     "lazy_attn_decode_shared_alibi": (ctypes.c_int,
                                       [_P] + [_vp] * 6 + [_i32, _vp, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "lazy_attn_alibi_slopes_host": (ctypes.c_int, [_i32, _vp]),
+    "lazy_attn_decode_shared_partials": (ctypes.c_int, [_P] + [_vp] * 6 + [_i32, _vp, _i32, _vp, _sz, _vp]),
+    "lazy_attn_decode_shared_combine": (ctypes.c_int, [_P, _i32, _vp, _vp, _sz, _vp, _vp]),
     "lazy_attn_decode_alibi": (ctypes.c_int, [_P] + [_vp] * 9 + [_vp, _sz, _vp]),
 }
 for _name, (_res, _args) in _sig.items():
@@ -308,18 +311,28 @@ class SharedPlan:
 
 
 def plan_shared_host(p: Params, num_docs: int, seg_indptr, seg_doc, seg_len, doc_block_indptr, doc_blocks,
-                     chunk_blocks: int = 0):
-    """Host planner of the shared-run decode. Returns (items [n, PLAN_ITEM_INTS], slot_indptr [B+1]), int32."""
+                     chunk_blocks: int = 0, out=None):
+    """Host planner of the shared-run decode. Returns (items [n, PLAN_ITEM_INTS], slot_indptr [B+1]), int32.
+
+    ``out`` = (items [capacity, PLAN_ITEM_INTS], slot_indptr [B+1], counts [2]) int32 arrays
+    (pinned host memory, for instance) that the planner fills in place; the call then
+    returns views of them and allocates nothing."""
     arrs = [_i32_np(x) if np.size(x) else np.zeros(1, np.int32)
             for x in (seg_indptr, seg_doc, seg_len, doc_block_indptr, doc_blocks)]
-    cap = int(np.sum((np.asarray(seg_len, dtype=np.int64) + BLOCK - 1) // BLOCK)) + 1
-    items = np.zeros((cap, PLAN_ITEM_INTS), np.int32)
-    slot_indptr = np.zeros(p.num_seqs + 1, np.int32)
-    counts = np.zeros(2, np.int32)
+    if out is None:
+        cap = int(np.sum((np.asarray(seg_len, dtype=np.int64) + BLOCK - 1) // BLOCK)) + 1
+        items = np.zeros((cap, PLAN_ITEM_INTS), np.int32)
+        slot_indptr = np.zeros(p.num_seqs + 1, np.int32)
+        counts = np.zeros(2, np.int32)
+    else:
+        items, slot_indptr, counts = out
+        cap = int(items.shape[0])
     rc = _lib.lazy_attn_plan_shared_host(ctypes.byref(p), int(num_docs), *[a.ctypes.data for a in arrs],
                                          int(chunk_blocks), cap, items.ctypes.data, slot_indptr.ctypes.data,
                                          counts.ctypes.data)
     _check(rc, "plan_shared_host")
+    if out is not None:
+        return items[: counts[0]], slot_indptr
     return items[: counts[0]].copy(), slot_indptr
 
 
@@ -353,6 +366,33 @@ def decode_shared(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torc
             raise ValueError("alibi_slopes needs one slope per query head")
         rc = _lib.lazy_attn_decode_shared_alibi(*args, _dptr(alibi_slopes, "alibi_slopes", torch.float32), *tail)
     _check(rc, "decode_shared")
+    return out
+
+
+def decode_shared_partials(p: Params, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                           block_words: torch.Tensor, q_pos: torch.Tensor, rope_table: torch.Tensor, plan: SharedPlan,
+                           workspace: torch.Tensor, stream=None) -> torch.Tensor:
+    """First pass of decode_shared: fp32 partials of every slot into ``workspace``."""
+    wsz = workspace.numel() * workspace.element_size()
+    i32 = torch.int32
+    rc = _lib.lazy_attn_decode_shared_partials(
+        ctypes.byref(p), _dptr(q, "q", _tdt(p)), _dptr(k_pool, "k_pool", _kvdt(p)), _dptr(v_pool, "v_pool", _kvdt(p)),
+        _dptr(block_words, "block_words"), _dptr(q_pos, "q_pos", i32), _dptr(rope_table, "rope_table"),
+        plan.num_items, _dptr(plan.items, "items", i32), plan.num_slots, _dptr(workspace, "workspace"), wsz,
+        _stream(stream))
+    _check(rc, "decode_shared_partials")
+    return workspace
+
+
+def decode_shared_combine(p: Params, plan: SharedPlan, workspace: torch.Tensor, out: torch.Tensor,
+                          stream=None) -> torch.Tensor:
+    """Second pass of decode_shared: each sequence's slots merged into ``out``."""
+    wsz = workspace.numel() * workspace.element_size()
+    rc = _lib.lazy_attn_decode_shared_combine(ctypes.byref(p), plan.num_slots,
+                                              _dptr(plan.slot_indptr, "slot_indptr", torch.int32),
+                                              _dptr(workspace, "workspace"), wsz, _dptr(out, "out", _tdt(p)),
+                                              _stream(stream))
+    _check(rc, "decode_shared_combine")
     return out
 
 

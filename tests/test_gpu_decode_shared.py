@@ -197,3 +197,32 @@ def test_mixed_shared_decode_full_sampled():
     d, _ = W.mixed_mqa()
     rng = np.random.default_rng(5)
     _check(d, rows=sorted(rng.choice(d.num_seqs, 6, replace=False).tolist()))
+
+
+@pytest.mark.parametrize("hq,hkv", EDGE_SHAPES)
+def test_split_phase_calls_equal_the_fused_call(hq, hkv):
+    # lazy_attn_decode_shared_partials then lazy_attn_decode_shared_combine run the same
+    # two kernels as lazy_attn_decode_shared: bit-identical outputs, and the partials
+    # left in the workspace merge (here in fp64 on the host) to the oracle's result.
+    L = la()
+    w = W.decode_zipf("ssplit", batch=6, hq=hq, hkv=hkv, d=128, docs_per_seq=4, doc_tokens=120, pool_docs=3,
+                      zipf_s=1.0, suffix_tokens=13, seed=175)
+    dv = to_device(w)
+    plan = shared_plan(dv)
+    fused = decode_shared(dv, plan)
+    ws = torch.empty(L.decode_shared_workspace_bytes(dv.p, plan.num_slots), dtype=torch.uint8, device="cuda")
+    L.decode_shared_partials(dv.p, dv.q, dv.k_pool, dv.v_pool, dv.words, dv.q_pos, dv.rope, plan, ws)
+    out = L.decode_shared_combine(dv.p, plan, ws, torch.empty_like(dv.q))
+    assert torch.equal(out.view(torch.int16), fused.view(torch.int16))
+    S, Hq, D = plan.num_slots, w.num_q_heads, w.head_dim
+    f = ws.view(torch.float32).cpu().double().numpy()
+    o, ml = f[: S * Hq * D].reshape(S, Hq, D), f[S * Hq * D: S * Hq * (D + 2)].reshape(S, Hq, 2)
+    si = plan.slot_indptr_host
+    merged = np.zeros((w.num_seqs, Hq, D))
+    for s in range(w.num_seqs):
+        m = ml[si[s]:si[s + 1], :, 0]
+        M = m.max(0)
+        wgt = np.exp2(m - M)
+        merged[s] = (wgt[..., None] * o[si[s]:si[s + 1]]).sum(0) / (wgt * ml[si[s]:si[s + 1], :, 1]).sum(0)[:, None]
+    assert_close(torch.from_numpy(merged), oracle.attention(w), "bf16", "partials merged on the host",
+                 emulate=lambda r: emulate(w, r))
