@@ -261,7 +261,6 @@ def oracle_sample_rate(w, budget_s=10.0, seqs_per_call=2):
     """Runs the oracle over consecutive sequences of ``w`` until ``budget_s`` has elapsed;
     returns (logical KV GB/s, seconds, sequences, threads)."""
     import oracle
-    from paged_kv_cache_57_gb300 import workloads as W
     oracle.build()
     elt = 2 if w.dtype == "bf16" else 4
     toks = w.tokens_per_seq()
@@ -277,8 +276,90 @@ def oracle_sample_rate(w, budget_s=10.0, seqs_per_call=2):
             return nbytes / el / 1e9, el, done, oracle.num_threads()
 
 
+def _prefill_row_flops(w):
+    """Algorithmic FLOPs of each query row of a prefill workload: 4 d Hq x visible keys."""
+    toks = w.tokens_per_seq()
+    cu = np.asarray(w.cu_seqlens_q)
+    keys = np.concatenate([toks[s] - (cu[s + 1] - cu[s]) + np.arange(1, cu[s + 1] - cu[s] + 1)
+                           for s in range(w.num_seqs)])
+    return 4.0 * w.head_dim * w.num_q_heads * keys
+
+
+def cpu_baseline_table(budget_s=1.0, workloads=None):
+    """The oracle as it stands (fp64, materialised position-adjusted K, one-shot
+    softmax) on the host cores, with every thread and with one, on each workload the
+    GPU legs run. A cell runs consecutive units (sequences, or prefill query rows)
+    until ``budget_s`` has passed (at least one call) and reports the rate in the
+    workload's unit; the mixed batch's prefill chunks are sampled at 64 rows per chunk
+    and their step time extrapolated from that rate."""
+    import oracle
+    from paged_kv_cache_57_gb300 import workloads as W
+    oracle.build()
+    all_threads = oracle.num_threads()
+    wl = dict(workloads or {})  # workloads the GPU legs already built, reused
+    if "mixed_mqa_decode" not in wl or "mixed_mqa_prefill" not in wl:
+        wl["mixed_mqa_decode"], wl["mixed_mqa_prefill"] = W.mixed_mqa()
+    for name in ("llama8b_decode", "llama8b_prefill", "llama70b_decode"):
+        if name not in wl:
+            wl[name] = W.FULL[name]()
+    loads = [("tiny_fp32", W.tiny_fp32())] + [(n, wl[n]) for n in ("llama8b_decode", "llama8b_prefill",
+                                                                   "llama70b_decode", "mixed_mqa_decode",
+                                                                   "mixed_mqa_prefill")]
+    out = []
+    try:
+        for name, w in loads:
+            for threads in (all_threads, 1):
+                oracle.set_num_threads(threads)
+                t0 = time.perf_counter()
+                if w.kind == "decode":
+                    elt = 2 if w.dtype == "bf16" else 4
+                    toks = w.tokens_per_seq()
+                    done, nbytes = 0, 0
+                    while True:
+                        r = done % w.num_seqs
+                        oracle.attention(w, rows=[r])
+                        nbytes += int(toks[r]) * w.num_kv_heads * w.head_dim * 2 * elt
+                        done += 1
+                        if time.perf_counter() - t0 >= budget_s:
+                            break
+                    el = time.perf_counter() - t0
+                    rate = nbytes / el / 1e9
+                    step_bytes = float(W.kv_bytes_logical(w))
+                    out.append({"workload": name, "threads": threads, "value": rate, "unit": "GB/s",
+                                "sample": f"{done} sequences, {el:.2f} s", "step_s": step_bytes / 1e9 / rate})
+                else:
+                    fl = _prefill_row_flops(w)
+                    cu = np.asarray(w.cu_seqlens_q)
+                    if name == "mixed_mqa_prefill":  # 64 rows spread over each chunk
+                        rows = np.concatenate([cu[s] + np.linspace(0, cu[s + 1] - cu[s] - 1, 64).astype(np.int64)
+                                               for s in range(w.num_seqs)])
+                    else:
+                        rows = np.arange(int(cu[-1]))
+                    done, flop = 0, 0.0
+                    while True:
+                        take = rows[done: done + 8]
+                        if len(take) == 0:
+                            break
+                        oracle.attention(w, rows=take.tolist())
+                        flop += float(fl[take].sum())
+                        done += len(take)
+                        if time.perf_counter() - t0 >= budget_s:
+                            break
+                    el = time.perf_counter() - t0
+                    rate = flop / el / 1e9
+                    cell = {"workload": name, "threads": threads, "value": rate, "unit": "GFLOP/s",
+                            "sample": f"{done} query rows, {el:.2f} s", "step_s": float(fl.sum()) / 1e9 / rate}
+                    if name == "mixed_mqa_prefill":
+                        cell["step_s_extrapolated"] = True
+                    out.append(cell)
+    finally:
+        oracle.set_num_threads(all_threads)
+    return out
+
+
 def reference_arm(args):
-    """The oracle timed on the host cores, as the reference arm."""
+    """The oracle timed on the host cores, as the reference arm: each step is the
+    whole headline batch (64 sequences x 32 query heads), as the GPU arm's step."""
     import oracle
     from paged_kv_cache_57_gb300 import workloads as W
     rank = int(os.environ.get("RANK", "0"))
@@ -288,27 +369,25 @@ def reference_arm(args):
     oracle.build()
     elt = 2
     toks = w.tokens_per_seq()
-    per_step = 2  # sequences per step (all heads)
-    times, nbytes = [], 0
+    step_bytes = int(toks.sum()) * w.num_kv_heads * w.head_dim * 2 * elt
+    times = []
     for i in range(args.warmup + args.steps):
-        rows = [(2 * i + j) % w.num_seqs for j in range(per_step)]
         t0 = time.perf_counter()
-        oracle.attention(w, rows=rows)
+        oracle.attention(w)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
-            nbytes += int(sum(toks[r] for r in rows)) * w.num_kv_heads * w.head_dim * 2 * elt
     total = sum(times)
-    value = nbytes / total / 1e9
+    value = step_bytes * len(times) / total / 1e9
     cores = oracle.num_threads()
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "batch": w.num_seqs, "context": int(toks[0]),
                        "heads": [w.num_q_heads, w.num_kv_heads], "head_dim": w.head_dim,
-                       "step": f"{per_step} sequences x all heads (bounded sample)"},
+                       "step": "the whole batch, all heads (the GPU arm's step)"},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                             "sample": f"{per_step} sequences per step, {args.steps} steps"},
+                             "sample": f"{args.steps} steps of {w.num_seqs} sequences"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -389,12 +468,17 @@ def main():
     t_max = max_over_ranks(t_dev, dist if world > 1 else None, device="cuda")
     ms = 1e3 * t_max / args.steps
     value = whole_job_rate(nbytes["kv_logical"], world, args.steps, t_max)
-    avg = t_dev / args.steps
-    achieved = nbytes["unique"] / avg / 1e9
+    call_avg = t_dev / args.steps
 
-    extras = {}
+    # The dominant kernel alone: the same decode as its two calls (work-item kernel,
+    # then combine), with CUDA events on the launching stream around the first.
+    kern = time_split_phase(d, min(max(20, args.steps), 300), 3, flush)
+    k_avg = statistics.mean(kern["partials"])
+    achieved = nbytes["unique"] / k_avg / 1e9
+
+    extras, keep = {}, {}
     if not args.no_extras and rank == 0:
-        extras = measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust)
+        extras, keep = measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust)
     e2e = measure_e2e(args, d, w, nbytes) if rank == 0 else None
 
     if world > 1:
@@ -402,6 +486,7 @@ def main():
     if rank != 0:
         dist.destroy_process_group()
         return 0
+    lz = extras.get("lazy_overhead_pct", {})
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -411,26 +496,73 @@ def main():
                    "docs": "8 x 512 Zipf(1.0) of 256 + 64 private", "l2": L2_NOTE,
                    "decode_path": "shared-run (lazy_attn_decode_shared)",
                    "parallelism": f"weak x{world} (independent batches)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": _traffic_if_current(), "peak_source": peak_src,
+                     "kernel": "decode_shared_kernel<128, lazy> alone: mean of CUDA-event durations around "
+                               "lazy_attn_decode_shared_partials; bytes = unique K/V blocks + q + out + words",
+                     "kernel_ms": 1e3 * k_avg, "bytes_per_launch": nbytes["unique"],
+                     "call_ms": 1e3 * call_avg, "call_achieved": nbytes["unique"] / call_avg / 1e9,
+                     "call_frac": nbytes["unique"] / call_avg / 1e9 / hbm,
+                     "lazy_overhead_pct": lz.get("decode"),
+                     "lazy_overhead_pct_per_sequence_path": lz.get("decode_per_sequence_path")},
         "decode": {"tokens_per_s": world * w.num_seqs / (t_max / args.steps),
                    "kv_gbs_logical": value, "kv_gbs_unique": world * nbytes["unique"] * args.steps / t_max / 1e9,
                    "bytes_logical": nbytes["logical"], "bytes_unique": nbytes["unique"],
-                   "hbm_frac_unique_of_measured": achieved / hbm, "hbm_frac_unique_of_8tbs": achieved / 8000.0,
-                   "ms_median": 1e3 * statistics.median(per_step)},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": _traffic_if_current(), "peak_source": peak_src,
-                     "kernel": "shared-run decode call (decode_shared_kernel + combine); bytes = unique K/V "
-                               "blocks + q + out + words"},
+                   "hbm_frac_unique_of_measured": nbytes["unique"] / call_avg / 1e9 / hbm,
+                   "hbm_frac_unique_of_8tbs": nbytes["unique"] / call_avg / 1e9 / 8000.0,
+                   "ms_median": 1e3 * statistics.median(per_step),
+                   "combine_ms": 1e3 * statistics.mean(kern["combine"])},
         "gpu_launches": launches, "wall_s_timed": t_wall, "clocks": clk, "e2e": e2e,
     }
     line.update(extras)
     if not args.no_cpu_baseline:
-        v, el, nseq, cores = oracle_sample_rate(w, budget_s=10.0)
-        line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                "sample": f"{nseq} sequences of the same workload (all heads), {el:.1f} s"}
+        table = cpu_baseline_table(budget_s=0.7, workloads=keep.get("workloads"))
+        head = next(c for c in table if c["workload"] == WORKLOAD and c["threads"] > 1)
+        line["cpu_baseline"] = {"value": head["value"], "unit": "GB/s", "cores": head["threads"], "kind": "oracle",
+                                "sample": f"{WORKLOAD}: {head['sample']}; table: every workload, all threads "
+                                          f"and 1", "table": table}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def time_split_phase(d, steps, warmup, flush):
+    """The shared-run decode as its two calls, lazy_attn_decode_shared_partials and
+    lazy_attn_decode_shared_combine, with CUDA events on the launching stream before,
+    between and after them; L2 flushed before each step. Returns per-step seconds of
+    each call. The host issues more per step here (two calls, three events) than in
+    the one-call loop; a short device-side wait after each flush keeps the launches
+    ahead of the device, so that no event interval includes the device waiting for
+    the host."""
+    import torch
+    from paged_kv_cache_57_gb300 import lazy_attn as L
+    st = torch.cuda.current_stream()
+    p, plan = d["p"], d["plan"]
+    p.lazy = 1
+
+    def run():
+        L.decode_shared_partials(p, d["q"], d["k"], d["v"], d["words"], d["q_pos"], d["rope"], plan, d["ws_sh"])
+
+    for _ in range(warmup):
+        flush()
+        run()
+        L.decode_shared_combine(p, plan, d["ws_sh"], d["out"])
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    spin = getattr(torch.cuda, "_sleep", None)
+    for a, b, c in evs:
+        flush()
+        if spin is not None:
+            spin(100000)  # about 50 us of device time, before the first event
+        a.record(st)
+        run()
+        b.record(st)
+        L.decode_shared_combine(p, plan, d["ws_sh"], d["out"])
+        c.record(st)
+    torch.cuda.synchronize()
+    return {"partials": [a.elapsed_time(b) * 1e-3 for a, b, _ in evs],
+            "combine": [b.elapsed_time(c) * 1e-3 for _, b, c in evs]}
 
 
 def single_workload(args):
@@ -476,50 +608,96 @@ def single_workload(args):
 
 
 def measure_e2e(args, d, w, nbytes):
-    """Same decode through the public API (shared-run path) with the step's inputs copied
-    from pinned host memory (q, block words, q positions, the plan's items and slot
-    offsets) and the output read back, per step. The inputs sit in one pinned staging
-    buffer and go up in one copy, as a serving loop that packs a step's metadata would
-    send them. The KV pool is the resident cache (it persists across steps), not a
-    per-step input."""
+    """The decode end to end through the public API, as a serving step whose batch
+    composition may change every step. Timed on the host clock, per step: the host
+    planner (lazy_attn_plan_shared_host) and the host packer
+    (lazy_attn_pack_block_words_host) write the plan and the block words into one
+    pinned staging buffer that also holds q and the query positions; one host-to-device
+    copy; lazy_attn_decode_shared; the output read back; a stream synchronisation.
+    The KV pool is the resident cache (it persists across steps), not a per-step
+    input. Beside it: the host planner and packer times alone, and the same step with
+    the plan and words kept from the previous step (device time between CUDA events)."""
     import torch
     from paged_kv_cache_57_gb300 import lazy_attn as L
     steps = max(3, min(args.steps, 50))
-    plan = d["plan"]
-    parts = [d["q"], d["words"], d["q_pos"], plan.items, plan.slot_indptr]
-    offs, total = [], 0
-    for x in parts:  # 256-byte aligned slices of one buffer
-        offs.append(total)
-        total += (x.numel() * x.element_size() + 255) // 256 * 256
+    p, plan = d["p"], d["plan"]
+    cap = int(plan.num_items) + 64  # item capacity of the staging buffer
+    B = w.num_seqs
+    shapes = [("q", d["q"].shape, torch.bfloat16), ("words", (B, p.max_blocks_per_seq), torch.int32),
+              ("q_pos", (B,), torch.int32), ("items", (cap, L.PLAN_ITEM_INTS), torch.int32),
+              ("slot_indptr", (B + 1,), torch.int32)]
+    offs, total = {}, 0
+    for name, shp, dt in shapes:  # 256-byte aligned slices of one buffer
+        offs[name] = total
+        total += (int(np.prod(shp)) * torch.empty((), dtype=dt).element_size() + 255) // 256 * 256
     hbuf = torch.empty(total, dtype=torch.uint8).pin_memory()
     dbuf = torch.empty(total, dtype=torch.uint8, device="cuda")
-    def view(buf, i):
-        x = parts[i]
-        n = x.numel() * x.element_size()
-        return buf[offs[i]: offs[i] + n].view(x.dtype).view(x.shape)
-    for i, x in enumerate(parts):
-        view(hbuf, i).copy_(x.cpu())
-    q, words, qp, items, slot_indptr = (view(dbuf, i) for i in range(len(parts)))
+
+    def view(buf, name):
+        _, shp, dt = next(x for x in shapes if x[0] == name)
+        n = int(np.prod(shp)) * torch.empty((), dtype=dt).element_size()
+        return buf[offs[name]: offs[name] + n].view(dt).view(shp)
+    view(hbuf, "q").copy_(d["q"].cpu())
+    view(hbuf, "q_pos").copy_(d["q_pos"].cpu())
+    h_items, h_si = view(hbuf, "items").numpy(), view(hbuf, "slot_indptr").numpy()
+    h_words = view(hbuf, "words").numpy().view(np.uint32)
+    h_lens = np.zeros(B, np.int32)
+    counts = np.zeros(2, np.int32)
+    q, words, qp, items, slot_indptr = (view(dbuf, n) for n in ("q", "words", "q_pos", "items", "slot_indptr"))
     dplan = L.SharedPlan.__new__(L.SharedPlan)
     dplan.__dict__.update(plan.__dict__)
     dplan.items, dplan.slot_indptr = items, slot_indptr
     hout = torch.empty_like(d["out"], device="cpu").pin_memory()
     st = torch.cuda.current_stream()
-    times = []
+    plan_args = (p, len(w.doc_len), w.seg_indptr, w.seg_doc, w.seg_len, w.doc_block_indptr, w.doc_blocks)
+
+    def plan_and_pack():
+        L.plan_shared_host(*plan_args, out=(h_items, h_si, counts))
+        L.pack_block_words_host(p, len(w.doc_len), w.seg_indptr, w.seg_doc, w.seg_len, w.seq_pos0,
+                                w.doc_block_indptr, w.doc_blocks, out=(h_words, h_lens))
+        dplan.num_items, dplan.num_slots = int(counts[0]), int(counts[1])
+
+    def step():
+        dbuf.copy_(hbuf, non_blocking=True)
+        L.decode_shared(p, q, d["k"], d["v"], words, qp, d["rope"], dplan, out=d["out"], workspace=d["ws_sh"])
+        hout.copy_(d["out"], non_blocking=True)
+
+    times, t_plan, t_pack = [], [], []
     for i in range(steps + 3):
+        t0 = time.perf_counter()
+        plan_and_pack()
+        step()
+        st.synchronize()
+        if i >= 3:
+            times.append(time.perf_counter() - t0)
+    assert int(counts[0]) == plan.num_items and np.array_equal(h_items[: plan.num_items], plan.items_host)
+    for _ in range(20):  # the host calls alone
+        t0 = time.perf_counter()
+        L.plan_shared_host(*plan_args, out=(h_items, h_si, counts))
+        t1 = time.perf_counter()
+        L.pack_block_words_host(p, len(w.doc_len), w.seg_indptr, w.seg_doc, w.seg_len, w.seq_pos0,
+                                w.doc_block_indptr, w.doc_blocks, out=(h_words, h_lens))
+        t_plan.append(t1 - t0)
+        t_pack.append(time.perf_counter() - t1)
+    static = []
+    for i in range(steps + 3):  # plan and words kept: device time of copies + decode
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(st)
-        dbuf.copy_(hbuf, non_blocking=True)
-        L.decode_shared(d["p"], q, d["k"], d["v"], words, qp, d["rope"], dplan, out=d["out"], workspace=d["ws_sh"])
-        hout.copy_(d["out"], non_blocking=True)
+        step()
         b.record(st)
         b.synchronize()
         if i >= 3:
-            times.append(a.elapsed_time(b) * 1e-3)
-    h2d = sum(x.numel() * x.element_size() for x in parts)
+            static.append(a.elapsed_time(b) * 1e-3)
+    h2d = total
     d2h = hout.numel() * hout.element_size()
-    return {"value": nbytes["kv_logical"] / statistics.mean(times) / 1e9, "unit": "GB/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * statistics.mean(times)}
+    mean = statistics.mean(times)
+    return {"value": nbytes["kv_logical"] / mean / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * mean,
+            "includes": "host planner + host packer into pinned staging, one H2D copy, decode, D2H of the output, "
+                        "stream sync (host clock)",
+            "plan_ms": 1e3 * statistics.median(t_plan), "pack_ms": 1e3 * statistics.median(t_pack),
+            "plan_kept": {"value": nbytes["kv_logical"] / statistics.mean(static) / 1e9,
+                          "ms_per_step": 1e3 * statistics.mean(static)}}
 
 
 def measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust):
@@ -527,6 +705,7 @@ def measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust):
     from paged_kv_cache_57_gb300 import lazy_attn as L
     from paged_kv_cache_57_gb300 import workloads as W
     out = {}
+    keep = {"workloads": {"llama8b_decode": w}}  # workloads built here, reused by the CPU legs
     n = max(20, min(args.steps, 200))
     nb8 = decode_bytes(w)
 
@@ -608,8 +787,8 @@ def measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust):
         ctl.update({key + "gbs": gbs, key + "frac_of_measured": gbs / hbm, key + "frac_of_8tbs": gbs / 8000.0,
                     key + "ms_median": 1e3 * tc})
     out["noshare_control"] = ctl
-    # FP8 KV (e4m3 codes, per-tensor scales) on the per-sequence decode, the headline
-    # and the no-sharing workloads, against the bf16 pools on the same path.
+    # FP8 KV (e4m3 codes, per-tensor scales) on both decode paths, the headline and
+    # the no-sharing workloads, against the bf16 pools on the same path.
     fp8 = {}
     for tag, ww, dd in (("llama8b_decode", w, d), ("llama8b_decode_noshare", wc, dc)):
         k8, v8, ks, vs = W.fp8_pools(ww)
@@ -618,14 +797,28 @@ def measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust):
                            head_dim=ww.head_dim, num_pool_blocks=ww.num_pool_blocks,
                            max_blocks_per_seq=dd["p"].max_blocks_per_seq, dtype=ww.dtype, rope_theta=ww.rope_theta,
                            kv_dtype="fp8_e4m3", k_scale=ks, v_scale=vs)
-        t8 = statistics.median(time_steps(lambda: L.decode(p8, dd["q"], k8, v8, dd["words"], dd["seq_lens"],
-                                                           dd["q_pos"], dd["rope"], out=dd["out"], workspace=dd["ws"]),
-                                          n, 3, flush))
-        t16 = statistics.median(time_steps(lambda: run_decode(dd, path="seq"), n, 3, flush))
+        items8, si8 = L.plan_shared_host(p8, len(ww.doc_len), ww.seg_indptr, ww.seg_doc, ww.seg_len,
+                                         ww.doc_block_indptr, ww.doc_blocks)
+        plan8 = L.SharedPlan(items8, si8)
+        ws8 = torch.empty(max(1, L.decode_shared_workspace_bytes(p8, plan8.num_slots)), dtype=torch.uint8,
+                          device="cuda")
         ub = decode_bytes(ww)["unique"]
-        fp8[tag] = {"fp8_ms": 1e3 * t8, "bf16_ms": 1e3 * t16, "fp8_unique_gbs": ub / 2 / t8 / 1e9,
-                    "fp8_frac_of_measured": ub / 2 / t8 / 1e9 / hbm, "kv_bytes_ratio": 0.5}
-        del k8, v8
+        row = {"kv_bytes_ratio": 0.5}
+        for path in ("shared", "seq"):
+            if path == "shared":
+                f8 = lambda: L.decode_shared(p8, dd["q"], k8, v8, dd["words"], dd["q_pos"], dd["rope"], plan8,
+                                             out=dd["out"], workspace=ws8)
+            else:
+                f8 = lambda: L.decode(p8, dd["q"], k8, v8, dd["words"], dd["seq_lens"], dd["q_pos"], dd["rope"],
+                                      out=dd["out"], workspace=dd["ws"])
+            t8 = statistics.median(time_steps(f8, n, 3, flush))
+            t16 = statistics.median(time_steps(lambda: run_decode(dd, path=path), n, 3, flush))
+            key = "shared_" if path == "shared" else "per_sequence_"
+            row.update({key + "fp8_ms": 1e3 * t8, key + "bf16_ms": 1e3 * t16,
+                        key + "fp8_unique_gbs": ub / 2 / t8 / 1e9,
+                        key + "fp8_frac_of_measured": ub / 2 / t8 / 1e9 / hbm})
+        fp8[tag] = row
+        del k8, v8, ws8
     out["fp8_kv_decode"] = fp8
     del dc
     # Prefill (Llama-3.1-8B-shaped, 8 x (6 x 1024 docs + 256-token chunk)).
@@ -637,11 +830,29 @@ def measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust):
         tp0 = time_steps(lambda: run_prefill(dp, lazy=False), n, 3, flush)
         tfl = fl / statistics.median(tp) / 1e12
         out["prefill"] = {"workload": "llama8b_prefill", "tflops": tfl, "frac_of_burst": tfl / tf_burst,
-                          "frac_of_sustained": tfl / tf_sust, "gflop_per_step": fl / 1e9,
+                          "frac_of_sustained_context": tfl / tf_sust, "gflop_per_step": fl / 1e9,
                           "ms_median": 1e3 * statistics.median(tp),
-                          "lazy_overhead_pct": 100.0 * (statistics.median(tp) / statistics.median(tp0) - 1.0)}
+                          "lazy_overhead_pct": 100.0 * (statistics.median(tp) / statistics.median(tp0) - 1.0),
+                          "prerotated_control_ms": 1e3 * statistics.median(tp0)}
+        # ALiBi on the same shapes: key-position words, a zero-rate table, the usual slopes.
+        pa = L.make_params(num_seqs=wp.num_seqs, num_q_heads=wp.num_q_heads, num_kv_heads=wp.num_kv_heads,
+                           head_dim=wp.head_dim, num_pool_blocks=wp.num_pool_blocks,
+                           max_blocks_per_seq=dp["p"].max_blocks_per_seq, dtype=wp.dtype, rope_theta=wp.rope_theta,
+                           key_positions=True)
+        c = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+        wa, sla = L.pack_block_words(pa, len(wp.doc_len), c(wp.seg_indptr), c(wp.seg_doc), c(wp.seg_len),
+                                     c(wp.seq_pos0), c(wp.doc_block_indptr), c(wp.doc_blocks))
+        ra = L.rope_table_init(pa, freqs=np.zeros(wp.head_dim // 2))
+        sl = torch.from_numpy(L.alibi_slopes(wp.num_q_heads)).cuda()
+        ta = statistics.median(time_steps(lambda: L.prefill(
+            pa, dp["q"], dp["cu"], dp["q_start"], dp["max_q"], dp["k"], dp["v"], wa, sla, ra, out=dp["out"],
+            workspace=dp["ws_pf"], alibi_slopes=sl), n, 3, flush))
+        out["prefill"].update({"alibi_ms": 1e3 * ta, "alibi_tflops": fl / ta / 1e12,
+                               "alibi_vs_rope_pct": 100.0 * (ta / statistics.median(tp) - 1.0)})
+        del wa, sla, ra, sl
     except L.LazyAttnError as e:
         out["prefill"] = {"unavailable": str(e)}
+    keep["workloads"]["llama8b_prefill"] = wp
     del dp
     # Llama-3.1-70B-shaped decode: 32 x 16 x 1024 Zipf(1.0) of 512, pool capped at 1 GiB.
     w4 = W.FULL["llama70b_decode"]()
@@ -649,6 +860,7 @@ def measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust):
     b4 = decode_bytes(w4)
     s41, s40 = ab(d4, "shared")
     q41, _ = ab(d4, "seq")
+    keep["workloads"]["llama70b_decode"] = w4
     out["llama70b_decode"] = {"kv_gbs_logical": b4["kv_logical"] / s41 / 1e9,
                               "kv_gbs_unique": b4["unique"] / s41 / 1e9,
                               "hbm_frac_unique_of_measured": b4["unique"] / s41 / 1e9 / hbm,
@@ -659,6 +871,7 @@ def measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust):
     # Mixed continuous batch, MQA 32/1: 48 decode sequences + 4 prefill chunks of 512, one
     # shared pool, both calls on one stream and timed as one step.
     wd, wp = W.mixed_mqa()
+    keep["workloads"]["mixed_mqa_decode"], keep["workloads"]["mixed_mqa_prefill"] = wd, wp
     dd = build_device(wd)
     dp5 = build_device(wp, k_pool=None)
     dp5["k"], dp5["v"] = dd["k"], dd["v"]  # the two halves index the same physical pool
@@ -689,7 +902,7 @@ def measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust):
             cp[f"zipf{s}_{tag}"] = {p: round(CM.simulate(p, budget, reqs, pos0, concurrency=4)["hit_rate"], 4)
                                     for p in ("agnostic", "aware", "prefix")}
     out["cache_policies"] = cp
-    return out
+    return out, keep
 
 
 if __name__ == "__main__":

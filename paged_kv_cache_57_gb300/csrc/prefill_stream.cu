@@ -438,18 +438,27 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t wcur = cbase + lane < un.nb ? __ldg(&wrow[cbase + lane]) : 0u;
       uint32_t wnext = cbase + 32 + lane < un.nb ? __ldg(&wrow[cbase + 32 + lane]) : 0u;
       for (int j = j0; j < j1; ++j, ++g) {
-        if (j * BLOCKS >= cbase + 32) {  // warp-uniform: the tile starts in the next chunk
-          cbase += 32;
-          wcur = wnext;
-          wnext = cbase + 32 + lane < un.nb ? __ldg(&wrow[cbase + 32 + lane]) : 0u;
+        // ALiBi walks a unit's tiles from the last (the keys nearest the queries, with
+        // the largest bias) to the first, so that the running maximum is met early and
+        // later tiles seldom raise it (each raise rescales the running output).
+        const int jt = ALIBI ? j0 + j1 - 1 - j : j;
+        uint32_t w;
+        const int b = jt * BLOCKS + min(lane, BLOCKS);
+        if constexpr (ALIBI) {
+          w = (lane <= BLOCKS && b < un.nb) ? __ldg(&wrow[b]) : 0u;
+        } else {
+          if (j * BLOCKS >= cbase + 32) {  // warp-uniform: the tile starts in the next chunk
+            cbase += 32;
+            wcur = wnext;
+            wnext = cbase + 32 + lane < un.nb ? __ldg(&wrow[cbase + 32 + lane]) : 0u;
+          }
+          // Lanes 0..BLOCKS-1 describe the tile's blocks; lane BLOCKS takes the next block's
+          // word so that the tile's last block knows where the following one starts.
+          const int rel = b - cbase;  // 0 .. 40
+          const uint32_t w0 = __shfl_sync(0xffffffffu, wcur, rel & 31);
+          const uint32_t w1 = __shfl_sync(0xffffffffu, wnext, rel & 31);
+          w = (lane <= BLOCKS && b < un.nb) ? (rel < 32 ? w0 : w1) : 0u;
         }
-        // Lanes 0..BLOCKS-1 describe the tile's blocks; lane BLOCKS takes the next block's
-        // word so that the tile's last block knows where the following one starts.
-        const int b = j * BLOCKS + min(lane, BLOCKS);
-        const int rel = b - cbase;  // 0 .. 40
-        const uint32_t w0 = __shfl_sync(0xffffffffu, wcur, rel & 31);
-        const uint32_t w1 = __shfl_sync(0xffffffffu, wnext, rel & 31);
-        const uint32_t w = (lane <= BLOCKS && b < un.nb) ? (rel < 32 ? w0 : w1) : 0u;
         const BlockInfo bi = decode_word(w, b, a.id_bits);
         const int p_after = __shfl_down_sync(0xffffffffu, bi.p, 1);
         int y = -kBlock, nv = 0;  // rows of an invalid block start at -16: read as zeros
@@ -809,21 +818,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         // Per-block key limits for this row (holes; causal inside the chunk).
         int lim[BLOCKS];
-        float bias0[ALIBI ? BLOCKS : 1];  // ALiBi: slope (n0 - m_i) of each block's first key
         bool full_tile = true;
 #pragma unroll
         for (int bl = 0; bl < BLOCKS; ++bl) {
           const VMeta m = vmeta[vs * BLOCKS + bl];
           full_tile &= (m.nvalid == kBlock) & (m.chunk_j0 < 0);
           lim[bl] = m.chunk_j0 >= 0 ? max(0, min(m.nvalid, iq - m.chunk_j0 + 1)) : m.nvalid;
-          if constexpr (ALIBI) bias0[bl] = slope2 * (float)(m.pos - m_row);
         }
-        // Scores of chunk q (32 keys: blocks 2q, 2q + 1) plus the ALiBi bias.
-        auto add_bias = [&](float (&sv)[32], int q) {
-          if constexpr (ALIBI) {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) sv[k] = fmaf(slope2, (float)(k & 15), sv[k] + bias0[2 * q + (k >> 4)]);
-          }
+        // ALiBi bias of key k (0..31) of chunk q (blocks 2q, 2q + 1): slope (n - m_i) =
+        // b0 + slope (k & 15), with b0 = slope (n0 - m_i) of the key's block.
+        auto bias0 = [&](int q, int h2) {
+          return slope2 * (float)(vmeta[vs * BLOCKS + 2 * q + h2].pos - m_row);
         };
         // Pass 1: row maximum.
         float mx = -INFINITY;
@@ -832,7 +837,28 @@ __global__ void __launch_bounds__(THREADS, 1)
           float sv[32];
           tmem_ld32(tS + lane_base + 32 * q, sv);
           tmem_ld_wait(sv);
-          add_bias(sv, q);
+          if constexpr (ALIBI) {
+            // An upper bound of the biased maximum: each block's largest score plus the
+            // largest bias in the block, b0 + max(0, 15 slope). It exceeds the exact
+            // maximum by at most 15 |slope| (log2 units), so the second pass's weights
+            // shrink by at most that factor, far inside fp32 and bf16 range; the
+            // softmax itself is unchanged.
+            const float kmax = fmaxf(0.f, 15.f * slope2);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              float mb = -INFINITY;
+              if (full_tile) {
+#pragma unroll
+                for (int k = 0; k < 16; k += 2) mb = fmax3(mb, sv[16 * h2 + k], sv[16 * h2 + k + 1]);
+              } else {
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                  if (k < lim[2 * q + h2]) mb = fmaxf(mb, sv[16 * h2 + k]);
+              }
+              mx = fmaxf(mx, mb + (bias0(q, h2) + kmax));
+            }
+            continue;
+          }
           if (full_tile) {
             float m2[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -864,16 +890,27 @@ __global__ void __launch_bounds__(THREADS, 1)
           float sv[32];
           tmem_ld32(tS + lane_base + 32 * q, sv);
           tmem_ld_wait(sv);
-          add_bias(sv, q);
           if (!full_tile) {
 #pragma unroll
             for (int k = 0; k < 32; ++k)
               if ((k & 15) >= lim[2 * q + (k >> 4)]) sv[k] = -INFINITY;
           }
+          // ALiBi: the bias moves into the subtrahend, m - b0 - slope (k & 15), stepped
+          // by 2 slope from pair to pair of a block.
+          uint64_t sub = mm, step2 = 0;
+          if constexpr (ALIBI) step2 = f2(2.f * slope2, 2.f * slope2);
           uint32_t pw[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const float2 dv = f2_split(f2_sub(f2(sv[2 * k], sv[2 * k + 1]), mm));
+            if constexpr (ALIBI) {
+              if ((k & 7) == 0) {
+                const float b = m_use - bias0(q, k >> 3);
+                sub = f2(b, b - slope2);
+              } else {
+                sub = f2_sub(sub, step2);
+              }
+            }
+            const float2 dv = f2_split(f2_sub(f2(sv[2 * k], sv[2 * k + 1]), sub));
             const float e0 = ex2(dv.x), e1 = ex2(dv.y);
             pw[k] = pack_bf16x2(e0, e1);
             acc = f2_add(acc, f2(e0, e1));

@@ -188,18 +188,27 @@ __global__ void __launch_bounds__(THREADS, 1)
     int issued = 0;
     bool ok = true;
     for (int j = 0; j < n_tiles && ok; ++j) {
-      if (j * BLOCKS >= cbase + 32) {  // warp-uniform: the tile starts in the next chunk
-        cbase += 32;
-        wcur = wnext;
-        wnext = cbase + 32 + lane < nb ? __ldg(&wrow[cbase + 32 + lane]) : 0u;
+      // ALiBi walks the tiles from the last (the keys nearest the queries, with the
+      // largest bias) to the first, so that the running maximum is met early and later
+      // tiles seldom raise it (each raise rescales the running output).
+      const int jt = ALIBI ? n_tiles - 1 - j : j;
+      const int b = jt * BLOCKS + min(lane, BLOCKS);
+      uint32_t w;
+      if constexpr (ALIBI) {
+        w = (lane <= BLOCKS && b < nb) ? __ldg(&wrow[b]) : 0u;
+      } else {
+        if (j * BLOCKS >= cbase + 32) {  // warp-uniform: the tile starts in the next chunk
+          cbase += 32;
+          wcur = wnext;
+          wnext = cbase + 32 + lane < nb ? __ldg(&wrow[cbase + 32 + lane]) : 0u;
+        }
+        // Lanes 0..BLOCKS-1 describe the tile's blocks; lane BLOCKS takes the next
+        // block's word so that the tile's last block knows where the following one starts.
+        const int rel = b - cbase;  // 0 .. 40
+        const uint32_t w0 = __shfl_sync(0xffffffffu, wcur, rel & 31);
+        const uint32_t w1 = __shfl_sync(0xffffffffu, wnext, rel & 31);
+        w = (lane <= BLOCKS && b < nb) ? (rel < 32 ? w0 : w1) : 0u;
       }
-      // Lanes 0..BLOCKS-1 describe the tile's blocks; lane BLOCKS takes the next
-      // block's word so that the tile's last block knows where the following one starts.
-      const int b = j * BLOCKS + min(lane, BLOCKS);
-      const int rel = b - cbase;  // 0 .. 40
-      const uint32_t w0 = __shfl_sync(0xffffffffu, wcur, rel & 31);
-      const uint32_t w1 = __shfl_sync(0xffffffffu, wnext, rel & 31);
-      const uint32_t w = (lane <= BLOCKS && b < nb) ? (rel < 32 ? w0 : w1) : 0u;
       const BlockInfo bi = decode_word(w, b, a.id_bits);
       const int p_after = __shfl_down_sync(0xffffffffu, bi.p, 1);
       int y = -kBlock, nv = 0;  // rows of an invalid block start at -16: read as zeros

@@ -209,11 +209,15 @@ def _i32_np(a) -> np.ndarray:
 
 
 def pack_block_words_host(p: Params, num_docs: int, seg_indptr, seg_doc, seg_len, seq_pos0, doc_block_indptr,
-                          doc_blocks):
-    """Host packer; arrays are numpy-compatible. Returns (words [B, max_blocks] uint32, seq_lens [B] int32)."""
+                          doc_blocks, out=None):
+    """Host packer; arrays are numpy-compatible. Returns (words [B, max_blocks] uint32, seq_lens [B] int32),
+    written into ``out`` = (words, seq_lens) when given (caller buffers, e.g. pinned host memory)."""
     B, MB = p.num_seqs, p.max_blocks_per_seq
-    words = np.zeros((B, MB), dtype=np.uint32)
-    seq_lens = np.zeros(B, dtype=np.int32)
+    if out is None:
+        words = np.zeros((B, MB), dtype=np.uint32)
+        seq_lens = np.zeros(B, dtype=np.int32)
+    else:
+        words, seq_lens = out
     # None stays NULL; an empty array is passed as a valid (never read) one-element buffer.
     arrs = [None if x is None else (_i32_np(x) if np.size(x) else np.zeros(1, np.int32))
             for x in (seg_indptr, seg_doc, seg_len, seq_pos0, doc_block_indptr, doc_blocks)]
