@@ -882,9 +882,19 @@ def measure_extras(args, d, w, flush, hbm, tf_burst, tf_sust):
     t5 = time_steps(mixed_step, max(10, n // 2), 3, flush)
     td = time_steps(lambda: run_decode(dd, lazy=True), max(10, n // 2), 3, flush)
     tp = time_steps(lambda: run_prefill(dp5, lazy=True), max(10, n // 2), 3, flush)
+    # The same step as one launch (lazy_attn_mixed): decode items and prefill tiles in
+    # the prefill kernel's persistent pipeline.
+    ws_mix = torch.empty(L.mixed_workspace_bytes(dd["p"], dp5["p"], dd["plan"].num_slots), dtype=torch.uint8,
+                         device="cuda")
+    tf = time_steps(lambda: L.mixed(dd["p"], dd["q"], dd["words"], dd["q_pos"], dd["plan"], dp5["p"], dp5["q"],
+                                    dp5["cu"], dp5["q_start"], dp5["max_q"], dp5["words"], dp5["seq_lens"], dd["k"],
+                                    dd["v"], dd["rope"], out_dec=dd["out"], out_pf=dp5["out"], workspace=ws_mix),
+                    max(10, n // 2), 3, flush)
+    del ws_mix
     b5 = decode_bytes(wd)
     f5 = prefill_flops(wp)
     out["mixed_mqa"] = {"step_ms": 1e3 * statistics.median(t5),
+                        "one_launch_step_ms": 1e3 * statistics.median(tf),
                         "decode_ms": 1e3 * statistics.median(td), "prefill_ms": 1e3 * statistics.median(tp),
                         "decode_kv_gbs_logical": b5["kv_logical"] / statistics.median(td) / 1e9,
                         "decode_kv_gbs_unique": b5["unique"] / statistics.median(td) / 1e9,

@@ -430,6 +430,38 @@ int lazy_attn_prefill_alibi(const lazy_attn_params *p, const void *q, const int3
                             const void *rope_table, const float *alibi_slopes, void *out, void *workspace,
                             size_t workspace_bytes, lazy_stream_t stream);
 
+/* ---------------------------------------------------------------- one launch for a mixed batch
+ * A continuous-batching step ("KV Cache, Flash Attention & Otimização de Inferência",
+ * "Continuous batching": new requests' prompts are prefilled in the same step as the
+ * running sequences' decode) as ONE kernel launch: the shared-run decode of a batch
+ * (p_dec, its plan and inputs, as lazy_attn_decode_shared takes them) and the
+ * prefill of other sequences' chunks (p_pf and the inputs of lazy_attn_prefill),
+ * over the same pools and rotation table. The prefill kernel's persistent pipeline
+ * also runs the decode's work items: each item is a one-tile unit (member x query
+ * head rows, each member rotated by R_{m-p} from its own block word, K used as
+ * stored), dealt round robin to the CTAs before their share of the prefill, and the
+ * launch ends by merging every decode sequence's partials (the combine of
+ * lazy_attn_decode_shared) once its items are done; the launch is cooperative (one
+ * CTA per SM, all resident), so that wait always ends.
+ * Requirements: dtype bf16, head_dim 128, the same heads, pool, id_bits, sm_scale
+ * and lazy = 1 in both params, query heads per KV head a multiple of 16 (the
+ * decode's 128-row tensor-core items, plan with p_dec, whose 16-row groups each
+ * hold one member's heads); p_dec->kv_dtype and
+ * key_positions 0 (LAZY_ERR_UNSUPPORTED otherwise). workspace: at least
+ * lazy_attn_mixed_workspace_bytes bytes, 256-byte aligned (the prefill's merge
+ * area, the decode partials, one counter per decode sequence; the call zeroes the
+ * counters with cudaMemsetAsync on `stream`). A batch with no prefill rows (or no
+ * decode sequence) runs as the plain call of the other kind. */
+size_t lazy_attn_mixed_workspace_bytes(const lazy_attn_params *p_dec, const lazy_attn_params *p_pf,
+                                       int32_t num_slots);
+int lazy_attn_mixed(const lazy_attn_params *p_dec, const void *q_dec, const uint32_t *block_words_dec,
+                    const int32_t *q_pos, int32_t num_items, const int32_t *items, int32_t num_slots,
+                    const int32_t *slot_indptr, void *out_dec, const lazy_attn_params *p_pf, const void *q_pf,
+                    const int32_t *cu_seqlens_q, const int32_t *q_start, int32_t total_q, int32_t max_q_len,
+                    const uint32_t *block_words_pf, const int32_t *seq_lens_pf, void *out_pf, const void *k_pool,
+                    const void *v_pool, const void *rope_table, void *workspace, size_t workspace_bytes,
+                    lazy_stream_t stream);
+
 /* ---------------------------------------------------------------- eager materialisation (baseline)
  * The alternative the lazy method avoids ("Declaração do Problema"): a reused
  * document's keys re-rotated to their absolute positions and copied per sequence.

@@ -156,6 +156,14 @@ bool encode_q_map(CUtensorMap* m, const void* base, uint64_t total_q, int hq, in
   return encode_cached(m, 3, base, dims, strides, box);
 }
 
+// Decode queries [B][Hq][d] for the mixed launch: box = 64 columns x g heads x 1 sequence.
+bool encode_dec_q_map(CUtensorMap* m, const void* base, uint64_t B, int hq, int d, int g) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hq, (cuuint64_t)B};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)hq * d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)g, 1};
+  return encode_cached(m, 3, base, dims, strides, box);
+}
+
 // The pools hold e4m3 codes (FP8 KV; only the per-sequence decode reads them).
 static bool kv_fp8(const lazy_attn_params* p) { return p->kv_dtype == LAZY_FP8_E4M3 && p->dtype != LAZY_FP8_E4M3; }
 
@@ -713,6 +721,117 @@ int lazy_attn_prefill_alibi(const lazy_attn_params* p, const void* q, const int3
   if (!alibi_slopes) return LAZY_ERR_INVALID_ARG;
   return prefill_impl(p, q, cu_seqlens_q, q_start, total_q, max_q_len, k_pool, v_pool, block_words, seq_lens,
                       rope_table, alibi_slopes, out, workspace, workspace_bytes, stream);
+}
+
+// ---------------------------------------------------------------- one launch for a mixed batch
+
+static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+static bool mixed_compatible(const lazy_attn_params* pd, const lazy_attn_params* pp, const Checked& cd) {
+  return pd->num_q_heads == pp->num_q_heads && pd->num_kv_heads == pp->num_kv_heads &&
+         pd->head_dim == pp->head_dim && pd->num_pool_blocks == pp->num_pool_blocks && pd->id_bits == pp->id_bits &&
+         pd->dtype == pp->dtype && pd->sm_scale == pp->sm_scale && pd->lazy == pp->lazy &&
+         pd->key_positions == pp->key_positions && pd->kv_dtype == pp->kv_dtype && pd->head_dim == 128 &&
+         pd->dtype == LAZY_BF16 && !kv_fp8(pd) && pd->lazy != 0 && !pd->key_positions && cd.G % 16 == 0 &&
+         lazy::shared_rows_cap(cd.G, pd->head_dim) == 128;
+}
+
+size_t lazy_attn_mixed_workspace_bytes(const lazy_attn_params* p_dec, const lazy_attn_params* p_pf, int32_t num_slots) {
+  Checked cd, cp;
+  if (check_params(p_dec, &cd) != LAZY_OK || check_params(p_pf, &cp) != LAZY_OK || num_slots < 0) return 0;
+  const int grid = current_device() >= 0 ? lazy::prefill_stream_grid() : kDefaultSmCount;
+  return align256(lazy::prefill_stream_workspace_bytes(grid)) +
+         align256((size_t)num_slots * p_dec->num_q_heads * (p_dec->head_dim + 2) * sizeof(float)) +
+         align256((size_t)p_dec->num_seqs * sizeof(int));
+}
+
+int lazy_attn_mixed(const lazy_attn_params* p_dec, const void* q_dec, const uint32_t* words_dec, const int32_t* q_pos,
+                    int32_t num_items, const int32_t* items, int32_t num_slots, const int32_t* slot_indptr,
+                    void* out_dec, const lazy_attn_params* p_pf, const void* q_pf, const int32_t* cu_seqlens_q,
+                    const int32_t* q_start, int32_t total_q, int32_t max_q_len, const uint32_t* words_pf,
+                    const int32_t* seq_lens_pf, void* out_pf, const void* k_pool, const void* v_pool,
+                    const void* rope_table, void* workspace, size_t workspace_bytes, lazy_stream_t stream) {
+  Checked cd, cp;
+  int rc = check_params(p_dec, &cd);
+  if (rc != LAZY_OK) return rc;
+  rc = check_params(p_pf, &cp);
+  if (rc != LAZY_OK) return rc;
+  if (!mixed_compatible(p_dec, p_pf, cd)) return LAZY_ERR_UNSUPPORTED;
+  if (num_items < 0 || num_slots < 0 || total_q < 0 || max_q_len < 0) return LAZY_ERR_INVALID_ARG;
+  // A batch with only one kind of work is the plain call of that kind.
+  if (p_pf->num_seqs == 0 || total_q == 0 || max_q_len == 0)
+    return lazy_attn_decode_shared(p_dec, q_dec, k_pool, v_pool, words_dec, q_pos, rope_table, num_items, items,
+                                   num_slots, slot_indptr, out_dec, workspace, workspace_bytes, stream);
+  if (p_dec->num_seqs == 0) {
+    const size_t need = lazy_attn_prefill_workspace_bytes(p_pf, total_q);
+    return lazy_attn_prefill(p_pf, q_pf, cu_seqlens_q, q_start, total_q, max_q_len, k_pool, v_pool, words_pf,
+                             seq_lens_pf, rope_table, out_pf, workspace, workspace_bytes < need ? 0 : workspace_bytes,
+                             stream);
+  }
+  if (!q_dec || !words_dec || !q_pos || !slot_indptr || !out_dec || !q_pf || !cu_seqlens_q || !q_start || !words_pf ||
+      !seq_lens_pf || !out_pf || !k_pool || !v_pool || !rope_table)
+    return LAZY_ERR_INVALID_ARG;
+  if (num_items > 0 && (!items || num_slots == 0)) return LAZY_ERR_INVALID_ARG;
+  if ((int64_t)num_items * p_dec->num_kv_heads > INT32_MAX) return LAZY_ERR_UNSUPPORTED;
+  if (p_dec->num_pool_blocks == 0 || p_dec->max_blocks_per_seq == 0 || p_pf->max_blocks_per_seq == 0)
+    return LAZY_ERR_INVALID_ARG;
+  if (!aligned16(q_dec) || !aligned16(q_pf) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out_dec) ||
+      !aligned16(out_pf) || !aligned16(rope_table) || (items && !aligned16(items)))
+    return LAZY_ERR_INVALID_ARG;
+  const int grid = lazy::prefill_stream_grid();
+  const size_t pf_bytes = align256(lazy::prefill_stream_workspace_bytes(grid));
+  const size_t dec_bytes = align256((size_t)num_slots * p_dec->num_q_heads * (p_dec->head_dim + 2) * sizeof(float));
+  const size_t need = lazy_attn_mixed_workspace_bytes(p_dec, p_pf, num_slots);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return LAZY_ERR_WORKSPACE;
+  unsigned int* st = status_ptr();
+  if (!st) return LAZY_ERR_CUDA;
+  CUtensorMap qmap, qmap_dec, kmap, vmap;
+  const uint64_t rows = (uint64_t)p_pf->num_pool_blocks * p_pf->num_kv_heads * lazy::kBlock;
+  // decode queries [B_dec][Hq][d]: one box is the G query heads of one KV head of one sequence
+  if (!encode_q_map(&qmap, q_pf, (uint64_t)total_q, p_pf->num_q_heads, p_pf->head_dim, 128) ||
+      !encode_dec_q_map(&qmap_dec, q_dec, (uint64_t)p_dec->num_seqs, p_dec->num_q_heads, p_dec->head_dim, cd.G) ||
+      !encode_rows_map(&kmap, k_pool, rows, p_pf->head_dim, lazy::kBlock) ||
+      !encode_rows_map(&vmap, v_pool, rows, p_pf->head_dim, lazy::kBlock))
+    return LAZY_ERR_CUDA;
+  lazy::MixedArgs a{};
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.q_start = q_start;
+  a.words = words_pf;
+  a.seq_lens = seq_lens_pf;
+  a.rope = static_cast<const float2*>(rope_table);
+  a.out = out_pf;
+  a.status = st;
+  a.B = p_pf->num_seqs;
+  a.Hq = p_pf->num_q_heads;
+  a.Hkv = p_pf->num_kv_heads;
+  a.G = cp.G;
+  a.D = p_pf->head_dim;
+  a.total_q = total_q;
+  a.max_q_len = max_q_len;
+  a.max_blocks = p_pf->max_blocks_per_seq;
+  a.id_bits = cp.id_bits;
+  a.num_pool_blocks = p_pf->num_pool_blocks;
+  a.scale_log2 = scale_log2(p_pf);
+  a.T = (max_q_len + lazy::pf_tile_rows - 1) / lazy::pf_tile_rows;
+  a.counters = static_cast<int*>(workspace);
+  a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + lazy::prefill_stream_counter_bytes(grid));
+  a.q_dec = q_dec;
+  a.words_dec = words_dec;
+  a.q_pos = q_pos;
+  a.items = items;
+  a.slot_indptr = slot_indptr;
+  a.out_dec = out_dec;
+  a.ws_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + pf_bytes);
+  a.ws_ml = a.ws_o + (size_t)num_slots * p_dec->num_q_heads * p_dec->head_dim;
+  a.seq_done = reinterpret_cast<int*>(static_cast<char*>(workspace) + pf_bytes + dec_bytes);
+  a.B_dec = p_dec->num_seqs;
+  a.max_blocks_dec = p_dec->max_blocks_per_seq;
+  a.num_items = num_items;
+  a.num_slots = num_slots;
+  cudaError_t e = lazy::launch_mixed(a, qmap, qmap_dec, kmap, vmap, grid, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return LAZY_ERR_UNSUPPORTED;
+  return launched(e);
 }
 
 int lazy_attn_materialize(const lazy_attn_params* p, const void* k_pool, const void* v_pool,

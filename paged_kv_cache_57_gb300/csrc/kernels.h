@@ -106,6 +106,21 @@ struct PrefillArgs {
 struct PrefillAlibiArgs : PrefillArgs {
   const float* alibi;  // [Hq] slopes
 };
+// One launch for a continuous batch (prefill_stream.cu): the stream-K prefill kernel
+// also runs the shared-run decode's work items, as one-tile units of its pipeline,
+// and merges each decode sequence's partials at its end.
+struct MixedArgs : PrefillArgs {
+  const void* q_dec;           // [B_dec][Hq][D] unrotated
+  const uint32_t* words_dec;   // [B_dec][max_blocks_dec]
+  const int32_t* q_pos;        // [B_dec]
+  const int32_t* items;        // the shared-run plan's items
+  const int32_t* slot_indptr;  // [B_dec + 1]
+  void* out_dec;               // [B_dec][Hq][D] bf16
+  float* ws_o;                 // [num_slots][Hq][D] decode partials
+  float* ws_ml;                // [num_slots][Hq][2]
+  int* seq_done;               // [B_dec] decode units finished per sequence (zeroed before the launch)
+  int B_dec, max_blocks_dec, num_items, num_slots;
+};
 constexpr int PREFILL_PARTIAL_ROW_FLOATS = 128 + 4;
 constexpr int pf_tile_rows = 128;  // query rows per prefill tile
 
@@ -199,6 +214,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, bool lazy, const CUtensorMap& q
 // Two query tiles per CTA, one CTA per SM, stream-K over (unit, K tile); even GQA ratio.
 cudaError_t launch_prefill_stream(const PrefillArgs& a, bool lazy, const CUtensorMap& qmap, const CUtensorMap& kmap,
                                   const CUtensorMap& vmap, int grid, cudaStream_t st, const float* alibi = nullptr);
+cudaError_t launch_mixed(const MixedArgs& a, const CUtensorMap& qmap, const CUtensorMap& qmap_dec,
+                         const CUtensorMap& kmap, const CUtensorMap& vmap, int grid, cudaStream_t st);
 size_t prefill_stream_workspace_bytes(int grid);  // counters, then partials
 size_t prefill_stream_counter_bytes(int grid);
 int prefill_stream_grid();

@@ -64,7 +64,11 @@ constexpr int OFF_QCS = (OFF_BAR + NBARS * 8 + 15) & ~15;
 constexpr int OFF_ROWS = OFF_QCS + 2 * 8 * (D / 2) * 8;
 constexpr int OFF_SCHED = OFF_ROWS + kAngleRows * (D / 2) * 8;
 constexpr int SCHED_BYTES = 64;  // room for Sched (checked below)
-constexpr int OFF_TMEM = OFF_SCHED + SCHED_BYTES;
+// Mixed launches: per decode unit, whether each member passed its checks; a ring of
+// 4 segments (written in the Q prologue one segment ahead, read in the deferred epilogue).
+constexpr int OFF_DECOK = OFF_SCHED + SCHED_BYTES;
+constexpr int DECOK_BYTES = 4 * 16 * 4;
+constexpr int OFF_TMEM = OFF_DECOK + DECOK_BYTES;
 constexpr int SMEM = 1024 + OFF_TMEM + 16;
 static_assert(OFF_QCS % 16 == 0 && OFF_ROWS % 16 == 0, "angle rows are written as 16-byte vectors");
 static_assert(SMEM <= 227 * 1024, "prefill (stream) shared memory");
@@ -72,10 +76,12 @@ static_assert(SMEM <= 227 * 1024, "prefill (stream) shared memory");
 // One unit's geometry. n = K tiles it needs (0: the tile holds no query row).
 struct UnitDesc {
   int s, tile, hp, q0, C, row0, seq_len, nb, b_chunk, n;
+  int dec;  // decode work unit (item * Hkv + KV head) in a mixed launch, else -1
 };
 
 __device__ __forceinline__ UnitDesc unit_desc(const PrefillArgs& a, int u, int P) {
   UnitDesc d;
+  d.dec = -1;
   const int TP = a.T * P;
   d.s = u / TP;
   const int rem = u - d.s * TP;
@@ -100,13 +106,40 @@ __device__ __forceinline__ UnitDesc unit_desc(const PrefillArgs& a, int u, int P
   return d;
 }
 
+// Decode unit ud of a mixed launch: item ud / Hkv of the shared-run plan on KV head
+// ud % Hkv, one 128-row tile (members x query heads) over the item's blocks,
+// n = ceil(nblk / 8) key tiles. s = the item's source sequence, nb = nblk; hp puts
+// the tile on its KV head.
+__device__ __forceinline__ UnitDesc dec_desc(const MixedArgs& a, int ud) {
+  UnitDesc d;
+  const int* rec = a.items + (size_t)(ud / a.Hkv) * LAZY_PLAN_ITEM_INTS;
+  d.dec = ud;
+  d.s = __ldg(&rec[0]);
+  d.nb = __ldg(&rec[2]);
+  const int b0 = __ldg(&rec[1]), last = __ldg(&rec[3]), nmem = __ldg(&rec[4]);
+  if (d.s < 0 || d.s >= a.B_dec || b0 < 0 || d.nb < 1 || d.nb > a.max_blocks_dec - b0 || last < 1 ||
+      last > kBlock || nmem < 1 || nmem * a.G > BM) {  // not a valid item: skipped
+    raise_status(a.status, LAZY_DEV_LAYOUT);
+    d.nb = 0;
+  }
+  d.hp = (ud % a.Hkv) * (a.G / 2);
+  d.tile = d.q0 = d.row0 = 0;
+  d.C = BM;
+  d.seq_len = 0;
+  d.b_chunk = INT_MAX;
+  d.n = d.nb > 0 ? (d.nb + BLOCKS - 1) / BLOCKS : 0;
+  return d;
+}
+
 // Rotates row i of a 128-row Q tile in place (both 64-column halves, 128-byte
 // swizzled) by R_{base+i}, pre-scaled by `scale`: bq holds (cos, sin) of
-// (base + 16 k) w_f at [k][f], rows the row-offset table at [f][24].
+// (base + 16 k) w_f at [k][f], rows the row-offset table at [f][24]. With
+// row_offsets = false every row of group k takes bq[k] itself (decode units, whose
+// rows are query heads of one member sequence at one rotation offset).
 __device__ __forceinline__ void rotate_q_row_bq(uint8_t* sQ, int i, const float2* bq, const float2* rows,
-                                                float scale) {
+                                                float scale, bool row_offsets = true) {
   const float2* b = bq + (i >> 4) * (D / 2);
-  const int s1 = 8 + (i & 15);
+  const int s1 = 8 + (row_offsets ? (i & 15) : 0);  // table row 0 is the identity (1, 0)
 #pragma unroll 1
   for (int c = 0; c < 8; ++c) {
     float2 cs[8];
@@ -170,12 +203,96 @@ static_assert(OFF_SCHED % 16 == 0 && OFF_TMEM % 16 == 0, "shared-memory slots ar
 #endif
 #define LAZY_PF_TRACE(sg, i, v) LAZY_PF_TRACE_IF(threadIdx.x == 0, sg, i, v)
 
-template <bool LAZY, bool ALIBI = false>
+// The decode half of a mixed launch, merged: warp w of CTA c takes (sequence s,
+// query head h) pairs c * nw + w, + grid * nw, ...; out[s][h] = sum_k 2^(m_k - M) o_k /
+// sum_k 2^(m_k - M) l_k over the sequence's slots k, as shared_combine_kernel. A
+// sequence is merged once its decode units have all written their partials (their
+// count of written rows, acquired, reaches slots x Hq); the launch is cooperative, so
+// every unit is resident or done, and the wait is bounded (LAZY_DEV_TIMEOUT after it).
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void mixed_combine(const MixedArgs& a, int warp, int nw) {
+  constexpr int PER = D / 32, BATCH = 8;
+  const int lane = threadIdx.x & 31;
+  const float2* ml = reinterpret_cast<const float2*>(a.ws_ml);
+  for (long long task = (long long)blockIdx.x * nw + warp; task < (long long)a.B_dec * a.Hq;
+       task += (long long)gridDim.x * nw) {
+    const int s = (int)(task / a.Hq), h = (int)(task - (long long)s * a.Hq);
+    int k0 = __ldg(&a.slot_indptr[s]), k1 = __ldg(&a.slot_indptr[s + 1]);
+    if (k0 < 0 || k1 < k0 || k1 > a.num_slots) {
+      if (lane == 0) raise_status(a.status, LAZY_DEV_LAYOUT);
+      k0 = k1 = 0;
+    }
+    const int need = (k1 - k0) * a.Hq;  // rows: every slot holds Hq query heads
+    int ok = 1;
+    if (lane == 0 && need > 0) {
+      const uint64_t t0 = global_timer_ns();
+      while (ld_acquire_gpu(&a.seq_done[s]) < need) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          raise_status(a.status, LAZY_DEV_TIMEOUT);
+          ok = 0;
+          break;
+        }
+        __nanosleep(256);
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) continue;
+    float M = -INFINITY, L = 0.f, acc[PER];
+#pragma unroll
+    for (int c = 0; c < PER; ++c) acc[c] = 0.f;
+    for (int kc = k0; kc < k1; kc += BATCH) {
+      const int n = min(BATCH, k1 - kc);
+      float2 mlj[BATCH];
+      float4 vj[BATCH];
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        mlj[u] = make_float2(-INFINITY, 0.f);
+        vj[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (u < n) {
+          const size_t pidx = (size_t)(kc + u) * a.Hq + h;
+          mlj[u] = __ldcg(ml + pidx);
+          vj[u] = __ldcg(reinterpret_cast<const float4*>(a.ws_o + pidx * D) + lane);
+        }
+      }
+      float Mn = M;
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) Mn = fmaxf(Mn, mlj[u].x);
+      if (Mn == -INFINITY) continue;
+      const float r = ex2(M - Mn);
+      L *= r;
+#pragma unroll
+      for (int c = 0; c < PER; ++c) acc[c] *= r;
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        const float w = ex2(mlj[u].x - Mn);  // an empty slot weighs 0
+        L = fmaf(w, mlj[u].y, L);
+        acc[0] = fmaf(w, vj[u].x, acc[0]);
+        acc[1] = fmaf(w, vj[u].y, acc[1]);
+        acc[2] = fmaf(w, vj[u].z, acc[2]);
+        acc[3] = fmaf(w, vj[u].w, acc[3]);
+      }
+      M = Mn;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out_dec) + ((size_t)s * a.Hq + h) * D + lane * PER;
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                                pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  }
+}
+
+template <bool LAZY, bool ALIBI = false, bool MIXED = false>
 __global__ void __launch_bounds__(THREADS, 1)
-    prefill_stream_kernel(const std::conditional_t<ALIBI, PrefillAlibiArgs, PrefillArgs> a,
+    prefill_stream_kernel(const std::conditional_t<ALIBI, PrefillAlibiArgs,
+                                                   std::conditional_t<MIXED, MixedArgs, PrefillArgs>> a,
                           const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                          const __grid_constant__ CUtensorMap vmap) {
+                          const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap_dec) {
   static_assert(!(ALIBI && LAZY), "the ALiBi prefill does not rotate");
+  static_assert(!(ALIBI && MIXED), "mixed launches rotate");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   uint8_t* sQ[2] = {base + OFF_QA, base + OFF_QB};
@@ -202,6 +319,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   float2* angle_rows = reinterpret_cast<float2*>(base + OFF_ROWS);
   Sched* sched = reinterpret_cast<Sched*>(base + OFF_SCHED);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base + OFF_TMEM);
+  int* dec_ok = reinterpret_cast<int*>(base + OFF_DECOK);  // [4][16]
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -357,7 +475,21 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     int kd = blockIdx.x;                                     // next whole unit
     int x = sc.start, ks = sc.k, jn = sc.j, U0n = sc.U0;     // split-space cursor
+    int kdec = blockIdx.x;                                   // next decode unit (mixed launches)
+    (void)kdec;
     auto next = [&](Seg& sgm) -> bool {
+      if constexpr (MIXED) {  // decode units first, whole, dealt round robin
+        while (kdec < a.num_items * a.Hkv) {
+          sgm.un = dec_desc(a, kdec);
+          kdec += gridDim.x;
+          if (sgm.un.n == 0) continue;  // an invalid item (flagged)
+          sgm.u = -1;
+          sgm.j0 = 0;
+          sgm.j1 = sgm.un.n;
+          sgm.U0 = -1;
+          return true;
+        }
+      }
       if (kd < sc.D) {
         seek(kd);
         sgm.un = gd;
@@ -419,10 +551,27 @@ __global__ void __launch_bounds__(THREADS, 1)
       (void)u;
       (void)U0;
       const int kvh = (2 * un.hp) / a.G;
+      const bool dec = MIXED && un.dec >= 0;
       if (!is_v) {  // Q of both tiles; the previous segment's S products must be done with sQ
         if (sg > 0 && !warp_wait(q_empty, (sg - 1) & 1, a.status)) return ok = false;
         LAZY_PF_TRACE_IF(lane == 0, sg, 4, global_timer_ns());
-        if (lane == 0) {
+        if (dec) {
+          if constexpr (MIXED) {
+            // Decode unit: row r = member (r / G) x query head (r % G) of this KV head;
+            // both tiles get the same rows (tile B's results are not kept).
+            const int* rec = a.items + (size_t)(un.dec / a.Hkv) * LAZY_PLAN_ITEM_INTS;
+            const int nmem = min(__ldg(&rec[4]), BM / a.G);
+            if (lane == 0) {
+              mbar_arrive_expect_tx(q_full, 2u * (uint32_t)nmem * (uint32_t)a.G * 256u);
+              for (int t = 0; t < 2; ++t)
+                for (int m = 0; m < nmem; ++m) {
+                  const int seq = min(max(__ldg(&rec[8 + 4 * m]), 0), a.B_dec - 1);
+                  tma_load_3d(sQ[t] + m * a.G * 128, &qmap_dec, q_full, 0, kvh * a.G, seq);
+                  tma_load_3d(sQ[t] + HALF + m * a.G * 128, &qmap_dec, q_full, 64, kvh * a.G, seq);
+                }
+            }
+          }
+        } else if (lane == 0) {
           mbar_arrive_expect_tx(q_full, 2 * TILE);
           for (int t = 0; t < 2; ++t) {
             tma_load_3d(sQ[t], &qmap, q_full, 0, 2 * un.hp + t, un.q0 + un.row0);
@@ -431,12 +580,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         qs = sg + 1;
       }
-      const uint32_t* wrow = a.words + (size_t)un.s * a.max_blocks;
+      // (decode units read the decode batch's words, below; nb_pf = 0 keeps them away
+      // from the prefill words)
+      const int nb_pf = dec ? 0 : un.nb;
+      const uint32_t* wrow = a.words + (size_t)(dec ? 0 : un.s) * a.max_blocks;
       // Block words 32 at a time, a chunk ahead: lane l holds block cbase + l (wcur) and
       // cbase + 32 + l (wnext).
       int cbase = (j0 * BLOCKS) & ~31;
-      uint32_t wcur = cbase + lane < un.nb ? __ldg(&wrow[cbase + lane]) : 0u;
-      uint32_t wnext = cbase + 32 + lane < un.nb ? __ldg(&wrow[cbase + 32 + lane]) : 0u;
+      uint32_t wcur = cbase + lane < nb_pf ? __ldg(&wrow[cbase + lane]) : 0u;
+      uint32_t wnext = cbase + 32 + lane < nb_pf ? __ldg(&wrow[cbase + 32 + lane]) : 0u;
       for (int j = j0; j < j1; ++j, ++g) {
         // ALiBi walks a unit's tiles from the last (the keys nearest the queries, with
         // the largest bias) to the first, so that the running maximum is met early and
@@ -445,26 +597,46 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t w;
         const int b = jt * BLOCKS + min(lane, BLOCKS);
         if constexpr (ALIBI) {
-          w = (lane <= BLOCKS && b < un.nb) ? __ldg(&wrow[b]) : 0u;
+          w = (lane <= BLOCKS && b < nb_pf) ? __ldg(&wrow[b]) : 0u;
         } else {
           if (j * BLOCKS >= cbase + 32) {  // warp-uniform: the tile starts in the next chunk
             cbase += 32;
             wcur = wnext;
-            wnext = cbase + 32 + lane < un.nb ? __ldg(&wrow[cbase + 32 + lane]) : 0u;
+            wnext = cbase + 32 + lane < nb_pf ? __ldg(&wrow[cbase + 32 + lane]) : 0u;
           }
           // Lanes 0..BLOCKS-1 describe the tile's blocks; lane BLOCKS takes the next block's
           // word so that the tile's last block knows where the following one starts.
           const int rel = b - cbase;  // 0 .. 40
           const uint32_t w0 = __shfl_sync(0xffffffffu, wcur, rel & 31);
           const uint32_t w1 = __shfl_sync(0xffffffffu, wnext, rel & 31);
-          w = (lane <= BLOCKS && b < un.nb) ? (rel < 32 ? w0 : w1) : 0u;
+          w = (lane <= BLOCKS && b < nb_pf) ? (rel < 32 ? w0 : w1) : 0u;
         }
-        const BlockInfo bi = decode_word(w, b, a.id_bits);
+        BlockInfo bi = decode_word(w, b, a.id_bits);
         const int p_after = __shfl_down_sync(0xffffffffu, bi.p, 1);
         int y = -kBlock, nv = 0;  // rows of an invalid block start at -16: read as zeros
+        if constexpr (MIXED) {
+          if (dec) {  // item block b of the source sequence's run: full but the last
+            const int* rec = a.items + (size_t)(un.dec / a.Hkv) * LAZY_PLAN_ITEM_INTS;
+            const uint32_t wd = (lane < BLOCKS && b < un.nb)
+                                    ? __ldg(&a.words_dec[(size_t)un.s * a.max_blocks_dec + __ldg(&rec[1]) + b])
+                                    : 0u;
+            bi.phys = (int)(wd & ((1u << a.id_bits) - 1u));
+            bi.p = 0;
+          }
+        }
         if (lane < BLOCKS && b < un.nb) {
-          nv = block_valid(b, un.nb, un.seq_len, bi.p, b + 1 < un.nb ? p_after : bi.p);
-          nv = nv < 0 ? 0 : (nv > kBlock ? kBlock : nv);
+          bool item_nv = false;
+          if constexpr (MIXED) {
+            if (dec) {
+              const int* rec = a.items + (size_t)(un.dec / a.Hkv) * LAZY_PLAN_ITEM_INTS;
+              nv = b == un.nb - 1 ? min(max(__ldg(&rec[3]), 0), kBlock) : kBlock;
+              item_nv = true;
+            }
+          }
+          if (!item_nv) {
+            nv = block_valid(b, un.nb, un.seq_len, bi.p, b + 1 < un.nb ? p_after : bi.p);
+            nv = nv < 0 ? 0 : (nv > kBlock ? kBlock : nv);
+          }
           if (bi.phys < a.num_pool_blocks) {
             y = (bi.phys * a.Hkv + kvh) * kBlock;
           } else {
@@ -609,7 +781,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const KMeta m = kmeta[st * BLOCKS + bl];
           holes |= m.nvalid < kBlock;
           if constexpr (LAZY) {
-            if (m.nvalid > 0) {
+            if (m.nvalid > 0 && !(MIXED && un.dec >= 0)) {  // decode units: K as stored
               if (m.p != p_cached) {
                 float2 cs[8];
 #pragma unroll
@@ -666,9 +838,48 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (threadIdx.x < D / 2) {
         float2* bq = base_cs + (sg & 1) * 8 * (D / 2);
         const int f = threadIdx.x;
-        const float2 b = rope_cs(__ldg(&a.rope[f]), __ldg(&a.q_start[un.s]) + un.row0, a.status);
+        if (MIXED && un.dec >= 0) {
+          if constexpr (MIXED) {
+            // Decode unit: rows of member m (16-row groups k with 16 k / G == m) are rotated
+            // by R_{m_pos - p}, p = the member's document start from its own first block
+            // word, whose block must be the item's (else the member is dropped).
+            const int* rec = a.items + (size_t)(un.dec / a.Hkv) * LAZY_PLAN_ITEM_INTS;
+            const int nmem = min(__ldg(&rec[4]), BM / a.G), b0 = __ldg(&rec[1]);
+            const uint32_t id_mask = (1u << a.id_bits) - 1u;
+            const uint32_t src_phys = __ldg(&a.words_dec[(size_t)un.s * a.max_blocks_dec + b0]) & id_mask;
+            const float2 tf = __ldg(&a.rope[f]);
+            int m_prev = -1;
+            float2 cs = make_float2(0.f, 0.f);
+#pragma unroll 1
+            for (int k = 0; k < 8; ++k) {
+              const int m = (16 * k) / a.G;
+              if (m != m_prev) {
+                m_prev = m;
+                bool good = false;
+                if (m < nmem) {
+                  const int seq = __ldg(&rec[8 + 4 * m]), bm = __ldg(&rec[8 + 4 * m + 1]);
+                  const int slot = __ldg(&rec[8 + 4 * m + 2]);
+                  good = seq >= 0 && seq < a.B_dec && bm >= 0 && bm <= a.max_blocks_dec - un.nb && slot >= 0 &&
+                         slot < a.num_slots;
+                  if (good) {
+                    const BlockInfo mi = decode_word(__ldg(&a.words_dec[(size_t)seq * a.max_blocks_dec + bm]), bm,
+                                                     a.id_bits);
+                    good = (uint32_t)mi.phys == src_phys;
+                    if (good) cs = rope_cs(tf, __ldg(&a.q_pos[seq]) - mi.p, a.status);
+                  }
+                  if (!good && f == 0) raise_status(a.status, LAZY_DEV_LAYOUT);
+                  if (f == 0) dec_ok[(sg & 3) * 16 + m] = good;
+                }
+                if (!good) cs = make_float2(0.f, 0.f);  // a dropped member's rows are 0
+              }
+              bq[k * (D / 2) + f] = cs;
+            }
+          }
+        } else {
+          const float2 b = rope_cs(__ldg(&a.rope[f]), __ldg(&a.q_start[un.s]) + un.row0, a.status);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) bq[k * (D / 2) + f] = add_angles(b, angle_rows[f * kAngleRows + k]);
+          for (int k = 0; k < 8; ++k) bq[k * (D / 2) + f] = add_angles(b, angle_rows[f * kAngleRows + k]);
+        }
         mbar_arrive(&bcs_ready[sg & 1]);
       }
     };
@@ -686,6 +897,49 @@ __global__ void __launch_bounds__(THREADS, 1)
     // its first segment, 2c+1 for its last), and the thread that completes the row's
     // arrival count merges the pieces.
     auto epilogue = [&](const Pend& pd) -> bool {
+      if constexpr (MIXED) {
+        if (pd.un.dec >= 0) {
+          // Decode unit: tile A's rows (member m = row / G, query head row % G of the
+          // KV head) go to the members' partial slots; tile B repeated them.
+          if (t == 1) return true;
+          if (!warp_wait(&pv_done[0], pd.g_last & 1, a.status)) return false;
+          tc_fence_after();
+          const int* rec = a.items + (size_t)(pd.un.dec / a.Hkv) * LAZY_PLAN_ITEM_INTS;
+          const int nmem = min(__ldg(&rec[4]), BM / a.G), kvh = (2 * pd.un.hp) / a.G;
+          const int m = i / a.G, h = i - m * a.G;
+          const int slot = m < nmem ? __ldg(&rec[8 + 4 * m + 2]) : -1;
+          const bool slot_ok = slot >= 0 && slot < a.num_slots;
+          // a member that failed its checks leaves an empty partial (weight 0 in the merge)
+          const bool good = slot_ok && dec_ok[(pd.sg & 3) * 16 + m];
+          const size_t pidx = ((size_t)(slot_ok ? slot : 0) * a.Hq + (size_t)kvh * a.G + h);
+#pragma unroll 1
+          for (int q = 0; q < 4; ++q) {
+            float o[32];
+            tmem_ld32(tO + lane_base + 32 * q, o);
+            tmem_ld_wait(o);
+            if (slot_ok) {
+              float4* dst = reinterpret_cast<float4*>(a.ws_o + pidx * D + 32 * q);
+#pragma unroll
+              for (int k = 0; k < 32; k += 4)
+                dst[k / 4] = good ? make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+          if (slot_ok)
+            *reinterpret_cast<float2*>(a.ws_ml + 2 * pidx) =
+                good ? make_float2(pd.m_run, pd.l_run) : make_float2(-INFINITY, 0.f);
+          // Count this row as written for its sequence (the merge waits for slots x Hq
+          // rows): each thread fences its own writes, then one lane per sequence in the
+          // warp adds its lanes' rows. No barrier beyond the warp: a warp whose wait gave
+          // up never holds the others.
+          __threadfence();
+          __syncwarp();
+          const int seq = slot_ok ? __ldg(&rec[8 + 4 * m]) : -1;
+          const bool counts = seq >= 0 && seq < a.B_dec;
+          const unsigned same = __match_any_sync(0xffffffffu, counts ? seq : -1);
+          if (counts && (threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(&a.seq_done[seq], __popc(same));
+          return true;
+        }
+      }
       if (!warp_wait(&pv_done[t], pd.g_last & 1, a.status)) return false;
       LAZY_PF_TRACE(pd.sg, 1, global_timer_ns());
       LAZY_PF_TRACE(pd.sg, 3, (unsigned long long)pd.j0 | ((unsigned long long)pd.j1 << 16) |
@@ -797,7 +1051,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       ok = warp_wait(&bcs_ready[sg & 1], (sg >> 1) & 1, a.status) && warp_wait(q_full, sg & 1, a.status);
       if (!ok) return false;
       LAZY_PF_TRACE(sg, 5, global_timer_ns());
-      rotate_q_row_bq(sQ[t], i, base_cs + (sg & 1) * 8 * (D / 2), angle_rows, a.scale_log2);
+      rotate_q_row_bq(sQ[t], i, base_cs + (sg & 1) * 8 * (D / 2), angle_rows, a.scale_log2,
+                      !(MIXED && un.dec >= 0));
       fence_proxy_async_smem();
       mbar_arrive(q_ready);
       LAZY_PF_TRACE(sg, 6, global_timer_ns());
@@ -954,6 +1209,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (!ok) abort_flag = 1;
     LAZY_PF_TRACE(7, 7, global_timer_ns());
   }
+  if constexpr (MIXED) mixed_combine(a, warp, THREADS / 32);
   tc_fence_before();
   __syncthreads();
   LAZY_PF_TRACE(7, 2, global_timer_ns());
@@ -961,6 +1217,25 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
+}
+
+cudaError_t launch_mixed(const MixedArgs& a, const CUtensorMap& qmap, const CUtensorMap& qmap_dec,
+                         const CUtensorMap& kmap, const CUtensorMap& vmap, int grid, cudaStream_t st) {
+  // a decode unit's 16-row groups each hold the query heads of one member: G % 16 == 0
+  if (a.D != D || a.G % 16 != 0) return cudaErrorNotSupported;
+  if (grid <= 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(a.counters, 0, (size_t)(grid + 1) * 2 * BM * sizeof(int), st);
+  if (e == cudaSuccess && a.B_dec > 0) e = cudaMemsetAsync(a.seq_done, 0, (size_t)a.B_dec * sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  auto kern = prefill_stream_kernel<true, false, true>;
+  e = set_smem_once<prefill_stream_kernel<true, false, true>>(SMEM);
+  if (e != cudaSuccess) return e;
+  // Cooperative: the decode merges wait for decode units of other CTAs, which must
+  // therefore all be resident at once (one CTA per SM).
+  MixedArgs ac = a;
+  CUtensorMap mq = qmap, mk = kmap, mv = vmap, mqd = qmap_dec;
+  void* args[] = {&ac, &mq, &mk, &mv, &mqd};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(THREADS), args, SMEM, st);
 }
 
 int prefill_stream_grid() {
@@ -997,13 +1272,13 @@ cudaError_t launch_prefill_stream(const PrefillArgs& a, bool lazy, const CUtenso
     PrefillAlibiArgs aa;
     static_cast<PrefillArgs&>(aa) = a;
     aa.alibi = alibi;
-    prefill_stream_kernel<false, true><<<grid, THREADS, SMEM, st>>>(aa, qmap, kmap, vmap);
+    prefill_stream_kernel<false, true><<<grid, THREADS, SMEM, st>>>(aa, qmap, kmap, vmap, qmap);
     return cudaGetLastError();
   }
   auto kern = lazy ? prefill_stream_kernel<true> : prefill_stream_kernel<false>;
   e = lazy ? set_smem_once<prefill_stream_kernel<true>>(SMEM) : set_smem_once<prefill_stream_kernel<false>>(SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, THREADS, SMEM, st>>>(a, qmap, kmap, vmap);
+  kern<<<grid, THREADS, SMEM, st>>>(a, qmap, kmap, vmap, qmap);  // (no decode units: qmap_dec unused)
   return cudaGetLastError();
 }
 

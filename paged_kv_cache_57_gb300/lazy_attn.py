@@ -37,7 +37,8 @@ EXPORTED = (
     "lazy_attn_materialize", "lazy_attn_rope_table_init_scaled", "lazy_attn_rope_table_init_freqs",
     "lazy_attn_rotary_layout_host", "lazy_attn_decode_shared_alibi", "lazy_attn_alibi_slopes_host",
     "lazy_attn_decode_alibi", "lazy_attn_debug_gather_withheld", "lazy_attn_prefill_alibi",
-    "lazy_attn_decode_shared_partials", "lazy_attn_decode_shared_combine",
+    "lazy_attn_decode_shared_partials", "lazy_attn_decode_shared_combine", "lazy_attn_mixed_workspace_bytes",
+    "lazy_attn_mixed",
 )
 PLAN_MAX_MEMBERS = 16
 PLAN_ITEM_BLOCK_IDS = 32
@@ -94,6 +95,9 @@ _sig = {
     "lazy_attn_alibi_slopes_host": (ctypes.c_int, [_i32, _vp]),
     "lazy_attn_decode_shared_partials": (ctypes.c_int, [_P] + [_vp] * 6 + [_i32, _vp, _i32, _vp, _sz, _vp]),
     "lazy_attn_decode_shared_combine": (ctypes.c_int, [_P, _i32, _vp, _vp, _sz, _vp, _vp]),
+    "lazy_attn_mixed_workspace_bytes": (_sz, [_P, _P, _i32]),
+    "lazy_attn_mixed": (ctypes.c_int, [_P] + [_vp] * 3 + [_i32, _vp, _i32, _vp, _vp, _P] + [_vp] * 3 +
+                        [_i32, _i32] + [_vp] * 6 + [_sz, _vp]),
     "lazy_attn_decode_alibi": (ctypes.c_int, [_P] + [_vp] * 9 + [_vp, _sz, _vp]),
 }
 for _name, (_res, _args) in _sig.items():
@@ -398,6 +402,36 @@ def decode_shared_combine(p: Params, plan: SharedPlan, workspace: torch.Tensor, 
                                               _stream(stream))
     _check(rc, "decode_shared_combine")
     return out
+
+
+def mixed_workspace_bytes(p_dec: Params, p_pf: Params, num_slots: int) -> int:
+    return int(_lib.lazy_attn_mixed_workspace_bytes(ctypes.byref(p_dec), ctypes.byref(p_pf), int(num_slots)))
+
+
+def mixed(p_dec: Params, q_dec: torch.Tensor, words_dec: torch.Tensor, q_pos: torch.Tensor, plan: SharedPlan,
+          p_pf: Params, q_pf: torch.Tensor, cu_seqlens_q: torch.Tensor, q_start: torch.Tensor, max_q_len: int,
+          words_pf: torch.Tensor, seq_lens_pf: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+          rope_table: torch.Tensor, out_dec: Optional[torch.Tensor] = None, out_pf: Optional[torch.Tensor] = None,
+          workspace: Optional[torch.Tensor] = None, stream=None):
+    """One launch: shared-run decode of one batch and prefill of another. Returns (out_dec, out_pf)."""
+    dt = _tdt(p_dec)
+    out_dec = torch.empty_like(q_dec) if out_dec is None else out_dec
+    out_pf = torch.empty_like(q_pf) if out_pf is None else out_pf
+    if workspace is None:
+        workspace = torch.empty(max(1, mixed_workspace_bytes(p_dec, p_pf, plan.num_slots)), dtype=torch.uint8,
+                                device=q_dec.device)
+    wsz = workspace.numel() * workspace.element_size()
+    i32 = torch.int32
+    rc = _lib.lazy_attn_mixed(
+        ctypes.byref(p_dec), _dptr(q_dec, "q_dec", dt), _dptr(words_dec, "words_dec"), _dptr(q_pos, "q_pos", i32),
+        plan.num_items, _dptr(plan.items, "items", i32), plan.num_slots, _dptr(plan.slot_indptr, "slot_indptr", i32),
+        _dptr(out_dec, "out_dec", dt), ctypes.byref(p_pf), _dptr(q_pf, "q_pf", dt),
+        _dptr(cu_seqlens_q, "cu_seqlens_q", i32), _dptr(q_start, "q_start", i32), int(q_pf.shape[0]), int(max_q_len),
+        _dptr(words_pf, "words_pf"), _dptr(seq_lens_pf, "seq_lens_pf", i32), _dptr(out_pf, "out_pf", dt),
+        _dptr(k_pool, "k_pool", dt), _dptr(v_pool, "v_pool", dt), _dptr(rope_table, "rope_table"),
+        _dptr(workspace, "workspace"), wsz, _stream(stream))
+    _check(rc, "mixed")
+    return out_dec, out_pf
 
 
 def alibi_slopes(num_heads: int) -> np.ndarray:
