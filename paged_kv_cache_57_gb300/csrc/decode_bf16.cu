@@ -51,7 +51,7 @@ struct DecodeCfg {
   static constexpr int BOX_BYTES = kBlock * 128;
   static constexpr int KV_BYTES = NBOX * BOX_BYTES;
   static constexpr int STAGE_BYTES = FP8 ? 2 * kBlock * D : 2 * KV_BYTES;
-  static constexpr int CONV_BYTES = FP8 ? 2 * KV_BYTES : 0;
+  static constexpr int CONV_BYTES = FP8 ? KV_BYTES : 0;  // the f16 V tile
   static constexpr int TEAM_BYTES = SPT * STAGE_BYTES + CONV_BYTES;
   static constexpr int ROWS = MT * 16;
   static constexpr int QS_STRIDE = D + 8;  // fp32 q rows, padded against bank conflicts
@@ -321,8 +321,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, SPT>::NTHREADS, MT == 1 ? 3 :
       else __syncwarp();
       if constexpr (FP8) {  // always true here; keeps the D = 128 call out of other instantiations
         if (ok)
-          attend_block_fp8(smem_u32(tst + slot * C::STAGE_BYTES), conv + C::KV_BYTES, ln, qa, nvalid, o, m_r, l_r,
-                           lane, a.k_scale);
+          attend_block_fp8(smem_u32(tst + slot * C::STAGE_BYTES), conv, ln, qa, nvalid, o, m_r, l_r, lane,
+                           a.k_scale);
       }
     } else {
       if (ok) attend_block<D>(smem_u32(tst + slot * C::STAGE_BYTES), ln, qa, nvalid, o, m_r, l_r, lane);

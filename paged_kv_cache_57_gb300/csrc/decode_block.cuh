@@ -55,23 +55,23 @@ __device__ __forceinline__ void load_block_fp8(uint8_t* stage, uint64_t* bar, in
   }
 }
 
-// Converts one landed e4m3 block (K box then V box, 16 rows x 128 bytes, 128-byte
-// swizzle: 16-byte chunk c of row r at r * 128 + ((c ^ r) & 7) * 16) into f16 tiles
-// laid out as the bf16 path's (per 64-column box of 2048 bytes, the same swizzle),
-// so that the ldmatrix fragments of attend_block_impl read them unchanged. Only the
-// V box is converted (K fragments come from the codes directly). Thread tid of nt; a
-// chunk of 16 codes becomes two 16-byte f16 chunks.
+// Converts the V box of one landed e4m3 block (K box then V box, 16 rows x 128 bytes,
+// 128-byte swizzle: 16-byte chunk c of row r at r * 128 + ((c ^ r) & 7) * 16) into
+// an f16 tile at dst laid out as the bf16 path's V tile (per 64-column box of 2048
+// bytes, the same swizzle; 4 KB), so that the ldmatrix fragments of
+// attend_block_impl read it unchanged (K fragments come from the codes directly).
+// Thread tid of nt; a chunk of 16 codes becomes two 16-byte f16 chunks.
 __device__ __forceinline__ void convert_fp8_block(const uint8_t* src, uint8_t* dst, int tid, int nt) {
   using G = BlockGeom<128>;
-  for (int it = kBlock * 8 + tid; it < 2 * kBlock * 8; it += nt) {  // V only: K fragments read the codes
-    const int kv = it >> 7, r = (it >> 3) & 15, c = it & 7;
-    const uint4 x = *reinterpret_cast<const uint4*>(src + kv * (kBlock * 128) + r * 128 + (((c ^ r) & 7) << 4));
+  for (int it = tid; it < kBlock * 8; it += nt) {
+    const int r = it >> 3, c = it & 7;
+    const uint4 x = *reinterpret_cast<const uint4*>(src + kBlock * 128 + r * 128 + (((c ^ r) & 7) << 4));
     uint4 lo, hi;
     e4m3x4_to_f16x4(x.x, lo.x, lo.y);
     e4m3x4_to_f16x4(x.y, lo.z, lo.w);
     e4m3x4_to_f16x4(x.z, hi.x, hi.y);
     e4m3x4_to_f16x4(x.w, hi.z, hi.w);
-    uint8_t* row = dst + kv * G::KV_BYTES + (c >> 2) * G::BOX_BYTES + r * 128;
+    uint8_t* row = dst + (c >> 2) * G::BOX_BYTES + r * 128;
     const int ch = 2 * (c & 3);  // f16 columns 16c .. 16c + 15: chunks ch, ch + 1 of box c / 4
     *reinterpret_cast<uint4*>(row + (((ch ^ r) & 7) << 4)) = lo;
     *reinterpret_cast<uint4*>(row + ((((ch + 1) ^ r) & 7) << 4)) = hi;

@@ -52,17 +52,21 @@ struct SharedCfg {
   using G = BlockGeom<D>;
   static constexpr int RED_STRIDE = D + 4;  // merge rows: o[D], m, l, padding to 16 bytes
   static constexpr int STAGE_BYTES = FP8 ? 2 * kBlock * D : G::STAGE_BYTES;  // e4m3: one byte per element
-  static constexpr int RING_BYTES = kShStages * STAGE_BYTES;
-  // FP8: one f16 tile buffer per team (at most kShWarps teams), the bf16 tile layout
-  static constexpr int CONV_BYTES = FP8 ? kShWarps * G::STAGE_BYTES : 0;
+  // e4m3 blocks are half the size: 12 stages (divisible by 1, 2 and 4 teams) keep
+  // three quarters of the bytes in flight while three CTAs still fit an SM
+  static constexpr int STAGES = FP8 ? 12 : kShStages;
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  // FP8: one f16 V tile per team (at most kShWarps teams), the bf16 tile layout
+  static constexpr int CONV_BYTES = FP8 ? kShWarps * G::KV_BYTES : 0;
   static constexpr int MERGE_BYTES = kShRows * RED_STRIDE * 4;
   static constexpr int BUF_BYTES =
       ((RING_BYTES + CONV_BYTES > MERGE_BYTES ? RING_BYTES + CONV_BYTES : MERGE_BYTES) + 1023) / 1024 * 1024;
   static constexpr int CS_BYTES = kShMembers * (D / 2) * 8;  // (cos, sin) per member and frequency
-  static constexpr int BAR_BYTES = kShStages * 8;
+  static constexpr int BAR_BYTES = STAGES * 8;
   static constexpr int REC_BYTES = kItemInts * 4;
   static constexpr int META_BYTES = 2 * kShMembers * 4;
   static constexpr int SMEM = 1024 + BUF_BYTES + CS_BYTES + BAR_BYTES + REC_BYTES + META_BYTES;
+  static_assert(!FP8 || 3 * SMEM <= 227 * 1024, "three e4m3 CTAs per SM");
 };
 
 }  // namespace
@@ -117,7 +121,7 @@ __global__ void __launch_bounds__(kShThreads, 3)
   uint8_t* ring = align1024(smem_raw);
   float2* cs_tab = reinterpret_cast<float2*>(ring + C::BUF_BYTES);
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + C::BUF_BYTES + C::CS_BYTES);
-  int* rec = reinterpret_cast<int*>(full + kShStages);  // the item record
+  int* rec = reinterpret_cast<int*>(full + C::STAGES);  // the item record
   int* m_delta = rec + kItemInts;                        // rotation offset of each member
   int* m_ok = m_delta + kShMembers;                      // member passed its checks
   __shared__ int abort_flag;
@@ -135,7 +139,7 @@ __global__ void __launch_bounds__(kShThreads, 3)
         __ldg(reinterpret_cast<const int4*>(a.items) + (size_t)item * (kItemInts / 4) + threadIdx.x);
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int i = 0; i < kShStages; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < C::STAGES; ++i) mbar_init(&full[i], 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -211,13 +215,13 @@ __global__ void __launch_bounds__(kShThreads, 3)
 
   // ------------------------------------------------------------ teams and first loads
   const int TEAMS = kShWarps / RT;
-  const int NS = kShStages / TEAMS;  // ring stages of each team: 2, 4 or 8
+  const int NS = C::STAGES / TEAMS;  // ring stages of each team: 2, 4 or 8 (twice that for e4m3)
   const int team = warp / RT;
   const int per_team = (nblk + TEAMS - 1) / TEAMS;
   const int kb0 = team * per_team;
   const int nk = max(0, min(nblk, kb0 + per_team) - kb0);  // blocks of this team
   uint8_t* tst = ring + team * NS * C::STAGE_BYTES;
-  uint8_t* tconv = ring + C::RING_BYTES + team * G::STAGE_BYTES;  // FP8: the team's f16 tile buffer
+  uint8_t* tconv = ring + C::RING_BYTES + team * G::KV_BYTES;  // FP8: the team's f16 V tile
   auto issue = [&](uint8_t* stage, uint64_t* bar, int phys) {
     if constexpr (FP8) load_block_fp8(stage, bar, phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
     else load_block_3d<D>(stage, bar, phys, a.num_pool_blocks, a.Hkv, kvh, &kmap, &vmap);
@@ -378,8 +382,7 @@ __global__ void __launch_bounds__(kShThreads, 3)
       if (RT > 1) ok = team_and(team, 32 * RT, ok);
       else __syncwarp();
       if (ok)
-        attend_block_fp8(smem_u32(stage), smem_u32(tconv) + G::KV_BYTES, ln, qa, nvalid, o, m_r, l_r, lane,
-                         a.k_scale);
+        attend_block_fp8(smem_u32(stage), smem_u32(tconv), ln, qa, nvalid, o, m_r, l_r, lane, a.k_scale);
     } else if (ok) {
       if constexpr (ALIBI) {
         const int j0 = kBlock * (kb0 + k);
