@@ -557,18 +557,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         LAZY_PF_TRACE_IF(lane == 0, sg, 4, global_timer_ns());
         if (dec) {
           if constexpr (MIXED) {
-            // Decode unit: row r = member (r / G) x query head (r % G) of this KV head;
-            // both tiles get the same rows (tile B's results are not kept).
+            // Decode unit: tile A's row r = member (r / G) x query head (r % G) of this KV
+            // head; tile B idles through the unit.
             const int* rec = a.items + (size_t)(un.dec / a.Hkv) * LAZY_PLAN_ITEM_INTS;
             const int nmem = min(__ldg(&rec[4]), BM / a.G);
             if (lane == 0) {
-              mbar_arrive_expect_tx(q_full, 2u * (uint32_t)nmem * (uint32_t)a.G * 256u);
-              for (int t = 0; t < 2; ++t)
-                for (int m = 0; m < nmem; ++m) {
-                  const int seq = min(max(__ldg(&rec[8 + 4 * m]), 0), a.B_dec - 1);
-                  tma_load_3d(sQ[t] + m * a.G * 128, &qmap_dec, q_full, 0, kvh * a.G, seq);
-                  tma_load_3d(sQ[t] + HALF + m * a.G * 128, &qmap_dec, q_full, 64, kvh * a.G, seq);
-                }
+              mbar_arrive_expect_tx(q_full, (uint32_t)nmem * (uint32_t)a.G * 256u);
+              for (int m = 0; m < nmem; ++m) {
+                const int seq = min(max(__ldg(&rec[8 + 4 * m]), 0), a.B_dec - 1);
+                tma_load_3d(sQ[0] + m * a.G * 128, &qmap_dec, q_full, 0, kvh * a.G, seq);
+                tma_load_3d(sQ[0] + HALF + m * a.G * 128, &qmap_dec, q_full, 64, kvh * a.G, seq);
+              }
             }
           }
         } else if (lane == 0) {
@@ -695,12 +694,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                     (acc || ks > 0) ? 1u : 0u);
         tc_commit(&pv_done[t]);
       };
-      int g = 0;  // tiles whose S has been issued == tiles started
+      int g = 0;   // tiles whose S has been issued == tiles started
+      int gb = 0;  // tiles tile B has taken part in (it idles through decode units)
       bool ok = true;
       for_segments([&](int u, const UnitDesc& un, int j0, int j1, int U0, int sg, bool, const UnitDesc&) {
         (void)u;
-        (void)un;
         (void)U0;
+        const bool two = !(MIXED && un.dec >= 0);  // both tiles (prefill) or tile A only (decode)
         // The segment's first S pair: its Q is rotated. S_t overwrites P_t of the previous
         // tile, whose P V was issued earlier by this thread: one thread's MMAs execute in
         // issue order, so that P V has read P_t before S_t writes the columns.
@@ -708,7 +708,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!ok) return false;
         tc_fence_after();
         issue_s(g, 0);
-        issue_s(g, 1);
+        if (two) issue_s(g, 1);
         LAZY_PF_TRACE_IF(true, sg, 7, global_timer_ns());
         tc_commit(&k_empty[g % NK]);
         if (j1 - j0 == 1) tc_commit(q_empty);  // the segment's last S product is issued
@@ -731,19 +731,22 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_after();
             issue_s(g + 1, 0);
           }
-          LAZY_PF_CLK(c4);
-          ok = mbar_wait(&p_full[1], g & 1, a.status);
-          LAZY_PF_CLK(c5);
-          LAZY_PF_COUNT(6, c5 - c4);
-          if (!ok) return false;
-          tc_fence_after();
-          issue_pv(g, 1, j > j0);
+          if (two) {
+            LAZY_PF_CLK(c4);
+            ok = mbar_wait(&p_full[1], gb & 1, a.status);
+            LAZY_PF_CLK(c5);
+            LAZY_PF_COUNT(6, c5 - c4);
+            if (!ok) return false;
+            tc_fence_after();
+            issue_pv(g, 1, j > j0);
+          }
           tc_commit(&v_empty[g % NV]);
           if (more) {
-            issue_s(g + 1, 1);
+            if (two) issue_s(g + 1, 1);
             tc_commit(&k_empty[(g + 1) % NK]);
             if (j + 2 == j1) tc_commit(q_empty);  // the segment's last S product is issued
           }
+          if (two) ++gb;
         }
         return true;
       });
@@ -828,7 +831,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int i = threadIdx.x & 127;  // query row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t tS = tmem + 128 * t, tO = tmem + 256 + 128 * t;
-    int g = 0;
+    // g counts every tile (the K/V rings' phases); gt the tiles this query tile took part
+    // in (its own barriers' phases; tile B idles through decode units of a mixed launch)
+    int g = 0, gt = 0;
     bool ok = true;
     // Angles of the 8 row multiples of 16 of segment sg's tiles (its base angle added),
     // into buffer sg & 1. Computed one segment ahead; rewriting a buffer for segment
@@ -1051,8 +1056,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       ok = warp_wait(&bcs_ready[sg & 1], (sg >> 1) & 1, a.status) && warp_wait(q_full, sg & 1, a.status);
       if (!ok) return false;
       LAZY_PF_TRACE(sg, 5, global_timer_ns());
-      rotate_q_row_bq(sQ[t], i, base_cs + (sg & 1) * 8 * (D / 2), angle_rows, a.scale_log2,
-                      !(MIXED && un.dec >= 0));
+      // Tile B idles through a decode unit (its Q buffer is not loaded), but still
+      // counts in the segment's Q handshake.
+      const bool idle = MIXED && un.dec >= 0 && t == 1;
+      if (!idle)
+        rotate_q_row_bq(sQ[t], i, base_cs + (sg & 1) * 8 * (D / 2), angle_rows, a.scale_log2,
+                        !(MIXED && un.dec >= 0));
       fence_proxy_async_smem();
       mbar_arrive(q_ready);
       LAZY_PF_TRACE(sg, 6, global_timer_ns());
@@ -1062,11 +1071,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         pend.valid = false;
         if (!ok) return false;
       }
+      if (idle) {
+        g += j1 - j0;
+        return true;
+      }
       float m_run = -INFINITY, l_run = 0.f;
-      for (int j = j0; j < j1; ++j, ++g) {
+      for (int j = j0; j < j1; ++j, ++g, ++gt) {
         const int vs = g % NV;
         LAZY_PF_CLK(k0);
-        ok = warp_wait(&s_full[t], g & 1, a.status) && warp_wait(&v_full[vs], (g / NV) & 1, a.status);
+        ok = warp_wait(&s_full[t], gt & 1, a.status) && warp_wait(&v_full[vs], (g / NV) & 1, a.status);
         LAZY_PF_CLK(k1);
         if (!ok) return false;
         if (j == j0) LAZY_PF_TRACE(sg, 0, global_timer_ns());
@@ -1202,7 +1215,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
 #endif
       }
-      pend = Pend{un, j0, j1, U0, g - 1, sg, m_run, l_run, true};
+      pend = Pend{un, j0, j1, U0, gt - 1, sg, m_run, l_run, true};
       return true;
     });
     if (ok && pend.valid) ok = epilogue(pend);
