@@ -41,6 +41,17 @@ namespace {
 using namespace pf;
 
 constexpr int NK = 2, NV = 2;
+
+// Rotation coefficients (cos, sin) (p w_f) of frequencies 8 c .. 8 c + 7, for a K block
+// at position p (the table's first D / 2 entries are the frequencies in turns). Out of
+// line: the position changes only at document boundaries.
+__device__ __noinline__ Rot8 block_rot8(const float2* __restrict__ rope, int c, int p, unsigned int* status) {
+  float2 cs[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) cs[e] = rope_cs(__ldg(&rope[8 * c + e]), p, status);
+  return make_rot8(cs, 1.f);
+}
+
 constexpr int THREADS = 480;  // 15 warps
 // A tile's fp32 partial: 33 column groups x 128 rows x 4 floats (groups 0..31: o
 // columns 4c..4c+3; group 32: m, l). Thread = row, so every float4 access of a warp
@@ -57,7 +68,7 @@ constexpr int OFF_V = OFF_K + NK * TILE;
 constexpr int OFF_KMETA = OFF_V + NV * TILE;
 constexpr int OFF_VMETA = OFF_KMETA + NK * BLOCKS * (int)sizeof(KMeta);
 constexpr int OFF_BAR = OFF_VMETA + NV * BLOCKS * (int)sizeof(VMeta);
-constexpr int NBARS = 3 + 3 * NK + 3 * NV + 7 + 2;
+constexpr int NBARS = 3 + 3 * NK + 3 * NV + 7 + 2 + 2;
 // float2 [2][8][64]: per segment parity, angles of rows 16 k of both Q tiles (the
 // segment's base angle already added); then float2 [64][24]: angles of row offsets.
 constexpr int OFF_QCS = (OFF_BAR + NBARS * 8 + 15) & ~15;
@@ -315,6 +326,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* pv_done = p_full + 2;    // [2]
   uint64_t* mma_drain = pv_done + 2;
   uint64_t* bcs_ready = mma_drain + 1;  // [2]: base angles of segment parity 0 / 1 written
+  uint64_t* p_half = bcs_ready + 2;     // [2]: P of a tile's first 64 keys written (tile A, B)
   float2* base_cs = reinterpret_cast<float2*>(base + OFF_QCS);
   float2* angle_rows = reinterpret_cast<float2*>(base + OFF_ROWS);
   Sched* sched = reinterpret_cast<Sched*>(base + OFF_SCHED);
@@ -345,6 +357,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 128);
+      mbar_init(&p_half[t], 128);
       mbar_init(&pv_done[t], 1);
     }
     mbar_init(mma_drain, 1);
@@ -686,13 +699,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc_commit(&s_full[t]);
       };
-      auto issue_pv = [&](int g, int t, bool acc) {
+      // P V over the 64 keys from 16 ks0 (P_t: 8 TMEM columns, 16 keys, per k-step); the
+      // second half commits pv_done.
+      auto issue_pv = [&](int g, int t, bool acc, int ks0) {
         const uint64_t v0 = dV + (uint64_t)(((g % NV) * TILE) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks)  // P_t: 8 TMEM columns (16 keys) per k-step
+        for (int k = 0; k < BN / 32; ++k) {
+          const int ks = ks0 + k;
           tc_mma_ta(tmem + 256 + 128 * t, tmem + 128 * t + 8 * ks, v0 + (uint32_t)(ks * 2048 >> 4), idO,
                     (acc || ks > 0) ? 1u : 0u);
-        tc_commit(&pv_done[t]);
+        }
+        if (ks0 > 0) tc_commit(&pv_done[t]);
       };
       int g = 0;   // tiles whose S has been issued == tiles started
       int gb = 0;  // tiles tile B has taken part in (it idles through decode units)
@@ -714,14 +731,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (j1 - j0 == 1) tc_commit(q_empty);  // the segment's last S product is issued
         for (int j = j0; j < j1; ++j, ++g) {
           const bool more = j + 1 < j1;
+          // V(g) before P_A(g): each wait on a shared-memory barrier takes a round trip
+          // that the tensor core's operand reads make long, and V(g) is usually ready
+          // first. (v_ready is arrived only after V(g) has landed, so it covers v_full.)
+          // P V of each tile in two halves: the first 64 keys' P is handed over while the
+          // softmax still computes the rest, so its products run meanwhile.
           LAZY_PF_CLK(c0);
-          ok = mbar_wait(&p_full[0], g & 1, a.status) && mbar_wait(&v_full[g % NV], (g / NV) & 1, a.status) &&
-               mbar_wait(&v_ready[g % NV], (g / NV) & 1, a.status);
+          ok = mbar_wait(&v_ready[g % NV], (g / NV) & 1, a.status) && mbar_wait(&p_half[0], g & 1, a.status);
+          if (!ok) return false;
+          tc_fence_after();
+          issue_pv(g, 0, j > j0, 0);
+          ok = mbar_wait(&p_full[0], g & 1, a.status);
           LAZY_PF_CLK(c1);
           LAZY_PF_COUNT(5, c1 - c0);
           if (!ok) return false;
           tc_fence_after();
-          issue_pv(g, 0, j > j0);
+          issue_pv(g, 0, j > j0, BN / 32);
           if (more) {  // S_A(g+1) overwrites P_A(g), read by PV_A(g) issued just above (in order)
             LAZY_PF_CLK(c2);
             ok = mbar_wait(&k_ready[(g + 1) % NK], ((g + 1) / NK) & 1, a.status);
@@ -733,12 +758,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           if (two) {
             LAZY_PF_CLK(c4);
+            ok = mbar_wait(&p_half[1], gb & 1, a.status);
+            if (!ok) return false;
+            tc_fence_after();
+            issue_pv(g, 1, j > j0, 0);
             ok = mbar_wait(&p_full[1], gb & 1, a.status);
             LAZY_PF_CLK(c5);
             LAZY_PF_COUNT(6, c5 - c4);
             if (!ok) return false;
             tc_fence_after();
-            issue_pv(g, 1, j > j0);
+            issue_pv(g, 1, j > j0, BN / 32);
           }
           tc_commit(&v_empty[g % NV]);
           if (more) {
@@ -760,12 +789,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------------------------------------------------------- Q prologue, K rotation, V holes
     const int r = threadIdx.x - 256;  // 0..127
     const int c = r & 7, rb = r >> 3;  // 16-byte chunk (8 frequencies) and row within a block
-    float2 tr[8];
     Rot8 rot;
-    if constexpr (LAZY) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) tr[e] = __ldg(&a.rope[8 * c + e]);
-    }
     int p_cached = INT_MIN;
     int g = 0;
     bool ok = true;
@@ -778,26 +802,41 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int st = g % NK;
         if (!warp_wait(&k_full[st], (g / NK) & 1, a.status)) return ok = false;
         uint8_t* kt = sK + st * TILE;
+        // The tile's block records and its data are read up front, four blocks' chunks
+        // per round: shared-memory loads wait long behind the tensor core's operand
+        // reads, so they are issued together rather than one block at a time.
+        KMeta km[BLOCKS];
         bool holes = false;
-#pragma unroll 1
-        for (int bl = 0; bl < BLOCKS; ++bl) {
-          const KMeta m = kmeta[st * BLOCKS + bl];
-          holes |= m.nvalid < kBlock;
-          if constexpr (LAZY) {
-            if (m.nvalid > 0 && !(MIXED && un.dec >= 0)) {  // decode units: K as stored
-              if (m.p != p_cached) {
-                float2 cs[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) cs[e] = rope_cs(tr[e], m.p, a.status);
-                rot = make_rot8(cs, 1.f);
-                p_cached = m.p;
+        for (int bl = 0; bl < BLOCKS; ++bl) {
+          km[bl] = kmeta[st * BLOCKS + bl];
+          holes |= km[bl].nvalid < kBlock;
+        }
+        if constexpr (LAZY) {
+          if (!(MIXED && un.dec >= 0)) {  // decode units: K as stored
+#pragma unroll 1
+            for (int h = 0; h < BLOCKS; h += 4) {
+              uint4 X[4], Y[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const uint32_t off = (h + u) * (kBlock * 128) + sw128(rb, c);
+                X[u] = *reinterpret_cast<const uint4*>(kt + off);
+                Y[u] = *reinterpret_cast<const uint4*>(kt + HALF + off);
               }
-              const uint32_t off = bl * (kBlock * 128) + sw128(rb, c);
-              uint4 X = *reinterpret_cast<uint4*>(kt + off);
-              uint4 Y = *reinterpret_cast<uint4*>(kt + HALF + off);
-              rotate_chunk(X, Y, rot);
-              *reinterpret_cast<uint4*>(kt + off) = X;
-              *reinterpret_cast<uint4*>(kt + HALF + off) = Y;
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const KMeta m = h == 0 ? km[u] : km[4 + u];
+                if (m.nvalid > 0) {
+                  if (m.p != p_cached) {
+                    rot = block_rot8(a.rope, c, m.p, a.status);
+                    p_cached = m.p;
+                  }
+                  rotate_chunk(X[u], Y[u], rot);
+                  const uint32_t off = (h + u) * (kBlock * 128) + sw128(rb, c);
+                  *reinterpret_cast<uint4*>(kt + off) = X[u];
+                  *reinterpret_cast<uint4*>(kt + HALF + off) = Y[u];
+                }
+              }
             }
           }
         }
@@ -1039,6 +1078,28 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       return true;
     };
+    // A K tile's masks for this row: the valid keys of each of its blocks (8 bits per
+    // block; holes, and the causal limit inside the chunk), whether all its keys are
+    // valid for every row, and (ALiBi) each block's bias slope (n0 - m_i) in log2 units.
+    struct TileMask {
+      uint64_t lim;
+      bool full;
+      float b0[ALIBI ? BLOCKS : 1];
+    };
+    auto read_mask = [&](int vs, int iq, float slope2, int m_row) {
+      TileMask tm;
+      tm.lim = 0;
+      tm.full = true;
+#pragma unroll
+      for (int bl = 0; bl < BLOCKS; ++bl) {
+        const VMeta m = vmeta[vs * BLOCKS + bl];
+        tm.full &= (m.nvalid == kBlock) & (m.chunk_j0 < 0);
+        const int l = m.chunk_j0 >= 0 ? max(0, min(m.nvalid, iq - m.chunk_j0 + 1)) : m.nvalid;
+        tm.lim |= (uint64_t)(uint32_t)l << (8 * bl);
+        if constexpr (ALIBI) tm.b0[bl] = slope2 * (float)(m.pos - m_row);
+      }
+      return tm;
+    };
     for_segments([&](int u, const UnitDesc& un, int j0, int j1, int U0, int sg, bool has_next,
                      const UnitDesc& next_un) {
       (void)u;
@@ -1076,42 +1137,39 @@ __global__ void __launch_bounds__(THREADS, 1)
         return true;
       }
       float m_run = -INFINITY, l_run = 0.f;
+      // The key limits of a tile are read from its V metadata one tile ahead, while the
+      // tensor core still computes its S: shared-memory loads wait long behind the
+      // products' operand reads, and this keeps them off the softmax's path.
+      if (!warp_wait(&v_full[g % NV], (g / NV) & 1, a.status)) return ok = false;
+      TileMask tm = read_mask(g % NV, iq, slope2, m_row);
       for (int j = j0; j < j1; ++j, ++g, ++gt) {
-        const int vs = g % NV;
         LAZY_PF_CLK(k0);
-        ok = warp_wait(&s_full[t], gt & 1, a.status) && warp_wait(&v_full[vs], (g / NV) & 1, a.status);
+        ok = warp_wait(&s_full[t], gt & 1, a.status);
         LAZY_PF_CLK(k1);
         if (!ok) return false;
         if (j == j0) LAZY_PF_TRACE(sg, 0, global_timer_ns());
         tc_fence_after();
-        // Per-block key limits for this row (holes; causal inside the chunk).
-        int lim[BLOCKS];
-        bool full_tile = true;
-#pragma unroll
-        for (int bl = 0; bl < BLOCKS; ++bl) {
-          const VMeta m = vmeta[vs * BLOCKS + bl];
-          full_tile &= (m.nvalid == kBlock) & (m.chunk_j0 < 0);
-          lim[bl] = m.chunk_j0 >= 0 ? max(0, min(m.nvalid, iq - m.chunk_j0 + 1)) : m.nvalid;
-        }
+        const bool full_tile = tm.full;
+        // Valid keys of block b for this row (holes; causal inside the chunk).
+        auto limb = [&](int b) { return (int)((tm.lim >> (8 * b)) & 0xffu); };
         // ALiBi bias of key k (0..31) of chunk q (blocks 2q, 2q + 1): slope (n - m_i) =
         // b0 + slope (k & 15), with b0 = slope (n0 - m_i) of the key's block.
         auto bias0 = [&](int q, int h2) {
-          return slope2 * (float)(vmeta[vs * BLOCKS + 2 * q + h2].pos - m_row);
+          const int b = 2 * q + h2;
+          float r = tm.b0[0];
+#pragma unroll
+          for (int e = 1; e < BLOCKS; ++e) r = b == e ? tm.b0[e] : r;
+          return r;
         };
-        // Pass 1: row maximum.
-        float mx = -INFINITY;
-#pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-          float sv[32];
-          tmem_ld32(tS + lane_base + 32 * q, sv);
-          tmem_ld_wait(sv);
+        // Maximum of chunk q (keys 32 q .. 32 q + 31) over the row's valid keys. ALiBi: an
+        // upper bound of the biased maximum, each block's largest score plus the largest
+        // bias in the block, b0 + max(0, 15 slope). It exceeds the exact maximum by at
+        // most 15 |slope| (log2 units), so the second pass's weights shrink by at most
+        // that factor, far inside fp32 and bf16 range; the softmax itself is unchanged.
+        auto chunk_max = [&](const float(&sv)[32], int q) {
           if constexpr (ALIBI) {
-            // An upper bound of the biased maximum: each block's largest score plus the
-            // largest bias in the block, b0 + max(0, 15 slope). It exceeds the exact
-            // maximum by at most 15 |slope| (log2 units), so the second pass's weights
-            // shrink by at most that factor, far inside fp32 and bf16 range; the
-            // softmax itself is unchanged.
             const float kmax = fmaxf(0.f, 15.f * slope2);
+            float mx = -INFINITY;
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
               float mb = -INFINITY;
@@ -1119,26 +1177,54 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int k = 0; k < 16; k += 2) mb = fmax3(mb, sv[16 * h2 + k], sv[16 * h2 + k + 1]);
               } else {
+                const int l = limb(2 * q + h2);
 #pragma unroll
                 for (int k = 0; k < 16; ++k)
-                  if (k < lim[2 * q + h2]) mb = fmaxf(mb, sv[16 * h2 + k]);
+                  if (k < l) mb = fmaxf(mb, sv[16 * h2 + k]);
               }
               mx = fmaxf(mx, mb + (bias0(q, h2) + kmax));
             }
-            continue;
-          }
-          if (full_tile) {
-            float m2[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-            for (int k = 0; k < 32; k += 4) {
-              m2[0] = fmax3(m2[0], sv[k], sv[k + 1]);
-              m2[1] = fmax3(m2[1], sv[k + 2], sv[k + 3]);
-            }
-            mx = fmax3(mx, m2[0], m2[1]);
+            return mx;
           } else {
+            if (full_tile) {  // four independent chains
+              float m4[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+              for (int k = 4; k < 28; k += 8) {
+                m4[0] = fmax3(m4[0], sv[k], sv[k + 1]);
+                m4[1] = fmax3(m4[1], sv[k + 2], sv[k + 3]);
+                m4[2] = fmax3(m4[2], sv[k + 4], sv[k + 5]);
+                m4[3] = fmax3(m4[3], sv[k + 6], sv[k + 7]);
+              }
+              m4[0] = fmax3(m4[0], sv[28], sv[29]);
+              m4[1] = fmax3(m4[1], sv[30], sv[31]);
+              return fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+            }
+            float mx = -INFINITY;
+            const int l0 = limb(2 * q), l1 = limb(2 * q + 1);
 #pragma unroll
             for (int k = 0; k < 32; ++k)
-              if ((k & 15) < lim[2 * q + (k >> 4)]) mx = fmaxf(mx, sv[k]);
+              if ((k & 15) < (k < 16 ? l0 : l1)) mx = fmaxf(mx, sv[k]);
+            return mx;
+          }
+        };
+        // Pass 1: row maximum, two chunks per TMEM wait (one where registers are short).
+        float mx = -INFINITY;
+        if constexpr (ALIBI || MIXED) {
+#pragma unroll 1
+          for (int q = 0; q < 4; ++q) {
+            float sv[32];
+            tmem_ld32(tS + lane_base + 32 * q, sv);
+            tmem_ld_wait(sv);
+            mx = fmaxf(mx, chunk_max(sv, q));
+          }
+        } else {
+#pragma unroll 1
+          for (int q = 0; q < 4; q += 2) {
+            float sv[32], sw[32];
+            tmem_ld32(tS + lane_base + 32 * q, sv);
+            tmem_ld32(tS + lane_base + 32 * (q + 1), sw);
+            tmem_ld_wait(sv, sw);
+            mx = fmax3(mx, chunk_max(sv, q), chunk_max(sw, q + 1));
           }
         }
         // Refresh the running maximum only when it grows by more than 2^8 (weights stay <= 256).
@@ -1148,6 +1234,20 @@ __global__ void __launch_bounds__(THREADS, 1)
           m_run = mx;
         }
         const float m_use = m_run == -INFINITY ? 0.f : m_run;
+        // Rescale the running output when this row's maximum was refreshed (warp-uniform),
+        // before any of this tile's P V; PV_t(g-1) has completed, since S_t(g) was issued
+        // after it.
+        if (j > j0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int q = 0; q < 4; ++q) {
+            float o[32];
+            tmem_ld32(tO + lane_base + 32 * q, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] *= alpha;
+            tmem_st32(tO + lane_base + 32 * q, o);
+          }
+        }
         LAZY_PF_CLK(k2);
         // Pass 2: weights -> bf16 P over S's first 64 columns (chunk q's 16 words land on
         // columns already read), row sum in fp32.
@@ -1159,9 +1259,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld32(tS + lane_base + 32 * q, sv);
           tmem_ld_wait(sv);
           if (!full_tile) {
+            const int l0 = limb(2 * q), l1 = limb(2 * q + 1);
 #pragma unroll
             for (int k = 0; k < 32; ++k)
-              if ((k & 15) >= lim[2 * q + (k >> 4)]) sv[k] = -INFINITY;
+              if ((k & 15) >= (k < 16 ? l0 : l1)) sv[k] = -INFINITY;
           }
           // ALiBi: the bias moves into the subtrahend, m - b0 - slope (k & 15), stepped
           // by 2 slope from pair to pair of a block.
@@ -1184,26 +1285,22 @@ __global__ void __launch_bounds__(THREADS, 1)
             acc = f2_add(acc, f2(e0, e1));
           }
           tmem_st16(tS + lane_base + 16 * q, pw);
+          if (q == 1) {  // the first 64 keys' P (and any rescaled O) are in TMEM
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&p_half[t]);
+          }
         }
         const float2 sa = f2_split(acc);
         l_run = l_run * alpha + (sa.x + sa.y);
         LAZY_PF_CLK(k3);
-        // Rescale the running output when this row's maximum was refreshed (warp-uniform);
-        // PV_t(g-1) has completed, since S_t(g) was issued after it.
-        if (j > j0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-          for (int q = 0; q < 4; ++q) {
-            float o[32];
-            tmem_ld32(tO + lane_base + 32 * q, o);
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] *= alpha;
-            tmem_st32(tO + lane_base + 32 * q, o);
-          }
-        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&p_full[t]);
+        if (j + 1 < j1) {
+          if (!warp_wait(&v_full[(g + 1) % NV], ((g + 1) / NV) & 1, a.status)) return ok = false;
+          tm = read_mask((g + 1) % NV, iq, slope2, m_row);
+        }
 #ifdef LAZY_PREFILL_TRACE
         if (threadIdx.x == 0) {
           LAZY_PF_CLK(k4);
