@@ -42,7 +42,7 @@ WORKLOAD = "llama8b_decode"
 NCU_TRAFFIC = {"sources": ["paged_kv_cache_57_gb300/csrc/decode_shared.cu",
                            "paged_kv_cache_57_gb300/csrc/decode_block.cuh",
                            "paged_kv_cache_57_gb300/csrc/common.cuh"],
-               "sha16": "4d57f666d092d81a", "bytes_per_launch": 302178560 + 9623040}
+               "sha16": "54297fb7bc4f9285", "bytes_per_launch": 302164480 + 9733632}
 
 
 def _traffic_if_current():
