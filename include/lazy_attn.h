@@ -74,7 +74,7 @@ typedef struct CUstream_st *lazy_stream_t; /* same type as cudaStream_t; NULL = 
 typedef enum {
   LAZY_OK = 0,
   LAZY_ERR_INVALID_ARG = 1, /* null pointer, bad size or head count */
-  LAZY_ERR_UNSUPPORTED = 2, /* a shape or dtype this build has no kernel for */
+  LAZY_ERR_UNSUPPORTED = 2, /* a shape or dtype the library has no kernel for */
   LAZY_ERR_WORKSPACE = 3,   /* workspace or table buffer too small */
   LAZY_ERR_LAYOUT = 4,      /* documents/blocks do not form a valid block table */
   LAZY_ERR_CUDA = 5,        /* a CUDA call or launch failed */
