@@ -487,9 +487,11 @@ int lazy_attn_plan_shared_host(const lazy_attn_params* p, int32_t num_docs, cons
   // gives about one item per resident CTA.
   const int cb = chunk_blocks > 0 ? chunk_blocks : (cap == 128 ? 0 : 32);
   const int auto_items = std::max(1, lazy::kSharedTcSlots / std::max(1, p->num_kv_heads));
+  // small items spread through the launch: measured for the bf16 mma.sync kernel only
+  const bool spread = !kv_fp8(p) && cap == 64;
   return lazy::plan_shared_host(p->num_seqs, c.G, cap, p->max_blocks_per_seq, p->num_pool_blocks, num_docs,
                                 seg_indptr, seg_doc, seg_len, doc_block_indptr, doc_blocks, cb, auto_items, capacity,
-                                items, slot_indptr, counts);
+                                items, slot_indptr, counts, spread);
 }
 
 size_t lazy_attn_decode_shared_workspace_bytes(const lazy_attn_params* p, int32_t num_slots) {

@@ -180,11 +180,12 @@ constexpr int kSharedTcSlots = 2 * 152;
 
 // Host planner of the shared-run decode (shared_plan.cu). counts = {items, slots}.
 // chunk_blocks <= 0 picks the chunk from the batch: about auto_items items in all,
-// 32 to 256 blocks in multiples of 4.
+// 32 to 256 blocks in multiples of 4. Items run longest first; with spread_small,
+// items of at most 8 blocks are spread evenly through the order instead.
 int plan_shared_host(int B, int G, int rows_cap, int max_blocks, int num_pool_blocks, int num_docs, const int32_t* seg_indptr,
                      const int32_t* seg_doc, const int32_t* seg_len, const int32_t* doc_block_indptr,
                      const int32_t* doc_blocks, int chunk_blocks, int auto_items, int capacity, int32_t* items,
-                     int32_t* slot_indptr, int32_t* counts);
+                     int32_t* slot_indptr, int32_t* counts, bool spread_small = false);
 
 // Every launcher returns the cudaError_t of its launch.
 // explicit_w (host, head_dim/2 rates in radians per position) overrides theta and scaling.
