@@ -93,3 +93,28 @@ def test_fp8_argument_rules_without_cuda():
     assert L._lib.lazy_attn_materialize(ctypes.byref(p), *([fake] * 8), None) == un
     assert L._lib.lazy_attn_decode_alibi(ctypes.byref(params(key_positions=True)), *([fake] * 7), fake, fake, fake,
                                          1 << 20, None) == un
+
+
+def test_fp8_plan_keeps_longest_first_and_bf16_plan_spreads_small_items():
+    """The planner's item order for the same batch: with e4m3 params the items run
+    longest first; with bf16 params (mma.sync kernel) the items of at most 8 blocks
+    (the 64-token private tails here) are spread through the order instead of ending it."""
+    from paged_kv_cache_57_gb300 import lazy_attn as L
+    w = W.decode_zipf("planord", batch=16, hq=32, hkv=8, d=128, docs_per_seq=4, doc_tokens=512, pool_docs=24,
+                      zipf_s=1.0, suffix_tokens=64, seed=77)
+
+    def plan(**kw):
+        p = L.make_params(num_seqs=w.num_seqs, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                          head_dim=w.head_dim, num_pool_blocks=w.num_pool_blocks,
+                          max_blocks_per_seq=w.max_blocks_per_seq, dtype="bf16", rope_theta=w.rope_theta, **kw)
+        items, _ = L.plan_shared_host(p, len(w.doc_len), w.seg_indptr, w.seg_doc, w.seg_len, w.doc_block_indptr,
+                                      w.doc_blocks)
+        return items[:, 2]
+
+    nb8 = plan(kv_dtype="fp8_e4m3", k_scale=1.0, v_scale=1.0)
+    assert (np.diff(nb8) <= 0).all()
+    nb16 = plan()
+    small = np.flatnonzero(nb16 <= 8)
+    assert 0 < len(small) < len(nb16)
+    assert sorted(nb16.tolist()) == sorted(nb8.tolist())  # the same items, another order
+    assert small[0] < len(nb16) // 2 and (np.diff(nb16[nb16 > 8]) <= 0).all()
