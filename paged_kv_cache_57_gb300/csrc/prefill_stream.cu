@@ -21,7 +21,10 @@
 //               segment R_m of the row of Q (angle addition from per-segment angles
 //               of the 16-row multiples); softmax: S read from TMEM in 32-column
 //               chunks twice (row maximum, then weights); P written back as bf16
-//               over the tile's S columns (A operand of P V from TMEM); epilogue.
+//               over the tile's S columns (A operand of P V from TMEM), the first 64
+//               keys' P handed over before the rest; the next K tile's key masks
+//               read right after (shared-memory loads wait long while the S
+//               products stream their operands); epilogue.
 //   warps 8-11  per K tile, R_p of each 16-row block and V hole zeroing.
 //   warp 12     TMA producer of Q and the K ring; warp 14 of the V ring. A tile is
 //               16 boxes of 16 rows x 64 columns issued by 16 lanes.
