@@ -35,7 +35,7 @@ def test_prefill_single_tile():
     _check(w)
 
 
-@pytest.mark.parametrize("chunks", [[1], [17, 130], [128, 256], [255, 3, 64]])
+@pytest.mark.parametrize("chunks", [[1], [17, 130], [128, 256], [255, 3, 64], [64, 0, 17], [0, 1]])
 def test_prefill_varlen_chunks(chunks):
     w = W.prefill_zipf("pv", batch=len(chunks), hq=8, hkv=2, docs_per_seq=3, doc_tokens=200, pool_docs=5,
                        zipf_s=1.2, chunk_tokens=chunks, seed=72 + len(chunks))
